@@ -121,8 +121,9 @@ void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2],
 
 /* The uniforms of one verify position.  Counter = (request id, position in
  * the block, decode step, 0); key = the 64-bit seed split low/high.  Word 0
- * feeds the accept test, word 1 the resample.  A uniform is the top 24 bits
- * of the word times 2^-24: exact in binary32 and binary64, in [0, 1). */
+ * feeds the accept test (word 1 is reported too but unused: draws take their
+ * noise from counters with a non-zero last word).  A uniform is the top 24
+ * bits of the word times 2^-24: exact in binary32 and binary64, in [0, 1). */
 static void verify_uniforms(uint64_t seed, uint32_t request, uint32_t pos,
                             uint32_t step, double *u_accept, double *u_sample) {
     uint32_t ctr[4] = {request, pos, step, 0u};
@@ -351,29 +352,45 @@ static int64_t argmax_row(const float *x, int64_t V) {
     return best;
 }
 
-/* Inverse-CDF draw from the unnormalised non-negative weights w[0..V-1]:
- * the smallest v whose running sum C_v exceeds u * R (R = total).  If
- * rounding leaves no such v, the last v with w[v] > 0.  *margin receives
- * min(u*R - C_{v-1}, C_v - u*R) / R, the distance of the threshold from the
- * chosen interval's ends. */
-static int64_t inverse_cdf(const double *w, int64_t V, double u, double *margin) {
-    double R = 0.0;
-    for (int64_t v = 0; v < V; ++v) R += w[v];
-    double thr = u * R;
-    double c = 0.0;
-    int64_t last_pos = -1;
+/* Gumbel noise of vocabulary entry v for the draw made at block row `row`:
+ * Philox4x32-10 with counter (request, row, step, 1 + v/4), word v mod 4,
+ * U = (w >> 8 + 1/2) * 2^-24 in (0, 1), G = -log(-log U). */
+static double gumbel_noise(uint64_t seed, uint32_t req, uint32_t row, uint32_t step, int64_t v) {
+    uint32_t ctr[4] = {req, row, step, 1u + (uint32_t)(v / 4)};
+    uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    double u = ((double)(w[v % 4] >> 8) + 0.5) * (1.0 / 16777216.0);
+    return -log(-log(u));
+}
+
+/* One draw from the distribution proportional to exp(logw[v]) (logw = -inf
+ * for zero weight) by the Gumbel-max rule: the smallest v maximising
+ * logw[v] + G_v.  Returns -1 when every weight is zero.
+ *
+ * Diagnostics for parity accounting (not part of the method): err[v] is a
+ * bound on how far a binary32 evaluation of logw[v] may stray; *margin =
+ * (best - second best) - (bound of both, noise error included).  A negative
+ * margin means a faithful fp32 implementation may pick the runner-up. */
+static int64_t gumbel_draw(const double *logw, const double *err, int64_t V, uint64_t seed,
+                           uint32_t req, uint32_t row, uint32_t step, double *margin) {
+    const double eps = 1.0 / 524288.0; /* 2^-19: a few binary32 ulps of headroom */
+    int64_t best = -1, second = -1;
+    double kb = -INFINITY, ks = -INFINITY, eb = 0.0, es = 0.0;
     for (int64_t v = 0; v < V; ++v) {
-        double prevc = c;
-        c += w[v];
-        if (w[v] > 0.0) last_pos = v;
-        if (c > thr) {
-            double a = thr - prevc, bnd = c - thr;
-            *margin = (a < bnd ? a : bnd) / R;
-            return v;
+        if (logw[v] == -INFINITY) continue;
+        double g = gumbel_noise(seed, req, row, step, v);
+        double key = logw[v] + g;
+        double e = err[v] + eps * (fabs(g) + 1.0);
+        if (best < 0 || key > kb) {
+            second = best; ks = kb; es = eb;
+            best = v; kb = key; eb = e;
+        } else if (second < 0 || key > ks) {
+            second = v; ks = key; es = e;
         }
     }
-    *margin = 0.0;
-    return last_pos;
+    *margin = (second < 0) ? INFINITY : (kb - ks) - (eb + es);
+    return best;
 }
 
 /*
@@ -393,12 +410,14 @@ static int64_t inverse_cdf(const double *w, int64_t V, double u, double *margin)
  * drawn from max(0, p_j - q_j) normalised (one-hot q: p_j with d_j removed);
  * if its total is zero it is drawn from p_j.  If all L drafts are accepted,
  * the bonus token is drawn from p_L.  accepted_len = number of accepted
- * drafts.
+ * drafts.  The pages fix only these distributions; every draw here is the
+ * Gumbel-max rule of gumbel_draw (exact in distribution), so that the drawn
+ * index is an argmax and not a running-sum threshold.
  *
  * Layouts: target [B, k+1, V]; drafts [B, k]; draft_len [B] (NULL = k);
  * z [B, k, V].  Diagnostics (each may be NULL):
  *   accept_margin [B, k] : |u - p/q| of each decided position, NaN elsewhere
- *   sample_margin [B]    : interval margin of the inverse-CDF draw (NaN when
+ *   sample_margin [B]    : Gumbel-max gap minus its rounding bound (NaN when
  *                          no draw happened, i.e. greedy)
  *   sample_row    [B]    : block row the draw used (-1 greedy)
  */
@@ -439,7 +458,9 @@ int oracle_verify(int mode, const float *target, const int32_t *drafts,
         }
         double *p = (double *)malloc(sizeof(double) * (size_t)V);
         double *q = (double *)malloc(sizeof(double) * (size_t)V);
-        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        double *lw = (double *)malloc(sizeof(double) * (size_t)V);
+        double *er = (double *)malloc(sizeof(double) * (size_t)V);
+        const double eps = 1.0 / 524288.0;
         int a = 0;
         int rejected = 0;
         for (; a < L; ++a) {
@@ -450,7 +471,8 @@ int oracle_verify(int mode, const float *target, const int32_t *drafts,
                 rejected = 1;
                 break;
             }
-            softmax_row(trow0 + (int64_t)a * V, V, p);
+            const float *trow = trow0 + (int64_t)a * V;
+            softmax_row(trow, V, p);
             double qd = 1.0;
             if (z) {
                 softmax_row(z + ((int64_t)b * k + a) * V, V, q);
@@ -461,18 +483,31 @@ int oracle_verify(int mode, const float *target, const int32_t *drafts,
             double ratio = p[d] / qd;
             if (accept_margin) accept_margin[(int64_t)b * k + a] = fabs(ua - ratio);
             if (ua < ratio) continue;
-            /* rejected at position a: residual distribution */
+            /* rejected at position a: log of the residual weights */
+            double R = 0.0;
             for (int64_t v = 0; v < V; ++v) {
                 double qv = z ? q[v] : (v == d ? 1.0 : 0.0);
                 double rv = p[v] - qv;
-                w[v] = rv > 0.0 ? rv : 0.0;
+                if (rv > 0.0) {
+                    R += rv;
+                    lw[v] = log(rv);
+                    /* binary32 evaluation: log p and log q each to ~eps*(1+|log|); the
+                     * difference amplifies that by 1/(1 - q/p) */
+                    double lp = log(p[v]), lq = qv > 0.0 ? log(qv) : 0.0;
+                    double amp = qv > 0.0 ? 1.0 + qv / rv : 1.0;
+                    er[v] = eps * (2.0 + fabs(lp) + fabs(lq) + fabs(lw[v])) * amp;
+                } else {
+                    lw[v] = -INFINITY;
+                    er[v] = 0.0;
+                }
             }
-            double R = 0.0;
-            for (int64_t v = 0; v < V; ++v) R += w[v];
             if (!(R > 0.0))
-                for (int64_t v = 0; v < V; ++v) w[v] = p[v];
+                for (int64_t v = 0; v < V; ++v) {
+                    lw[v] = log(p[v]);
+                    er[v] = eps * (2.0 + fabs(lw[v]));
+                }
             double mg;
-            next_token[b] = (int32_t)inverse_cdf(w, V, us, &mg);
+            next_token[b] = (int32_t)gumbel_draw(lw, er, V, seed, req, (uint32_t)a, step, &mg);
             if (sample_margin) sample_margin[b] = mg;
             if (sample_row) sample_row[b] = a;
             rejected = 1;
@@ -480,15 +515,18 @@ int oracle_verify(int mode, const float *target, const int32_t *drafts,
         }
         if (!rejected) {
             /* every draft accepted: bonus token from p_L */
-            double ua, us, mg;
-            verify_uniforms(seed, req, (uint32_t)L, step, &ua, &us);
             softmax_row(trow0 + (int64_t)L * V, V, p);
-            next_token[b] = (int32_t)inverse_cdf(p, V, us, &mg);
+            for (int64_t v = 0; v < V; ++v) {
+                lw[v] = log(p[v]);
+                er[v] = eps * (2.0 + fabs(lw[v]));
+            }
+            double mg;
+            next_token[b] = (int32_t)gumbel_draw(lw, er, V, seed, req, (uint32_t)L, step, &mg);
             if (sample_margin) sample_margin[b] = mg;
             if (sample_row) sample_row[b] = L;
         }
         accepted_len[b] = a;
-        free(p); free(q); free(w);
+        free(p); free(q); free(lw); free(er);
     }
     return status;
 }

@@ -354,27 +354,48 @@ def test_verify_draft_len_zero_takes_bonus_from_row_zero():
     np.testing.assert_array_equal(out["sample_row"], [0, 0])
 
 
-def test_verify_inverse_cdf_threshold_closed_form():
-    """Bonus draw from p at full acceptance: next = smallest v with cumsum(p)_v > u' (u' =
-    the documented Philox uniform), computed here with numpy's cumsum."""
+def _gumbel(seed, req, row, step, V):
+    """Gumbel noise of the documented draw counters, from the Philox pinned above."""
+    g = np.empty(V)
+    for v in range(V):
+        w = oracle.philox4x32_10((req, row, step, 1 + v // 4), (seed & 0xFFFFFFFF, seed >> 32))
+        u = ((w[v % 4] >> 8) + 0.5) / 2.0 ** 24
+        g[v] = -math.log(-math.log(u))
+    return g
+
+
+def test_verify_draws_are_gumbel_argmax():
+    """Draws: next = argmax_v log w_v + G_v with G from the documented Philox counters
+    (numpy recomputation); accept iff u < p(d)/q(d) with q one-hot at the argmax draft."""
     V = 12
     tgt = syn.uniform_logits(31, (64, 2, V), 1.5)
     d = tgt[:, 0].argmax(axis=-1).astype(np.int32)[:, None]
     out = oracle.verify(0, tgt, d)
     assert np.all(out["accepted_len"] == 1)
-    # probabilistic with one-hot q at the argmax: accept iff u < p(d)
     outp = oracle.verify(1, tgt, d, None, None, seed=42, step=9)
     for b in range(64):
-        ua, us = oracle.verify_uniforms(42, b, 0, 9)
+        ua, _ = oracle.verify_uniforms(42, b, 0, 9)
         p0 = _softmax64(tgt[b, 0])
         if ua < p0[d[b, 0]]:
             assert outp["accepted_len"][b] == 1
-            _, us1 = oracle.verify_uniforms(42, b, 1, 9)
-            c = np.cumsum(_softmax64(tgt[b, 1]))
-            assert outp["next_token"][b] == int(np.argmax(c > us1))
+            key = np.log(_softmax64(tgt[b, 1])) + _gumbel(42, b, 1, 9, V)
         else:
             assert outp["accepted_len"][b] == 0
-            w = p0.copy()
-            w[d[b, 0]] = 0.0
-            c = np.cumsum(w)
-            assert outp["next_token"][b] == int(np.argmax(c > us * c[-1]))
+            lw = np.log(p0)
+            lw[d[b, 0]] = -np.inf
+            key = lw + _gumbel(42, b, 0, 9, V)
+        assert outp["next_token"][b] == int(np.argmax(key))
+
+
+def test_gumbel_draw_distribution_large_vocab():
+    """Bonus draws from p over V = 37 (several Philox blocks per row, a ragged last block):
+    chi-square against p over 200k requests."""
+    N, V = 200_000, 37
+    tl = syn.uniform_logits(77, (V,), 1.0)
+    p = _softmax64(tl)
+    target = np.broadcast_to(np.stack([tl, tl])[None], (N, 2, V)).copy()
+    drafts = np.full((N, 1), -1, np.int32)
+    out = oracle.verify(1, target, drafts, np.zeros(N, np.int32), None, seed=3, step=4)
+    assert np.all(out["accepted_len"] == 0) and np.all(out["sample_row"] == 0)
+    assert _chi2_pvalue(np.bincount(out["next_token"], minlength=V), p) > 1e-3
+    assert np.nanmin(out["sample_margin"]) > -1.0
