@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Draft+verify step benchmark of the GB300 DSpark readout + verify path.
+
+One step = the whole hot path for one batch: fc projection of the 5 tapped hidden
+states -> LM head over every block position -> Markov-biased semi-autoregressive
+greedy drafting (k positions) -> [confidence truncation] -> verification against the
+target logits.  Every step goes through the C ABI (libdspark.so).
+
+Prints ONE JSON line (rank 0).  Default workload: Qwen3.8-27B-DSpark shapes at batch 1
+(H=5120, 5 taps, V=151936, r=64, k=7, probabilistic verify).  Weights are random-init
+and inputs synthetic (seeded); see synthetic.py for the recipe.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own requests
+(the path has no cross-request exchange); value = all ranks' steps / max time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "draft+verify steps/sec and drafted tok/s at batch 1/16; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="27b_b1", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", type=int, default=None, help="verify mode override (0 greedy, 1 prob)")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sets", type=int, default=4, help="input sets rotated across steps")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, tflops, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        flat = {}
+
+        def walk(x, pre=""):
+            if isinstance(x, dict):
+                for kk, vv in x.items():
+                    walk(vv, pre + kk + ".")
+            else:
+                flat[pre[:-1]] = x
+        walk(d)
+        for kk, vv in flat.items():
+            if isinstance(vv, (int, float)) and "hbm" in kk.lower() and "gbs" in kk.lower():
+                hbm, src = float(vv), "measured"
+                break
+        for kk, vv in flat.items():
+            if isinstance(vv, (int, float)) and kk.lower().endswith("bf16_tflops"):
+                tflops = float(vv)
+                break
+    except (OSError, ValueError):
+        pass
+    return hbm, tflops, src
+
+
+def step_bytes(cfg, mode):
+    """Algorithmic bytes of one step: each weight once, activations, the fp32 draft
+    logits written once, the target logits read, one resample row pair per request."""
+    B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
+    M = B * k
+    fc = H * T * H * 2 + T * M * H * 2 + M * H * 2
+    lm = V * H * 2 + M * H * 2 + M * V * 4
+    chain = V * r * 2
+    verify = B * (k + 1) * V * 4 + (B * 2 * V * 4 if mode == 1 else 0)
+    return {"fc": fc, "lm_head": lm, "chain": chain, "verify": verify,
+            "total": fc + lm + chain + verify}
+
+
+def step_flops(cfg):
+    B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
+    M = B * k
+    return 2 * M * (T * H * H + V * H + V * r)
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = "/tmp/dspark_clocks_%d_%d.csv" % (os.getpid(), gpu_index)
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample_step(ora, host, cfg, mode, frac, step):
+    """The oracle's whole step restricted to a fraction of the output columns of fc and of
+    the vocabulary (LM head rows, chain, verify), so its cost is about frac x a full step.
+    Returns seconds."""
+    B, k, H, V = cfg["B"], cfg["k"], cfg["H"], cfg["V"]
+    nh = max(1, int(round(frac * H)))
+    nv = max(8, int(round(frac * V)))
+    t0 = time.perf_counter()
+    ora.fc_project(host["taps"], host["fc_w"][:nh])  # fc over nh output columns
+    t1 = time.perf_counter()
+    logits = ora.lm_head(host["h"], host["lm_w"][:nv]).reshape(B, k, nv)
+    prev = (host["prev"] % nv).astype(np.int32)
+    gs = ora.greedy_sample(logits, host["w1"][:nv], host["w2"][:nv], prev)
+    tgt = np.ascontiguousarray(host["target"][:, :, :nv])
+    ora.verify(mode, tgt, gs["draft_tokens"], None, gs["z"] if mode == 1 else None, seed=0,
+               step=step)
+    t2 = time.perf_counter()
+    # the fc slice costs nh/H of the fc; the rest nv/V of its full cost
+    return (t1 - t0) * (H / nh) + (t2 - t1) * (V / nv)
+
+
+def cpu_oracle_baseline(host, cfg, mode, budget_s, steps=None):
+    """Times the oracle (as it stands) on bounded samples of the workload; returns
+    (full steps/s extrapolated from the samples, cores, sample description, n)."""
+    import oracle as ora
+    # calibrate: one small sample
+    est = oracle_sample_step(ora, host, cfg, mode, 1.0 / 256, 0)
+    per_sample = budget_s / (steps if steps else 8)
+    frac = min(1.0, max(1.0 / 512, per_sample / max(est, 1e-6)))
+    n = steps if steps else 0
+    full_times = []
+    t_start = time.perf_counter()
+    i = 0
+    while True:
+        full_times.append(oracle_sample_step(ora, host, cfg, mode, frac, i + 1))
+        i += 1
+        if steps is not None and i >= steps:
+            break
+        if steps is None and time.perf_counter() - t_start > budget_s and i >= 2:
+            break
+    mean_full = statistics.mean(full_times)
+    desc = ("%d oracle samples, each the whole step on %.4f of the fc output columns and of the "
+            "vocabulary (LM head rows, Markov chain, verify), scaled to a full step"
+            % (len(full_times), frac))
+    return 1.0 / mean_full, ora.num_threads(), desc, len(full_times)
+
+
+def host_workload(cfg):
+    """Host copies of the weights and one step's inputs (for the CPU baseline)."""
+    import oracle as ora
+    B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
+    w = syn.weights(H, T, V, r, with_conf=cfg["conf"])
+    st = syn.step_inputs(0, B, k, H, T, V, cfg["sigma"])
+    h = ora.fc_project(st["taps"], w["fc_w"])
+    # target logits: the oracle's own draft logits (on the vocabulary) plus noise
+    host = {"taps": st["taps"], "fc_w": w["fc_w"], "lm_w": w["lm_w"], "w1": w["w1"],
+            "w2": w["w2"], "prev": st["prev"], "h": h}
+    host["target"] = st["noise"]  # noise alone stands in: the cost does not depend on values
+    return host
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    cfg = dict(syn.CONFIGS[args.config])
+    mode = cfg["mode"] if args.mode is None else args.mode
+    host = host_workload(cfg)
+    budget = 150.0
+    import oracle as ora
+    est = oracle_sample_step(ora, host, cfg, mode, 1.0 / 256, 0)
+    # size the sample so that warmup + steps finish within the budget
+    per_step = budget / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1.0 / 4096, per_step / max(est * 256 * 1.0, 1e-9)))
+    for i in range(args.warmup):
+        oracle_sample_step(ora, host, cfg, mode, frac, i)
+    t0 = time.perf_counter()
+    full = [oracle_sample_step(ora, host, cfg, mode, frac, args.warmup + i) for i in range(args.steps)]
+    wall = time.perf_counter() - t0
+    sps = 1.0 / statistics.mean(full)
+    desc = ("each step: the oracle's whole step on %.5f of the fc output columns and of the "
+            "vocabulary, scaled to a full step" % frac)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": sps, "unit": "steps/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / sps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "wall_s": wall,
+        "config": {"workload": args.config, **{kk: cfg[kk] for kk in ("B", "k", "H", "T", "V", "r")},
+                   "verify": "probabilistic" if mode == 1 else "greedy"},
+        "cpu_baseline": {"value": sps, "unit": "steps/s", "cores": ora.num_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": sps, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_fc_gb300 as ds
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    cfg = dict(syn.CONFIGS[args.config])
+    mode = cfg["mode"] if args.mode is None else args.mode
+    B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
+    M = B * k
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    w = syn.weights(H, T, V, r, with_conf=cfg["conf"])
+    fc_w, lm_w, w1, w2 = d16(w["fc_w"]), d16(w["lm_w"]), d16(w["w1"]), d16(w["w2"])
+    conf_w = d16(w["conf_w"]) if cfg["conf"] else None
+    host_w = w if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    del w
+
+    # input sets: taps, prev, target logits = own draft logits + noise (built once)
+    sets = []
+    for s in range(args.sets):
+        st = syn.step_inputs(s + 100 * rank, B, k, H, T, V, cfg["sigma"])
+        taps = [d16(t) for t in st["taps"]]
+        prev = torch.from_numpy(st["prev"]).to(device)
+        h = ds.fc_project(taps, fc_w)
+        logits = ds.lm_head(h, lm_w).view(B, k, V)
+        ds.greedy_sample(logits, w1, w2, prev)
+        noise = torch.from_numpy(st["noise"]).to(device)
+        target = torch.cat([logits, logits[:, -1:]], dim=1) + noise
+        sets.append({"taps": taps, "prev": prev, "target": target.contiguous(),
+                     "host": st if s == 0 else None})
+    torch.cuda.synchronize()
+
+    h_buf = torch.empty((M, H), dtype=torch.bfloat16, device=device)
+    logits = torch.empty((B, k, V), dtype=torch.float32, device=device)
+    drafts = torch.empty((B, k), dtype=torch.int32, device=device)
+    q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=device)
+    dlen = torch.empty((B,), dtype=torch.int32, device=device) if cfg["conf"] else None
+    K, W = args.steps, args.warmup
+    acc_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
+    nxt_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
+    dlen_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    lm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+    wsp = ds.Workspaces()
+
+    def one_step(i, st, ev=None):
+        ds.fc_project(st["taps"], fc_w, out=h_buf, stream=stream, workspaces=wsp)
+        if ev is not None:
+            ev[0].record(stream)
+        ds.lm_head(h_buf, lm_w, out=logits.view(M, V), stream=stream, workspaces=wsp)
+        if ev is not None:
+            ev[1].record(stream)
+        ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
+                         stream=stream, workspaces=wsp)
+        if conf_w is not None:
+            ds.confidence_truncate(h_buf, conf_w, drafts, B, k, w_conf_b, w_conf_tau,
+                                   draft_len=dlen_hist[i], stream=stream)
+        ds.verify(mode, st["target"], drafts, dlen_hist[i] if conf_w is not None else None,
+                  logits if mode == 1 else None, q_stats if mode == 1 else None, seed=12345,
+                  request_id=None, step=i, accepted_len=acc_hist[i], next_token=nxt_hist[i],
+                  stream=stream, workspaces=wsp)
+
+    w_conf_b, w_conf_tau = 0.0, 0.5
+    for i in range(W):
+        one_step(K + i, sets[i % len(sets)])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.1)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        one_step(i, sets[i % len(sets)], lm_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    lm_ms = statistics.mean(a.elapsed_time(b) for a, b in lm_ev)
+    max_ms = ms
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    Ke = min(args.e2e_steps, K)
+    st0 = sets[0]
+    pin_taps = torch.empty((T, M, H), dtype=torch.bfloat16).pin_memory()
+    for j in range(T):
+        pin_taps[j].copy_(st0["taps"][j].cpu())
+    pin_prev = st0["prev"].cpu().pin_memory()
+    pin_target = st0["target"].cpu().pin_memory()
+    out_acc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    out_nxt = torch.empty((B,), dtype=torch.int32).pin_memory()
+    out_drafts = torch.empty((B, k), dtype=torch.int32).pin_memory()
+    dev_taps = torch.empty((T, M, H), dtype=torch.bfloat16, device=device)
+    dev_prev = torch.empty((B,), dtype=torch.int32, device=device)
+    dev_target = torch.empty_like(st0["target"])
+    e2e_set = {"taps": [dev_taps[j] for j in range(T)], "prev": dev_prev, "target": dev_target}
+    h2d = pin_taps.numel() * 2 + pin_prev.numel() * 4 + pin_target.numel() * 4
+    d2h = (2 * B + B * k) * 4
+    for rep in range(2):
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        n = 3 if rep == 0 else Ke
+        t0 = time.perf_counter()
+        for i in range(n):
+            dev_taps.copy_(pin_taps, non_blocking=True)
+            dev_prev.copy_(pin_prev, non_blocking=True)
+            dev_target.copy_(pin_target, non_blocking=True)
+            one_step(i, e2e_set)
+            out_acc.copy_(acc_hist[i], non_blocking=True)
+            out_nxt.copy_(nxt_hist[i], non_blocking=True)
+            out_drafts.copy_(drafts, non_blocking=True)
+            stream.synchronize()  # the host reads this step's result
+        wall = time.perf_counter() - t0
+    e2e_t = torch.tensor([wall], device=device)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e = {"value": world * Ke / float(e2e_t.item()), "unit": "steps/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # ---------------------------------------------------------------- acceptance statistics
+    acc = acc_hist[:K].cpu().numpy()
+    if conf_w is not None:
+        drafted = float(dlen_hist[:K].cpu().numpy().sum()) / K
+    else:
+        drafted = float(B * k)
+    mean_acc_len = float(acc.mean()) + 1.0   # accepted drafts + the bonus/corrected token
+    per_pos = [float((acc > j).mean()) for j in range(k)]
+
+    steps_per_s = world * K / (max_ms / 1000.0)
+    peak_gbs, peak_tf, peak_src = measured_peaks()
+    sb = step_bytes(cfg, mode)
+    lm_bytes = sb["lm_head"]
+    achieved = lm_bytes / (lm_ms / 1000.0) / 1e9
+    t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
+    launches_per_step = 1 + 1 + k + (1 if conf_w is not None else 0) + (2 if mode == 1 else 1)
+
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "B": B, "k": k, "H": H, "taps": T, "V": V, "r": r,
+                   "verify": "probabilistic" if mode == 1 else "greedy",
+                   "confidence_head": bool(conf_w is not None),
+                   "l2": "inputs larger than L2: %.2f GB of weights streamed per step"
+                         % ((sb["fc"] + sb["lm_head"]) / 1e9),
+                   "parallelism": "replicas%d" % world},
+        "drafted_tok_s": steps_per_s * drafted,
+        "accepted_tok_s": steps_per_s * B * mean_acc_len,
+        "mean_acceptance_length": mean_acc_len,
+        "per_position_acceptance": per_pos,
+        "roofline": {"bound": "hbm", "kernel": "gemm_tcgen05 (LM head)", "achieved": achieved,
+                     "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
+                     "traffic": None, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
+        "step_roofline": {"bytes": sb["total"], "flops": step_flops(cfg),
+                          "t_roofline_ms": t_roof * 1000.0,
+                          "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src},
+        "gpu_launches": launches_per_step * K,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+
+    # ---------------------------------------------------------------- CPU oracle baseline
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle as ora
+        st = sets[0]["host"]
+        host = {"taps": st["taps"], "fc_w": host_w["fc_w"], "lm_w": host_w["lm_w"],
+                "w1": host_w["w1"], "w2": host_w["w2"], "prev": st["prev"],
+                "target": np.ascontiguousarray(sets[0]["target"].cpu().numpy())}
+        host["h"] = ora.fc_project(st["taps"], host_w["fc_w"])
+        sps, cores, desc, _ = cpu_oracle_baseline(host, cfg, mode, args.cpu_budget)
+        line["cpu_baseline"] = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, local_rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

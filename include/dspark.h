@@ -1,0 +1,234 @@
+/*
+ * dspark.h - C ABI of the GB300 (sm_103a) DSpark / DFlash speculative-decoding
+ * readout + verify hot path.
+ *
+ * The method (web pages this library follows):
+ *   [PR620]  "Qwen3.8-27B DFlash drafter recipe - 72.2 tok/s on Arc Pro B70",
+ *            the embedded DSpark port description: VanillaMarkov (markov_w1
+ *            embedding, markov_w2 projection), AcceptRatePredictor
+ *            (confidence head), propose() capturing the accepted bonus token,
+ *            _greedy_sample applying the full-vocab bigram bias
+ *            semi-autoregressively, _truncate_by_confidence.
+ *   [CARD]   "Qwen3.8-27B-DSpark-vLLM" model card: draft config fields,
+ *            "num_speculative_tokens": 7, "draft_sample_method":
+ *            "probabilistic", taps at layers 4/16/28/40/52, fc 5 x 5120.
+ *   [PR128]  "Qwen4Exp DFlash2 hidden-state capture": fc.weight
+ *            [2560, 12800] = 5 concatenated layer outputs; acceptance length
+ *            = accepted tokens per verification step; "verified by rejection
+ *            sampling".
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller (allocated
+ *     e.g. by PyTorch).  The library allocates no device memory per call and
+ *     keeps no pointer after a call returns.
+ *   - Tensors are dense row-major; the innermost dimension is contiguous.
+ *     bf16 operands read by the tensor-memory engine or with 128-bit loads
+ *     (taps, fc_w, h, lm_w, markov_w2, conf_w) must start on a 16-byte
+ *     boundary; every other pointer on a multiple of its element size
+ *     (else DSPARK_ERR_MISALIGNED).
+ *   - bf16 = IEEE bfloat16 bit pattern (dspark_bf16_t); fp32 = IEEE binary32.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work on it and returns; nothing
+ *     synchronises the host.
+ *   - ws / ws_bytes: a caller-owned DEVICE workspace of at least
+ *     dspark_<call>_workspace_size(...) bytes, 256-byte aligned, ZERO-FILLED
+ *     ONCE before its first use.  Every call leaves its counters at zero
+ *     again, so the same workspace serves any number of later calls with the
+ *     same or smaller sizes.  Calls that share a workspace must not overlap in
+ *     time (same stream, or ordered by events).
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned as a negative dspark_status_t.  Errors the device finds
+ *     (a token id outside [0, V), a bounded internal wait running out) are
+ *     recorded in the first 4 bytes of ws and read with
+ *     dspark_workspace_status(); the kernels then skip the offending access
+ *     instead of faulting.
+ *   - Sizes: B requests, k draft positions per block (1 <= k <= 16), H hidden
+ *     size (multiple of 64), V vocabulary size (>= 1), r Markov rank
+ *     (multiple of 8, <= 256), T taps (1..8).
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int dspark_status_t;
+typedef uint16_t dspark_bf16_t;
+
+#define DSPARK_OK 0
+#define DSPARK_ERR_INVALID_ARG (-1)       /* null pointer, negative size, bad mode */
+#define DSPARK_ERR_UNSUPPORTED_SHAPE (-2) /* size outside the caps listed above */
+#define DSPARK_ERR_MISALIGNED (-3)        /* pointer or row stride not 16-byte aligned */
+#define DSPARK_ERR_WORKSPACE (-4)         /* workspace missing or smaller than required */
+#define DSPARK_ERR_CUDA (-5)              /* a CUDA runtime or driver call failed */
+#define DSPARK_ERR_DEVICE_TIMEOUT (-6)    /* (device) a bounded wait ran out; work skipped */
+#define DSPARK_ERR_BAD_TOKEN (-7)         /* (device) token id outside [0, V) */
+#define DSPARK_ERR_NO_DEVICE (-8)         /* no sm_100-family GPU is current */
+
+/* Human-readable name of a status code.  Never returns NULL. */
+const char *dspark_status_string(dspark_status_t status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dspark_version(void);
+
+/* Reads the device-side status word at the start of ws (enqueued on stream,
+ * then the host waits for the stream), stores it in *status_out and resets
+ * it to 0.  DSPARK_OK means no device-side error since the last read. */
+dspark_status_t dspark_workspace_status(void *ws, void *stream, int32_t *status_out);
+
+/* ------------------------------------------------------------------------
+ * fc projection  ([PR128] "fc.weight is [2560, 12800], i.e. 5 features of
+ * width 2560", captured features are the layers' completed outputs; [CARD]
+ * "the drafter's fc expects 5 x 5120", target hidden states read at layers
+ * 4/16/28/40/52.)
+ *
+ *   h[m, n] = bf16_rne( sum_{j<T} sum_{c<H} taps[j][m, c] * fc_w[n, j*H + c] )
+ *
+ * accumulated in fp32 on the tensor cores; no bias, no normalisation.  The
+ * concatenation of the taps is never materialised: taps is a HOST array of T
+ * device pointers, tap j being the output of target layer target_layer_ids[j]
+ * in list order, each [M, H] bf16 with row stride tap_ld elements
+ * (tap_ld >= H, tap_ld % 8 == 0).  fc_w is [H, T*H] bf16 (PyTorch Linear
+ * [out, in]); h_out is [M, H] bf16.  M >= 1 (decode: M = B*k block
+ * positions; prefill: M = context tokens).
+ * ---------------------------------------------------------------------- */
+size_t dspark_fc_project_workspace_size(int M, int H, int T);
+dspark_status_t dspark_fc_project(const dspark_bf16_t *const *taps, int T, int64_t tap_ld,
+                                  const dspark_bf16_t *fc_w, dspark_bf16_t *h_out, int M,
+                                  int H, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * LM head over every block position of every request in one pass over the
+ * [V, H] weight ([PR620] drafter readout; one pass serves all B*k rows).
+ *
+ *   logits[m, v] = sum_{c<H} h[m, c] * lm_w[v, c]      (fp32 accumulate)
+ *
+ * h [M, H] bf16, lm_w [V, H] bf16, logits [M, V] fp32.
+ * ---------------------------------------------------------------------- */
+size_t dspark_lm_head_workspace_size(int M, int H, int V);
+dspark_status_t dspark_lm_head(const dspark_bf16_t *h, const dspark_bf16_t *lm_w,
+                               float *logits, int M, int H, int V, void *ws,
+                               size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Markov-biased semi-autoregressive greedy drafting ([PR620] VanillaMarkov;
+ * _greedy_sample "applies the full-vocab bigram bias semi-autoregressively
+ * across block positions (position i conditioned on position i-1's biased
+ * prediction)"; propose() "captures the accepted bonus token as the Markov
+ * previous-token context").
+ *
+ * For each request b and position i = 0..k-1, with prev_0 = prev_token[b]:
+ *   e[t]    = w1[prev_i, t]                                   (bf16 -> fp32)
+ *   bias[v] = fmaf chain over t = 0..r-1 of w2[v, t] * e[t], from +0.0f
+ *   z[v]    = logits[b, i, v] + bias[v]                       (fp32 add)
+ *   d_i     = smallest v with z[v] == max z   (-0 == +0; NaN never wins)
+ *   prev_{i+1} = d_i
+ * logits [B, k, V] fp32 is overwritten with z (the biased draft logits).
+ * draft_tokens [B, k] int32 receives d; q_stats [B, k, 2] fp32 receives
+ * (max z, sum_v exp(z[v] - max z)), the softmax statistics of the draft
+ * distribution q used by probabilistic verify (may be NULL).
+ * w1 [V, r] and w2 [V, r] bf16 (w2 is the Linear(r -> V) weight); w1 == NULL
+ * means no bias (plain argmax), then w2 and r are ignored.
+ * prev_token [B] int32 in [0, V) (else DSPARK_ERR_BAD_TOKEN is recorded and
+ * that request is drafted without bias).  Launches k kernels, one per
+ * position.
+ * ---------------------------------------------------------------------- */
+size_t dspark_greedy_sample_workspace_size(int B, int k, int V, int r);
+dspark_status_t dspark_greedy_sample(float *logits, const dspark_bf16_t *w1,
+                                     const dspark_bf16_t *w2, int r,
+                                     const int32_t *prev_token, int32_t *draft_tokens,
+                                     float *q_stats, int B, int k, int V, void *ws,
+                                     size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Confidence head and adaptive truncation alone ([PR620] AcceptRatePredictor,
+ * _truncate_by_confidence, DSPARK_ADAPTIVE_BLOCK).  The pages give no
+ * formula; the head is read as c[b, i] = sigmoid(conf_w . h[b*k+i] + conf_b),
+ * tested per position: draft_len[b] = first i with c[b, i] < conf_tau (k if
+ * none) and draft_tokens[b, i >= draft_len[b]] = -1 (in place).
+ * conf_tau <= 0 keeps every position; conf_tau >= 1 keeps none.
+ *   h [B*k, H] bf16 (the fc output), conf_w [H] bf16, draft_tokens [B, k]
+ *   int32 (in/out), draft_len [B] int32 (out), conf_out [B, k] fp32 or NULL.
+ * One kernel; needs no workspace.
+ * ---------------------------------------------------------------------- */
+dspark_status_t dspark_confidence_truncate(const dspark_bf16_t *h, const dspark_bf16_t *conf_w,
+                                           float conf_b, float conf_tau, int32_t *draft_tokens,
+                                           int32_t *draft_len, float *conf_out, int B, int k,
+                                           int H, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Whole drafter readout: LM head (as dspark_lm_head) + Markov greedy
+ * drafting (as dspark_greedy_sample) + optional confidence truncation
+ * ([PR620] AcceptRatePredictor "optional per-position acceptance-confidence
+ * head", _truncate_by_confidence "adaptive draft block length").
+ *
+ * Confidence (when conf_w != NULL): c[b, i] = sigmoid(conf_w . h[b*k+i] +
+ * conf_b), evaluated per position; draft_len[b] = first i with
+ * c[b, i] < conf_tau (k if none); draft_tokens[b, i >= draft_len[b]] = -1.
+ * conf_tau <= 0 keeps every position, conf_tau >= 1 keeps none.  Without a
+ * confidence head draft_len[b] = k.
+ *   h [B*k, H] bf16 (the fc output), lm_w [V, H] bf16,
+ *   logits [B, k, V] fp32 (out: biased draft logits z),
+ *   q_stats [B, k, 2] fp32 or NULL, draft_tokens [B, k] int32,
+ *   draft_len [B] int32 or NULL, conf_out [B, k] fp32 or NULL.
+ * ---------------------------------------------------------------------- */
+size_t dspark_draft_readout_workspace_size(int B, int k, int H, int V, int r);
+dspark_status_t dspark_draft_readout(const dspark_bf16_t *h, const dspark_bf16_t *lm_w,
+                                     const dspark_bf16_t *w1, const dspark_bf16_t *w2, int r,
+                                     const int32_t *prev_token, const dspark_bf16_t *conf_w,
+                                     float conf_b, float conf_tau, float *logits,
+                                     float *q_stats, int32_t *draft_tokens,
+                                     int32_t *draft_len, float *conf_out, int B, int k, int H,
+                                     int V, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Verification of one draft block per request.
+ *
+ * mode 0, greedy exact match ([PR620] "greedy spec decode is lossless by
+ * construction"): t_j = argmax target[b, j] (lowest index on ties);
+ * accepted_len[b] = longest prefix (<= draft_len[b]) with
+ * draft_tokens[b, j] == t_j; next_token[b] = t_{accepted_len}.
+ *
+ * mode 1, probabilistic ([CARD] "draft_sample_method": "probabilistic";
+ * [PR128] "verified by rejection sampling"): p_j = softmax(target[b, j]),
+ * q_j = softmax(draft_logits[b, j]) (one-hot at the draft when draft_logits
+ * is NULL).  Positions are tested in order; draft d_j is accepted iff
+ * u_j < p_j(d_j) / q_j(d_j).  At the first rejection j, next_token is drawn
+ * from max(0, p_j - q_j) normalised (p_j if that is all zero); if every one
+ * of the draft_len drafts is accepted, the bonus token is drawn from
+ * p_{draft_len}.  The pages fix only these distributions; every draw here is
+ * the Gumbel-max rule: the smallest v maximising log w_v + G_v, where w is
+ * the (unnormalised) weight vector and G_v = -log(-log U_v), which samples
+ * exactly from w normalised.
+ * Uniforms: Philox4x32-10 (Salmon et al., SC'11) with key = (seed low 32
+ * bits, seed high 32 bits).  Accept test of position j: counter
+ * (request_id[b], j, step, 0), u_j = (word0 >> 8) * 2^-24.  Draw at block row
+ * j: counter (request_id[b], j, step, 1 + v/4), word v mod 4, U_v =
+ * (2 * (word >> 9) + 1) * 2^-24.
+ *
+ *   target_logits [B, k+1, V] fp32 (row k+1 of a block is the bonus row),
+ *   draft_tokens [B, k] int32, draft_len [B] int32 or NULL (= k),
+ *   draft_logits [B, k, V] fp32 (biased draft logits) or NULL,
+ *   q_stats [B, k, 2] fp32 from dspark_greedy_sample, or NULL: then the
+ *     statistics are recomputed from draft_logits (one more read of it),
+ *   request_id [B] uint32 or NULL (= b),
+ *   accepted_len [B] int32, next_token [B] int32 (outputs).
+ * Mode 0 ignores draft_logits, q_stats, seed, request_id and step.
+ * ---------------------------------------------------------------------- */
+size_t dspark_verify_workspace_size(int B, int k, int V);
+dspark_status_t dspark_verify(int mode, const float *target_logits,
+                              const int32_t *draft_tokens, const int32_t *draft_len,
+                              const float *draft_logits, const float *q_stats, uint64_t seed,
+                              const uint32_t *request_id, uint32_t step,
+                              int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
+                              void *ws, size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -353,14 +353,15 @@ static int64_t argmax_row(const float *x, int64_t V) {
 }
 
 /* Gumbel noise of vocabulary entry v for the draw made at block row `row`:
- * Philox4x32-10 with counter (request, row, step, 1 + v/4), word v mod 4,
- * U = (w >> 8 + 1/2) * 2^-24 in (0, 1), G = -log(-log U). */
+ * Philox4x32-10 with counter (request, row, step, 1 + v/4), word w = word
+ * v mod 4, U = (2 * (w >> 9) + 1) * 2^-24 (an odd multiple of 2^-24, so U is
+ * exact in binary32 and lies strictly inside (0, 1)), G = -log(-log U). */
 static double gumbel_noise(uint64_t seed, uint32_t req, uint32_t row, uint32_t step, int64_t v) {
     uint32_t ctr[4] = {req, row, step, 1u + (uint32_t)(v / 4)};
     uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
     uint32_t w[4];
     oracle_philox4x32_10(ctr, key, w);
-    double u = ((double)(w[v % 4] >> 8) + 0.5) * (1.0 / 16777216.0);
+    double u = (double)(2u * (w[v % 4] >> 9) + 1u) * (1.0 / 16777216.0);
     return -log(-log(u));
 }
 

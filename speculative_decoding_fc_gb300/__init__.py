@@ -1,0 +1,331 @@
+"""GB300 (sm_103a) DSpark / DFlash speculative-decoding readout + verify.
+
+Thin Python binding over ``libdspark.so`` (C ABI in ``include/dspark.h``).  This
+module only checks tensors and marshals pointers; every step of the path runs
+in the library's CUDA kernels.  There is no CPU fallback: if the library is
+missing or no sm_103 GPU is present, calls raise.
+
+Functions follow the pages' notation:
+  fc_project      concat(taps) . fc.weight^T -> h (bf16)
+  lm_head         h . lm_head.weight^T -> fp32 logits for every block position
+  greedy_sample   Markov-biased, semi-autoregressive argmax drafting (in place)
+  draft_readout   lm_head + greedy_sample + optional confidence truncation
+  verify          greedy exact match or probabilistic rejection sampling
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["DSparkError", "lib", "fc_project", "lm_head", "greedy_sample", "confidence_truncate",
+           "draft_readout",
+           "verify", "workspace_status", "Workspaces", "library_path"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libdspark.so")
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+
+class DSparkError(RuntimeError):
+    """A libdspark call returned a non-zero status."""
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libdspark (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise DSparkError("libdspark.so is not built (%s); build it with "
+                              "`python -m speculative_decoding_fc_gb300._build`" % _LIB_PATH)
+        L = ctypes.CDLL(_LIB_PATH)
+        L.dspark_status_string.restype = ctypes.c_char_p
+        L.dspark_status_string.argtypes = [ctypes.c_int]
+        L.dspark_version.restype = ctypes.c_int
+        L.dspark_workspace_status.restype = ctypes.c_int
+        L.dspark_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
+        L.dspark_fc_project_workspace_size.restype = _sz
+        L.dspark_fc_project_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.dspark_fc_project.restype = ctypes.c_int
+        L.dspark_fc_project.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _i64, _vp, _vp,
+                                        ctypes.c_int, ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_lm_head_workspace_size.restype = _sz
+        L.dspark_lm_head_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.dspark_lm_head.restype = ctypes.c_int
+        L.dspark_lm_head.argtypes = [_vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp,
+                                     _sz, _vp]
+        L.dspark_greedy_sample_workspace_size.restype = _sz
+        L.dspark_greedy_sample_workspace_size.argtypes = [ctypes.c_int] * 4
+        L.dspark_greedy_sample.restype = ctypes.c_int
+        L.dspark_greedy_sample.argtypes = [_vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_confidence_truncate.restype = ctypes.c_int
+        L.dspark_confidence_truncate.argtypes = [_vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp,
+                                                 _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
+        L.dspark_draft_readout_workspace_size.restype = _sz
+        L.dspark_draft_readout_workspace_size.argtypes = [ctypes.c_int] * 5
+        L.dspark_draft_readout.restype = ctypes.c_int
+        L.dspark_draft_readout.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, ctypes.c_float,
+                                           ctypes.c_float, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_verify_workspace_size.restype = _sz
+        L.dspark_verify_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.dspark_verify.restype = ctypes.c_int
+        L.dspark_verify.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_uint64, _vp,
+                                    ctypes.c_uint32, _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, _vp, _sz, _vp]
+        _lib = L
+    return _lib
+
+
+def _check(rc, what):
+    if rc != 0:
+        name = lib().dspark_status_string(rc).decode()
+        raise DSparkError("%s failed: %s (%d)" % (what, name, rc))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise DSparkError("%s must be a CUDA tensor (no CPU path exists)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+class Workspaces:
+    """Zero-initialised device workspaces, one per (call kind, device), grown on
+    demand.  Calls that share a workspace must be ordered on the GPU (one stream,
+    or events); pass a separate Workspaces object to run calls concurrently."""
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, kind, device, nbytes):
+        key = (kind, torch.device(device).index)
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        return buf
+
+
+_default_ws = Workspaces()
+
+
+def workspace_status(ws, stream=None):
+    """Reads and clears the device-side status word of a workspace tensor."""
+    out = _i32(0)
+    _check(lib().dspark_workspace_status(_ptr(ws), _stream(stream, ws.device), ctypes.byref(out)),
+           "dspark_workspace_status")
+    return int(out.value)
+
+
+def fc_project(taps, fc_w, out=None, stream=None, workspaces=None):
+    """h[M, H] (bf16) = concat(taps) . fc_w^T.  taps: T bf16 tensors [M, H] (row stride
+    may exceed H); fc_w: [H, T*H] bf16."""
+    T = len(taps)
+    M, H = taps[0].shape
+    dev = fc_w.device
+    _need(fc_w, "fc_w", torch.bfloat16, (H, T * H))
+    ld = taps[0].stride(0)
+    for j, t in enumerate(taps):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (M, H) \
+                or t.stride(1) != 1 or t.stride(0) != ld:
+            raise ValueError("tap %d must be a CUDA bf16 [%d, %d] tensor with row stride %d" % (j, M, H, ld))
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (M, H))
+    L = lib()
+    nbytes = L.dspark_fc_project_workspace_size(M, H, T)
+    ws = (workspaces or _default_ws).get("fc", dev, nbytes)
+    arr = (_vp * T)(*[t.data_ptr() for t in taps])
+    _check(L.dspark_fc_project(arr, T, ld, _ptr(fc_w), _ptr(out), M, H, _ptr(ws), ws.numel(),
+                               _stream(stream, dev)), "dspark_fc_project")
+    return out
+
+
+def lm_head(h, lm_w, out=None, stream=None, workspaces=None):
+    """fp32 logits [M, V] = h . lm_w^T (h [M, H] bf16, lm_w [V, H] bf16)."""
+    M, H = h.shape
+    V = lm_w.shape[0]
+    _need(h, "h", torch.bfloat16)
+    _need(lm_w, "lm_w", torch.bfloat16, (V, H))
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.float32, device=h.device)
+    _need(out, "out", torch.float32)
+    if out.numel() != M * V:
+        raise ValueError("out must hold M*V floats")
+    L = lib()
+    ws = (workspaces or _default_ws).get("lm", h.device, L.dspark_lm_head_workspace_size(M, H, V))
+    _check(L.dspark_lm_head(_ptr(h), _ptr(lm_w), _ptr(out), M, H, V, _ptr(ws), ws.numel(),
+                            _stream(stream, h.device)), "dspark_lm_head")
+    return out
+
+
+def greedy_sample(logits, w1, w2, prev_token, draft_tokens=None, q_stats=None, stream=None,
+                  workspaces=None):
+    """Markov-biased greedy drafting.  logits fp32 [B, k, V] is biased in place; returns
+    (draft_tokens int32 [B, k], q_stats fp32 [B, k, 2])."""
+    B, k, V = logits.shape
+    _need(logits, "logits", torch.float32)
+    r = 0
+    if w1 is not None:
+        r = w1.shape[1]
+        _need(w1, "w1", torch.bfloat16, (V, r))
+        _need(w2, "w2", torch.bfloat16, (V, r))
+    _need(prev_token, "prev_token", torch.int32, (B,))
+    dev = logits.device
+    if draft_tokens is None:
+        draft_tokens = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if q_stats is None:
+        q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    _need(q_stats, "q_stats", torch.float32, (B, k, 2))
+    L = lib()
+    ws = (workspaces or _default_ws).get("chain", dev, L.dspark_greedy_sample_workspace_size(B, k, V, r))
+    _check(L.dspark_greedy_sample(_ptr(logits), _ptr(w1), _ptr(w2), r, _ptr(prev_token),
+                                  _ptr(draft_tokens), _ptr(q_stats), B, k, V, _ptr(ws), ws.numel(),
+                                  _stream(stream, dev)), "dspark_greedy_sample")
+    return draft_tokens, q_stats
+
+
+def confidence_truncate(h, conf_w, draft_tokens, B, k, conf_b=0.0, conf_tau=0.5, draft_len=None,
+                        conf_out=None, stream=None):
+    """Confidence head + adaptive truncation: c = sigmoid(conf_w . h + conf_b) per block
+    position; draft_len[b] = first position with c < conf_tau; later drafts become -1 (in
+    place).  Returns (draft_len int32 [B], conf fp32 [B, k] or None)."""
+    M, H = h.shape
+    if M != B * k:
+        raise ValueError("h must have B*k rows")
+    _need(h, "h", torch.bfloat16)
+    _need(conf_w, "conf_w", torch.bfloat16, (H,))
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    if draft_len is None:
+        draft_len = torch.empty((B,), dtype=torch.int32, device=h.device)
+    _need(draft_len, "draft_len", torch.int32, (B,))
+    if conf_out is not None:
+        _need(conf_out, "conf_out", torch.float32, (B, k))
+    _check(lib().dspark_confidence_truncate(_ptr(h), _ptr(conf_w), float(conf_b), float(conf_tau),
+                                            _ptr(draft_tokens), _ptr(draft_len), _ptr(conf_out), B,
+                                            k, H, _stream(stream, h.device)),
+           "dspark_confidence_truncate")
+    return draft_len, conf_out
+
+
+def draft_readout(h, lm_w, w1, w2, prev_token, B, k, conf_w=None, conf_b=0.0, conf_tau=0.5,
+                  out=None, stream=None, workspaces=None):
+    """LM head + Markov greedy drafting + optional confidence truncation.
+
+    h: [B*k, H] bf16.  Returns a dict with logits (biased, fp32 [B, k, V]), q_stats,
+    draft_tokens (-1 past the truncation point), draft_len, conf (or None)."""
+    M, H = h.shape
+    if M != B * k:
+        raise ValueError("h must have B*k rows")
+    V = lm_w.shape[0]
+    dev = h.device
+    _need(h, "h", torch.bfloat16)
+    _need(lm_w, "lm_w", torch.bfloat16, (V, H))
+    r = 0
+    if w1 is not None:
+        r = w1.shape[1]
+        _need(w1, "w1", torch.bfloat16, (V, r))
+        _need(w2, "w2", torch.bfloat16, (V, r))
+    _need(prev_token, "prev_token", torch.int32, (B,))
+    if conf_w is not None:
+        _need(conf_w, "conf_w", torch.bfloat16, (H,))
+    o = out if out is not None else {}
+    logits = o.get("logits")
+    if logits is None:
+        logits = torch.empty((B, k, V), dtype=torch.float32, device=dev)
+    q_stats = o.get("q_stats")
+    if q_stats is None:
+        q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
+    drafts = o.get("draft_tokens")
+    if drafts is None:
+        drafts = torch.empty((B, k), dtype=torch.int32, device=dev)
+    dlen = o.get("draft_len")
+    if dlen is None:
+        dlen = torch.empty((B,), dtype=torch.int32, device=dev)
+    conf = o.get("conf")
+    if conf is None and conf_w is not None:
+        conf = torch.empty((B, k), dtype=torch.float32, device=dev)
+    _need(logits, "logits", torch.float32, (B, k, V))
+    _need(q_stats, "q_stats", torch.float32, (B, k, 2))
+    _need(drafts, "draft_tokens", torch.int32, (B, k))
+    _need(dlen, "draft_len", torch.int32, (B,))
+    L = lib()
+    ws = (workspaces or _default_ws).get("readout", dev,
+                                         L.dspark_draft_readout_workspace_size(B, k, H, V, r))
+    _check(L.dspark_draft_readout(_ptr(h), _ptr(lm_w), _ptr(w1), _ptr(w2), r, _ptr(prev_token),
+                                  _ptr(conf_w), float(conf_b), float(conf_tau), _ptr(logits),
+                                  _ptr(q_stats), _ptr(drafts), _ptr(dlen), _ptr(conf), B, k, H, V,
+                                  _ptr(ws), ws.numel(), _stream(stream, dev)), "dspark_draft_readout")
+    return {"logits": logits, "q_stats": q_stats, "draft_tokens": drafts, "draft_len": dlen,
+            "conf": conf}
+
+
+def verify(mode, target_logits, draft_tokens, draft_len=None, draft_logits=None, q_stats=None,
+           seed=0, request_id=None, step=0, accepted_len=None, next_token=None, stream=None,
+           workspaces=None):
+    """Verify one draft block per request.  mode 0 greedy, 1 probabilistic.
+    target_logits fp32 [B, k+1, V]; returns (accepted_len int32 [B], next_token int32 [B])."""
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    _need(target_logits, "target_logits", torch.float32)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    if draft_len is not None:
+        _need(draft_len, "draft_len", torch.int32, (B,))
+    if draft_logits is not None:
+        _need(draft_logits, "draft_logits", torch.float32, (B, k, V))
+    if q_stats is not None:
+        _need(q_stats, "q_stats", torch.float32, (B, k, 2))
+    if request_id is not None:
+        if request_id.dtype not in (torch.int32, torch.uint32):
+            raise TypeError("request_id must be int32/uint32")
+        if not request_id.is_cuda or not request_id.is_contiguous() or tuple(request_id.shape) != (B,):
+            raise ValueError("request_id must be a contiguous CUDA [B] tensor")
+    if accepted_len is None:
+        accepted_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(accepted_len, "accepted_len", torch.int32, (B,))
+    _need(next_token, "next_token", torch.int32, (B,))
+    L = lib()
+    ws = (workspaces or _default_ws).get("verify", dev, L.dspark_verify_workspace_size(B, k, V))
+    _check(L.dspark_verify(int(mode), _ptr(target_logits), _ptr(draft_tokens), _ptr(draft_len),
+                           _ptr(draft_logits), _ptr(q_stats), int(seed) & (2 ** 64 - 1),
+                           _ptr(request_id), int(step) & 0xFFFFFFFF, _ptr(accepted_len),
+                           _ptr(next_token), B, k, V, _ptr(ws), ws.numel(), _stream(stream, dev)),
+           "dspark_verify")
+    return accepted_len, next_token

@@ -1,0 +1,312 @@
+// extern "C" entry points of libdspark: argument checks on the host, then the
+// kernels of the other translation units.  Nothing here allocates device
+// memory or synchronises the host (except dspark_workspace_status, which is a
+// diagnostic read).
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <cmath>
+
+#include "internal.h"
+
+namespace dspark {
+
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool device_is_blackwell() {
+  static int cache[64] = {};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev >= 0 && dev < 64 && cache[dev] != 0) return cache[dev] == 1;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  const bool ok = (major == 10 && minor == 3);  // the library is built for sm_103a only
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok;
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+namespace {
+
+constexpr size_t kHeader = kWsAlign;  // status word + padding at the start of every workspace
+constexpr int kMaxM = 1 << 20;
+constexpr int kMaxV = 1 << 26;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned2(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+int *status_word(void *ws) { return reinterpret_cast<int *>(ws); }
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+dspark_status_t check_ws(const void *ws, size_t have, size_t need) {
+  if (!ws) return DSPARK_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0) return DSPARK_ERR_MISALIGNED;
+  if (have < need) return DSPARK_ERR_WORKSPACE;
+  return DSPARK_OK;
+}
+
+dspark_status_t check_device() { return device_is_blackwell() ? DSPARK_OK : DSPARK_ERR_NO_DEVICE; }
+
+dspark_status_t check_lm_args(const void *h, const void *lm_w, const void *logits, int M, int H,
+                              int V) {
+  if (!h || !lm_w || !logits) return DSPARK_ERR_INVALID_ARG;
+  if (M < 1 || H < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (M > kMaxM || V > kMaxV || H % 64 != 0 || H > (1 << 20)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(h) || !aligned16(lm_w) || !aligned4(logits)) return DSPARK_ERR_MISALIGNED;
+  return DSPARK_OK;
+}
+
+dspark_status_t check_chain_args(const void *logits, const void *w1, const void *w2, int r,
+                                 const void *prev, const void *drafts, const void *q_stats, int B,
+                                 int k, int V) {
+  if (!logits || !prev || !drafts) return DSPARK_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (k > kMaxK || V > kMaxV || B > (1 << 16)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (w1) {
+    if (!w2) return DSPARK_ERR_INVALID_ARG;
+    if (r < 8 || r > kMaxRank || r % 8 != 0) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned2(w1) || !aligned16(w2)) return DSPARK_ERR_MISALIGNED;
+  }
+  if (!aligned4(logits) || !aligned4(prev) || !aligned4(drafts)) return DSPARK_ERR_MISALIGNED;
+  if (q_stats && !aligned4(q_stats)) return DSPARK_ERR_MISALIGNED;
+  return DSPARK_OK;
+}
+
+size_t chain_ws_bytes(int B, int k, int V) { return kHeader + chain_workspace_size(B, k, V); }
+
+}  // namespace
+
+extern "C" {
+
+const char *dspark_status_string(dspark_status_t s) {
+  switch (s) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_ERR_INVALID_ARG: return "DSPARK_ERR_INVALID_ARG";
+    case DSPARK_ERR_UNSUPPORTED_SHAPE: return "DSPARK_ERR_UNSUPPORTED_SHAPE";
+    case DSPARK_ERR_MISALIGNED: return "DSPARK_ERR_MISALIGNED";
+    case DSPARK_ERR_WORKSPACE: return "DSPARK_ERR_WORKSPACE";
+    case DSPARK_ERR_CUDA: return "DSPARK_ERR_CUDA";
+    case DSPARK_ERR_DEVICE_TIMEOUT: return "DSPARK_ERR_DEVICE_TIMEOUT";
+    case DSPARK_ERR_BAD_TOKEN: return "DSPARK_ERR_BAD_TOKEN";
+    case DSPARK_ERR_NO_DEVICE: return "DSPARK_ERR_NO_DEVICE";
+    default: return "DSPARK_ERR_UNKNOWN";
+  }
+}
+
+int dspark_version(void) { return 100; }
+
+dspark_status_t dspark_workspace_status(void *ws, void *stream, int32_t *status_out) {
+  if (!ws || !status_out) return DSPARK_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(v), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+  *status_out = v;
+  return DSPARK_OK;
+}
+
+// ---------------------------------------------------------------- fc projection
+size_t dspark_fc_project_workspace_size(int M, int H, int T) {
+  if (M < 1 || H < 64 || T < 1 || T > kMaxTaps) return 0;
+  return kHeader + gemm_workspace_size(M, H, T * H);
+}
+
+dspark_status_t dspark_fc_project(const dspark_bf16_t *const *taps, int T, int64_t tap_ld,
+                                  const dspark_bf16_t *fc_w, dspark_bf16_t *h_out, int M, int H,
+                                  void *ws, size_t ws_bytes, void *stream) {
+  if (!taps || !fc_w || !h_out) return DSPARK_ERR_INVALID_ARG;
+  if (T < 1 || M < 1 || H < 1 || tap_ld < H) return DSPARK_ERR_INVALID_ARG;
+  if (T > kMaxTaps || H % 64 != 0 || M > kMaxM || H > (1 << 16)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (tap_ld % 8 != 0 || !aligned16(fc_w) || !aligned2(h_out)) return DSPARK_ERR_MISALIGNED;
+  for (int j = 0; j < T; ++j) {
+    if (!taps[j]) return DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(taps[j])) return DSPARK_ERR_MISALIGNED;
+  }
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_fc_project_workspace_size(M, H, T));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  GemmProblem p;
+  memset(&p, 0, sizeof(p));
+  p.w = fc_w;
+  for (int j = 0; j < T; ++j) {
+    p.x[j] = taps[j];
+    p.x_ld[j] = tap_ld;
+  }
+  p.n_seg = T;
+  p.seg_k = H;
+  p.N = H;
+  p.M = M;
+  p.out = h_out;
+  p.ldo = H;
+  p.out_bf16 = true;
+  return gemm_launch(p, static_cast<char *>(ws) + kHeader, ws_bytes - kHeader, status_word(ws),
+                     as_stream(stream));
+}
+
+// ---------------------------------------------------------------- LM head
+size_t dspark_lm_head_workspace_size(int M, int H, int V) {
+  if (M < 1 || H < 64 || V < 1) return 0;
+  return kHeader + gemm_workspace_size(M, V, H);
+}
+
+static dspark_status_t lm_head_enqueue(const dspark_bf16_t *h, const dspark_bf16_t *lm_w,
+                                       float *logits, int M, int H, int V, void *gemm_ws,
+                                       size_t gemm_ws_bytes, int *status, cudaStream_t s) {
+  GemmProblem p;
+  memset(&p, 0, sizeof(p));
+  p.w = lm_w;
+  p.x[0] = h;
+  p.x_ld[0] = H;
+  p.n_seg = 1;
+  p.seg_k = H;
+  p.N = V;
+  p.M = M;
+  p.out = logits;
+  p.ldo = V;
+  p.out_bf16 = false;
+  return gemm_launch(p, gemm_ws, gemm_ws_bytes, status, s);
+}
+
+dspark_status_t dspark_lm_head(const dspark_bf16_t *h, const dspark_bf16_t *lm_w, float *logits,
+                               int M, int H, int V, void *ws, size_t ws_bytes, void *stream) {
+  dspark_status_t st = check_lm_args(h, lm_w, logits, M, H, V);
+  if (st != DSPARK_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, dspark_lm_head_workspace_size(M, H, V))) != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  return lm_head_enqueue(h, lm_w, logits, M, H, V, static_cast<char *>(ws) + kHeader,
+                         ws_bytes - kHeader, status_word(ws), as_stream(stream));
+}
+
+// ---------------------------------------------------------------- Markov greedy drafting
+size_t dspark_greedy_sample_workspace_size(int B, int k, int V, int r) {
+  (void)r;
+  if (B < 1 || k < 1 || V < 1) return 0;
+  return chain_ws_bytes(B, k, V);
+}
+
+dspark_status_t dspark_greedy_sample(float *logits, const dspark_bf16_t *w1,
+                                     const dspark_bf16_t *w2, int r, const int32_t *prev_token,
+                                     int32_t *draft_tokens, float *q_stats, int B, int k, int V,
+                                     void *ws, size_t ws_bytes, void *stream) {
+  dspark_status_t st = check_chain_args(logits, w1, w2, r, prev_token, draft_tokens, q_stats, B, k, V);
+  if (st != DSPARK_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, chain_ws_bytes(B, k, V))) != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  return chain_launch(logits, w1, w2, w1 ? r : 0, prev_token, draft_tokens, q_stats, nullptr, B,
+                      k, V, static_cast<char *>(ws) + kHeader, status_word(ws), as_stream(stream));
+}
+
+// ---------------------------------------------------------------- confidence truncation
+dspark_status_t dspark_confidence_truncate(const dspark_bf16_t *h, const dspark_bf16_t *conf_w,
+                                           float conf_b, float conf_tau, int32_t *draft_tokens,
+                                           int32_t *draft_len, float *conf_out, int B, int k,
+                                           int H, void *stream) {
+  if (!h || !conf_w || !draft_tokens || !draft_len) return DSPARK_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || H < 1) return DSPARK_ERR_INVALID_ARG;
+  if (k > kMaxK || B > (1 << 20) || H % 64 != 0) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (std::isnan(conf_tau) || std::isnan(conf_b)) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(conf_w) || !aligned4(draft_tokens) || !aligned4(draft_len) ||
+      (conf_out && !aligned4(conf_out)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return confidence_launch(h, conf_w, conf_b, conf_tau, draft_tokens, draft_len, conf_out, B, k,
+                           H, as_stream(stream));
+}
+
+// ---------------------------------------------------------------- whole readout
+size_t dspark_draft_readout_workspace_size(int B, int k, int H, int V, int r) {
+  (void)r;
+  if (B < 1 || k < 1 || H < 64 || V < 1) return 0;
+  return kHeader + align_up(gemm_workspace_size(B * k, V, H), kWsAlign) +
+         chain_workspace_size(B, k, V);
+}
+
+dspark_status_t dspark_draft_readout(const dspark_bf16_t *h, const dspark_bf16_t *lm_w,
+                                     const dspark_bf16_t *w1, const dspark_bf16_t *w2, int r,
+                                     const int32_t *prev_token, const dspark_bf16_t *conf_w,
+                                     float conf_b, float conf_tau, float *logits, float *q_stats,
+                                     int32_t *draft_tokens, int32_t *draft_len, float *conf_out,
+                                     int B, int k, int H, int V, void *ws, size_t ws_bytes,
+                                     void *stream) {
+  if (B < 1 || k < 1) return DSPARK_ERR_INVALID_ARG;
+  if (B > (1 << 16) || k > kMaxK || static_cast<long long>(B) * k > kMaxM)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  const int M = B * k;
+  dspark_status_t st = check_lm_args(h, lm_w, logits, M, H, V);
+  if (st != DSPARK_OK) return st;
+  st = check_chain_args(logits, w1, w2, r, prev_token, draft_tokens, q_stats, B, k, V);
+  if (st != DSPARK_OK) return st;
+  if (conf_w && !aligned16(conf_w)) return DSPARK_ERR_MISALIGNED;
+  if ((draft_len && !aligned4(draft_len)) || (conf_out && !aligned4(conf_out)))
+    return DSPARK_ERR_MISALIGNED;
+  if (conf_w && !draft_len) return DSPARK_ERR_INVALID_ARG;
+  if (std::isnan(conf_tau) || std::isnan(conf_b)) return DSPARK_ERR_INVALID_ARG;
+  const size_t need = dspark_draft_readout_workspace_size(B, k, H, V, r);
+  if ((st = check_ws(ws, ws_bytes, need)) != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+
+  cudaStream_t s = as_stream(stream);
+  char *base = static_cast<char *>(ws);
+  const size_t gemm_bytes = align_up(gemm_workspace_size(M, V, H), kWsAlign);
+  st = lm_head_enqueue(h, lm_w, logits, M, H, V, base + kHeader, gemm_bytes, status_word(ws), s);
+  if (st != DSPARK_OK) return st;
+  st = chain_launch(logits, w1, w2, w1 ? r : 0, prev_token, draft_tokens, q_stats,
+                    conf_w ? nullptr : draft_len, B, k, V, base + kHeader + gemm_bytes,
+                    status_word(ws), s);
+  if (st != DSPARK_OK) return st;
+  if (conf_w)
+    st = confidence_launch(h, conf_w, conf_b, conf_tau, draft_tokens, draft_len, conf_out, B, k,
+                           H, s);
+  return st;
+}
+
+// ---------------------------------------------------------------- verify
+size_t dspark_verify_workspace_size(int B, int k, int V) {
+  if (B < 1 || k < 1 || k > kMaxK || V < 1) return 0;
+  return verify_workspace_size(B, k, V);
+}
+
+dspark_status_t dspark_verify(int mode, const float *target_logits, const int32_t *draft_tokens,
+                              const int32_t *draft_len, const float *draft_logits,
+                              const float *q_stats, uint64_t seed, const uint32_t *request_id,
+                              uint32_t step, int32_t *accepted_len, int32_t *next_token, int B,
+                              int k, int V, void *ws, size_t ws_bytes, void *stream) {
+  if (mode != 0 && mode != 1) return DSPARK_ERR_INVALID_ARG;
+  if (!target_logits || !draft_tokens || !accepted_len || !next_token) return DSPARK_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (k > kMaxK || V > kMaxV || B > (1 << 20)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (mode == 1 && draft_logits && q_stats && !aligned4(q_stats)) return DSPARK_ERR_MISALIGNED;
+  if (!aligned4(target_logits) || !aligned4(draft_tokens) || !aligned4(accepted_len) ||
+      !aligned4(next_token))
+    return DSPARK_ERR_MISALIGNED;
+  if ((draft_len && !aligned4(draft_len)) || (draft_logits && !aligned4(draft_logits)) ||
+      (request_id && !aligned4(request_id)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_verify_workspace_size(B, k, V));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  return verify_launch(mode, target_logits, draft_tokens, draft_len, draft_logits, q_stats, seed,
+                       request_id, step, accepted_len, next_token, B, k, V, ws, status_word(ws),
+                       as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,606 @@
+// Dense bf16 GEMM on the 5th-generation tensor cores (sm_103a):
+//   out[m, n] = sum_k X[m, k] * W[n, k]        fp32 accumulate in TMEM
+//
+// Serves both contractions of the drafter readout:
+//   - fc projection: W = fc.weight [H, T*H], X = the T tapped hidden-state
+//     tensors, read as T consecutive K segments (the concatenation is never
+//     materialised); out = h, bf16.
+//   - LM head: W = lm_head.weight [V, H], X = h [B*k, H]; out = fp32 logits.
+//
+// Design (GB300-first):
+//   * "Swap-AB": the weight supplies the 128-row M side of tcgen05.mma and the
+//     (few) activation rows the N side, so a decode batch of B*k = 7 rows is a
+//     legal N = 16 tile and the kernel streams the weight exactly once.
+//   * Persistent grid of one CTA per SM, 192 threads, warp-specialised:
+//     warp 0 issues TMA loads into a ring of shared-memory stages, warp 1 issues
+//     tcgen05.mma (one thread) into one of two TMEM accumulators, warps 2-5
+//     drain TMEM with tcgen05.ld and store the tile.
+//   * Work is split "stream-K": the (tile, k-block) units are cut into equal
+//     contiguous ranges, one per CTA, so every SM streams the same number of
+//     weight bytes whatever the tile count.  A tile cut between CTAs is
+//     finished by the last CTA to arrive (atomic ticket, no spinning), which
+//     adds the fp32 partials in CTA order: results do not depend on timing.
+//   * Operands are 128-byte-swizzled K-major tiles (64 bf16 of K per row) as
+//     TMA writes them; the UMMA shared-memory descriptors describe exactly that
+//     layout.  Weights are loaded with an L2 evict-first policy, activations
+//     with evict-last.
+//   * Every wait on an mbarrier is bounded: on timeout the CTA records
+//     DSPARK_ERR_DEVICE_TIMEOUT, stops issuing, waits (bounded) for its own
+//     copies and MMAs in flight, frees its TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;          // weight rows per tile (UMMA M)
+constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
+constexpr int kMaxStages = 12;
+constexpr uint32_t kABytes = kBM * kBK * 2;
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+struct GemmParams {
+  CUtensorMap tm_w;
+  CUtensorMap tm_x[kMaxTaps];
+  void *out;
+  float *partials;
+  int *tickets;
+  int *status;
+  long long ldo;
+  long long units;
+  int kb_per_seg;
+  int kb_total;
+  int N;
+  int M;
+  int BN;
+  int tiles_m;
+  int stages;
+  int out_bf16;
+  uint32_t tmem_cols;
+  uint32_t idesc;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of the given parity to complete.  Returns false
+// (without waiting further) once the CTA's abort flag is set or the budget
+// runs out; the latter sets the flag and records the timeout.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                      int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      record_error(status, DSPARK_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
+// tile: rows of 128 bytes, groups of 8 rows 1024 bytes apart (stride byte
+// offset); the leading byte offset is unused by this layout.  Bits 46-48 hold
+// the descriptor version 1, bits 61-63 the swizzle mode (2 = 128 bytes).
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ schedule
+struct Range {
+  long long begin, end;
+};
+
+__device__ __forceinline__ Range cta_range(long long units, int cta, int grid) {
+  return {units * cta / grid, units * (cta + 1) / grid};
+}
+
+// CTA whose range holds unit x: the largest c with floor(U*c/G) <= x.
+__device__ __forceinline__ int cta_of_unit(long long x, long long units, int grid) {
+  return static_cast<int>(((x + 1) * grid - 1) / units);
+}
+
+__device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, float v) {
+  if (m >= p.M || n >= p.N) return;
+  const long long off = static_cast<long long>(m) * p.ldo + n;
+  if (p.out_bf16)
+    reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float *>(p.out)[off] = v;
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *sbase = smem_raw + (base - raw);
+  const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * kBK * 2;
+  const uint32_t stage_bytes = kABytes + b_bytes;
+  const int S = p.stages;
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + S * stage_bytes);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8u * S;
+  const uint32_t tfull0 = empty0 + 8u * S;
+  const uint32_t tempty0 = tfull0 + 16u;
+  const uint32_t drain_bar = tempty0 + 16u;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 2 * S + 5);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  volatile int *ticket_slot = reinterpret_cast<volatile int *>(tmem_holder + 2);
+  volatile int *ok_slot = reinterpret_cast<volatile int *>(tmem_holder + 3);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int grid = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(tfull0, 1);
+    mbar_init(tfull0 + 8u, 1);
+    mbar_init(tempty0, 4);
+    mbar_init(tempty0 + 8u, 4);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_map(&p.tm_w);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const Range rg = cta_range(p.units, cta, grid);
+  const int kbt = p.kb_total;
+  const int first_tile = static_cast<int>(rg.begin / kbt);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const CUtensorMap *xmaps = &p.tm_x[0];
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (long long u = rg.begin; u < rg.end && ok;) {
+        const int tile = static_cast<int>(u / kbt);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+        const long long left = rg.end - u;
+        const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+        const int n_tile = tile / p.tiles_m;
+        const int m_tile = tile - n_tile * p.tiles_m;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8u * stage;
+          mbar_expect_tx(fb, stage_bytes);
+          const uint32_t sa = base + stage * stage_bytes;
+          tma_load_2d(sa, &p.tm_w, kb * kBK, n_tile * kBM, fb, pol_w);
+          const int seg = kb / p.kb_per_seg;
+          const int xk = (kb - seg * p.kb_per_seg) * kBK;
+          tma_load_2d(sa + kABytes, xmaps + seg, xk, m_tile * p.BN, fb, pol_x);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        u += kb1 - kb0;
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA exits.
+        const long long first = issued > S ? issued - S : 0;
+        for (long long j = first; j < issued; ++j) {
+          const int s = static_cast<int>(j % S);
+          const uint32_t par = static_cast<uint32_t>((j / S) & 1);
+          const long long t0 = clock64();
+          while (!mbar_try_wait(full0 + 8u * s, par) && clock64() - t0 < kWaitCycles) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (long long u = rg.begin; u < rg.end && ok;) {
+        const int tile = static_cast<int>(u / kbt);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+        const long long left = rg.end - u;
+        const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+        if (!wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bar(full0 + 8u * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * stage_bytes;
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            tc_mma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
+                        p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8u * stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8u * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+        u += kb1 - kb0;
+      }
+      // Every MMA issued by this thread has completed once this arrives.
+      tc_commit(drain_bar);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long u = rg.begin; u < rg.end;) {
+      const int tile = static_cast<int>(u / kbt);
+      const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+      const long long left = rg.end - u;
+      const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+      const int n_tile = tile / p.tiles_m;
+      const int m_tile = tile - n_tile * p.tiles_m;
+      const int n = n_tile * kBM + row;
+      const int m_base = m_tile * p.BN;
+      const bool whole = (kb0 == 0 && kb1 == kbt);
+
+      // One thread waits for the accumulator; the decision is shared by all
+      // four epilogue warps so that they leave the loop together on abort.
+      if (threadIdx.x == 64)
+        *ok_slot = wait_bar(tfull0 + 8u * acc, acc_phase, abort_flag, p.status) ? 1 : 0;
+      epi_bar_sync();
+      const int ok = *ok_slot;
+      epi_bar_sync();
+      if (!ok) break;
+      tc_fence_after();
+
+      float *part = nullptr;
+      if (!whole) {
+        const int slot = (tile == first_tile) ? 0 : 1;
+        part = p.partials + (static_cast<size_t>(cta) * 2 + slot) * static_cast<size_t>(p.BN) * kBM;
+      }
+      for (int cc = 0; cc < p.BN; cc += 16) {
+        uint32_t r[16];
+        tmem_ld16(lane_addr + static_cast<uint32_t>(acc * p.BN + cc), r);
+        if (whole) {
+          if (m_base + cc < p.M) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) store_out(p, m_base + cc + j, n, __uint_as_float(r[j]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) part[(cc + j) * kBM + row] = __uint_as_float(r[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+
+      if (!whole) {
+        // Stream-K fix-up: the last CTA to finish a piece of this tile adds the
+        // pieces in CTA order and stores the tile.
+        __threadfence();
+        epi_bar_sync();
+        if (threadIdx.x == 64) *ticket_slot = atomicAdd(&p.tickets[tile], 1);
+        epi_bar_sync();
+        const int ticket = *ticket_slot;
+        const long long t_first = static_cast<long long>(tile) * kbt;
+        const int c_first = cta_of_unit(t_first, p.units, grid);
+        const int c_last = cta_of_unit(t_first + kbt - 1, p.units, grid);
+        const int nseg = c_last - c_first + 1;
+        if (ticket == nseg - 1) {
+          __threadfence();
+          const int mcount = min(p.BN, p.M - m_base);
+          for (int col = 0; col < mcount; ++col) {
+            float s = 0.0f;
+            for (int sg = 0; sg < nseg; ++sg) {
+              const int c2 = c_first + sg;
+              const int tile_c2 = static_cast<int>((p.units * c2 / grid) / kbt);
+              const int slot = (tile == tile_c2) ? 0 : 1;
+              const float *src = p.partials + (static_cast<size_t>(c2) * 2 + slot) *
+                                                  static_cast<size_t>(p.BN) * kBM;
+              s += __ldcg(src + col * kBM + row);
+            }
+            store_out(p, m_base + col, n, s);
+          }
+          if (threadIdx.x == 64) p.tickets[tile] = 0;
+        }
+        epi_bar_sync();
+      }
+      u += kb1 - kb0;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(p.tmem_cols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] with the given row stride, read in boxes of
+// 64 (one 128-byte swizzle row) x box_rows.
+bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t rows,
+              uint64_t row_stride_bytes, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Tiling {
+  int BN, tiles_m, tiles_n, kb_total, stages;
+  long long units;
+  uint32_t tmem_cols;
+  size_t smem;
+};
+
+Tiling plan(int M, int N, int K) {
+  Tiling t;
+  t.tiles_m = (M + 255) / 256;
+  int bn = (M + t.tiles_m - 1) / t.tiles_m;
+  bn = (bn + 15) / 16 * 16;
+  if (bn < 16) bn = 16;
+  t.BN = bn;
+  t.tiles_n = (N + kBM - 1) / kBM;
+  t.kb_total = K / kBK;
+  t.units = static_cast<long long>(t.tiles_m) * t.tiles_n * t.kb_total;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(2 * bn)) cols <<= 1;
+  t.tmem_cols = cols;
+  const size_t stage = kABytes + static_cast<size_t>(bn) * kBK * 2;
+  const size_t budget = 227 * 1024 - 1024 - 256;
+  int st = static_cast<int>(budget / stage);
+  if (st > kMaxStages) st = kMaxStages;
+  t.stages = st;
+  t.smem = 1024 + stage * st + 256;
+  return t;
+}
+
+size_t partial_bytes(const Tiling &t) {
+  return static_cast<size_t>(kMaxGemmCtas) * 2 * t.BN * kBM * sizeof(float);
+}
+
+}  // namespace
+
+size_t gemm_workspace_size(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < kBK) return 0;
+  Tiling t = plan(M, N, K);
+  const size_t tickets = align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
+  return tickets + align_up(partial_bytes(t), kWsAlign);
+}
+
+dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, int *status,
+                            cudaStream_t stream) {
+  const int K = pr.n_seg * pr.seg_k;
+  Tiling t = plan(pr.M, pr.N, K);
+  if (ws_bytes < gemm_workspace_size(pr.M, pr.N, K)) return DSPARK_ERR_WORKSPACE;
+  const int sms = device_sm_count();
+  if (sms <= 0) return DSPARK_ERR_NO_DEVICE;
+
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_map(&p.tm_w, pr.w, static_cast<uint64_t>(K), static_cast<uint64_t>(pr.N),
+                static_cast<uint64_t>(K) * 2, kBM))
+    return DSPARK_ERR_CUDA;
+  for (int s = 0; s < pr.n_seg; ++s) {
+    if (!make_map(&p.tm_x[s], pr.x[s], static_cast<uint64_t>(pr.seg_k),
+                  static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.x_ld[s]) * 2,
+                  static_cast<uint32_t>(t.BN)))
+      return DSPARK_ERR_CUDA;
+  }
+  const size_t tickets = align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
+  p.tickets = reinterpret_cast<int *>(ws);
+  p.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + tickets);
+  p.out = pr.out;
+  p.status = status;
+  p.ldo = pr.ldo;
+  p.units = t.units;
+  p.kb_per_seg = pr.seg_k / kBK;
+  p.kb_total = t.kb_total;
+  p.N = pr.N;
+  p.M = pr.M;
+  p.BN = t.BN;
+  p.tiles_m = t.tiles_m;
+  p.stages = t.stages;
+  p.out_bf16 = pr.out_bf16 ? 1 : 0;
+  p.tmem_cols = t.tmem_cols;
+  // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B bf16
+  // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
+  // bits 24-28.
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(t.BN >> 3) << 17) |
+            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+  long long grid = sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
+  const long long by_work = t.units / 4 > 0 ? t.units / 4 : 1;
+  if (grid > by_work) grid = by_work;
+
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  gemm_tcgen05_kernel<<<static_cast<unsigned>(grid), kThreads, t.smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+}  // namespace dspark

@@ -1,0 +1,64 @@
+// Host-side declarations shared by the DSpark translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+constexpr size_t kWsAlign = 256;
+constexpr int kMaxTaps = 8;
+constexpr int kMaxK = 16;
+constexpr int kMaxRank = 256;
+constexpr int kMaxGemmCtas = 160;  // upper bound of the persistent GEMM grid
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ GEMM
+// out[m, n] = sum_k X[m, k] * W[n, k]   (bf16 in, fp32 accumulate)
+// X is the concatenation along k of n_seg segments, each [M, seg_k] with row
+// stride x_ld[s] elements.  out is fp32 or bf16 with row stride ldo.
+struct GemmProblem {
+  const void *w;          // [N, K] bf16
+  const void *x[kMaxTaps];
+  int64_t x_ld[kMaxTaps];
+  int n_seg;
+  int seg_k;              // K of one segment (multiple of 64)
+  int N;                  // weight rows
+  int M;                  // activation rows
+  void *out;
+  int64_t ldo;
+  bool out_bf16;
+};
+
+size_t gemm_workspace_size(int M, int N, int K);
+// Enqueues the GEMM.  ws must hold gemm_workspace_size bytes (zeroed once).
+dspark_status_t gemm_launch(const GemmProblem &p, void *ws, size_t ws_bytes, int *status,
+                            cudaStream_t stream);
+
+// ------------------------------------------------------------------ Markov chain
+size_t chain_workspace_size(int B, int k, int V);
+dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *w2, int r,
+                             const int32_t *prev_token, int32_t *draft_tokens, float *q_stats,
+                             int32_t *draft_len_fill, int B, int k, int V, void *ws,
+                             int *status, cudaStream_t stream);
+dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, float conf_b,
+                                  float conf_tau, int32_t *draft_tokens, int32_t *draft_len,
+                                  float *conf_out, int B, int k, int H, cudaStream_t stream);
+
+// ------------------------------------------------------------------ verify
+size_t verify_workspace_size(int B, int k, int V);
+dspark_status_t verify_launch(int mode, const float *target, const int32_t *drafts,
+                              const int32_t *draft_len, const float *zlog, const float *q_stats,
+                              uint64_t seed, const uint32_t *request_id, uint32_t step,
+                              int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
+                              void *ws, int *status, cudaStream_t stream);
+
+// ------------------------------------------------------------------ device info
+int device_sm_count();  // cached per current device; 0 when no device
+bool device_is_blackwell();
+
+}  // namespace dspark

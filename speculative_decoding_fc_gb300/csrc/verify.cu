@@ -1,0 +1,463 @@
+// Verification of one draft block per request: greedy exact match or
+// probabilistic rejection sampling.
+//
+// Pages: "Qwen3.8-27B DFlash drafter recipe" ("greedy spec decode is lossless
+// by construction"), the "Qwen3.8-27B-DSpark-vLLM" card ("draft_sample_method":
+// "probabilistic"), "Qwen4Exp DFlash2 hidden-state capture" ("verified by
+// rejection sampling"; acceptance length = accepted tokens per verification
+// step).  Rejection rule: accept d with probability min(1, p(d)/q(d)); at the
+// first rejection draw from max(0, p - q) normalised; after a fully accepted
+// block draw the bonus token from p.
+//
+// Pass 1 (verify_stats_kernel): one streaming read of every needed row
+// (target rows 0..draft_len, and the draft-logit rows when their softmax
+// statistics were not supplied) with 128-bit loads; each CTA reduces a
+// 4096-entry slice to (argmax key, max, sum exp).  The last CTA of a request
+// (atomic ticket) merges the slices in a fixed order and takes the
+// accept/reject decisions with Philox uniforms.
+// Pass 2 (verify_sample_kernel, probabilistic only): the one row per request
+// that needs a draw is re-read.  The draw is the Gumbel-max rule: the index
+// maximising log w_v + G_v, G_v = -log(-log U_v) with U_v from Philox counter
+// (request, row, step, 1 + v/4).  That samples exactly from w normalised and
+// makes the draw an argmax, reduced like every other argmax here (per-CTA
+// 64-bit keys, merged by the request's last CTA).
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kPer = 16;                    // entries per thread per slice
+constexpr int kSlice = kThreads * kPer;     // 4096 entries per CTA
+
+struct __align__(16) RowPartial {
+  unsigned long long key;
+  float m;
+  float s;
+};
+
+enum SampleKind { kNone = 0, kResidual = 1, kResidualOneHot = 2, kFromP = 3 };
+
+struct __align__(16) SampleJob {
+  int row;     // block row of the target (and draft) logits to draw from
+  int kind;
+  int d;       // draft token removed by the one-hot residual
+  int pad;
+  double cp;   // log-normaliser of the target row: max + log(sum exp)
+  double cq;   // log-normaliser of the draft row (kResidual)
+};
+
+struct __align__(16) SamplePartial {
+  unsigned long long best_r;  // argmax key of log w + G over the slice
+  unsigned long long best_p;  // argmax key of log p + G (fallback: residual all zero)
+};
+
+struct VerifyArgs {
+  const float *target;
+  const int32_t *drafts;
+  const int32_t *draft_len;
+  const float *zlog;
+  const float *q_stats;
+  const uint32_t *request_id;
+  int32_t *accepted_len;
+  int32_t *next_token;
+  RowPartial *rows;
+  SampleJob *jobs;
+  SamplePartial *sparts;
+  int *req_ticket;
+  int *samp_ticket;
+  int *status;
+  unsigned long long seed;
+  unsigned int step;
+  int mode;
+  int B, k, V;
+  int nslices;
+  int zrows;      // 1 when draft-logit statistics are computed here
+  int vec;        // 1 when every row starts on a 16-byte boundary (128-bit loads)
+};
+
+__device__ __forceinline__ int request_len(const VerifyArgs &a, int b, bool record) {
+  int L = a.draft_len ? a.draft_len[b] : a.k;
+  if (L < 0 || L > a.k) {
+    if (record) record_error(a.status, DSPARK_ERR_INVALID_ARG);
+    L = L < 0 ? 0 : a.k;
+  }
+  return L;
+}
+
+// ------------------------------------------------------------------ pass 1
+__global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs a) {
+  __shared__ RowPartial red[kWarps];
+  __shared__ int is_last;
+  __shared__ unsigned long long tkey[kMaxK + 1];
+  __shared__ double tM[kMaxK + 1], tS[kMaxK + 1];
+  __shared__ double zM[kMaxK], zS[kMaxK];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice
+  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
+  const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
+  const int k = a.k, V = a.V;
+  const int trows = a.B * (k + 1);
+  const bool is_z = rho >= trows;
+  const int b = is_z ? (rho - trows) / k : rho / (k + 1);
+  const int j = is_z ? (rho - trows) - b * k : rho - b * (k + 1);
+  const int L = request_len(a, b, false);
+  const bool needed = is_z ? (a.mode == 1 && j < L) : (j <= L);
+  const bool want_stats = (a.mode == 1);
+
+  if (needed) {
+    const float *row = is_z ? a.zlog + (static_cast<long long>(b) * k + j) * V
+                            : a.target + (static_cast<long long>(b) * (k + 1) + j) * V;
+    const int base = slice * kSlice;
+    unsigned long long best = 0ull;
+    SoftStat st{-INFINITY, 0.0f};
+    if (a.vec) {
+      float4 q[kPer / 4];
+#pragma unroll
+      for (int it = 0; it < kPer / 4; ++it) {
+        const int v = base + it * (kThreads * 4) + tid * 4;
+        q[it] = v < V ? __ldcs(reinterpret_cast<const float4 *>(row + v))
+                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int it = 0; it < kPer / 4; ++it) {
+        const int v = base + it * (kThreads * 4) + tid * 4;
+        if (v < V) {
+          const float x[4] = {q[it].x, q[it].y, q[it].z, q[it].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const unsigned long long key = argmax_key(x[e], static_cast<uint32_t>(v + e));
+            best = key > best ? key : best;
+            if (want_stats) softstat_add(st, x[e]);
+          }
+        }
+      }
+    } else {
+#pragma unroll 4
+      for (int it = 0; it < kPer; ++it) {
+        const int v = base + it * kThreads + tid;
+        if (v < V) {
+          const float x = __ldcs(row + v);
+          const unsigned long long key = argmax_key(x, static_cast<uint32_t>(v));
+          best = key > best ? key : best;
+          if (want_stats) softstat_add(st, x);
+        }
+      }
+    }
+    best = warp_max_u64(best);
+    if (want_stats) st = warp_softstat(st);
+    if (lane == 0) red[warp] = RowPartial{best, st.m, st.s};
+    __syncthreads();
+    if (tid == 0) {
+      RowPartial acc = red[0];
+      SoftStat sacc{acc.m, acc.s};
+      for (int w = 1; w < kWarps; ++w) {
+        acc.key = red[w].key > acc.key ? red[w].key : acc.key;
+        sacc = softstat_merge(sacc, SoftStat{red[w].m, red[w].s});
+      }
+      acc.m = sacc.m;
+      acc.s = sacc.s;
+      a.rows[static_cast<long long>(rho) * a.nslices + slice] = acc;
+    }
+  }
+
+  __threadfence();
+  __syncthreads();
+  const int rows_per_req = (k + 1) + (a.zrows ? k : 0);
+  if (tid == 0)
+    is_last = (atomicAdd(&a.req_ticket[b], 1) == rows_per_req * a.nslices - 1) ? 1 : 0;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // ---------------------------------------------------------------- merge rows of request b
+  const int n_t = L + 1;
+  const int n_z = a.zrows ? L : 0;
+  for (int q = warp; q < n_t + n_z; q += kWarps) {
+    const bool qz = q >= n_t;
+    const int jj = qz ? q - n_t : q;
+    const int r_idx = qz ? trows + b * k + jj : b * (k + 1) + jj;
+    const RowPartial *pr = a.rows + static_cast<long long>(r_idx) * a.nslices;
+    unsigned long long kb = 0ull;
+    float mm = -INFINITY;
+    for (int c = lane; c < a.nslices; c += 32) {
+      const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
+      kb = raw.x > kb ? raw.x : kb;
+      mm = fmaxf(mm, __uint_as_float(static_cast<uint32_t>(raw.y)));
+    }
+    kb = warp_max_u64(kb);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    double s = 0.0;
+    if (want_stats && mm != -INFINITY) {
+      for (int c = lane; c < a.nslices; c += 32) {
+        const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
+        const float cm = __uint_as_float(static_cast<uint32_t>(raw.y));
+        const float cs = __uint_as_float(static_cast<uint32_t>(raw.y >> 32));
+        if (cm != -INFINITY) s += static_cast<double>(cs) * static_cast<double>(expf(cm - mm));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    }
+    if (lane == 0) {
+      if (qz) {
+        zM[jj] = mm;
+        zS[jj] = s;
+      } else {
+        tkey[jj] = kb;
+        tM[jj] = mm;
+        tS[jj] = s;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (tid == 0) {
+    const long long drow = static_cast<long long>(b) * k;
+    int acc_len = 0;
+    if (a.mode == 0) {
+      while (acc_len < L &&
+             a.drafts[drow + acc_len] == static_cast<int32_t>(key_index(tkey[acc_len])))
+        ++acc_len;
+      a.accepted_len[b] = acc_len;
+      a.next_token[b] = static_cast<int32_t>(key_index(tkey[acc_len]));
+    } else {
+      const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
+      SampleJob job;
+      job.kind = kNone;
+      job.d = -1;
+      job.pad = 0;
+      job.cq = 0.0;
+      for (; acc_len < L; ++acc_len) {
+        const int jj = acc_len;
+        const int d = a.drafts[drow + jj];
+        double ua, us;
+        verify_uniforms(a.seed, req, static_cast<uint32_t>(jj), a.step, ua, us);
+        if (d < 0 || d >= V) {
+          record_error(a.status, DSPARK_ERR_BAD_TOKEN);
+          job.row = jj;
+          job.kind = kFromP;
+          job.cp = tM[jj] + log(tS[jj]);
+          break;
+        }
+        const double tT = a.target[(static_cast<long long>(b) * (k + 1) + jj) * V + d];
+        const double pd = exp(tT - tM[jj]) / tS[jj];
+        double qd = 1.0, qm = 0.0, qs = 1.0;
+        if (a.zlog) {
+          if (a.zrows) {
+            qm = zM[jj];
+            qs = zS[jj];
+          } else {
+            qm = a.q_stats[2 * (drow + jj)];
+            qs = a.q_stats[2 * (drow + jj) + 1];
+          }
+          const double zd = a.zlog[(drow + jj) * V + d];
+          qd = exp(zd - qm) / qs;
+        }
+        if (ua < pd / qd) continue;
+        job.row = jj;
+        job.kind = a.zlog ? kResidual : kResidualOneHot;
+        job.d = d;
+        job.cp = tM[jj] + log(tS[jj]);
+        job.cq = qm + log(qs);
+        break;
+      }
+      if (job.kind == kNone) {
+        job.row = L;
+        job.kind = kFromP;
+        job.cp = tM[L] + log(tS[L]);
+      }
+      a.accepted_len[b] = acc_len;
+      a.jobs[b] = job;
+    }
+    a.req_ticket[b] = 0;
+  }
+}
+
+// ------------------------------------------------------------------ pass 2
+// Noise of entry v of a draw at block row `row`: Philox4x32-10 counter
+// (request, row, step, 1 + v/4), word v mod 4; U = (2 (w >> 9) + 1) 2^-24 is an
+// odd multiple of 2^-24, exact in fp32 and strictly inside (0, 1).
+__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
+  const float u = static_cast<float>(2u * (w >> 9) + 1u) * (1.0f / 16777216.0f);
+  return -logf(-logf(u));
+}
+
+__global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArgs a) {
+  __shared__ unsigned long long red_r[kWarps], red_p[kWarps];
+  __shared__ int is_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
+  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
+  const int k = a.k, V = a.V;
+  const SampleJob job = a.jobs[b];
+  const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
+  const uint32_t k0 = static_cast<uint32_t>(a.seed & 0xffffffffull);
+  const uint32_t k1 = static_cast<uint32_t>(a.seed >> 32);
+  const float *trow = a.target + (static_cast<long long>(b) * (k + 1) + job.row) * V;
+  const float *zrow = (job.kind == kResidual)
+                          ? a.zlog + (static_cast<long long>(b) * k + job.row) * V
+                          : nullptr;
+  const float cpf = static_cast<float>(job.cp);
+  const float cqf = static_cast<float>(job.cq);
+
+  unsigned long long best_r = 0ull, best_p = 0ull;
+  const int v0 = slice * kSlice + tid * kPer;
+#pragma unroll
+  for (int g4 = 0; g4 < kPer / 4; ++g4) {
+    const int vg = v0 + 4 * g4;
+    if (vg < V) {
+      const U4 w = philox4x32_10(U4{req, static_cast<uint32_t>(job.row), a.step,
+                                    1u + static_cast<uint32_t>(vg >> 2)},
+                                 k0, k1);
+      const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = vg + e;
+        if (v < V) {
+          const float g = gumbel_from_word(words[e]);
+          const float t = trow[v];
+          const float kp = t + g;
+          float kr;
+          if (job.kind == kResidual) {
+            const float av = t - cpf;
+            const float bv = zrow[v] - cqf;
+            kr = (av > bv) ? av + log1pf(-expf(bv - av)) + g : -INFINITY;
+          } else if (job.kind == kResidualOneHot) {
+            kr = (v == job.d) ? -INFINITY : kp;
+          } else {
+            kr = kp;
+          }
+          const unsigned long long keyr = argmax_key(kr, static_cast<uint32_t>(v));
+          const unsigned long long keyp = argmax_key(kp, static_cast<uint32_t>(v));
+          best_r = keyr > best_r ? keyr : best_r;
+          best_p = keyp > best_p ? keyp : best_p;
+        }
+      }
+    }
+  }
+  best_r = warp_max_u64(best_r);
+  best_p = warp_max_u64(best_p);
+  if (lane == 0) {
+    red_r[warp] = best_r;
+    red_p[warp] = best_p;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long br = red_r[0], bp = red_p[0];
+    for (int w2 = 1; w2 < kWarps; ++w2) {
+      br = red_r[w2] > br ? red_r[w2] : br;
+      bp = red_p[w2] > bp ? red_p[w2] : bp;
+    }
+    a.sparts[static_cast<long long>(b) * a.nslices + slice] = SamplePartial{br, bp};
+  }
+
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = (atomicAdd(&a.samp_ticket[b], 1) == a.nslices - 1) ? 1 : 0;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  if (warp == 0) {
+    const SamplePartial *sp = a.sparts + static_cast<long long>(b) * a.nslices;
+    unsigned long long br = 0ull, bp = 0ull;
+    for (int c = lane; c < a.nslices; c += 32) {
+      const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(sp + c));
+      br = raw.x > br ? raw.x : br;
+      bp = raw.y > bp ? raw.y : bp;
+    }
+    br = warp_max_u64(br);
+    bp = warp_max_u64(bp);
+    if (lane == 0) {
+      // The residual is empty only if p <= q everywhere (then draw from p).
+      const float vr = key_value(br);
+      const bool has_r = br != 0ull && vr != -INFINITY && vr == vr;
+      a.next_token[b] = static_cast<int32_t>(key_index(has_r ? br : bp));
+      a.samp_ticket[b] = 0;
+    }
+  }
+}
+
+struct VerifyLayout {
+  size_t req_ticket, samp_ticket, rows, jobs, sparts, total;
+  int nslices;
+};
+
+VerifyLayout layout(int B, int k, int V) {
+  VerifyLayout L;
+  L.nslices = (V + kSlice - 1) / kSlice;
+  size_t off = kWsAlign;
+  L.req_ticket = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
+  L.samp_ticket = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
+  L.rows = off;
+  off += align_up(static_cast<size_t>(B) * (2 * k + 1) * L.nslices * sizeof(RowPartial), kWsAlign);
+  L.jobs = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(SampleJob), kWsAlign);
+  L.sparts = off;
+  off += align_up(static_cast<size_t>(B) * L.nslices * sizeof(SamplePartial), kWsAlign);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+size_t verify_workspace_size(int B, int k, int V) { return layout(B, k, V).total; }
+
+dspark_status_t verify_launch(int mode, const float *target, const int32_t *drafts,
+                              const int32_t *draft_len, const float *zlog, const float *q_stats,
+                              uint64_t seed, const uint32_t *request_id, uint32_t step,
+                              int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
+                              void *ws, int *status, cudaStream_t stream) {
+  const VerifyLayout L = layout(B, k, V);
+  char *w = static_cast<char *>(ws);
+  VerifyArgs a;
+  a.target = target;
+  a.drafts = drafts;
+  a.draft_len = draft_len;
+  a.zlog = (mode == 1) ? zlog : nullptr;
+  a.q_stats = q_stats;
+  a.request_id = request_id;
+  a.accepted_len = accepted_len;
+  a.next_token = next_token;
+  a.rows = reinterpret_cast<RowPartial *>(w + L.rows);
+  a.jobs = reinterpret_cast<SampleJob *>(w + L.jobs);
+  a.sparts = reinterpret_cast<SamplePartial *>(w + L.sparts);
+  a.req_ticket = reinterpret_cast<int *>(w + L.req_ticket);
+  a.samp_ticket = reinterpret_cast<int *>(w + L.samp_ticket);
+  a.status = status;
+  a.seed = seed;
+  a.step = step;
+  a.mode = mode;
+  a.B = B;
+  a.k = k;
+  a.V = V;
+  a.nslices = L.nslices;
+  a.zrows = (mode == 1 && zlog != nullptr && q_stats == nullptr) ? 1 : 0;
+  a.vec = ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(target) & 15u) == 0 &&
+           (a.zlog == nullptr || (reinterpret_cast<uintptr_t>(a.zlog) & 15u) == 0))
+              ? 1
+              : 0;
+  const long long nrows = static_cast<long long>(B) * (k + 1) + (a.zrows ? static_cast<long long>(B) * k : 0);
+  const long long g1 = nrows * L.nslices;
+  if (g1 > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  verify_stats_kernel<<<static_cast<unsigned>(g1), kThreads, 0, stream>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (mode == 1) {
+    const long long g2 = static_cast<long long>(B) * L.nslices;
+    verify_sample_kernel<<<static_cast<unsigned>(g2), kThreads, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+  return DSPARK_OK;
+}
+
+}  // namespace dspark

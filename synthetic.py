@@ -18,6 +18,8 @@ Workload recipe (weights are random-init: no trained drafter is used):
     (whoever holds the draft logits adds them).
 Seeds: tensor i of the weights uses seed 1 + i; step s uses seed 1000 + s.
 """
+import os
+
 import numpy as np
 import torch
 
@@ -48,8 +50,30 @@ def _rng(seed):
     return np.random.Generator(np.random.PCG64(seed))
 
 
+_BLOCK = 1 << 22  # elements per independently seeded block of a large draw
+
+
 def normal_f32(seed, shape, std=1.0):
-    a = _rng(seed).standard_normal(size=shape, dtype=np.float32)
+    """N(0, std^2) fp32.  Large arrays are drawn in blocks of 2^22 elements, block i from
+    the i-th child of SeedSequence(seed), in parallel threads; the result depends only on
+    (seed, shape)."""
+    n = int(np.prod(shape))
+    if n <= _BLOCK:
+        a = _rng(seed).standard_normal(size=shape, dtype=np.float32)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        a = np.empty(n, dtype=np.float32)
+        nb = (n + _BLOCK - 1) // _BLOCK
+        kids = np.random.SeedSequence(seed).spawn(nb)
+
+        def fill(i):
+            lo, hi = i * _BLOCK, min(n, (i + 1) * _BLOCK)
+            np.random.Generator(np.random.PCG64(kids[i])).standard_normal(
+                size=hi - lo, dtype=np.float32, out=a[lo:hi])
+
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nb)))
+        a = a.reshape(shape)
     if std != 1.0:
         a *= np.float32(std)
     return a

@@ -1,0 +1,81 @@
+"""The C ABI library loads and exports every function declared in include/dspark.h,
+and its host-side argument checks answer without a GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dspark.h")
+
+
+@pytest.fixture(scope="module")
+def libdspark():
+    from speculative_decoding_fc_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(dspark_[a-z0-9_]+)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("dspark_fc_project", "dspark_lm_head", "dspark_greedy_sample", "dspark_draft_readout",
+              "dspark_verify", "dspark_status_string", "dspark_workspace_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(libdspark):
+    missing = [n for n in declared_functions() if not hasattr(libdspark, n)]
+    assert not missing, missing
+
+
+def test_status_strings(libdspark):
+    f = libdspark.dspark_status_string
+    f.restype = ctypes.c_char_p
+    f.argtypes = [ctypes.c_int]
+    assert f(0) == b"DSPARK_OK"
+    assert f(-1) == b"DSPARK_ERR_INVALID_ARG"
+    assert f(-6) == b"DSPARK_ERR_DEVICE_TIMEOUT"
+    assert f(12345) == b"DSPARK_ERR_UNKNOWN"
+
+
+def test_workspace_sizes_are_host_only(libdspark):
+    sz = ctypes.c_size_t
+    libdspark.dspark_lm_head_workspace_size.restype = sz
+    libdspark.dspark_verify_workspace_size.restype = sz
+    libdspark.dspark_draft_readout_workspace_size.restype = sz
+    libdspark.dspark_fc_project_workspace_size.restype = sz
+    assert libdspark.dspark_lm_head_workspace_size(7, 5120, 151936) > 0
+    assert libdspark.dspark_fc_project_workspace_size(7, 5120, 5) > 0
+    assert libdspark.dspark_draft_readout_workspace_size(16, 7, 5120, 151936, 64) > 0
+    assert libdspark.dspark_verify_workspace_size(16, 7, 151936) > 0
+    assert libdspark.dspark_verify_workspace_size(16, 17, 151936) == 0   # k > 16
+    assert libdspark.dspark_lm_head_workspace_size(0, 5120, 151936) == 0
+
+
+def test_argument_errors_are_caught_before_any_launch(libdspark):
+    vp = ctypes.c_void_p
+    f = libdspark.dspark_verify
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_uint64, vp, ctypes.c_uint32, vp, vp,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    fake = vp(1 << 20)  # never dereferenced: the checks reject the call first
+    assert f(2, fake, fake, None, None, None, 0, None, 0, fake, fake, 1, 7, 100, fake, 1 << 20, None) == -1
+    assert f(0, None, fake, None, None, None, 0, None, 0, fake, fake, 1, 7, 100, fake, 1 << 20, None) == -1
+    assert f(0, fake, fake, None, None, None, 0, None, 0, fake, fake, 1, 17, 100, fake, 1 << 20, None) == -2
+    assert f(0, vp((1 << 20) + 2), fake, None, None, None, 0, None, 0, fake, fake, 1, 7, 100, fake,
+             1 << 20, None) == -3
+    assert f(0, fake, fake, None, None, None, 0, None, 0, fake, fake, 1, 7, 100, fake, 16, None) == -4
+    g = libdspark.dspark_lm_head
+    g.restype = ctypes.c_int
+    g.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    assert g(fake, fake, fake, 7, 100, 1000, fake, 1 << 30, None) == -2   # H not a multiple of 64
+    assert g(fake, fake, fake, 0, 128, 1000, fake, 1 << 30, None) == -1

@@ -359,7 +359,7 @@ def _gumbel(seed, req, row, step, V):
     g = np.empty(V)
     for v in range(V):
         w = oracle.philox4x32_10((req, row, step, 1 + v // 4), (seed & 0xFFFFFFFF, seed >> 32))
-        u = ((w[v % 4] >> 8) + 0.5) / 2.0 ** 24
+        u = (2 * (w[v % 4] >> 9) + 1) / 2.0 ** 24
         g[v] = -math.log(-math.log(u))
     return g
 
