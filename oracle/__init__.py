@@ -39,7 +39,7 @@ def lib():
                                              ctypes.c_uint32, _f64p]
         L.oracle_fc_project.restype = ctypes.c_int
         L.oracle_fc_project.argtypes = [ctypes.POINTER(_u16p), ctypes.c_int, ctypes.c_int64, _u16p,
-                                        ctypes.c_int, ctypes.c_int, _u16p, _f32p]
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p, _f32p]
         L.oracle_lm_head.restype = ctypes.c_int
         L.oracle_lm_head.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, _u16p, ctypes.c_int64, _f32p]
         L.oracle_greedy_sample.restype = ctypes.c_int
@@ -116,17 +116,19 @@ def verify_uniforms(seed, request, pos, step):
 
 # ---------------------------------------------------------------- hot path
 def fc_project(taps, fc_w, return_f32=False):
-    """taps: list of T uint16 arrays [M, H]; fc_w: uint16 [H, T*H] -> h uint16 [M, H]."""
+    """taps: list of T uint16 arrays [M, H]; fc_w: uint16 [N, T*H] (N = H, or fewer rows to
+    compute only the first N output features) -> h uint16 [M, N]."""
     taps = [_c(t, np.uint16) for t in taps]
     T = len(taps)
     M, H = taps[0].shape
     fc_w = _c(fc_w, np.uint16)
-    assert fc_w.shape == (H, T * H)
+    N = fc_w.shape[0]
+    assert fc_w.shape == (N, T * H) and N <= H
     arr = (_u16p * T)(*[_p(t, _u16p) for t in taps])
-    h = np.empty((M, H), dtype=np.uint16)
-    hf = np.empty((M, H), dtype=np.float32) if return_f32 else None
-    _check(lib().oracle_fc_project(arr, T, H, _p(fc_w, _u16p), M, H, _p(h, _u16p), _p(hf, _f32p)),
-           "oracle_fc_project")
+    h = np.empty((M, N), dtype=np.uint16)
+    hf = np.empty((M, N), dtype=np.float32) if return_f32 else None
+    _check(lib().oracle_fc_project(arr, T, H, _p(fc_w, _u16p), N, M, H, _p(h, _u16p),
+                                   _p(hf, _f32p)), "oracle_fc_project")
     return (h, hf) if return_f32 else h
 
 

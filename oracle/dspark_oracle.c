@@ -148,18 +148,19 @@ void oracle_verify_uniforms(uint64_t seed, uint32_t request, uint32_t pos,
  * W_fc is stored [out = H, in = T*H] (PyTorch Linear layout).  No bias and
  * no normalisation are mentioned on the pages, so none is applied.
  *   taps[j]    : M x H bf16, row stride tap_ld elements
- *   fc_w       : H x (T*H) bf16, row-major
- *   h_out      : M x H bf16 (row stride H)
- *   h_f32      : optional M x H fp32 copy of the value before bf16 rounding
+ *   fc_w       : N x (T*H) bf16, row-major (N = H for the method; a smaller N
+ *                computes the first N output features only)
+ *   h_out      : M x N bf16 (row stride N)
+ *   h_f32      : optional M x N fp32 copy of the value before bf16 rounding
  */
 int oracle_fc_project(const uint16_t *const *taps, int T, int64_t tap_ld,
-                      const uint16_t *fc_w, int M, int H, uint16_t *h_out,
+                      const uint16_t *fc_w, int N, int M, int H, uint16_t *h_out,
                       float *h_f32) {
-    if (T < 1 || M < 0 || H < 1 || tap_ld < H || !taps || !fc_w || !h_out)
+    if (T < 1 || M < 0 || H < 1 || N < 1 || tap_ld < H || !taps || !fc_w || !h_out)
         return ORACLE_ERR_ARG;
     const int64_t K = (int64_t)T * H;
 #pragma omp parallel for schedule(static)
-    for (int64_t n = 0; n < H; ++n) {
+    for (int64_t n = 0; n < N; ++n) {
         const uint16_t *wrow = fc_w + n * K;
         for (int m = 0; m < M; ++m) {
             double acc = 0.0;
@@ -171,8 +172,8 @@ int oracle_fc_project(const uint16_t *const *taps, int T, int64_t tap_ld,
                            (double)bf16_bits_to_float(wseg[c]);
             }
             float a32 = (float)acc;
-            h_out[(int64_t)m * H + n] = oracle_f32_to_bf16(a32);
-            if (h_f32) h_f32[(int64_t)m * H + n] = a32;
+            h_out[(int64_t)m * N + n] = oracle_f32_to_bf16(a32);
+            if (h_f32) h_f32[(int64_t)m * N + n] = a32;
         }
     }
     return ORACLE_OK;

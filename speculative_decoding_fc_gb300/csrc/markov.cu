@@ -35,6 +35,7 @@ struct __align__(16) ChainPartial {
   float s;
 };
 
+template <int G>
 __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
     float *__restrict__ logits, const uint16_t *__restrict__ w1, const uint16_t *__restrict__ w2,
     int r, const int32_t *prev_src, int prev_stride, int32_t *draft_tokens, float *q_stats,
@@ -50,11 +51,11 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
   const int chunk = blockIdx.x;
   const bool biased = (w1 != nullptr);
 
-  for (int g0 = 0; g0 < B; g0 += kGroup) {
-    const int gb = min(kGroup, B - g0);
+  for (int g0 = 0; g0 < B; g0 += G) {
+    const int gb = min(G, B - g0);
     if (biased) {
       // e_g[t] = markov_w1[prev_g, t]; requests past the group end get zeros.
-      for (int idx = tid; idx < kGroup * r; idx += kThreads) {
+      for (int idx = tid; idx < G * r; idx += kThreads) {
         const int g = idx / r;
         const int t = idx - g * r;
         float e = 0.0f;
@@ -71,52 +72,72 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
       __syncthreads();
     }
 
-    unsigned long long best[kGroup];
-    SoftStat st[kGroup];
+    float acc[kVPT][G];
 #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
+    for (int j = 0; j < kVPT; ++j)
+#pragma unroll
+      for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
+
+    if (biased) {
+      // bias[v] = sequential fp32 fma chain over t = 0..r-1, 64 ranks at a time; every
+      // markov_w2 load of the thread for those ranks is issued before the first fma.
+      for (int tc = 0; tc < r; tc += 64) {
+        const int n8 = min(8, (r - tc) >> 3);
+        uint4 wq[kVPT][8];
+#pragma unroll
+        for (int j = 0; j < kVPT; ++j) {
+          const int v = chunk * kChunk + j * kThreads + tid;
+          const uint4 *wrow =
+              reinterpret_cast<const uint4 *>(w2 + static_cast<long long>(v < V ? v : 0) * r + tc);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < n8) wq[j][q] = __ldg(wrow + q);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q < n8) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float4 ea = *reinterpret_cast<const float4 *>(&e_s[g * r + tc + q * 8]);
+              const float4 eb = *reinterpret_cast<const float4 *>(&e_s[g * r + tc + q * 8 + 4]);
+#pragma unroll
+              for (int j = 0; j < kVPT; ++j) {
+                const uint4 w = wq[j][q];
+                float x = acc[j][g];
+                x = __fmaf_rn(bf16_lo(w.x), ea.x, x);
+                x = __fmaf_rn(bf16_hi(w.x), ea.y, x);
+                x = __fmaf_rn(bf16_lo(w.y), ea.z, x);
+                x = __fmaf_rn(bf16_hi(w.y), ea.w, x);
+                x = __fmaf_rn(bf16_lo(w.z), eb.x, x);
+                x = __fmaf_rn(bf16_hi(w.z), eb.y, x);
+                x = __fmaf_rn(bf16_lo(w.w), eb.z, x);
+                x = __fmaf_rn(bf16_hi(w.w), eb.w, x);
+                acc[j][g] = x;
+              }
+            }
+          }
+        }
+      }
+    }
+
+    unsigned long long best[G];
+    SoftStat st[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
       best[g] = 0ull;
       st[g] = SoftStat{-INFINITY, 0.0f};
     }
-
 #pragma unroll
     for (int j = 0; j < kVPT; ++j) {
       const int v = chunk * kChunk + j * kThreads + tid;
       if (v < V) {
-        float acc[kGroup];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) acc[g] = 0.0f;
-        if (biased) {
-          // bias[v] = sequential fp32 fma chain over t = 0..r-1.
-          const uint4 *wrow = reinterpret_cast<const uint4 *>(w2 + static_cast<long long>(v) * r);
-          for (int t8 = 0; t8 < r / 8; ++t8) {
-            const uint4 wq = __ldg(wrow + t8);
-            const float wv[8] = {bf16_lo(wq.x), bf16_hi(wq.x), bf16_lo(wq.y), bf16_hi(wq.y),
-                                 bf16_lo(wq.z), bf16_hi(wq.z), bf16_lo(wq.w), bf16_hi(wq.w)};
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g) {
-              const float4 ea = *reinterpret_cast<const float4 *>(&e_s[g * r + t8 * 8]);
-              const float4 eb = *reinterpret_cast<const float4 *>(&e_s[g * r + t8 * 8 + 4]);
-              float a = acc[g];
-              a = __fmaf_rn(wv[0], ea.x, a);
-              a = __fmaf_rn(wv[1], ea.y, a);
-              a = __fmaf_rn(wv[2], ea.z, a);
-              a = __fmaf_rn(wv[3], ea.w, a);
-              a = __fmaf_rn(wv[4], eb.x, a);
-              a = __fmaf_rn(wv[5], eb.y, a);
-              a = __fmaf_rn(wv[6], eb.z, a);
-              a = __fmaf_rn(wv[7], eb.w, a);
-              acc[g] = a;
-            }
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
+        for (int g = 0; g < G; ++g) {
           if (g < gb) {
             float *rowp = logits + (static_cast<long long>(g0 + g) * k + pos) * V;
             float z = rowp[v];
             if (biased) {
-              z = __fadd_rn(z, acc[g]);
+              z = __fadd_rn(z, acc[j][g]);
               rowp[v] = z;
             }
             const unsigned long long key = argmax_key(z, static_cast<uint32_t>(v));
@@ -128,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
     }
 
 #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
+    for (int g = 0; g < G; ++g) {
       if (g < gb) {
         const unsigned long long kmax = warp_max_u64(best[g]);
         const SoftStat ws = warp_softstat(st[g]);
@@ -137,16 +158,16 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
     }
     __syncthreads();
     if (tid < gb) {
-      ChainPartial acc = red[tid][0];
-      SoftStat sacc{acc.m, acc.s};
+      ChainPartial acc2 = red[tid][0];
+      SoftStat sacc{acc2.m, acc2.s};
       for (int w = 1; w < kWarps; ++w) {
         const ChainPartial o = red[tid][w];
-        acc.key = o.key > acc.key ? o.key : acc.key;
+        acc2.key = o.key > acc2.key ? o.key : acc2.key;
         sacc = softstat_merge(sacc, SoftStat{o.m, o.s});
       }
-      acc.m = sacc.m;
-      acc.s = sacc.s;
-      partials[static_cast<long long>(g0 + tid) * nchunks + chunk] = acc;
+      acc2.m = sacc.m;
+      acc2.s = sacc.s;
+      partials[static_cast<long long>(g0 + tid) * nchunks + chunk] = acc2;
     }
     __syncthreads();
   }
@@ -261,9 +282,12 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
   for (int pos = 0; pos < k; ++pos) {
     const int32_t *prev_src = pos == 0 ? prev_token : draft_tokens + (pos - 1);
     const int prev_stride = pos == 0 ? 1 : k;
-    markov_chain_kernel<<<nchunks, kThreads, 0, stream>>>(
-        logits, w1, w2, r, prev_src, prev_stride, draft_tokens, q_stats, draft_len_fill, B, k, V,
-        pos, nchunks, partials, counter, status);
+    auto kern = B >= 8 ? markov_chain_kernel<8>
+                       : (B >= 4 ? markov_chain_kernel<4>
+                                 : (B >= 2 ? markov_chain_kernel<2> : markov_chain_kernel<1>));
+    kern<<<nchunks, kThreads, 0, stream>>>(logits, w1, w2, r, prev_src, prev_stride, draft_tokens,
+                                           q_stats, draft_len_fill, B, k, V, pos, nchunks,
+                                           partials, counter, status);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   }
   return DSPARK_OK;
