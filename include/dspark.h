@@ -227,6 +227,41 @@ dspark_status_t dspark_verify(int mode, const float *target_logits,
                               int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
                               void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free verify.  No counterpart in the pages: a library
+ * convenience with the semantics, arguments and outputs of dspark_verify,
+ * minus the workspace.
+ *
+ * For callers that cannot supply a workspace: code that a host framework
+ * hands only its input and output buffers while it owns every other device
+ * allocation (a serving engine's custom-operator interface, for instance),
+ * and code that must not call cudaMalloc while it runs, because cudaMalloc
+ * may synchronise the device or the process keeps to a fixed memory budget.
+ *
+ * Scratch: one fixed array of DSPARK_VERIFY_NOALLOC_MAX_BYTES inside the
+ * library's device image, held by every GPU that loads the library until the
+ * process exits.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Each call first clears the part of the
+ * array it uses (cudaMemsetAsync on `stream`), then enqueues the same kernels
+ * as dspark_verify.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ * All calls share the one array, so calls whose GPU work overlaps (streams
+ * not ordered with respect to each other, or several host threads) race and
+ * corrupt each other's results: order them.
+ * Limit: dspark_verify_workspace_size(B, k, V) must not exceed
+ * DSPARK_VERIFY_NOALLOC_MAX_BYTES (4 MiB; e.g. B = 64, k = 16, V = 262144
+ * fits), otherwise DSPARK_ERR_WORKSPACE is returned and nothing is enqueued.
+ * Device-side errors are recorded in the array's status word, which the next
+ * call clears; this variant does not report them.
+ * ---------------------------------------------------------------------- */
+#define DSPARK_VERIFY_NOALLOC_MAX_BYTES ((size_t)4 << 20)
+dspark_status_t dspark_verify_noalloc(int mode, const float *target_logits,
+                                      const int32_t *draft_tokens, const int32_t *draft_len,
+                                      const float *draft_logits, const float *q_stats,
+                                      uint64_t seed, const uint32_t *request_id, uint32_t step,
+                                      int32_t *accepted_len, int32_t *next_token, int B, int k,
+                                      int V, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
