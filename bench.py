@@ -307,26 +307,32 @@ def run_ours(args, rank, local_rank, world):
     nxt_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
     dlen_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream(device)
-    lm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(K)]
+    # events at the stage boundaries of every timed step: fc | LM head | chain | verify
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     wsp = ds.Workspaces()
 
     def one_step(i, st, ev=None):
-        ds.fc_project(st["taps"], fc_w, out=h_buf, stream=stream, workspaces=wsp)
         if ev is not None:
             ev[0].record(stream)
-        ds.lm_head(h_buf, lm_w, out=logits.view(M, V), stream=stream, workspaces=wsp)
+        ds.fc_project(st["taps"], fc_w, out=h_buf, stream=stream, workspaces=wsp)
         if ev is not None:
             ev[1].record(stream)
+        ds.lm_head(h_buf, lm_w, out=logits.view(M, V), stream=stream, workspaces=wsp)
+        if ev is not None:
+            ev[2].record(stream)
         ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
                          stream=stream, workspaces=wsp)
         if conf_w is not None:
             ds.confidence_truncate(h_buf, conf_w, drafts, B, k, w_conf_b, w_conf_tau,
                                    draft_len=dlen_hist[i], stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
         ds.verify(mode, st["target"], drafts, dlen_hist[i] if conf_w is not None else None,
                   logits if mode == 1 else None, q_stats if mode == 1 else None, seed=12345,
                   request_id=None, step=i, accepted_len=acc_hist[i], next_token=nxt_hist[i],
                   stream=stream, workspaces=wsp)
+        if ev is not None:
+            ev[4].record(stream)
 
     w_conf_b, w_conf_tau = 0.0, 0.5
     for i in range(W):
@@ -343,16 +349,21 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = ds.launch_count()
     t_start.record(stream)
     for i in range(K):
-        one_step(i, sets[i % len(sets)], lm_ev[i])
+        one_step(i, sets[i % len(sets)], stage_ev[i])
     t_end.record(stream)
+    launches = ds.launch_count() - launches0
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     ms = t_start.elapsed_time(t_end)
-    lm_ms = statistics.mean(a.elapsed_time(b) for a, b in lm_ev)
+    stage_names = ["fc_project", "lm_head", "greedy_sample", "verify"]
+    stage_ms = {nm: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev)
+                for j, nm in enumerate(stage_names)}
+    lm_ms = stage_ms["lm_head"]
     max_ms = ms
     if world > 1:
         t = torch.tensor([ms], device=device)
@@ -414,7 +425,6 @@ def run_ours(args, rank, local_rank, world):
     lm_bytes = sb["lm_head"]
     achieved = lm_bytes / (lm_ms / 1000.0) / 1e9
     t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
-    launches_per_step = 1 + 1 + k + (1 if conf_w is not None else 0) + (2 if mode == 1 else 1)
 
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
@@ -437,7 +447,8 @@ def run_ours(args, rank, local_rank, world):
         "step_roofline": {"bytes": sb["total"], "flops": step_flops(cfg),
                           "t_roofline_ms": t_roof * 1000.0,
                           "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src},
-        "gpu_launches": launches_per_step * K,
+        "stage_ms": stage_ms,
+        "gpu_launches": launches,
         "e2e": e2e,
         "clocks": clk,
     }

@@ -75,6 +75,10 @@ const char *dspark_status_string(dspark_status_t status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int dspark_version(void);
 
+/* Number of kernels this library has enqueued in this process so far (all
+ * devices, all calls); a diagnostic for launch accounting. */
+long long dspark_launch_count(void);
+
 /* Reads the device-side status word at the start of ws (enqueued on stream,
  * then the host waits for the stream), stores it in *status_out and resets
  * it to 0.  DSPARK_OK means no device-side error since the last read. */

@@ -20,7 +20,7 @@ import torch
 
 __all__ = ["DSparkError", "lib", "fc_project", "lm_head", "greedy_sample", "confidence_truncate",
            "draft_readout",
-           "verify", "workspace_status", "Workspaces", "library_path"]
+           "verify", "workspace_status", "launch_count", "Workspaces", "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libdspark.so")
@@ -56,6 +56,7 @@ def lib():
         L.dspark_status_string.restype = ctypes.c_char_p
         L.dspark_status_string.argtypes = [ctypes.c_int]
         L.dspark_version.restype = ctypes.c_int
+        L.dspark_launch_count.restype = ctypes.c_longlong
         L.dspark_workspace_status.restype = ctypes.c_int
         L.dspark_workspace_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
         L.dspark_fc_project_workspace_size.restype = _sz
@@ -140,6 +141,11 @@ class Workspaces:
 
 
 _default_ws = Workspaces()
+
+
+def launch_count():
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().dspark_launch_count())
 
 
 def workspace_status(ws, stream=None):

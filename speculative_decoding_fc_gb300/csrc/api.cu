@@ -9,7 +9,15 @@
 
 #include "internal.h"
 
+#include <atomic>
+
 namespace dspark {
+
+namespace {
+std::atomic<long long> g_launches{0};
+}
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int device_sm_count() {
   static int cache[64] = {};
@@ -110,6 +118,8 @@ const char *dspark_status_string(dspark_status_t s) {
 }
 
 int dspark_version(void) { return 100; }
+
+long long dspark_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 dspark_status_t dspark_workspace_status(void *ws, void *stream, int32_t *status_out) {
   if (!ws || !status_out) return DSPARK_ERR_INVALID_ARG;

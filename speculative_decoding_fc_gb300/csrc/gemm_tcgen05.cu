@@ -437,17 +437,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
         if (ticket == nseg - 1) {
           __threadfence();
           const int mcount = min(p.BN, p.M - m_base);
-          for (int col = 0; col < mcount; ++col) {
-            float s = 0.0f;
+          // 16 columns at a time: the 16 loads of one piece are independent, so each
+          // piece costs one memory latency; pieces are added in CTA order.
+          for (int c0 = 0; c0 < mcount; c0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
             for (int sg = 0; sg < nseg; ++sg) {
               const int c2 = c_first + sg;
               const int tile_c2 = static_cast<int>((p.units * c2 / grid) / kbt);
               const int slot = (tile == tile_c2) ? 0 : 1;
               const float *src = p.partials + (static_cast<size_t>(c2) * 2 + slot) *
                                                   static_cast<size_t>(p.BN) * kBM;
-              s += __ldcg(src + col * kBM + row);
+              float v[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                v[j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) acc[j] += v[j];
             }
-            store_out(p, m_base + col, n, s);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < mcount) store_out(p, m_base + c0 + j, n, acc[j]);
           }
           if (threadIdx.x == 64) p.tickets[tile] = 0;
         }
@@ -600,7 +611,9 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   gemm_tcgen05_kernel<<<static_cast<unsigned>(grid), kThreads, t.smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  count_launches(1);
+  return DSPARK_OK;
 }
 
 }  // namespace dspark

@@ -57,6 +57,10 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
                               int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
                               void *ws, int *status, cudaStream_t stream);
 
+// ------------------------------------------------------------------ launch accounting
+// Counts every kernel this library enqueues (reported by dspark_launch_count).
+void count_launches(int n);
+
 // ------------------------------------------------------------------ device info
 int device_sm_count();  // cached per current device; 0 when no device
 bool device_is_blackwell();

@@ -7,15 +7,26 @@
 // on the accepted bonus token that propose() captured; AcceptRatePredictor +
 // _truncate_by_confidence shorten the block.
 //
-// One launch per block position (the argmax of position i is the context of
-// position i+1, a grid-wide dependency).  Each CTA owns a 512-entry slice of
-// the vocabulary for every request: it reads the slice of markov_w2 once per
-// group of 8 requests, adds the bias to the logits in place, and reduces a
-// (value, lowest index) argmax key and the softmax statistics of the slice.
-// The last CTA to finish (atomic ticket, nobody waits) merges the slices in a
-// fixed order and writes the draft token, which the next launch reads.
+// The argmax of position i is the context of position i+1: a grid-wide
+// dependency between positions.  Two implementations:
+//
+//  * markov_chain_persistent (default): ONE cooperative launch, one CTA per
+//    SM.  Each CTA owns a contiguous slice of the vocabulary for all k
+//    positions and keeps its slice of markov_w2 in shared memory (XOR-swizzled
+//    16-byte chunks, bank-conflict free), so the weight is read from memory
+//    once per step instead of once per position.  Positions are separated by
+//    a grid barrier (atomic arrival counter, bounded spin); after it every CTA
+//    merges the per-CTA partials itself, in the same fixed order, so all CTAs
+//    agree on the draft token without a second barrier.
+//  * markov_chain_kernel (fallback when a cooperative launch is not possible):
+//    one launch per position; the last CTA to finish (atomic ticket, nobody
+//    waits) merges the slices and writes the token the next launch reads.
+//
+// Each CTA reduces, per request, a (value, lowest index) argmax key and the
+// softmax statistics (max, sum exp) of its slice of the biased logits.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -216,6 +227,387 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
   if (tid == 0) *counter = 0;
 }
 
+// ---------------------------------------------------------------- persistent chain
+constexpr int kPThreads = 256;
+constexpr int kPWarps = kPThreads / 32;
+constexpr int kPVPT = 4;                      // vocab rows per thread (slice <= 2048 rows)
+constexpr int kMaxPGrid = kMaxGemmCtas;       // CTAs of the persistent chain (<= SMs)
+constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+struct ChainPArgs {
+  float *logits;
+  const uint16_t *w1;
+  const uint16_t *w2;
+  const int32_t *prev_token;
+  int32_t *draft_tokens;
+  float *q_stats;
+  int32_t *draft_len_fill;
+  ChainPartial *partials;   // [k][B][grid]
+  int *flags;               // [k][grid]: CTA c has published its partials of position pos
+  int *epoch;               // call counter: the flags of call e carry tags of epoch e
+  int *done;                // exit counter (the last CTA advances the epoch)
+  int *abort_flag;          // set when a wait gives up; later calls then do nothing
+  int *status;
+  int r, B, k, V;
+  int rows_per_cta;         // vocabulary rows owned by one CTA
+  int w2_in_smem;           // 1: the CTA's markov_w2 slice lives in shared memory
+  int w2_smem_bytes;        // bytes of shared memory reserved for that slice
+};
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed(const int *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(int *p, int v) {
+  asm volatile("st.release.gpu.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 16-byte chunk q of local row `row` of the shared-memory markov_w2 slice is
+// stored at chunk q ^ (row & mask): eight consecutive rows read at the same q
+// hit eight different bank groups.
+__device__ __forceinline__ int w2_swizzle(int row, int q, int chunks_per_row) {
+  const int mask = chunks_per_row < 8 ? chunks_per_row - 1 : 7;
+  return q ^ (row & mask);
+}
+
+// Tag a CTA writes into its flag once its partials of position `pos` are
+// visible; unique per (call, position) so flags never need clearing.
+__device__ __forceinline__ int flag_tag(int epoch, int pos) {
+  return 1 + static_cast<int>((static_cast<unsigned>(epoch) * 16u + static_cast<unsigned>(pos)) &
+                              0x3fffffffu);
+}
+
+// Rows of the vocabulary a thread of the persistent chain owns: 4 rows x up to 8
+// requests = 32 independent fma chains per thread.
+constexpr int kPRows = 4;
+
+// Warp-wide (key max, softmax stats) of one value pair per thread, with one exp per
+// thread: the max first, then the sum of s * exp(m - max).
+__device__ __forceinline__ void warp_key_stats(unsigned long long &key, float &m, float &s) {
+  key = warp_max_u64(key);
+  float mm = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+  float ss = (m == -INFINITY) ? 0.0f : s * expf(m - mm);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  m = mm;
+  s = ss;
+}
+
+template <int G, int CPR>
+__global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const ChainPArgs a) {
+  static_assert(G <= kPWarps, "one combining warp per request of a group");
+  __shared__ ChainPartial red[kGroup][kPWarps];
+  __shared__ int stop_s, epoch_s;
+  extern __shared__ __align__(16) uint8_t psmem[];
+  // dynamic shared memory: markov_w2 slice [rows][CPR] (1024-byte aligned), then the
+  // contexts e of all requests [B][r], then prev tokens [B]
+  uint4 *w2_s = reinterpret_cast<uint4 *>(psmem);
+  float *e_s = reinterpret_cast<float *>(psmem + a.w2_smem_bytes);
+  int *prev_s = reinterpret_cast<int *>(psmem + a.w2_smem_bytes + static_cast<size_t>(a.B) * CPR * 32);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const int B = a.B, k = a.k, V = a.V;
+  constexpr int r = CPR * 8;
+  const bool biased = (a.w1 != nullptr);
+  const int v_lo = cta * a.rows_per_cta;
+  const int v_hi = min(V, v_lo + a.rows_per_cta);
+  const int nrows = max(0, v_hi - v_lo);
+  // this thread's rows: tid and tid + 512 of the slice (clamped; results of the
+  // clamped copies are discarded)
+  bool valid[kPRows];
+  int vrow[kPRows];
+#pragma unroll
+  for (int j = 0; j < kPRows; ++j) {
+    const int row = j * kPThreads + tid;
+    valid[j] = row < nrows;
+    vrow[j] = v_lo + (row < nrows ? row : (nrows > 0 ? nrows - 1 : 0));
+  }
+
+  if (tid == 0) {
+    stop_s = ld_acquire(a.abort_flag);
+    epoch_s = ld_acquire(a.epoch);
+    if (stop_s && cta == 0) record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
+  }
+  // markov_w2 slice -> shared memory (16-byte chunks XOR-swizzled by row so that 8
+  // consecutive rows read at the same chunk hit 8 bank groups), asynchronous copies
+  // all in flight together.
+  if (biased) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
+    for (int i = tid; i < nrows * CPR; i += kPThreads) {
+      const int row = i / CPR, q = i - row * CPR;
+      const uint32_t dst = static_cast<uint32_t>(
+          __cvta_generic_to_shared(&w2_s[row * CPR + w2_swizzle(row, q, CPR)]));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + i)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int b = tid; b < B; b += kPThreads) {
+    int p = a.prev_token[b];
+    if (biased && (p < 0 || p >= V)) {
+      if (cta == 0) record_error(a.status, DSPARK_ERR_BAD_TOKEN);
+      p = -1;
+    }
+    prev_s[b] = p;
+  }
+  if (biased) asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (stop_s) return;
+  const int epoch = epoch_s;
+  int lrow[kPRows];  // local (slice) row of each of this thread's rows, clamped
+#pragma unroll
+  for (int j = 0; j < kPRows; ++j) lrow[j] = vrow[j] - v_lo;
+
+  // Logits of the first request group at the coming position, loaded ahead of the
+  // wait for the other CTAs (they do not depend on it).
+  float lg_next[kPRows][G];
+#pragma unroll
+  for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k) * V + vrow[j]] : 0.0f;
+
+  float acc[kPRows][G];  // bias, then the biased logit, of this thread's rows
+  for (int pos = 0; pos < k; ++pos) {
+    if (biased) {
+      // e_b = markov_w1[prev_b] for every request, once per position
+      for (int idx = tid; idx < B * r; idx += kPThreads) {
+        const int b = idx / r, t = idx - b * r;
+        const int p = prev_s[b];
+        e_s[idx] = p >= 0 ? __uint_as_float(static_cast<uint32_t>(a.w1[static_cast<long long>(p) * r + t]) << 16)
+                          : 0.0f;
+      }
+      __syncthreads();
+    }
+    for (int g0 = 0; g0 < B; g0 += G) {
+      const int gb = min(G, B - g0);
+      // later groups: their logits, loaded before the fma loop hides the latency
+      if (g0 > 0) {
+#pragma unroll
+        for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            lg_next[j][g] = (g < gb) ? a.logits[(static_cast<long long>(g0 + g) * k + pos) * V + vrow[j]] : 0.0f;
+      }
+      // bias[v] = sequential fp32 fma chain over t = 0..r-1 (the chain of each
+      // (row, request) is one thread's, in t order; chains interleave for ILP)
+#pragma unroll
+      for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
+      if (biased) {
+#pragma unroll
+        for (int q = 0; q < CPR; ++q) {
+          float w[kPRows][8];
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) {
+            const uint4 c = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+            w[j][0] = bf16_lo(c.x); w[j][1] = bf16_hi(c.x);
+            w[j][2] = bf16_lo(c.y); w[j][3] = bf16_hi(c.y);
+            w[j][4] = bf16_lo(c.z); w[j][5] = bf16_hi(c.z);
+            w[j][6] = bf16_lo(c.w); w[j][7] = bf16_hi(c.w);
+          }
+          float e[G][8];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            // requests past the batch end read request 0's context (results unused)
+            const int gg = (g < gb) ? g0 + g : 0;
+            const float4 ea = *reinterpret_cast<const float4 *>(&e_s[gg * r + q * 8]);
+            const float4 eb = *reinterpret_cast<const float4 *>(&e_s[gg * r + q * 8 + 4]);
+            e[g][0] = ea.x; e[g][1] = ea.y; e[g][2] = ea.z; e[g][3] = ea.w;
+            e[g][4] = eb.x; e[g][5] = eb.y; e[g][6] = eb.z; e[g][7] = eb.w;
+          }
+          // rank t of every (row, request) chain, then rank t + 1: all G x kPRows
+          // chains advance together
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+              for (int j = 0; j < kPRows; ++j) acc[j][g] = __fmaf_rn(w[j][t], e[g][t], acc[j][g]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (g < gb) {
+          unsigned long long key = 0ull;
+          float m = -INFINITY, sum = 0.0f;
+          float zv[kPRows];
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) {
+            float z = lg_next[j][g];
+            if (biased) z = __fadd_rn(z, acc[j][g]);
+            zv[j] = z;
+            acc[j][g] = z;  // kept for the write-back after this position's release
+            if (valid[j]) {
+              const unsigned long long kj = argmax_key(z, static_cast<uint32_t>(vrow[j]));
+              key = kj > key ? kj : key;
+              if (z == z && z != -INFINITY) m = fmaxf(m, z);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j)
+            if (valid[j] && m != -INFINITY && zv[j] == zv[j] && zv[j] != -INFINITY)
+              sum += expf(zv[j] - m);
+          warp_key_stats(key, m, sum);
+          if (lane == 0) red[g][warp] = ChainPartial{key, m, sum};
+        }
+      }
+      __syncthreads();
+      // one warp per request of the group combines the 16 warp partials
+      if (warp < gb) {
+        const int g = warp;
+        unsigned long long key = 0ull;
+        float m = -INFINITY, sum = 0.0f;
+        if (lane < kPWarps) {
+          const ChainPartial c0 = red[g][lane];
+          key = c0.key;
+          m = c0.m;
+          sum = c0.s;
+        }
+        warp_key_stats(key, m, sum);
+        if (lane == 0) {
+          a.partials[(static_cast<long long>(pos) * B + g0 + g) * grid + cta] = ChainPartial{key, m, sum};
+          // the global winner is one of the CTA winners: warm L2 with this one's
+          // markov_w1 row for the next position's gather
+          if (biased && pos + 1 < k)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.w1 + static_cast<long long>(key_index(key)) * r));
+        }
+      }
+      if (biased && B > G) {
+        // several groups share acc: store this group's biased logits now
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g < gb)
+#pragma unroll
+            for (int j = 0; j < kPRows; ++j)
+              if (valid[j]) a.logits[(static_cast<long long>(g0 + g) * k + pos) * V + vrow[j]] = acc[j][g];
+      }
+      __syncthreads();
+    }
+
+    // Publish this CTA's partials of `pos` (the barrier above orders every thread's
+    // partial stores before the release), then wait until every CTA has: warp 0 polls
+    // the flags with relaxed loads and takes one acquire fence once all are seen.
+    const int tag = flag_tag(epoch, pos);
+    if (tid == 0) st_release(a.flags + pos * grid + cta, tag);
+    if (biased && B <= G) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (g < B)
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j)
+            if (valid[j]) a.logits[(static_cast<long long>(g) * k + pos) * V + vrow[j]] = acc[j][g];
+    }
+    if (pos + 1 < k) {
+#pragma unroll
+      for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k + pos + 1) * V + vrow[j]] : 0.0f;
+    }
+    if (warp == 0) {
+      const int *f = a.flags + pos * grid;
+      const long long t0 = clock64();
+      int stop = 0;
+      while (true) {
+        // independent loads (no short-circuit): one round trip per pass
+        int seen = 0, want = 0;
+        for (int c = lane; c < grid; c += 32) {
+          seen += (ld_relaxed(f + c) == tag) ? 1 : 0;
+          ++want;
+        }
+        if (__all_sync(0xffffffffu, seen == want)) break;
+        int give_up = 0;
+        if (lane == 0)
+          give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > kBarrierCycles) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, give_up, 0)) {
+          if (lane == 0 && atomicExch(a.abort_flag, 1) == 0)
+            record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
+          stop = 1;
+          break;
+        }
+        __nanosleep(20);
+      }
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      if (lane == 0) stop_s = stop;
+    }
+    __syncthreads();
+    if (stop_s) return;
+
+    // Every CTA merges all CTAs' argmax keys (same data, same order -> same token).
+    for (int b = warp; b < B; b += kPWarps) {
+      const ChainPartial *pb = a.partials + (static_cast<long long>(pos) * B + b) * grid;
+      unsigned long long kb = 0ull;
+      for (int c = lane; c < grid; c += 32) {
+        const unsigned long long key = __ldcg(reinterpret_cast<const unsigned long long *>(pb + c));
+        kb = key > kb ? key : kb;
+      }
+      kb = warp_max_u64(kb);
+      if (lane == 0) {
+        const int d = static_cast<int>(key_index(kb));
+        prev_s[b] = d;
+        if (cta == 0) a.draft_tokens[static_cast<long long>(b) * k + pos] = d;
+      }
+    }
+    __syncthreads();
+  }
+
+  // Off the critical path: softmax statistics of q for every (position, request),
+  // spread over the CTAs, one warp each.
+  if (a.q_stats || a.draft_len_fill) {
+    const int pairs = k * B;
+    for (int pr = cta * kPWarps + warp; pr < pairs; pr += grid * kPWarps) {
+      const int pos = pr / B, b = pr - pos * B;
+      const ChainPartial *pb = a.partials + (static_cast<long long>(pos) * B + b) * grid;
+      float mmax = -INFINITY;
+      for (int c = lane; c < grid; c += 32)
+        mmax = fmaxf(mmax, __ldcg(reinterpret_cast<const float *>(pb + c) + 2));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+      double sd = 0.0;
+      if (mmax != -INFINITY) {
+        for (int c = lane; c < grid; c += 32) {
+          const float cm = __ldcg(reinterpret_cast<const float *>(pb + c) + 2);
+          const float cs = __ldcg(reinterpret_cast<const float *>(pb + c) + 3);
+          if (cm != -INFINITY) sd += static_cast<double>(cs) * static_cast<double>(expf(cm - mmax));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+      if (lane == 0) {
+        const long long at = static_cast<long long>(b) * k + pos;
+        if (a.q_stats) {
+          a.q_stats[2 * at] = mmax;
+          a.q_stats[2 * at + 1] = static_cast<float>(sd);
+        }
+        if (a.draft_len_fill && pos == k - 1) a.draft_len_fill[b] = k;
+      }
+    }
+  }
+
+  // The last CTA out advances the epoch for the next call.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.done, 1) == grid - 1) {
+      *a.done = 0;
+      __threadfence();
+      st_release(a.epoch, epoch + 1);
+    }
+  }
+}
+
 // c[b, i] = sigmoid(w . h[b*k+i] + bias); draft_len[b] = first i whose logit
 // falls below thr = logit(tau); later drafts are replaced by -1.
 constexpr int kConfThreads = 256;
@@ -266,19 +658,118 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(
 
 }  // namespace
 
-size_t chain_workspace_size(int B, int k, int V) {
-  (void)k;
-  const int nchunks = (V + kChunk - 1) / kChunk;
-  return kWsAlign + align_up(static_cast<size_t>(B) * nchunks * sizeof(ChainPartial), kWsAlign);
+// Chain workspace: [0] ticket of the per-position kernel, [4] epoch, [8] exit
+// count, [12] abort flag; position flags from byte 256 (k x kMaxPGrid ints);
+// partials after them.
+size_t chain_flags_bytes(int k) {
+  return align_up(static_cast<size_t>(k) * kMaxPGrid * sizeof(int), kWsAlign);
 }
+
+size_t chain_workspace_size(int B, int k, int V) {
+  const int nchunks = (V + kChunk - 1) / kChunk;
+  const size_t per_pos = static_cast<size_t>(B) * nchunks * sizeof(ChainPartial);
+  const size_t persistent = static_cast<size_t>(k) * B * kMaxPGrid * sizeof(ChainPartial);
+  return kWsAlign + chain_flags_bytes(k) +
+         align_up(per_pos > persistent ? per_pos : persistent, kWsAlign);
+}
+
+namespace {
+
+template <int G, int CPR>
+bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  int grid = sms < kMaxPGrid ? sms : kMaxPGrid;
+  const int by_rows = (V + 255) / 256;
+  if (grid > by_rows) grid = by_rows;
+  const int rows = (V + grid - 1) / grid;
+  if (rows > kPRows * kPThreads) return false;
+  ChainPArgs a = args0;
+  a.rows_per_cta = rows;
+  a.w2_in_smem = 1;
+  a.w2_smem_bytes = static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024));
+  const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + static_cast<size_t>(B) * CPR * 32 +
+                      static_cast<size_t>(B) * sizeof(int);
+  if (smem > 200 * 1024) return false;
+  auto kern = markov_chain_persistent<G, CPR>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    attr_set[dev] = true;
+  }
+  void *params[] = {const_cast<ChainPArgs *>(&a)};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid),
+                                  dim3(kPThreads), params, smem, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+template <int G>
+bool try_persistent(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
+  switch (r) {
+    case 0: return try_persistent_r<G, 1>(a, B, V, stream);  // no bias: rank unused
+    case 16: return try_persistent_r<G, 2>(a, B, V, stream);
+    case 32: return try_persistent_r<G, 4>(a, B, V, stream);
+    case 64: return try_persistent_r<G, 8>(a, B, V, stream);
+    default: return false;  // other ranks: per-position kernels
+  }
+}
+
+}  // namespace
 
 dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *w2, int r,
                              const int32_t *prev_token, int32_t *draft_tokens, float *q_stats,
                              int32_t *draft_len_fill, int B, int k, int V, void *ws,
                              int *status, cudaStream_t stream) {
+  int *ctrl = reinterpret_cast<int *>(ws);
+  int *flags = reinterpret_cast<int *>(static_cast<char *>(ws) + kWsAlign);
+  ChainPartial *partials = reinterpret_cast<ChainPartial *>(static_cast<char *>(ws) + kWsAlign +
+                                                           chain_flags_bytes(k));
+
+  ChainPArgs pa;
+  pa.logits = logits;
+  pa.w1 = w1;
+  pa.w2 = w2;
+  pa.prev_token = prev_token;
+  pa.draft_tokens = draft_tokens;
+  pa.q_stats = q_stats;
+  pa.draft_len_fill = draft_len_fill;
+  pa.partials = partials;
+  pa.flags = flags;
+  pa.epoch = ctrl + 1;
+  pa.done = ctrl + 2;
+  pa.abort_flag = ctrl + 3;
+  pa.status = status;
+  pa.r = w1 ? r : 0;
+  pa.B = B;
+  pa.k = k;
+  pa.V = V;
+  pa.rows_per_cta = 0;
+  pa.w2_in_smem = 0;
+  pa.w2_smem_bytes = 0;
+  // DSPARK_CHAIN_PER_POSITION=1 selects the per-position kernels (same results).
+  const char *env = getenv("DSPARK_CHAIN_PER_POSITION");
+  const bool per_position = env && env[0] == '1';
+  const bool ok = per_position ? false
+                  : B >= 8 ? try_persistent<8>(pa, pa.r, B, V, stream)
+                  : B >= 4 ? try_persistent<4>(pa, pa.r, B, V, stream)
+                  : B >= 2 ? try_persistent<2>(pa, pa.r, B, V, stream)
+                           : try_persistent<1>(pa, pa.r, B, V, stream);
+  if (ok) {
+    count_launches(1);
+    return DSPARK_OK;
+  }
+
   const int nchunks = (V + kChunk - 1) / kChunk;
-  int *counter = reinterpret_cast<int *>(ws);
-  ChainPartial *partials = reinterpret_cast<ChainPartial *>(static_cast<char *>(ws) + kWsAlign);
+  int *counter = ctrl;
   for (int pos = 0; pos < k; ++pos) {
     const int32_t *prev_src = pos == 0 ? prev_token : draft_tokens + (pos - 1);
     const int prev_stride = pos == 0 ? 1 : k;
@@ -289,6 +780,7 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
                                            q_stats, draft_len_fill, B, k, V, pos, nchunks,
                                            partials, counter, status);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    count_launches(1);
   }
   return DSPARK_OK;
 }
@@ -305,7 +797,9 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
     thr = static_cast<float>(log(static_cast<double>(conf_tau)) - log1p(-static_cast<double>(conf_tau)));
   confidence_kernel<<<B, kConfThreads, 0, stream>>>(h, conf_w, conf_b, thr, draft_tokens,
                                                     draft_len, conf_out, k, H);
-  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  count_launches(1);
+  return DSPARK_OK;
 }
 
 }  // namespace dspark

@@ -32,8 +32,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPer = 16;                    // entries per thread per slice
-constexpr int kSlice = kThreads * kPer;     // 4096 entries per CTA
+constexpr int kPer = 16;                    // entries per thread per slice (pass 1)
+constexpr int kSlice = kThreads * kPer;     // 4096 entries per CTA (pass 1)
+constexpr int kDrawSlice = kThreads * 4;    // 1024 entries per CTA (pass 2): one Philox block per thread
 
 struct __align__(16) RowPartial {
   unsigned long long key;
@@ -77,6 +78,7 @@ struct VerifyArgs {
   int mode;
   int B, k, V;
   int nslices;
+  int ndraw;      // slices of the draw pass
   int zrows;      // 1 when draft-logit statistics are computed here
   int vec;        // 1 when every row starts on a 16-byte boundary (128-bit loads)
 };
@@ -218,6 +220,36 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
   }
   __syncthreads();
 
+  // Probabilistic: every position's ratio p(d)/q(d) and accept uniform, in parallel
+  // (thread j takes position j); the sequential accept loop below only compares.
+  __shared__ double ratio_s[kMaxK], ua_s[kMaxK];
+  __shared__ int bad_s[kMaxK];
+  if (a.mode == 1 && tid < L) {
+    const int jj = tid;
+    const long long drow = static_cast<long long>(b) * k;
+    const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
+    const int d = a.drafts[drow + jj];
+    double ua, us;
+    verify_uniforms(a.seed, req, static_cast<uint32_t>(jj), a.step, ua, us);
+    ua_s[jj] = ua;
+    bad_s[jj] = (d < 0 || d >= V) ? 1 : 0;
+    double ratio = 0.0;
+    if (!bad_s[jj]) {
+      const double tT = a.target[(static_cast<long long>(b) * (k + 1) + jj) * V + d];
+      const double pd = exp(tT - tM[jj]) / tS[jj];
+      double qd = 1.0;
+      if (a.zlog) {
+        const double qm = a.zrows ? zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
+        const double qs = a.zrows ? zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
+        const double zd = a.zlog[(drow + jj) * V + d];
+        qd = exp(zd - qm) / qs;
+      }
+      ratio = pd / qd;
+    }
+    ratio_s[jj] = ratio;
+  }
+  __syncthreads();
+
   if (tid == 0) {
     const long long drow = static_cast<long long>(b) * k;
     int acc_len = 0;
@@ -228,7 +260,6 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
       a.accepted_len[b] = acc_len;
       a.next_token[b] = static_cast<int32_t>(key_index(tkey[acc_len]));
     } else {
-      const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
       SampleJob job;
       job.kind = kNone;
       job.d = -1;
@@ -236,31 +267,20 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
       job.cq = 0.0;
       for (; acc_len < L; ++acc_len) {
         const int jj = acc_len;
-        const int d = a.drafts[drow + jj];
-        double ua, us;
-        verify_uniforms(a.seed, req, static_cast<uint32_t>(jj), a.step, ua, us);
-        if (d < 0 || d >= V) {
+        if (bad_s[jj]) {
           record_error(a.status, DSPARK_ERR_BAD_TOKEN);
           job.row = jj;
           job.kind = kFromP;
           job.cp = tM[jj] + log(tS[jj]);
           break;
         }
-        const double tT = a.target[(static_cast<long long>(b) * (k + 1) + jj) * V + d];
-        const double pd = exp(tT - tM[jj]) / tS[jj];
-        double qd = 1.0, qm = 0.0, qs = 1.0;
+        if (ua_s[jj] < ratio_s[jj]) continue;
+        const int d = a.drafts[drow + jj];
+        double qm = 0.0, qs = 1.0;
         if (a.zlog) {
-          if (a.zrows) {
-            qm = zM[jj];
-            qs = zS[jj];
-          } else {
-            qm = a.q_stats[2 * (drow + jj)];
-            qs = a.q_stats[2 * (drow + jj) + 1];
-          }
-          const double zd = a.zlog[(drow + jj) * V + d];
-          qd = exp(zd - qm) / qs;
+          qm = a.zrows ? zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
+          qs = a.zrows ? zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
         }
-        if (ua < pd / qd) continue;
         job.row = jj;
         job.kind = a.zlog ? kResidual : kResidualOneHot;
         job.d = d;
@@ -294,8 +314,8 @@ __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArg
   __shared__ int is_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
-  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
+  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.ndraw));
+  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.ndraw));
   const int k = a.k, V = a.V;
   const SampleJob job = a.jobs[b];
   const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
@@ -309,37 +329,48 @@ __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArg
   const float cqf = static_cast<float>(job.cq);
 
   unsigned long long best_r = 0ull, best_p = 0ull;
-  const int v0 = slice * kSlice + tid * kPer;
-#pragma unroll
-  for (int g4 = 0; g4 < kPer / 4; ++g4) {
-    const int vg = v0 + 4 * g4;
-    if (vg < V) {
-      const U4 w = philox4x32_10(U4{req, static_cast<uint32_t>(job.row), a.step,
-                                    1u + static_cast<uint32_t>(vg >> 2)},
-                                 k0, k1);
-      const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+  const int vg = slice * kDrawSlice + tid * 4;   // this thread's 4 entries: one Philox block
+  if (vg < V) {
+    const U4 w = philox4x32_10(U4{req, static_cast<uint32_t>(job.row), a.step,
+                                  1u + static_cast<uint32_t>(vg >> 2)},
+                               k0, k1);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    float tv[4], zv[4];
+    if (a.vec && vg + 4 <= V) {
+      const float4 t4 = __ldcs(reinterpret_cast<const float4 *>(trow + vg));
+      tv[0] = t4.x; tv[1] = t4.y; tv[2] = t4.z; tv[3] = t4.w;
+      if (zrow) {
+        const float4 z4 = __ldcs(reinterpret_cast<const float4 *>(zrow + vg));
+        zv[0] = z4.x; zv[1] = z4.y; zv[2] = z4.z; zv[3] = z4.w;
+      }
+    } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int v = vg + e;
-        if (v < V) {
-          const float g = gumbel_from_word(words[e]);
-          const float t = trow[v];
-          const float kp = t + g;
-          float kr;
-          if (job.kind == kResidual) {
-            const float av = t - cpf;
-            const float bv = zrow[v] - cqf;
-            kr = (av > bv) ? av + log1pf(-expf(bv - av)) + g : -INFINITY;
-          } else if (job.kind == kResidualOneHot) {
-            kr = (v == job.d) ? -INFINITY : kp;
-          } else {
-            kr = kp;
-          }
-          const unsigned long long keyr = argmax_key(kr, static_cast<uint32_t>(v));
-          const unsigned long long keyp = argmax_key(kp, static_cast<uint32_t>(v));
-          best_r = keyr > best_r ? keyr : best_r;
-          best_p = keyp > best_p ? keyp : best_p;
+        tv[e] = vg + e < V ? trow[vg + e] : 0.0f;
+        zv[e] = (zrow && vg + e < V) ? zrow[vg + e] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int v = vg + e;
+      if (v < V) {
+        const float g = gumbel_from_word(words[e]);
+        const float t = tv[e];
+        const float kp = t + g;
+        float kr;
+        if (job.kind == kResidual) {
+          const float av = t - cpf;
+          const float bv = zv[e] - cqf;
+          kr = (av > bv) ? av + log1pf(-expf(bv - av)) + g : -INFINITY;
+        } else if (job.kind == kResidualOneHot) {
+          kr = (v == job.d) ? -INFINITY : kp;
+        } else {
+          kr = kp;
         }
+        const unsigned long long keyr = argmax_key(kr, static_cast<uint32_t>(v));
+        const unsigned long long keyp = argmax_key(kp, static_cast<uint32_t>(v));
+        best_r = keyr > best_r ? keyr : best_r;
+        best_p = keyp > best_p ? keyp : best_p;
       }
     }
   }
@@ -356,20 +387,20 @@ __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArg
       br = red_r[w2] > br ? red_r[w2] : br;
       bp = red_p[w2] > bp ? red_p[w2] : bp;
     }
-    a.sparts[static_cast<long long>(b) * a.nslices + slice] = SamplePartial{br, bp};
+    a.sparts[static_cast<long long>(b) * a.ndraw + slice] = SamplePartial{br, bp};
   }
 
   __threadfence();
   __syncthreads();
-  if (tid == 0) is_last = (atomicAdd(&a.samp_ticket[b], 1) == a.nslices - 1) ? 1 : 0;
+  if (tid == 0) is_last = (atomicAdd(&a.samp_ticket[b], 1) == a.ndraw - 1) ? 1 : 0;
   __syncthreads();
   if (!is_last) return;
   __threadfence();
 
   if (warp == 0) {
-    const SamplePartial *sp = a.sparts + static_cast<long long>(b) * a.nslices;
+    const SamplePartial *sp = a.sparts + static_cast<long long>(b) * a.ndraw;
     unsigned long long br = 0ull, bp = 0ull;
-    for (int c = lane; c < a.nslices; c += 32) {
+    for (int c = lane; c < a.ndraw; c += 32) {
       const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(sp + c));
       br = raw.x > br ? raw.x : br;
       bp = raw.y > bp ? raw.y : bp;
@@ -388,12 +419,13 @@ __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArg
 
 struct VerifyLayout {
   size_t req_ticket, samp_ticket, rows, jobs, sparts, total;
-  int nslices;
+  int nslices, ndraw;
 };
 
 VerifyLayout layout(int B, int k, int V) {
   VerifyLayout L;
   L.nslices = (V + kSlice - 1) / kSlice;
+  L.ndraw = (V + kDrawSlice - 1) / kDrawSlice;
   size_t off = kWsAlign;
   L.req_ticket = off;
   off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
@@ -404,7 +436,7 @@ VerifyLayout layout(int B, int k, int V) {
   L.jobs = off;
   off += align_up(static_cast<size_t>(B) * sizeof(SampleJob), kWsAlign);
   L.sparts = off;
-  off += align_up(static_cast<size_t>(B) * L.nslices * sizeof(SamplePartial), kWsAlign);
+  off += align_up(static_cast<size_t>(B) * L.ndraw * sizeof(SamplePartial), kWsAlign);
   L.total = off;
   return L;
 }
@@ -442,6 +474,7 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
   a.k = k;
   a.V = V;
   a.nslices = L.nslices;
+  a.ndraw = L.ndraw;
   a.zrows = (mode == 1 && zlog != nullptr && q_stats == nullptr) ? 1 : 0;
   a.vec = ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(target) & 15u) == 0 &&
            (a.zlog == nullptr || (reinterpret_cast<uintptr_t>(a.zlog) & 15u) == 0))
@@ -452,10 +485,13 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
   if (g1 > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
   verify_stats_kernel<<<static_cast<unsigned>(g1), kThreads, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  count_launches(1);
   if (mode == 1) {
-    const long long g2 = static_cast<long long>(B) * L.nslices;
+    const long long g2 = static_cast<long long>(B) * L.ndraw;
+    if (g2 > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
     verify_sample_kernel<<<static_cast<unsigned>(g2), kThreads, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    count_launches(1);
   }
   return DSPARK_OK;
 }

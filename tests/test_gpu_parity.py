@@ -120,6 +120,27 @@ def test_greedy_sample_bit_exact(B, k, V, r):
     np.testing.assert_allclose(q[..., 1], ref["q_sumexp"], rtol=1e-5)
 
 
+def test_greedy_sample_per_position_kernels_agree(monkeypatch):
+    """The per-position kernels (used when a cooperative launch is not possible) give
+    the same bits as the persistent kernel and the oracle."""
+    B, k, V, r = 5, 7, 30000, 64
+    logits = syn.uniform_logits(35, (B, k, V), 1.5)
+    w1 = syn.normal_bf16(36, (V, r))
+    w2 = syn.normal_bf16(37, (V, r), (1.0 / r) ** 0.5)
+    prev = np.array([0, 1, 29999, 12345, 777], np.int32)
+    ref = oracle.greedy_sample(logits, w1, w2, prev)
+    outs = []
+    for flag in ("0", "1"):
+        monkeypatch.setenv("DSPARK_CHAIN_PER_POSITION", flag)
+        lg = dev(logits)
+        d, qs = ds.greedy_sample(lg, dev_bf16(w1), dev_bf16(w2), dev(prev))
+        outs.append((host(d), host(lg), host(qs)))
+    for d, z, q in outs:
+        np.testing.assert_array_equal(d, ref["draft_tokens"])
+        np.testing.assert_array_equal(z, ref["z"])
+        np.testing.assert_allclose(q[..., 1], ref["q_sumexp"], rtol=1e-5)
+
+
 def test_greedy_sample_hand_enumerated_golden(golden_dir):
     import json, os
     with open(os.path.join(golden_dir, "markov_chain_v8.json")) as f:
