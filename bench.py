@@ -57,6 +57,27 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def replica_step_seed(step, rank):
+    """Input-set seed of a replica: every rank drafts for its own requests."""
+    return step + 100 * rank
+
+
+def max_over_ranks(x, world, device=None):
+    """The slowest rank's value (timings are taken as the max over ranks)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, max_seconds):
+    """Units all ranks processed divided by the slowest rank's time."""
+    return world * units_per_rank / max_seconds
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     hbm, tflops, src = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
@@ -83,6 +104,28 @@ def measured_peaks():
     except (OSError, ValueError):
         pass
     return hbm, tflops, src
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per LM-head launch from the committed ncu summary of this workload,
+    or None when there is none or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_tcgen05_lm_head_%s.md" % workload)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith(("|", "#", " ")):
+                    key, _, val = line.partition(":")
+                    fields[key.strip()] = val.strip()
+        src = os.path.join(ROOT, fields["source"])
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if sha != fields["source_sha256_16"]:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def step_bytes(cfg, mode):
@@ -232,7 +275,7 @@ def run_reference(args, rank, world):
     est = oracle_sample_step(ora, host, cfg, mode, 1.0 / 256, 0)
     # size the sample so that warmup + steps finish within the budget
     per_step = budget / max(1, args.steps + args.warmup)
-    frac = min(1.0, max(1.0 / 4096, per_step / max(est * 256 * 1.0, 1e-9)))
+    frac = min(1.0, max(1.0 / 4096, per_step / max(est, 1e-9)))
     for i in range(args.warmup):
         oracle_sample_step(ora, host, cfg, mode, frac, i)
     t0 = time.perf_counter()
@@ -242,7 +285,7 @@ def run_reference(args, rank, world):
     desc = ("each step: the oracle's whole step on %.5f of the fc output columns and of the "
             "vocabulary, scaled to a full step" % frac)
     line = {
-        "impl": "reference", "metric": METRIC, "value": sps, "unit": "steps/s", "n_gpus": 1,
+        "impl": "reference", "metric": METRIC, "value": sps, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / sps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "wall_s": wall,
@@ -285,7 +328,7 @@ def run_ours(args, rank, local_rank, world):
     # input sets: taps, prev, target logits = own draft logits + noise (built once)
     sets = []
     for s in range(args.sets):
-        st = syn.step_inputs(s + 100 * rank, B, k, H, T, V, cfg["sigma"])
+        st = syn.step_inputs(replica_step_seed(s, rank), B, k, H, T, V, cfg["sigma"])
         taps = [d16(t) for t in st["taps"]]
         prev = torch.from_numpy(st["prev"]).to(device)
         h = ds.fc_project(taps, fc_w)
@@ -364,11 +407,7 @@ def run_ours(args, rank, local_rank, world):
     stage_ms = {nm: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev)
                 for j, nm in enumerate(stage_names)}
     lm_ms = stage_ms["lm_head"]
-    max_ms = ms
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(ms, world, device)
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
@@ -404,10 +443,7 @@ def run_ours(args, rank, local_rank, world):
             out_drafts.copy_(drafts, non_blocking=True)
             stream.synchronize()  # the host reads this step's result
         wall = time.perf_counter() - t0
-    e2e_t = torch.tensor([wall], device=device)
-    if world > 1:
-        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-    e2e = {"value": world * Ke / float(e2e_t.item()), "unit": "steps/s",
+    e2e = {"value": whole_job_rate(Ke, world, max_over_ranks(wall, world, device)), "unit": "steps/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     # ---------------------------------------------------------------- acceptance statistics
@@ -419,7 +455,7 @@ def run_ours(args, rank, local_rank, world):
     mean_acc_len = float(acc.mean()) + 1.0   # accepted drafts + the bonus/corrected token
     per_pos = [float((acc > j).mean()) for j in range(k)]
 
-    steps_per_s = world * K / (max_ms / 1000.0)
+    steps_per_s = whole_job_rate(K, world, max_ms / 1000.0)
     peak_gbs, peak_tf, peak_src = measured_peaks()
     sb = step_bytes(cfg, mode)
     lm_bytes = sb["lm_head"]
@@ -442,7 +478,7 @@ def run_ours(args, rank, local_rank, world):
         "per_position_acceptance": per_pos,
         "roofline": {"bound": "hbm", "kernel": "gemm_tcgen05 (LM head)", "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": profiled_traffic(args.config), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
         "step_roofline": {"bytes": sb["total"], "flops": step_flops(cfg),
                           "t_roofline_ms": t_roof * 1000.0,
