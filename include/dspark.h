@@ -33,9 +33,13 @@
  *   - ws / ws_bytes: a caller-owned DEVICE workspace of at least
  *     dspark_<call>_workspace_size(...) bytes, 256-byte aligned, ZERO-FILLED
  *     ONCE before its first use.  Every call leaves its counters at zero
- *     again, so the same workspace serves any number of later calls with the
- *     same or smaller sizes.  Calls that share a workspace must not overlap in
- *     time (same stream, or ordered by events).
+ *     again.  The library remembers (on the host, per workspace address) the
+ *     layout a workspace was last used with; a call with another call kind or
+ *     other sizes first clears its own counter regions with cudaMemsetAsync on
+ *     the call's stream, so one workspace may serve calls of any shape that
+ *     fits.  Calls that share a workspace must not overlap in time (same
+ *     stream, or ordered by events).  After a device-side error, zero the
+ *     workspace again before reusing it.
  *   - Argument errors are detected on the host before anything is enqueued
  *     and returned as a negative dspark_status_t.  Errors the device finds
  *     (a token id outside [0, V), a bounded internal wait running out) are

@@ -10,6 +10,8 @@
 #include "internal.h"
 
 #include <atomic>
+#include <mutex>
+#include <unordered_map>
 
 namespace dspark {
 
@@ -98,6 +100,40 @@ dspark_status_t check_chain_args(const void *logits, const void *w1, const void 
 
 size_t chain_ws_bytes(int B, int k, int V) { return kHeader + chain_workspace_size(B, k, V); }
 
+// Every kernel leaves its counters at zero, but where the counters sit depends on
+// the call's shape: a workspace reused for another shape can hold old partial sums
+// where the new shape keeps counters.  The layout each workspace was last used with
+// is remembered here; on a change, the new layout's counter regions are cleared on
+// the stream first.
+std::mutex g_layout_mutex;
+std::unordered_map<const void *, uint64_t> g_layout;
+
+uint64_t layout_signature(std::initializer_list<long long> v) {
+  uint64_t h = 1469598103934665603ull;  // FNV-1a over the values' bytes
+  for (long long x : v)
+    for (int i = 0; i < 8; ++i) {
+      h ^= static_cast<uint64_t>((x >> (8 * i)) & 0xff);
+      h *= 1099511628211ull;
+    }
+  return h;
+}
+
+struct ZeroRange {
+  size_t offset, bytes;
+};
+
+dspark_status_t prepare_workspace(void *ws, uint64_t sig, std::initializer_list<ZeroRange> ranges,
+                                  cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_layout_mutex);
+  auto it = g_layout.find(ws);
+  if (it != g_layout.end() && it->second == sig) return DSPARK_OK;
+  for (const ZeroRange &z : ranges)
+    if (z.bytes && cudaMemsetAsync(static_cast<char *>(ws) + z.offset, 0, z.bytes, s) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  g_layout[ws] = sig;
+  return DSPARK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -153,6 +189,9 @@ dspark_status_t dspark_fc_project(const dspark_bf16_t *const *taps, int T, int64
   dspark_status_t st = check_ws(ws, ws_bytes, dspark_fc_project_workspace_size(M, H, T));
   if (st != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({1, M, H, T}),
+                         {{0, kHeader + gemm_counter_bytes(M, H, T * H)}}, as_stream(stream));
+  if (st != DSPARK_OK) return st;
   GemmProblem p;
   memset(&p, 0, sizeof(p));
   p.w = fc_w;
@@ -201,6 +240,9 @@ dspark_status_t dspark_lm_head(const dspark_bf16_t *h, const dspark_bf16_t *lm_w
   if (st != DSPARK_OK) return st;
   if ((st = check_ws(ws, ws_bytes, dspark_lm_head_workspace_size(M, H, V))) != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({2, M, H, V}),
+                         {{0, kHeader + gemm_counter_bytes(M, V, H)}}, as_stream(stream));
+  if (st != DSPARK_OK) return st;
   return lm_head_enqueue(h, lm_w, logits, M, H, V, static_cast<char *>(ws) + kHeader,
                          ws_bytes - kHeader, status_word(ws), as_stream(stream));
 }
@@ -220,6 +262,9 @@ dspark_status_t dspark_greedy_sample(float *logits, const dspark_bf16_t *w1,
   if (st != DSPARK_OK) return st;
   if ((st = check_ws(ws, ws_bytes, chain_ws_bytes(B, k, V))) != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({3, B, k, V}), {{0, kHeader + chain_counter_bytes(k)}},
+                         as_stream(stream));
+  if (st != DSPARK_OK) return st;
   return chain_launch(logits, w1, w2, w1 ? r : 0, prev_token, draft_tokens, q_stats, nullptr, B,
                       k, V, static_cast<char *>(ws) + kHeader, status_word(ws), as_stream(stream));
 }
@@ -277,6 +322,11 @@ dspark_status_t dspark_draft_readout(const dspark_bf16_t *h, const dspark_bf16_t
   cudaStream_t s = as_stream(stream);
   char *base = static_cast<char *>(ws);
   const size_t gemm_bytes = align_up(gemm_workspace_size(M, V, H), kWsAlign);
+  st = prepare_workspace(ws, layout_signature({4, B, k, H, V}),
+                         {{0, kHeader + gemm_counter_bytes(M, V, H)},
+                          {kHeader + gemm_bytes, chain_counter_bytes(k)}},
+                         s);
+  if (st != DSPARK_OK) return st;
   st = lm_head_enqueue(h, lm_w, logits, M, H, V, base + kHeader, gemm_bytes, status_word(ws), s);
   if (st != DSPARK_OK) return st;
   st = chain_launch(logits, w1, w2, w1 ? r : 0, prev_token, draft_tokens, q_stats,
@@ -314,6 +364,9 @@ dspark_status_t dspark_verify(int mode, const float *target_logits, const int32_
   dspark_status_t st = check_ws(ws, ws_bytes, dspark_verify_workspace_size(B, k, V));
   if (st != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({5, B, k, V}), {{0, verify_counter_bytes(B, k, V)}},
+                         as_stream(stream));
+  if (st != DSPARK_OK) return st;
   return verify_launch(mode, target_logits, draft_tokens, draft_len, draft_logits, q_stats, seed,
                        request_id, step, accepted_len, next_token, B, k, V, ws, status_word(ws),
                        as_stream(stream));

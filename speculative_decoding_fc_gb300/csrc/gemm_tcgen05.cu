@@ -549,6 +549,12 @@ size_t partial_bytes(const Tiling &t) {
 
 }  // namespace
 
+size_t gemm_counter_bytes(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < kBK) return 0;
+  Tiling t = plan(M, N, K);
+  return align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
+}
+
 size_t gemm_workspace_size(int M, int N, int K) {
   if (M < 1 || N < 1 || K < kBK) return 0;
   Tiling t = plan(M, N, K);

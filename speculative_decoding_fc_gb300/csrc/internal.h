@@ -35,12 +35,15 @@ struct GemmProblem {
 };
 
 size_t gemm_workspace_size(int M, int N, int K);
+// Bytes at the start of a GEMM workspace holding counters that must start at zero.
+size_t gemm_counter_bytes(int M, int N, int K);
 // Enqueues the GEMM.  ws must hold gemm_workspace_size bytes (zeroed once).
 dspark_status_t gemm_launch(const GemmProblem &p, void *ws, size_t ws_bytes, int *status,
                             cudaStream_t stream);
 
 // ------------------------------------------------------------------ Markov chain
 size_t chain_workspace_size(int B, int k, int V);
+size_t chain_counter_bytes(int k);
 dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *w2, int r,
                              const int32_t *prev_token, int32_t *draft_tokens, float *q_stats,
                              int32_t *draft_len_fill, int B, int k, int V, void *ws,
@@ -51,6 +54,7 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
 
 // ------------------------------------------------------------------ verify
 size_t verify_workspace_size(int B, int k, int V);
+size_t verify_counter_bytes(int B, int k, int V);
 dspark_status_t verify_launch(int mode, const float *target, const int32_t *drafts,
                               const int32_t *draft_len, const float *zlog, const float *q_stats,
                               uint64_t seed, const uint32_t *request_id, uint32_t step,

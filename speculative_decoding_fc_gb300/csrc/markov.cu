@@ -665,6 +665,8 @@ size_t chain_flags_bytes(int k) {
   return align_up(static_cast<size_t>(k) * kMaxPGrid * sizeof(int), kWsAlign);
 }
 
+size_t chain_counter_bytes(int k) { return kWsAlign + chain_flags_bytes(k); }
+
 size_t chain_workspace_size(int B, int k, int V) {
   const int nchunks = (V + kChunk - 1) / kChunk;
   const size_t per_pos = static_cast<size_t>(B) * nchunks * sizeof(ChainPartial);

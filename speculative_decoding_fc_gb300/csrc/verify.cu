@@ -445,6 +445,8 @@ VerifyLayout layout(int B, int k, int V) {
 
 size_t verify_workspace_size(int B, int k, int V) { return layout(B, k, V).total; }
 
+size_t verify_counter_bytes(int B, int k, int V) { return layout(B, k, V).rows; }
+
 dspark_status_t verify_launch(int mode, const float *target, const int32_t *drafts,
                               const int32_t *draft_len, const float *zlog, const float *q_stats,
                               uint64_t seed, const uint32_t *request_id, uint32_t step,

@@ -294,3 +294,29 @@ def test_draft_readout_with_confidence_matches_oracle():
                 top = zrow.max()
                 assert top - zrow[gd[b, i]] <= 2 * (LOGIT_ATOL + LOGIT_RTOL * abs(top))
                 break
+
+
+def test_one_workspace_serves_calls_of_different_shapes():
+    """A workspace reused for another shape can hold old partial sums where the new
+    shape keeps its counters; results must not depend on the call history."""
+    wsp = ds.Workspaces()
+    H = 256
+    cases = [(7, 4096), (300, 777), (7, 20000), (33, 1000), (7, 4096)]
+    for M, V in cases:
+        h = syn.normal_bf16(M, (M, H))
+        w = syn.normal_bf16(V, (V, H), (1.0 / H) ** 0.5)
+        got = host(ds.lm_head(dev_bf16(h), dev_bf16(w), workspaces=wsp))
+        _assert_logits_close(got, oracle.lm_head(h, w))
+    for B, k, V in [(1, 7, 4096), (9, 3, 30000), (1, 16, 4096), (2, 7, 30000)]:
+        z, drafts, target = _verify_inputs(B, k, V, 300 + B * k)
+        ref = oracle.verify(0, target, drafts)
+        a, n = ds.verify(0, dev(target), dev(drafts), workspaces=wsp)
+        np.testing.assert_array_equal(host(a), ref["accepted_len"])
+        np.testing.assert_array_equal(host(n), ref["next_token"])
+        logits = syn.uniform_logits(400 + B, (B, k, V), 1.0)
+        w1 = syn.normal_bf16(5, (V, 16))
+        w2 = syn.normal_bf16(6, (V, 16), 0.25)
+        prev = np.arange(B, dtype=np.int32)
+        refc = oracle.greedy_sample(logits, w1, w2, prev)
+        d, _ = ds.greedy_sample(dev(logits), dev_bf16(w1), dev_bf16(w2), dev(prev), workspaces=wsp)
+        np.testing.assert_array_equal(host(d), refc["draft_tokens"])
