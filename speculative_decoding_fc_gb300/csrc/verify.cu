@@ -9,18 +9,22 @@
 // first rejection draw from max(0, p - q) normalised; after a fully accepted
 // block draw the bonus token from p.
 //
-// Pass 1 (verify_stats_kernel): one streaming read of every needed row
-// (target rows 0..draft_len, and the draft-logit rows when their softmax
-// statistics were not supplied) with 128-bit loads; each CTA reduces a
-// 4096-entry slice to (argmax key, max, sum exp).  The last CTA of a request
-// (atomic ticket) merges the slices in a fixed order and takes the
-// accept/reject decisions with Philox uniforms.
-// Pass 2 (verify_sample_kernel, probabilistic only): the one row per request
-// that needs a draw is re-read.  The draw is the Gumbel-max rule: the index
-// maximising log w_v + G_v, G_v = -log(-log U_v) with U_v from Philox counter
-// (request, row, step, 1 + v/4).  That samples exactly from w normalised and
-// makes the draw an argmax, reduced like every other argmax here (per-CTA
-// 64-bit keys, merged by the request's last CTA).
+// Phase 1 (row statistics): one streaming read of every needed row (target
+// rows 0..draft_len, and the draft-logit rows when their softmax statistics
+// were not supplied) with 128-bit loads; each CTA reduces a 4096-entry slice to
+// (argmax key, max, sum exp).
+// Decision: the slices of a request are merged in a fixed order, then the
+// accept/reject tests run with Philox uniforms.
+// Phase 2 (draw, probabilistic only): the one row per request that needs a draw
+// is re-read.  The draw is the Gumbel-max rule: the index maximising
+// log w_v + G_v, G_v = -log(-log U_v) with U_v from Philox counter (request,
+// row, step, 1 + v/4).  That samples exactly from w normalised and makes the
+// draw an argmax, reduced like every other argmax here (per-CTA 64-bit keys,
+// merged by the request's last CTA).
+//
+// verify_stats_kernel does phase 1 and its last CTA per request (atomic
+// ticket, nobody waits) takes the decisions; verify_sample_kernel does phase 2
+// and its last CTA per request merges the draw.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -92,93 +96,127 @@ __device__ __forceinline__ int request_len(const VerifyArgs &a, int b, bool reco
   return L;
 }
 
-// ------------------------------------------------------------------ pass 1
-__global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs a) {
-  __shared__ RowPartial red[kWarps];
-  __shared__ int is_last;
-  __shared__ unsigned long long tkey[kMaxK + 1];
-  __shared__ double tM[kMaxK + 1], tS[kMaxK + 1];
-  __shared__ double zM[kMaxK], zS[kMaxK];
+// ------------------------------------------------------------------ shared pieces
 
+// Row index rho -> (request, block row, draft-logit row?).
+struct RowRef {
+  int b, j;
+  bool is_z;
+};
+
+__device__ __forceinline__ RowRef row_ref(const VerifyArgs &a, int rho) {
+  const int trows = a.B * (a.k + 1);
+  RowRef r;
+  r.is_z = rho >= trows;
+  r.b = r.is_z ? (rho - trows) / a.k : rho / (a.k + 1);
+  r.j = r.is_z ? (rho - trows) - r.b * a.k : rho - r.b * (a.k + 1);
+  return r;
+}
+
+__device__ __forceinline__ bool row_needed(const VerifyArgs &a, const RowRef &r) {
+  const int L = request_len(a, r.b, false);
+  return r.is_z ? (a.mode == 1 && r.j < L) : (r.j <= L);
+}
+
+// (argmax key, max, sum exp) of one 4096-entry slice of row rho -> rows partial.
+// Block-wide; `red` is shared scratch of kWarps entries.
+__device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *red) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice
-  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
-  const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
   const int k = a.k, V = a.V;
-  const int trows = a.B * (k + 1);
-  const bool is_z = rho >= trows;
-  const int b = is_z ? (rho - trows) / k : rho / (k + 1);
-  const int j = is_z ? (rho - trows) - b * k : rho - b * (k + 1);
-  const int L = request_len(a, b, false);
-  const bool needed = is_z ? (a.mode == 1 && j < L) : (j <= L);
+  const RowRef rr = row_ref(a, rho);
   const bool want_stats = (a.mode == 1);
-
-  if (needed) {
-    const float *row = is_z ? a.zlog + (static_cast<long long>(b) * k + j) * V
-                            : a.target + (static_cast<long long>(b) * (k + 1) + j) * V;
-    const int base = slice * kSlice;
-    unsigned long long best = 0ull;
-    SoftStat st{-INFINITY, 0.0f};
-    if (a.vec) {
-      float4 q[kPer / 4];
+  const float *row = rr.is_z ? a.zlog + (static_cast<long long>(rr.b) * k + rr.j) * V
+                             : a.target + (static_cast<long long>(rr.b) * (k + 1) + rr.j) * V;
+  const int base = slice * kSlice;
+  // This thread's 16 entries, in ascending index order: the argmax by strict float
+  // compare (first index wins ties, -0 == +0, NaN never wins), then the max and the
+  // sum of exp(x - max) from registers.
+  float x[kPer];
+  int xi[kPer];
+  if (a.vec) {
 #pragma unroll
-      for (int it = 0; it < kPer / 4; ++it) {
-        const int v = base + it * (kThreads * 4) + tid * 4;
-        q[it] = v < V ? __ldcs(reinterpret_cast<const float4 *>(row + v))
-                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
+    for (int it = 0; it < kPer / 4; ++it) {
+      const int v = base + it * (kThreads * 4) + tid * 4;
+      const float4 q = v < V ? __ldcs(reinterpret_cast<const float4 *>(row + v))
+                             : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      x[4 * it] = q.x; x[4 * it + 1] = q.y; x[4 * it + 2] = q.z; x[4 * it + 3] = q.w;
 #pragma unroll
-      for (int it = 0; it < kPer / 4; ++it) {
-        const int v = base + it * (kThreads * 4) + tid * 4;
-        if (v < V) {
-          const float x[4] = {q[it].x, q[it].y, q[it].z, q[it].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const unsigned long long key = argmax_key(x[e], static_cast<uint32_t>(v + e));
-            best = key > best ? key : best;
-            if (want_stats) softstat_add(st, x[e]);
-          }
-        }
-      }
-    } else {
-#pragma unroll 4
-      for (int it = 0; it < kPer; ++it) {
-        const int v = base + it * kThreads + tid;
-        if (v < V) {
-          const float x = __ldcs(row + v);
-          const unsigned long long key = argmax_key(x, static_cast<uint32_t>(v));
-          best = key > best ? key : best;
-          if (want_stats) softstat_add(st, x);
-        }
-      }
+      for (int e = 0; e < 4; ++e) xi[4 * it + e] = v + e;
     }
-    best = warp_max_u64(best);
-    if (want_stats) st = warp_softstat(st);
-    if (lane == 0) red[warp] = RowPartial{best, st.m, st.s};
-    __syncthreads();
-    if (tid == 0) {
-      RowPartial acc = red[0];
-      SoftStat sacc{acc.m, acc.s};
-      for (int w = 1; w < kWarps; ++w) {
-        acc.key = red[w].key > acc.key ? red[w].key : acc.key;
-        sacc = softstat_merge(sacc, SoftStat{red[w].m, red[w].s});
-      }
-      acc.m = sacc.m;
-      acc.s = sacc.s;
-      a.rows[static_cast<long long>(rho) * a.nslices + slice] = acc;
+  } else {
+#pragma unroll
+    for (int it = 0; it < kPer; ++it) {
+      const int v = base + it * kThreads + tid;
+      x[it] = v < V ? __ldcs(row + v) : -INFINITY;
+      xi[it] = v;
     }
   }
-
-  __threadfence();
+  float bv = -INFINITY;
+  int bi = -1;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    if (xi[e] < V && x[e] > bv) {
+      bv = x[e];
+      bi = xi[e];
+    }
+  }
+  unsigned long long best = bi >= 0 ? argmax_key(bv, static_cast<uint32_t>(bi))
+                                    : (xi[0] < V ? argmax_key(-INFINITY, static_cast<uint32_t>(xi[0])) : 0ull);
+  SoftStat st{-INFINITY, 0.0f};
+  if (want_stats && bi >= 0 && bv != INFINITY) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if (xi[e] < V && x[e] == x[e] && x[e] != -INFINITY) sum += __expf(x[e] - bv);
+    st = SoftStat{bv, sum};
+  }
+  best = warp_max_u64(best);
+  if (want_stats) {
+    // warp (max, sum): the max first, then the sum of s * exp(m - max)
+    float mm = st.m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    float ss = (st.m == -INFINITY) ? 0.0f : st.s * __expf(st.m - mm);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    st = SoftStat{mm, ss};
+  }
+  if (lane == 0) red[warp] = RowPartial{best, st.m, st.s};
   __syncthreads();
-  const int rows_per_req = (k + 1) + (a.zrows ? k : 0);
-  if (tid == 0)
-    is_last = (atomicAdd(&a.req_ticket[b], 1) == rows_per_req * a.nslices - 1) ? 1 : 0;
+  if (tid == 0) {
+    RowPartial acc = red[0];
+    SoftStat sacc{acc.m, acc.s};
+    for (int w = 1; w < kWarps; ++w) {
+      acc.key = red[w].key > acc.key ? red[w].key : acc.key;
+      sacc = softstat_merge(sacc, SoftStat{red[w].m, red[w].s});
+    }
+    acc.m = sacc.m;
+    acc.s = sacc.s;
+    a.rows[static_cast<long long>(rho) * a.nslices + slice] = acc;
+  }
   __syncthreads();
-  if (!is_last) return;
-  __threadfence();
+}
 
-  // ---------------------------------------------------------------- merge rows of request b
+// Decision state of one request, in shared memory.
+struct Decision {
+  unsigned long long tkey[kMaxK + 1];
+  double tM[kMaxK + 1], tS[kMaxK + 1];
+  double zM[kMaxK], zS[kMaxK];
+  double ratio[kMaxK], ua[kMaxK];
+  int bad[kMaxK];
+  SampleJob job;
+  int acc_len;
+  int next;  // greedy: the next token
+};
+
+// Merges the row partials of request b and takes its decisions (block-wide).
+// Greedy: acc_len and next.  Probabilistic: acc_len and the draw job.
+__device__ void decide_request(const VerifyArgs &a, int b, Decision &d, bool record) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int k = a.k, V = a.V;
+  const int trows = a.B * (k + 1);
+  const int L = request_len(a, b, record);
+  const bool want_stats = (a.mode == 1);
   const int n_t = L + 1;
   const int n_z = a.zrows ? L : 0;
   for (int q = warp; q < n_t + n_z; q += kWarps) {
@@ -186,35 +224,45 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
     const int jj = qz ? q - n_t : q;
     const int r_idx = qz ? trows + b * k + jj : b * (k + 1) + jj;
     const RowPartial *pr = a.rows + static_cast<long long>(r_idx) * a.nslices;
+    // one pass: each lane merges its slices online (fp64 sums), then the warp
     unsigned long long kb = 0ull;
     float mm = -INFINITY;
+    double s = 0.0;
     for (int c = lane; c < a.nslices; c += 32) {
       const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
       kb = raw.x > kb ? raw.x : kb;
-      mm = fmaxf(mm, __uint_as_float(static_cast<uint32_t>(raw.y)));
+      const float cm = __uint_as_float(static_cast<uint32_t>(raw.y));
+      const float cs = __uint_as_float(static_cast<uint32_t>(raw.y >> 32));
+      if (want_stats && cm != -INFINITY) {
+        if (cm > mm) {
+          s = (mm == -INFINITY) ? static_cast<double>(cs)
+                                : s * static_cast<double>(expf(mm - cm)) + static_cast<double>(cs);
+          mm = cm;
+        } else {
+          s += static_cast<double>(cs) * static_cast<double>(expf(cm - mm));
+        }
+      } else if (!want_stats) {
+        mm = fmaxf(mm, cm);
+      }
     }
     kb = warp_max_u64(kb);
+    float wm = mm;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-    double s = 0.0;
-    if (want_stats && mm != -INFINITY) {
-      for (int c = lane; c < a.nslices; c += 32) {
-        const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
-        const float cm = __uint_as_float(static_cast<uint32_t>(raw.y));
-        const float cs = __uint_as_float(static_cast<uint32_t>(raw.y >> 32));
-        if (cm != -INFINITY) s += static_cast<double>(cs) * static_cast<double>(expf(cm - mm));
-      }
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+    if (want_stats) {
+      s = (mm == -INFINITY) ? 0.0 : s * static_cast<double>(expf(mm - wm));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     }
+    mm = wm;
     if (lane == 0) {
       if (qz) {
-        zM[jj] = mm;
-        zS[jj] = s;
+        d.zM[jj] = mm;
+        d.zS[jj] = s;
       } else {
-        tkey[jj] = kb;
-        tM[jj] = mm;
-        tS[jj] = s;
+        d.tkey[jj] = kb;
+        d.tM[jj] = mm;
+        d.tS[jj] = s;
       }
     }
   }
@@ -222,43 +270,41 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
 
   // Probabilistic: every position's ratio p(d)/q(d) and accept uniform, in parallel
   // (thread j takes position j); the sequential accept loop below only compares.
-  __shared__ double ratio_s[kMaxK], ua_s[kMaxK];
-  __shared__ int bad_s[kMaxK];
+  const long long drow = static_cast<long long>(b) * k;
   if (a.mode == 1 && tid < L) {
     const int jj = tid;
-    const long long drow = static_cast<long long>(b) * k;
     const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
-    const int d = a.drafts[drow + jj];
+    const int dt = a.drafts[drow + jj];
     double ua, us;
     verify_uniforms(a.seed, req, static_cast<uint32_t>(jj), a.step, ua, us);
-    ua_s[jj] = ua;
-    bad_s[jj] = (d < 0 || d >= V) ? 1 : 0;
+    d.ua[jj] = ua;
+    d.bad[jj] = (dt < 0 || dt >= V) ? 1 : 0;
     double ratio = 0.0;
-    if (!bad_s[jj]) {
-      const double tT = a.target[(static_cast<long long>(b) * (k + 1) + jj) * V + d];
-      const double pd = exp(tT - tM[jj]) / tS[jj];
-      double qd = 1.0;
+    if (!d.bad[jj]) {
+      // p(d)/q(d) = exp((T_d - M) - (z_d - m)) * s / S: the exponent is formed
+      // exactly in fp64, the exponential in fp32 (relative error ~1e-7)
+      const double tT = a.target[(static_cast<long long>(b) * (k + 1) + jj) * V + dt];
+      double ex = tT - d.tM[jj], sc = 1.0 / d.tS[jj];
       if (a.zlog) {
-        const double qm = a.zrows ? zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
-        const double qs = a.zrows ? zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
-        const double zd = a.zlog[(drow + jj) * V + d];
-        qd = exp(zd - qm) / qs;
+        const double qm = a.zrows ? d.zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
+        const double qs = a.zrows ? d.zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
+        const double zd = a.zlog[(drow + jj) * V + dt];
+        ex -= zd - qm;
+        sc *= qs;
       }
-      ratio = pd / qd;
+      ratio = static_cast<double>(expf(static_cast<float>(ex))) * sc;
     }
-    ratio_s[jj] = ratio;
+    d.ratio[jj] = ratio;
   }
   __syncthreads();
 
   if (tid == 0) {
-    const long long drow = static_cast<long long>(b) * k;
     int acc_len = 0;
     if (a.mode == 0) {
       while (acc_len < L &&
-             a.drafts[drow + acc_len] == static_cast<int32_t>(key_index(tkey[acc_len])))
+             a.drafts[drow + acc_len] == static_cast<int32_t>(key_index(d.tkey[acc_len])))
         ++acc_len;
-      a.accepted_len[b] = acc_len;
-      a.next_token[b] = static_cast<int32_t>(key_index(tkey[acc_len]));
+      d.next = static_cast<int32_t>(key_index(d.tkey[acc_len]));
     } else {
       SampleJob job;
       job.kind = kNone;
@@ -267,57 +313,55 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
       job.cq = 0.0;
       for (; acc_len < L; ++acc_len) {
         const int jj = acc_len;
-        if (bad_s[jj]) {
-          record_error(a.status, DSPARK_ERR_BAD_TOKEN);
+        if (d.bad[jj]) {
+          if (record) record_error(a.status, DSPARK_ERR_BAD_TOKEN);
           job.row = jj;
           job.kind = kFromP;
-          job.cp = tM[jj] + log(tS[jj]);
+          job.cp = d.tM[jj] + log(d.tS[jj]);
           break;
         }
-        if (ua_s[jj] < ratio_s[jj]) continue;
-        const int d = a.drafts[drow + jj];
+        if (d.ua[jj] < d.ratio[jj]) continue;
         double qm = 0.0, qs = 1.0;
         if (a.zlog) {
-          qm = a.zrows ? zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
-          qs = a.zrows ? zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
+          qm = a.zrows ? d.zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
+          qs = a.zrows ? d.zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
         }
         job.row = jj;
         job.kind = a.zlog ? kResidual : kResidualOneHot;
-        job.d = d;
-        job.cp = tM[jj] + log(tS[jj]);
+        job.d = a.drafts[drow + jj];
+        job.cp = d.tM[jj] + log(d.tS[jj]);
         job.cq = qm + log(qs);
         break;
       }
       if (job.kind == kNone) {
         job.row = L;
         job.kind = kFromP;
-        job.cp = tM[L] + log(tS[L]);
+        job.cp = d.tM[L] + log(d.tS[L]);
       }
-      a.accepted_len[b] = acc_len;
-      a.jobs[b] = job;
+      d.job = job;
     }
-    a.req_ticket[b] = 0;
+    d.acc_len = acc_len;
   }
+  __syncthreads();
 }
 
-// ------------------------------------------------------------------ pass 2
 // Noise of entry v of a draw at block row `row`: Philox4x32-10 counter
 // (request, row, step, 1 + v/4), word v mod 4; U = (2 (w >> 9) + 1) 2^-24 is an
 // odd multiple of 2^-24, exact in fp32 and strictly inside (0, 1).
+// The inner logarithm is the accurate one (-log u is tiny when u is near 1,
+// where an approximate log would lose all relative precision); the outer one is
+// the fast intrinsic (absolute error ~2^-21 relative to |G| + 1).
 __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
   const float u = static_cast<float>(2u * (w >> 9) + 1u) * (1.0f / 16777216.0f);
-  return -logf(-logf(u));
+  return -__logf(-logf(u));
 }
 
-__global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArgs a) {
-  __shared__ unsigned long long red_r[kWarps], red_p[kWarps];
-  __shared__ int is_last;
-
+// Gumbel-max keys of one 1024-entry slice of the draw row of request b ->
+// draw partial (block-wide).  `red_r`, `red_p` are shared scratch of kWarps.
+__device__ void draw_item(const VerifyArgs &a, const SampleJob &job, int b, int slice,
+                          unsigned long long *red_r, unsigned long long *red_p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.ndraw));
-  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.ndraw));
   const int k = a.k, V = a.V;
-  const SampleJob job = a.jobs[b];
   const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
   const uint32_t k0 = static_cast<uint32_t>(a.seed & 0xffffffffull);
   const uint32_t k1 = static_cast<uint32_t>(a.seed >> 32);
@@ -389,32 +433,76 @@ __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArg
     }
     a.sparts[static_cast<long long>(b) * a.ndraw + slice] = SamplePartial{br, bp};
   }
-
-  __threadfence();
   __syncthreads();
-  if (tid == 0) is_last = (atomicAdd(&a.samp_ticket[b], 1) == a.ndraw - 1) ? 1 : 0;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
+}
 
-  if (warp == 0) {
-    const SamplePartial *sp = a.sparts + static_cast<long long>(b) * a.ndraw;
-    unsigned long long br = 0ull, bp = 0ull;
-    for (int c = lane; c < a.ndraw; c += 32) {
-      const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(sp + c));
-      br = raw.x > br ? raw.x : br;
-      bp = raw.y > bp ? raw.y : bp;
-    }
-    br = warp_max_u64(br);
-    bp = warp_max_u64(bp);
-    if (lane == 0) {
-      // The residual is empty only if p <= q everywhere (then draw from p).
-      const float vr = key_value(br);
-      const bool has_r = br != 0ull && vr != -INFINITY && vr == vr;
-      a.next_token[b] = static_cast<int32_t>(key_index(has_r ? br : bp));
-      a.samp_ticket[b] = 0;
-    }
+// Warp 0 merges the draw partials of request b and stores the next token.
+__device__ void finish_draw(const VerifyArgs &a, int b) {
+  const int lane = threadIdx.x & 31;
+  const SamplePartial *sp = a.sparts + static_cast<long long>(b) * a.ndraw;
+  unsigned long long br = 0ull, bp = 0ull;
+  for (int c = lane; c < a.ndraw; c += 32) {
+    const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(sp + c));
+    br = raw.x > br ? raw.x : br;
+    bp = raw.y > bp ? raw.y : bp;
   }
+  br = warp_max_u64(br);
+  bp = warp_max_u64(bp);
+  if (lane == 0) {
+    // The residual is empty only if p <= q everywhere (then draw from p).
+    const float vr = key_value(br);
+    const bool has_r = br != 0ull && vr != -INFINITY && vr == vr;
+    a.next_token[b] = static_cast<int32_t>(key_index(has_r ? br : bp));
+  }
+}
+
+// Atomic ticket of request b in `tickets`: true for the CTA that arrives last
+// (of `count`), which then resets the ticket.  Block-wide.
+__device__ __forceinline__ bool last_arrival(int *tickets, int b, int count, int *flag_s) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool last = atomicAdd(&tickets[b], 1) == count - 1;
+    if (last) tickets[b] = 0;
+    *flag_s = last ? 1 : 0;
+  }
+  __syncthreads();
+  const bool last = *flag_s != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// ------------------------------------------------------------------ two-launch path
+__global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs a) {
+  __shared__ RowPartial red[kWarps];
+  __shared__ int flag_s;
+  __shared__ Decision dec;
+  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice
+  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
+  const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
+  const RowRef rr = row_ref(a, rho);
+  if (row_needed(a, rr)) stats_item(a, rho, slice, red);
+  const int rows_per_req = (a.k + 1) + (a.zrows ? a.k : 0);
+  if (!last_arrival(a.req_ticket, rr.b, rows_per_req * a.nslices, &flag_s)) return;
+  decide_request(a, rr.b, dec, true);
+  if (threadIdx.x == 0) {
+    a.accepted_len[rr.b] = dec.acc_len;
+    if (a.mode == 0)
+      a.next_token[rr.b] = dec.next;
+    else
+      a.jobs[rr.b] = dec.job;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArgs a) {
+  __shared__ unsigned long long red_r[kWarps], red_p[kWarps];
+  __shared__ int flag_s;
+  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.ndraw));
+  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.ndraw));
+  const SampleJob job = a.jobs[b];
+  draw_item(a, job, b, slice, red_r, red_p);
+  if (!last_arrival(a.samp_ticket, b, a.ndraw, &flag_s)) return;
+  if (threadIdx.x < 32) finish_draw(a, b);
 }
 
 struct VerifyLayout {
@@ -484,7 +572,7 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
               : 0;
   const long long nrows = static_cast<long long>(B) * (k + 1) + (a.zrows ? static_cast<long long>(B) * k : 0);
   const long long g1 = nrows * L.nslices;
-  if (g1 > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+
   verify_stats_kernel<<<static_cast<unsigned>(g1), kThreads, 0, stream>>>(a);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   count_launches(1);
