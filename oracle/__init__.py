@@ -52,6 +52,18 @@ def lib():
         L.oracle_verify.argtypes = [ctypes.c_int, _f32p, _i32p, _i32p, _f32p, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, _u32p,
                                     ctypes.c_uint32, _i32p, _i32p, _f64p, _f64p, _i32p]
+        L.oracle_f32_to_bf16_n.argtypes = [_f32p, ctypes.c_int64, _u16p]
+        L.oracle_e4m3_to_f32.restype = ctypes.c_float
+        L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        L.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.oracle_quantize_fp8_rows.restype = ctypes.c_int
+        L.oracle_quantize_fp8_rows.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                               ctypes.POINTER(ctypes.c_uint8), _f32p]
+        L.oracle_gemm_fp8.restype = ctypes.c_int
+        L.oracle_gemm_fp8.argtypes = [ctypes.POINTER(ctypes.c_uint8), _f32p, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_uint8), _f32p, ctypes.c_int64,
+                                      ctypes.c_int, _f32p]
         _lib = L
     return _lib
 
@@ -232,3 +244,66 @@ def step(inputs, B, k, mode, target, seed=0, step=0, conf=None):
     out.update(verify(mode, target, out["draft_tokens"], out["draft_len"],
                       out["z"] if mode == 1 else None, seed=seed, step=step))
     return out
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) weights
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+
+def f32_to_e4m3(x):
+    x = np.asarray(x, dtype=np.float32)
+    f = lib().oracle_f32_to_e4m3
+    return np.array([f(float(v)) for v in x.reshape(-1)], dtype=np.uint8).reshape(x.shape)
+
+
+def e4m3_to_f32(codes):
+    codes = np.asarray(codes, dtype=np.uint8)
+    f = lib().oracle_e4m3_to_f32
+    return np.array([f(int(c)) for c in codes.reshape(-1)], dtype=np.float32).reshape(codes.shape)
+
+
+def quantize_fp8_rows(x):
+    """bf16 bits [R, C] -> (E4M3 codes uint8 [R, C], fp32 scales [R])."""
+    x = _c(x, np.uint16)
+    R, C = x.shape
+    codes = np.empty((R, C), dtype=np.uint8)
+    scales = np.empty((R,), dtype=np.float32)
+    _check(lib().oracle_quantize_fp8_rows(_p(x, _u16p), R, C, C, _p(codes, _u8p), _p(scales, _f32p)),
+           "oracle_quantize_fp8_rows")
+    return codes, scales
+
+
+def gemm_fp8(a, a_scale, w, w_scale):
+    """fp32 [M, N] = a_scale[m] * w_scale[n] * sum_k e4m3(a[m,k]) * e4m3(w[n,k])."""
+    a = _c(a, np.uint8)
+    w = _c(w, np.uint8)
+    a_scale = _c(np.asarray(a_scale, np.float32), np.float32)
+    w_scale = _c(np.asarray(w_scale, np.float32), np.float32)
+    M, K = a.shape
+    N = w.shape[0]
+    assert w.shape[1] == K
+    out = np.empty((M, N), dtype=np.float32)
+    _check(lib().oracle_gemm_fp8(_p(a, _u8p), _p(a_scale, _f32p), M, _p(w, _u8p), _p(w_scale, _f32p),
+                                 N, K, _p(out, _f32p)), "oracle_gemm_fp8")
+    return out
+
+
+def f32_to_bf16_array(x):
+    """bf16 rounding (ties to even) of a whole fp32 array, in C."""
+    x = _c(np.asarray(x, np.float32), np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_f32_to_bf16_n(_p(x, _f32p), x.size, _p(out, _u16p))
+    return out
+
+
+def fc_project_fp8(taps, fc_w8, fc_scale):
+    """FP8 fc: the concatenated taps are quantised per row; h = bf16(gemm)."""
+    x = np.concatenate([_c(t, np.uint16) for t in taps], axis=1)
+    a8, a_s = quantize_fp8_rows(x)
+    return f32_to_bf16_array(gemm_fp8(a8, a_s, fc_w8, fc_scale))
+
+
+def lm_head_fp8(h, lm_w8, lm_scale):
+    """FP8 LM head: h (bf16 bits [M, H]) quantised per row -> fp32 logits [M, V]."""
+    a8, a_s = quantize_fp8_rows(h)
+    return gemm_fp8(a8, a_s, lm_w8, lm_scale)

@@ -532,3 +532,91 @@ int oracle_verify(int mode, const float *target, const int32_t *drafts,
     }
     return status;
 }
+
+/* ------------------------------------------------------------------ */
+/* FP8 drafter weights (E4M3, per-row scales)                          */
+/* ------------------------------------------------------------------ */
+/*
+ * [PR620] / [CARD]: the drafters are FP8 checkpoints ("drafter-fp8-v5",
+ * "qwen3.8-27b-dflash-drafter-fp8-b70").  The pages do not give the scheme;
+ * the reading taken is the common W8A8 one: E4M3 codes (OCP FP8: 1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, no infinity, largest finite
+ * 448), one fp32 scale per weight output row and one per activation row,
+ * scale = amax / 448 (1 for an all-zero row), code = E4M3(x / scale) rounded
+ * to nearest even and saturated to +-448.
+ */
+
+/* E4M3 value of a code. */
+float oracle_e4m3_to_f32(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 0xF && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (float)(s ? -v : v);
+}
+
+/* Nearest E4M3 code (ties to even), saturating beyond +-448. */
+uint8_t oracle_f32_to_e4m3(float x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t s = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a > 448.0) return s | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormals: multiples of 2^-9 */
+        double q = nearbyint(a * 512.0);     /* exact scaling; default rounding: to even */
+        if (q >= 8.0) return s | 0x08;       /* rounds up to the smallest normal */
+        return s | (uint8_t)q;
+    }
+    int e;
+    double f = frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                  /* a = (2f) * 2^e, 2f in [1, 2) */
+    double q = nearbyint((2.0 * f - 1.0) * 8.0);
+    if (q >= 8.0) { q = 0.0; e += 1; }
+    int E = e + 7;
+    if (E > 15 || (E == 15 && q > 6.0)) return s | 0x7E;
+    return s | (uint8_t)((E << 3) | (int)q);
+}
+
+/* Per-row quantisation of a bf16 matrix [R, C] (row stride ld). */
+int oracle_quantize_fp8_rows(const uint16_t *x, int R, int C, int64_t ld, uint8_t *codes,
+                             float *scales) {
+    if (R < 0 || C < 1 || ld < C || !x || !codes || !scales) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < R; ++r) {
+        const uint16_t *row = x + (int64_t)r * ld;
+        float amax = 0.0f;
+        for (int c = 0; c < C; ++c) {
+            float v = fabsf(bf16_bits_to_float(row[c]));
+            if (v > amax) amax = v;
+        }
+        float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scales[r] = scale;
+        for (int c = 0; c < C; ++c)
+            codes[(int64_t)r * C + c] = oracle_f32_to_e4m3(bf16_bits_to_float(row[c]) / scale);
+    }
+    return ORACLE_OK;
+}
+
+/* out[m, n] = a_scale[m] * w_scale[n] * sum_k E4M3(a[m,k]) * E4M3(w[n,k]) (fp64 sum,
+ * rounded once to fp32).  a: [M, K] codes, w: [N, K] codes. */
+int oracle_gemm_fp8(const uint8_t *a, const float *a_scale, int M, const uint8_t *w,
+                    const float *w_scale, int64_t N, int K, float *out) {
+    if (M < 0 || N < 1 || K < 1 || !a || !a_scale || !w || !w_scale || !out) return ORACLE_ERR_ARG;
+    double lut[256];
+    for (int c = 0; c < 256; ++c) lut[c] = (double)oracle_e4m3_to_f32((uint8_t)c);
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t *wrow = w + n * K;
+        for (int m = 0; m < M; ++m) {
+            const uint8_t *arow = a + (int64_t)m * K;
+            double acc = 0.0;
+            for (int c = 0; c < K; ++c) acc += lut[arow[c]] * lut[wrow[c]];
+            out[(int64_t)m * N + n] = (float)(acc * (double)a_scale[m] * (double)w_scale[n]);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Element-wise bf16 rounding of an fp32 array (as oracle_f32_to_bf16). */
+void oracle_f32_to_bf16_n(const float *x, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(x[i]);
+}

@@ -399,3 +399,62 @@ def test_gumbel_draw_distribution_large_vocab():
     assert np.all(out["accepted_len"] == 0) and np.all(out["sample_row"] == 0)
     assert _chi2_pvalue(np.bincount(out["next_token"], minlength=V), p) > 1e-3
     assert np.nanmin(out["sample_margin"]) > -1.0
+
+
+# --------------------------------------------------------------------------- FP8 (E4M3)
+
+
+def test_e4m3_codes_match_torch_float8_cast():
+    """E4M3 rounding (ties to even) against torch's float8_e4m3fn cast (a library routine)
+    over the whole finite range, every code's decode, and saturation beyond 448 (torch
+    maps overflow to NaN; the oracle saturates, as cvt.satfinite does)."""
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-460, 460, 20000), rng.standard_normal(20000) * 1e-2,
+                        rng.standard_normal(5000) * 3e-3,
+                        # exact ties between neighbouring codes
+                        (np.arange(1, 40) + 0.5) * 2.0 ** -9, 1.0 + (np.arange(8) + 0.5) / 8.0,
+                        [0.0, -0.0, 448.0, -448.0, 2.0 ** -6, 2.0 ** -9]]).astype(np.float32)
+    ours = oracle.f32_to_e4m3(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    inr = np.abs(x) <= 448
+    np.testing.assert_array_equal(ours[inr], ref[inr])
+    codes = np.arange(256, dtype=np.uint8)
+    dec = oracle.e4m3_to_f32(codes)
+    tdec = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    np.testing.assert_array_equal(np.isnan(dec), np.isnan(tdec))
+    np.testing.assert_array_equal(dec[~np.isnan(dec)], tdec[~np.isnan(tdec)])
+    assert oracle.f32_to_e4m3(np.array([464.0, 1e6, -5000.0], np.float32)).tolist() == [0x7E, 0x7E, 0xFE]
+
+
+def test_fp8_row_quantisation_closed_form():
+    """scale = amax / 448; the row maximum maps to code 0x7E (448); all-zero rows use
+    scale 1; codes are the E4M3 rounding of x / scale."""
+    x = np.array([[1.0, -2.0, 0.5, 0.0], [0.0, 0.0, 0.0, 0.0], [3.0, 3.0, -3.0, 1e-3]], np.float32)
+    codes, scales = oracle.quantize_fp8_rows(syn.to_bf16_bits(x))
+    xb = syn.bf16_bits_to_f32(syn.to_bf16_bits(x))
+    np.testing.assert_array_equal(scales, [np.float32(2.0) / np.float32(448.0), 1.0,
+                                           np.float32(3.0) / np.float32(448.0)])
+    assert codes[0, 1] == 0xFE and codes[2, 0] == 0x7E and codes[2, 2] == 0xFE
+    np.testing.assert_array_equal(codes[1], 0)
+    for r in range(3):
+        np.testing.assert_array_equal(codes[r], oracle.f32_to_e4m3(xb[r] / scales[r]))
+
+
+def test_fp8_gemm_matches_numpy_on_decoded_operands():
+    """The FP8 GEMM is the fp64 dot product of the decoded codes times both scales:
+    numpy float64 matmul of torch-decoded operands (library routines)."""
+    M, N, K = 5, 33, 256
+    a = np.random.default_rng(1).integers(0, 256, (M, K), dtype=np.uint8)
+    w = np.random.default_rng(2).integers(0, 256, (N, K), dtype=np.uint8)
+    a[(a & 0x7F) == 0x7F] = 0
+    w[(w & 0x7F) == 0x7F] = 0
+    sa = np.random.default_rng(3).uniform(0.5, 2, M).astype(np.float32)
+    sw = np.random.default_rng(4).uniform(0.5, 2, N).astype(np.float32)
+    dec = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).double().numpy()
+    ref = (dec(a) @ dec(w).T) * sa[:, None].astype(np.float64) * sw[None, :].astype(np.float64)
+    np.testing.assert_allclose(oracle.gemm_fp8(a, sa, w, sw), ref.astype(np.float32), rtol=2e-7, atol=1e-30)
+
+
+def test_bf16_array_rounding_matches_torch():
+    x = np.random.default_rng(9).standard_normal(5000).astype(np.float32) * 7
+    np.testing.assert_array_equal(oracle.f32_to_bf16_array(x), syn.to_bf16_bits(x))
