@@ -134,8 +134,14 @@ def step_bytes(cfg, mode):
     logits written once, the target logits read, one resample row pair per request."""
     B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
     M = B * k
-    fc = H * T * H * 2 + T * M * H * 2 + M * H * 2
-    lm = V * H * 2 + M * H * 2 + M * V * 4
+    if cfg.get("fp8"):
+        # E4M3 weights + fp32 row scales; the activation rows are read as bf16, their codes
+        # written and read back once, their scales are negligible
+        fc = H * T * H + H * 4 + T * M * H * 2 + 2 * T * M * H + M * H * 2
+        lm = V * H + V * 4 + M * H * 2 + 2 * M * H + M * V * 4
+    else:
+        fc = H * T * H * 2 + T * M * H * 2 + M * H * 2
+        lm = V * H * 2 + M * H * 2 + M * V * 4
     chain = V * r * 2
     verify = B * (k + 1) * V * 4 + (B * 2 * V * 4 if mode == 1 else 0)
     return {"fc": fc, "lm_head": lm, "chain": chain, "verify": verify,
@@ -210,9 +216,15 @@ def oracle_sample_step(ora, host, cfg, mode, frac, step):
     nh = max(1, int(round(frac * H)))
     nv = max(8, int(round(frac * V)))
     t0 = time.perf_counter()
-    ora.fc_project(host["taps"], host["fc_w"][:nh])  # fc over nh output columns
+    if cfg.get("fp8"):
+        ora.fc_project_fp8(host["taps"], host["fc_w8"][:nh], host["fc_s"][:nh])
+    else:
+        ora.fc_project(host["taps"], host["fc_w"][:nh])  # fc over nh output columns
     t1 = time.perf_counter()
-    logits = ora.lm_head(host["h"], host["lm_w"][:nv]).reshape(B, k, nv)
+    if cfg.get("fp8"):
+        logits = ora.lm_head_fp8(host["h"], host["lm_w8"][:nv], host["lm_s"][:nv]).reshape(B, k, nv)
+    else:
+        logits = ora.lm_head(host["h"], host["lm_w"][:nv]).reshape(B, k, nv)
     prev = (host["prev"] % nv).astype(np.int32)
     gs = ora.greedy_sample(logits, host["w1"][:nv], host["w2"][:nv], prev)
     tgt = np.ascontiguousarray(host["target"][:, :, :nv])
@@ -255,12 +267,27 @@ def host_workload(cfg):
     B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
     w = syn.weights(H, T, V, r, with_conf=cfg["conf"])
     st = syn.step_inputs(0, B, k, H, T, V, cfg["sigma"])
-    h = ora.fc_project(st["taps"], w["fc_w"])
     # target logits: the oracle's own draft logits (on the vocabulary) plus noise
     host = {"taps": st["taps"], "fc_w": w["fc_w"], "lm_w": w["lm_w"], "w1": w["w1"],
-            "w2": w["w2"], "prev": st["prev"], "h": h}
+            "w2": w["w2"], "prev": st["prev"]}
+    add_host_fp8(ora, host, cfg)
+    host["h"] = oracle_h(ora, host, cfg)
     host["target"] = st["noise"]  # noise alone stands in: the cost does not depend on values
     return host
+
+
+def add_host_fp8(ora, host, cfg):
+    """FP8 workloads: the oracle's own E4M3 codes and row scales of the fc and LM-head
+    weights (the bf16 copies are then dropped)."""
+    if cfg.get("fp8"):
+        host["fc_w8"], host["fc_s"] = ora.quantize_fp8_rows(host.pop("fc_w"))
+        host["lm_w8"], host["lm_s"] = ora.quantize_fp8_rows(host.pop("lm_w"))
+
+
+def oracle_h(ora, host, cfg):
+    if cfg.get("fp8"):
+        return ora.fc_project_fp8(host["taps"], host["fc_w8"], host["fc_s"])
+    return ora.fc_project(host["taps"], host["fc_w"])
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -325,6 +352,23 @@ def run_ours(args, rank, local_rank, world):
     conf_w = d16(w["conf_w"]) if cfg["conf"] else None
     host_w = w if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     del w
+    fp8 = bool(cfg.get("fp8"))
+    if fp8:
+        # weights quantised once (E4M3 codes + row scales); the bf16 copies are dropped
+        fc_w8, fc_s = ds.quantize_fp8(fc_w)
+        lm_w8, lm_s = ds.quantize_fp8(lm_w)
+        torch.cuda.synchronize()
+        del fc_w, lm_w
+
+    def fc_call(taps, **kw):
+        if fp8:
+            return ds.fc_project_fp8(taps, fc_w8, fc_s, **kw)
+        return ds.fc_project(taps, fc_w, **kw)
+
+    def lm_call(h, **kw):
+        if fp8:
+            return ds.lm_head_fp8(h, lm_w8, lm_s, **kw)
+        return ds.lm_head(h, lm_w, **kw)
 
     # input sets: taps, prev, target logits = own draft logits + noise (built once)
     sets = []
@@ -332,8 +376,8 @@ def run_ours(args, rank, local_rank, world):
         st = syn.step_inputs(replica_step_seed(s, rank), B, k, H, T, V, cfg["sigma"])
         taps = [d16(t) for t in st["taps"]]
         prev = torch.from_numpy(st["prev"]).to(device)
-        h = ds.fc_project(taps, fc_w)
-        logits = ds.lm_head(h, lm_w).view(B, k, V)
+        h = fc_call(taps)
+        logits = lm_call(h).view(B, k, V)
         ds.greedy_sample(logits, w1, w2, prev)
         noise = torch.from_numpy(st["noise"]).to(device)
         target = torch.cat([logits, logits[:, -1:]], dim=1) + noise
@@ -360,10 +404,10 @@ def run_ours(args, rank, local_rank, world):
         acc_o, nxt_o, dlen_o = hist if hist is not None else (acc_hist[i], nxt_hist[i], dlen_hist[i])
         if ev is not None:
             ev[0].record(s)
-        ds.fc_project(st["taps"], fc_w, out=h_buf, stream=s, workspaces=wsp)
+        fc_call(st["taps"], out=h_buf, stream=s, workspaces=wsp)
         if ev is not None:
             ev[1].record(s)
-        ds.lm_head(h_buf, lm_w, out=logits.view(M, V), stream=s, workspaces=wsp)
+        lm_call(h_buf, out=logits.view(M, V), stream=s, workspaces=wsp)
         if ev is not None:
             ev[2].record(s)
         ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
@@ -515,10 +559,12 @@ def run_ours(args, rank, local_rank, world):
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": max_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": args.config, "B": B, "k": k, "H": H, "taps": T, "V": V, "r": r,
                    "verify": "probabilistic" if mode == 1 else "greedy",
                    "confidence_head": bool(conf_w is not None),
+                   "weights": "e4m3 codes + fp32 row scales (fc, LM head)" if fp8 else "bf16",
                    "l2": "inputs larger than L2: %.2f GB of weights streamed per step"
                          % ((sb["fc"] + sb["lm_head"]) / 1e9),
                    "parallelism": "replicas%d" % world},
@@ -526,7 +572,10 @@ def run_ours(args, rank, local_rank, world):
         "accepted_tok_s": steps_per_s * B * mean_acc_len,
         "mean_acceptance_length": mean_acc_len,
         "per_position_acceptance": per_pos,
-        "roofline": {"bound": "hbm", "kernel": "gemm_tcgen05 (LM head)", "achieved": achieved,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("quantize_rows + gemm_tcgen05<fp8> (LM head stage)" if fp8
+                                else "gemm_tcgen05 (LM head)"),
+                     "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
                      "traffic": profiled_traffic(args.config), "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
@@ -550,7 +599,8 @@ def run_ours(args, rank, local_rank, world):
         host = {"taps": st["taps"], "fc_w": host_w["fc_w"], "lm_w": host_w["lm_w"],
                 "w1": host_w["w1"], "w2": host_w["w2"], "prev": st["prev"],
                 "target": np.ascontiguousarray(sets[0]["target"].cpu().numpy())}
-        host["h"] = ora.fc_project(st["taps"], host_w["fc_w"])
+        add_host_fp8(ora, host, cfg)
+        host["h"] = oracle_h(ora, host, cfg)
         sps, cores, desc, _ = cpu_oracle_baseline(host, cfg, mode, args.cpu_budget)
         line["cpu_baseline"] = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}

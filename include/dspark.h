@@ -270,6 +270,52 @@ dspark_status_t dspark_verify_noalloc(int mode, const float *target_logits,
                                       int32_t *accepted_len, int32_t *next_token, int B, int k,
                                       int V, void *stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) drafter weights.  [PR620] ships the drafters as FP8 checkpoints
+ * ("drafter-fp8-v5", "qwen3.8-27b-dflash-drafter-fp8-b70") but does not give
+ * the scheme; the reading implemented here is per-row W8A8:
+ *   E4M3 = OCP FP8 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *   infinity, largest finite 448, code 0x7F/0xFF = NaN);
+ *   scale[r] = amax_c |x[r, c]| / 448 in fp32 (IEEE division), 1 for an
+ *   all-zero row; code[r, c] = E4M3(x[r, c] / scale[r]) (IEEE division),
+ *   rounded to nearest even and saturated to +-448 (NaN -> 0x7F).
+ * Weights are quantised once with dspark_quantize_fp8; the fc and LM-head
+ * calls below quantise their activation rows the same way on every call
+ * (into the workspace) and multiply the fp32 tensor-core sum by
+ * scale_x[m] * scale_w[n] in fp32.
+ * ---------------------------------------------------------------------- */
+
+/* Quantises rows of a bf16 matrix given as nseg column segments (HOST array of
+ * nseg device pointers, each [rows, seg_cols] with row stride seg_ld elements,
+ * 16-byte aligned; seg_ld % 8 == 0) whose concatenation is the row.
+ *   codes [rows, nseg*seg_cols] uint8 (16-byte aligned), scales [rows] fp32.
+ * 1 <= nseg <= 8, seg_cols % 16 == 0, nseg*seg_cols <= 2^24, rows <= 2^24.
+ * One kernel, no workspace; the result is bit-exact (no rounding choice is
+ * left to the implementation). */
+dspark_status_t dspark_quantize_fp8(const dspark_bf16_t *const *segs, int nseg, int64_t seg_ld,
+                                    int rows, int seg_cols, uint8_t *codes, float *scales,
+                                    void *stream);
+
+/* FP8 fc projection: as dspark_fc_project with fc_w8 [H, T*H] E4M3 codes and
+ * fc_scale [H] fp32 (from dspark_quantize_fp8 of the bf16 fc weight):
+ *   x = concat_j taps[j][m, :]  quantised per row m -> (x8, sx[m])
+ *   h[m, n] = bf16_rne( sx[m] * fc_scale[n] * sum_c E4M3(x8[m,c]) * E4M3(fc_w8[n,c]) )
+ * H % 128 == 0.  Two kernels (activation quantisation, FP8 tensor-core GEMM). */
+size_t dspark_fc_project_fp8_workspace_size(int M, int H, int T);
+dspark_status_t dspark_fc_project_fp8(const dspark_bf16_t *const *taps, int T, int64_t tap_ld,
+                                      const uint8_t *fc_w8, const float *fc_scale,
+                                      dspark_bf16_t *h_out, int M, int H, void *ws,
+                                      size_t ws_bytes, void *stream);
+
+/* FP8 LM head: as dspark_lm_head with lm_w8 [V, H] E4M3 codes and lm_scale [V]
+ * fp32; h [M, H] bf16 is quantised per row -> (h8, sh[m]) and
+ *   logits[m, v] = sh[m] * lm_scale[v] * sum_c E4M3(h8[m,c]) * E4M3(lm_w8[v,c])
+ * in fp32.  H % 128 == 0.  Two kernels. */
+size_t dspark_lm_head_fp8_workspace_size(int M, int H, int V);
+dspark_status_t dspark_lm_head_fp8(const dspark_bf16_t *h, const uint8_t *lm_w8,
+                                   const float *lm_scale, float *logits, int M, int H, int V,
+                                   void *ws, size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

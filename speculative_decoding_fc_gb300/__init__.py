@@ -19,7 +19,7 @@ import threading
 import torch
 
 __all__ = ["DSparkError", "lib", "fc_project", "lm_head", "greedy_sample", "confidence_truncate",
-           "draft_readout",
+           "draft_readout", "quantize_fp8", "fc_project_fp8", "lm_head_fp8",
            "verify", "workspace_status", "launch_count", "Workspaces", "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -89,6 +89,19 @@ def lib():
         L.dspark_verify.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_uint64, _vp,
                                     ctypes.c_uint32, _vp, _vp, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_quantize_fp8.restype = ctypes.c_int
+        L.dspark_quantize_fp8.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _i64, ctypes.c_int,
+                                          ctypes.c_int, _vp, _vp, _vp]
+        L.dspark_fc_project_fp8_workspace_size.restype = _sz
+        L.dspark_fc_project_fp8_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.dspark_fc_project_fp8.restype = ctypes.c_int
+        L.dspark_fc_project_fp8.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _i64, _vp, _vp, _vp,
+                                            ctypes.c_int, ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_lm_head_fp8_workspace_size.restype = _sz
+        L.dspark_lm_head_fp8_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.dspark_lm_head_fp8.restype = ctypes.c_int
+        L.dspark_lm_head_fp8.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, _vp, _sz, _vp]
         _lib = L
     return _lib
 
@@ -335,3 +348,74 @@ def verify(mode, target_logits, draft_tokens, draft_len=None, draft_logits=None,
                            _ptr(next_token), B, k, V, _ptr(ws), ws.numel(), _stream(stream, dev)),
            "dspark_verify")
     return accepted_len, next_token
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) weights
+def _segments(segs, name):
+    rows, cols = segs[0].shape
+    ld = segs[0].stride(0)
+    for j, t in enumerate(segs):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (rows, cols) \
+                or t.stride(1) != 1 or t.stride(0) != ld:
+            raise ValueError("%s %d must be a CUDA bf16 [%d, %d] tensor with row stride %d"
+                             % (name, j, rows, cols, ld))
+    return rows, cols, ld
+
+
+def quantize_fp8(x, codes=None, scales=None, stream=None):
+    """Per-row E4M3 quantisation of a bf16 matrix (or a list of column segments of
+    one): returns (codes uint8 [R, C], scales fp32 [R])."""
+    segs = list(x) if isinstance(x, (list, tuple)) else [x]
+    R, C, ld = _segments(segs, "segment")
+    dev = segs[0].device
+    if codes is None:
+        codes = torch.empty((R, C * len(segs)), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((R,), dtype=torch.float32, device=dev)
+    _need(codes, "codes", torch.uint8, (R, C * len(segs)))
+    _need(scales, "scales", torch.float32, (R,))
+    arr = (_vp * len(segs))(*[t.data_ptr() for t in segs])
+    _check(lib().dspark_quantize_fp8(arr, len(segs), ld, R, C, _ptr(codes), _ptr(scales),
+                                     _stream(stream, dev)), "dspark_quantize_fp8")
+    return codes, scales
+
+
+def fc_project_fp8(taps, fc_w8, fc_scale, out=None, stream=None, workspaces=None):
+    """FP8 fc: h[M, H] (bf16) from bf16 taps (quantised per row on the fly) and the
+    E4M3 weight fc_w8 [H, T*H] with per-row scales fc_scale [H]."""
+    T = len(taps)
+    M, H, ld = _segments(taps, "tap")
+    dev = fc_w8.device
+    _need(fc_w8, "fc_w8", torch.uint8, (H, T * H))
+    _need(fc_scale, "fc_scale", torch.float32, (H,))
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (M, H))
+    L = lib()
+    ws = (workspaces or _default_ws).get("fc8", dev, L.dspark_fc_project_fp8_workspace_size(M, H, T))
+    arr = (_vp * T)(*[t.data_ptr() for t in taps])
+    _check(L.dspark_fc_project_fp8(arr, T, ld, _ptr(fc_w8), _ptr(fc_scale), _ptr(out), M, H,
+                                   _ptr(ws), ws.numel(), _stream(stream, dev)),
+           "dspark_fc_project_fp8")
+    return out
+
+
+def lm_head_fp8(h, lm_w8, lm_scale, out=None, stream=None, workspaces=None):
+    """FP8 LM head: fp32 logits [M, V] from h [M, H] bf16 (quantised per row on the fly)
+    and the E4M3 weight lm_w8 [V, H] with per-row scales lm_scale [V]."""
+    M, H = h.shape
+    V = lm_w8.shape[0]
+    _need(h, "h", torch.bfloat16)
+    _need(lm_w8, "lm_w8", torch.uint8, (V, H))
+    _need(lm_scale, "lm_scale", torch.float32, (V,))
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.float32, device=h.device)
+    _need(out, "out", torch.float32)
+    if out.numel() != M * V:
+        raise ValueError("out must hold M*V floats")
+    L = lib()
+    ws = (workspaces or _default_ws).get("lm8", h.device, L.dspark_lm_head_fp8_workspace_size(M, H, V))
+    _check(L.dspark_lm_head_fp8(_ptr(h), _ptr(lm_w8), _ptr(lm_scale), _ptr(out), M, H, V,
+                                _ptr(ws), ws.numel(), _stream(stream, h.device)),
+           "dspark_lm_head_fp8")
+    return out

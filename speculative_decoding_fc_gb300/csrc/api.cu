@@ -372,4 +372,109 @@ dspark_status_t dspark_verify(int mode, const float *target_logits, const int32_
                        as_stream(stream));
 }
 
+// ---------------------------------------------------------------- FP8 (E4M3) drafter weights
+dspark_status_t dspark_quantize_fp8(const dspark_bf16_t *const *segs, int nseg, int64_t seg_ld,
+                                    int rows, int seg_cols, uint8_t *codes, float *scales,
+                                    void *stream) {
+  if (!segs || !codes || !scales) return DSPARK_ERR_INVALID_ARG;
+  if (nseg < 1 || rows < 1 || seg_cols < 1 || seg_ld < seg_cols) return DSPARK_ERR_INVALID_ARG;
+  if (nseg > kMaxTaps || seg_cols % 16 != 0 || rows > (1 << 24) ||
+      static_cast<long long>(nseg) * seg_cols > (1 << 24))
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (seg_ld % 8 != 0 || !aligned16(codes) || !aligned4(scales)) return DSPARK_ERR_MISALIGNED;
+  const uint16_t *p[kMaxTaps];
+  for (int j = 0; j < nseg; ++j) {
+    if (!segs[j]) return DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(segs[j])) return DSPARK_ERR_MISALIGNED;
+    p[j] = reinterpret_cast<const uint16_t *>(segs[j]);
+  }
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return quantize_fp8_launch(p, nseg, seg_ld, rows, seg_cols, codes, scales, as_stream(stream));
+}
+
+// Workspace of the FP8 GEMMs: [header][GEMM][activation codes M x K][activation scales M].
+static size_t fp8_ws_bytes(int M, int N, int K) {
+  return kHeader + align_up(gemm_workspace_size_fp8(M, N, K), kWsAlign) +
+         align_up(static_cast<size_t>(M) * K, kWsAlign) + align_up(static_cast<size_t>(M) * 4, kWsAlign);
+}
+
+static dspark_status_t fp8_gemm(const uint16_t *const *segs, int nseg, int64_t seg_ld, int seg_k,
+                                const uint8_t *w8, const float *w_scale, int M, int N, void *out,
+                                int64_t ldo, bool out_bf16, long long kind, void *ws,
+                                cudaStream_t s) {
+  const int K = nseg * seg_k;
+  char *base = static_cast<char *>(ws);
+  const size_t gemm_bytes = align_up(gemm_workspace_size_fp8(M, N, K), kWsAlign);
+  uint8_t *a8 = reinterpret_cast<uint8_t *>(base + kHeader + gemm_bytes);
+  float *a_scale =
+      reinterpret_cast<float *>(base + kHeader + gemm_bytes + align_up(static_cast<size_t>(M) * K, kWsAlign));
+  dspark_status_t st = prepare_workspace(ws, layout_signature({kind, M, N, K}),
+                                         {{0, kHeader + gemm_counter_bytes(M, N, K)}}, s);
+  if (st != DSPARK_OK) return st;
+  if ((st = quantize_fp8_launch(segs, nseg, seg_ld, M, seg_k, a8, a_scale, s)) != DSPARK_OK) return st;
+  GemmProblem p;
+  memset(&p, 0, sizeof(p));
+  p.w = w8;
+  p.x[0] = a8;
+  p.x_ld[0] = K;
+  p.n_seg = 1;
+  p.seg_k = K;
+  p.N = N;
+  p.M = M;
+  p.out = out;
+  p.ldo = ldo;
+  p.out_bf16 = out_bf16;
+  p.fp8 = true;
+  p.a_scale = a_scale;
+  p.w_scale = w_scale;
+  return gemm_launch(p, base + kHeader, gemm_bytes, status_word(ws), s);
+}
+
+size_t dspark_fc_project_fp8_workspace_size(int M, int H, int T) {
+  if (M < 1 || H < 128 || T < 1 || T > kMaxTaps) return 0;
+  return fp8_ws_bytes(M, H, T * H);
+}
+
+dspark_status_t dspark_fc_project_fp8(const dspark_bf16_t *const *taps, int T, int64_t tap_ld,
+                                      const uint8_t *fc_w8, const float *fc_scale,
+                                      dspark_bf16_t *h_out, int M, int H, void *ws,
+                                      size_t ws_bytes, void *stream) {
+  if (!taps || !fc_w8 || !fc_scale || !h_out) return DSPARK_ERR_INVALID_ARG;
+  if (T < 1 || M < 1 || H < 1 || tap_ld < H) return DSPARK_ERR_INVALID_ARG;
+  if (T > kMaxTaps || H % 128 != 0 || M > kMaxM || H > (1 << 16)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (tap_ld % 8 != 0 || !aligned16(fc_w8) || !aligned4(fc_scale) || !aligned2(h_out))
+    return DSPARK_ERR_MISALIGNED;
+  const uint16_t *p[kMaxTaps];
+  for (int j = 0; j < T; ++j) {
+    if (!taps[j]) return DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(taps[j])) return DSPARK_ERR_MISALIGNED;
+    p[j] = reinterpret_cast<const uint16_t *>(taps[j]);
+  }
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_fc_project_fp8_workspace_size(M, H, T));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  return fp8_gemm(p, T, tap_ld, H, fc_w8, fc_scale, M, H, h_out, H, true, 6, ws, as_stream(stream));
+}
+
+size_t dspark_lm_head_fp8_workspace_size(int M, int H, int V) {
+  if (M < 1 || H < 128 || V < 1) return 0;
+  return fp8_ws_bytes(M, V, H);
+}
+
+dspark_status_t dspark_lm_head_fp8(const dspark_bf16_t *h, const uint8_t *lm_w8,
+                                   const float *lm_scale, float *logits, int M, int H, int V,
+                                   void *ws, size_t ws_bytes, void *stream) {
+  if (!h || !lm_w8 || !lm_scale || !logits) return DSPARK_ERR_INVALID_ARG;
+  if (M < 1 || H < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (M > kMaxM || V > kMaxV || H % 128 != 0 || H > (1 << 20)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(h) || !aligned16(lm_w8) || !aligned4(lm_scale) || !aligned4(logits))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_lm_head_fp8_workspace_size(M, H, V));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  const uint16_t *p[1] = {reinterpret_cast<const uint16_t *>(h)};
+  return fp8_gemm(p, 1, H, H, lm_w8, lm_scale, M, V, logits, V, false, 7, ws, as_stream(stream));
+}
+
 }  // extern "C"

@@ -24,6 +24,9 @@
 //     TMA writes them; the UMMA shared-memory descriptors describe exactly that
 //     layout.  Weights are loaded with an L2 evict-first policy, activations
 //     with evict-last.
+//   * FP8 variant (kind::f8f6f4, E4M3 x E4M3): the same 128-byte rows hold 128
+//     codes, each MMA consumes K = 32, and the epilogue multiplies by the
+//     activation-row and weight-row scales.
 //   * Every wait on an mbarrier is bounded: on timeout the CTA records
 //     DSPARK_ERR_DEVICE_TIMEOUT, stops issuing, waits (bounded) for its own
 //     copies and MMAs in flight, frees its TMEM and returns.
@@ -41,7 +44,8 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kBM = 128;          // weight rows per tile (UMMA M)
-constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
+constexpr int kBK = 64;           // bf16 K per stage: one 128-byte swizzle row
+constexpr int kRowBytes = 128;    // bytes of K per operand row and stage (both kinds)
 constexpr int kMaxStages = 12;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
@@ -49,6 +53,8 @@ constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 struct GemmParams {
   CUtensorMap tm_w;
   CUtensorMap tm_x[kMaxTaps];
+  const float *a_scale;   // FP8: scale of each activation row (else null)
+  const float *w_scale;   // FP8: scale of each weight row (else null)
   void *out;
   float *partials;
   int *tickets;
@@ -171,6 +177,16 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -208,6 +224,7 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long units, int gri
 
 __device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, float v) {
   if (m >= p.M || n >= p.N) return;
+  if (p.w_scale) v *= __ldg(p.a_scale + m) * __ldg(p.w_scale + n);
   const long long off = static_cast<long long>(m) * p.ldo + n;
   if (p.out_bf16)
     reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(v);
@@ -216,12 +233,14 @@ __device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, flo
 }
 
 // ------------------------------------------------------------------ kernel
+template <bool kFP8>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int kElemK = kFP8 ? 128 : kBK;  // K elements per stage row
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sbase = smem_raw + (base - raw);
-  const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * kBK * 2;
+  const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * kRowBytes;
   const uint32_t stage_bytes = kABytes + b_bytes;
   const int S = p.stages;
 
@@ -299,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
           const uint32_t fb = full0 + 8u * stage;
           mbar_expect_tx(fb, stage_bytes);
           const uint32_t sa = base + stage * stage_bytes;
-          tma_load_2d(sa, &p.tm_w, kb * kBK, n_tile * kBM, fb, pol_w);
+          tma_load_2d(sa, &p.tm_w, kb * kElemK, n_tile * kBM, fb, pol_w);
           const int seg = kb / p.kb_per_seg;
-          const int xk = (kb - seg * p.kb_per_seg) * kBK;
+          const int xk = (kb - seg * p.kb_per_seg) * kElemK;
           tma_load_2d(sa + kABytes, xmaps + seg, xk, m_tile * p.BN, fb, pol_x);
           ++issued;
           if (++stage == S) {
@@ -347,10 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
           tc_fence_after();
           const uint32_t sa = base + stage * stage_bytes;
           const uint32_t sb = sa + kABytes;
+          // 4 MMAs per stage, each over 32 bytes of K (16 bf16 or 32 E4M3)
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
-                        p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+            if constexpr (kFP8)
+              tc_mma_e4m3(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
+                          p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            else
+              tc_mma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
+                          p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(empty0 + 8u * stage);
           if (++stage == S) {
@@ -501,14 +525,15 @@ EncodeTiledFn encode_fn() {
 // 2-D bf16 tensor [rows, inner] with the given row stride, read in boxes of
 // 64 (one 128-byte swizzle row) x box_rows.
 bool make_map(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t rows,
-              uint64_t row_stride_bytes, uint32_t box_rows) {
+              uint64_t row_stride_bytes, uint32_t box_rows, bool fp8) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_stride_bytes};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8 ? kRowBytes : kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void *>(ptr), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -521,7 +546,8 @@ struct Tiling {
   size_t smem;
 };
 
-Tiling plan(int M, int N, int K) {
+// K is counted in elements; esize = bytes per element (2 bf16, 1 E4M3).
+Tiling plan(int M, int N, int K, int esize = 2) {
   Tiling t;
   t.tiles_m = (M + 255) / 256;
   int bn = (M + t.tiles_m - 1) / t.tiles_m;
@@ -529,12 +555,12 @@ Tiling plan(int M, int N, int K) {
   if (bn < 16) bn = 16;
   t.BN = bn;
   t.tiles_n = (N + kBM - 1) / kBM;
-  t.kb_total = K / kBK;
+  t.kb_total = K * esize / kRowBytes;
   t.units = static_cast<long long>(t.tiles_m) * t.tiles_n * t.kb_total;
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(2 * bn)) cols <<= 1;
   t.tmem_cols = cols;
-  const size_t stage = kABytes + static_cast<size_t>(bn) * kBK * 2;
+  const size_t stage = kABytes + static_cast<size_t>(bn) * kRowBytes;
   const size_t budget = 227 * 1024 - 1024 - 256;
   int st = static_cast<int>(budget / stage);
   if (st > kMaxStages) st = kMaxStages;
@@ -551,7 +577,7 @@ size_t partial_bytes(const Tiling &t) {
 
 size_t gemm_counter_bytes(int M, int N, int K) {
   if (M < 1 || N < 1 || K < kBK) return 0;
-  Tiling t = plan(M, N, K);
+  Tiling t = plan(M, N, K);  // the tile grid does not depend on the element size
   return align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
 }
 
@@ -562,10 +588,14 @@ size_t gemm_workspace_size(int M, int N, int K) {
   return tickets + align_up(partial_bytes(t), kWsAlign);
 }
 
+// The tile grid and the partial tiles do not depend on the element size.
+size_t gemm_workspace_size_fp8(int M, int N, int K) { return gemm_workspace_size(M, N, K); }
+
 dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, int *status,
                             cudaStream_t stream) {
   const int K = pr.n_seg * pr.seg_k;
-  Tiling t = plan(pr.M, pr.N, K);
+  const int esize = pr.fp8 ? 1 : 2;
+  Tiling t = plan(pr.M, pr.N, K, esize);
   if (ws_bytes < gemm_workspace_size(pr.M, pr.N, K)) return DSPARK_ERR_WORKSPACE;
   const int sms = device_sm_count();
   if (sms <= 0) return DSPARK_ERR_NO_DEVICE;
@@ -573,14 +603,16 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
   GemmParams p;
   memset(&p, 0, sizeof(p));
   if (!make_map(&p.tm_w, pr.w, static_cast<uint64_t>(K), static_cast<uint64_t>(pr.N),
-                static_cast<uint64_t>(K) * 2, kBM))
+                static_cast<uint64_t>(K) * esize, kBM, pr.fp8))
     return DSPARK_ERR_CUDA;
   for (int s = 0; s < pr.n_seg; ++s) {
     if (!make_map(&p.tm_x[s], pr.x[s], static_cast<uint64_t>(pr.seg_k),
-                  static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.x_ld[s]) * 2,
-                  static_cast<uint32_t>(t.BN)))
+                  static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.x_ld[s]) * esize,
+                  static_cast<uint32_t>(t.BN), pr.fp8))
       return DSPARK_ERR_CUDA;
   }
+  p.a_scale = pr.a_scale;
+  p.w_scale = pr.w_scale;
   const size_t tickets = align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
   p.tickets = reinterpret_cast<int *>(ws);
   p.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + tickets);
@@ -588,7 +620,7 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
   p.status = status;
   p.ldo = pr.ldo;
   p.units = t.units;
-  p.kb_per_seg = pr.seg_k / kBK;
+  p.kb_per_seg = pr.seg_k * esize / kRowBytes;
   p.kb_total = t.kb_total;
   p.N = pr.N;
   p.M = pr.M;
@@ -597,26 +629,28 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
   p.stages = t.stages;
   p.out_bf16 = pr.out_bf16 ? 1 : 0;
   p.tmem_cols = t.tmem_cols;
-  // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B bf16
-  // (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
-  // bits 24-28.
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(t.BN >> 3) << 17) |
+  // Instruction descriptor: D fp32 (bits 4-5 = 1); A and B format at bits 7-9 and
+  // 10-12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3); both K-major; N >> 3 at
+  // bits 17-22, M >> 4 at bits 24-28.
+  const uint32_t fmt = pr.fp8 ? 0u : 1u;
+  p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(t.BN >> 3) << 17) |
             (static_cast<uint32_t>(kBM >> 4) << 24);
 
   long long grid = sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
   const long long by_work = t.units / 4 > 0 ? t.units / 4 : 1;
   if (grid > by_work) grid = by_work;
 
-  static bool configured[64] = {};
+  static bool configured[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(gemm_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024) != cudaSuccess)
+  auto kern = pr.fp8 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  if (dev < 0 || dev >= 64 || !configured[pr.fp8 ? 1 : 0][dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+        cudaSuccess)
       return DSPARK_ERR_CUDA;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[pr.fp8 ? 1 : 0][dev] = true;
   }
-  gemm_tcgen05_kernel<<<static_cast<unsigned>(grid), kThreads, t.smem, stream>>>(p);
+  kern<<<static_cast<unsigned>(grid), kThreads, t.smem, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;

@@ -32,9 +32,13 @@ struct GemmProblem {
   void *out;
   int64_t ldo;
   bool out_bf16;
+  bool fp8;                 // E4M3 operands (w, x as uint8 codes); K multiple of 128
+  const float *a_scale;     // FP8: per activation row
+  const float *w_scale;     // FP8: per weight row
 };
 
 size_t gemm_workspace_size(int M, int N, int K);
+size_t gemm_workspace_size_fp8(int M, int N, int K);
 // Bytes at the start of a GEMM workspace holding counters that must start at zero.
 size_t gemm_counter_bytes(int M, int N, int K);
 // Enqueues the GEMM.  ws must hold gemm_workspace_size bytes (zeroed once).
@@ -51,6 +55,14 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
 dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, float conf_b,
                                   float conf_tau, int32_t *draft_tokens, int32_t *draft_len,
                                   float *conf_out, int B, int k, int H, cudaStream_t stream);
+
+// ------------------------------------------------------------------ FP8 quantisation
+// codes[r, :] = E4M3(x[r, :] / scale[r]), scale = amax(row) / 448 (1 if zero); the
+// row is the concatenation of nseg segments, each [rows, seg_cols] with row
+// stride seg_ld elements.
+dspark_status_t quantize_fp8_launch(const uint16_t *const *segs, int nseg, int64_t seg_ld,
+                                    int rows, int seg_cols, uint8_t *codes, float *scales,
+                                    cudaStream_t stream);
 
 // ------------------------------------------------------------------ verify
 size_t verify_workspace_size(int B, int k, int V);

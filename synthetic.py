@@ -30,6 +30,9 @@ CONFIGS = {
                  sigma=("const", 1.0), conf=False),
     "27b_b1": dict(H=5120, T=5, V=151936, r=64, k=7, B=1, steps=1, mode=1,
                    sigma=("ramp", 0.5, 3.0), conf=False),
+    # the same workload with the fc and LM-head weights held as E4M3 codes + row scales
+    "27b_b1_fp8": dict(H=5120, T=5, V=151936, r=64, k=7, B=1, steps=1, mode=1,
+                       sigma=("ramp", 0.5, 3.0), conf=False, fp8=True),
     "27b_b16": dict(H=5120, T=5, V=151936, r=64, k=7, B=16, steps=1, mode=1,
                     sigma=("ramp", 0.5, 3.0), conf=True),
     "flash_b4": dict(H=2560, T=5, V=151936, r=64, k=7, B=4, steps=1, mode=1,

@@ -79,3 +79,35 @@ def test_argument_errors_are_caught_before_any_launch(libdspark):
     g.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
     assert g(fake, fake, fake, 7, 100, 1000, fake, 1 << 30, None) == -2   # H not a multiple of 64
     assert g(fake, fake, fake, 0, 128, 1000, fake, 1 << 30, None) == -1
+
+
+def test_fp8_argument_errors_are_caught_before_any_launch(libdspark):
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    fake = vp(1 << 20)
+    q = libdspark.dspark_quantize_fp8
+    q.restype = ctypes.c_int
+    q.argtypes = [ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, vp,
+                  vp, vp]
+    segs = (vp * 2)(1 << 20, 1 << 21)
+    assert q(segs, 0, 64, 4, 64, fake, fake, None) == -1          # no segment
+    assert q(segs, 2, 64, 4, 24, fake, fake, None) == -2          # seg_cols % 16
+    assert q(segs, 2, 60, 4, 48, fake, fake, None) == -3          # seg_ld % 8
+    assert q(segs, 2, 64, 4, 64, vp((1 << 20) + 8), fake, None) == -3   # codes not 16-B aligned
+    libdspark.dspark_lm_head_fp8_workspace_size.restype = sz
+    libdspark.dspark_fc_project_fp8_workspace_size.restype = sz
+    assert libdspark.dspark_lm_head_fp8_workspace_size(7, 5120, 151936) > 7 * 5120
+    assert libdspark.dspark_fc_project_fp8_workspace_size(7, 5120, 5) > 7 * 5 * 5120
+    assert libdspark.dspark_fc_project_fp8_workspace_size(7, 5120, 9) == 0
+    g = libdspark.dspark_lm_head_fp8
+    g.restype = ctypes.c_int
+    g.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, sz, vp]
+    assert g(fake, fake, fake, fake, 7, 192, 1000, fake, 1 << 30, None) == -2   # H % 128
+    assert g(fake, fake, None, fake, 7, 256, 1000, fake, 1 << 30, None) == -1   # no scales
+    assert g(fake, fake, fake, fake, 7, 256, 1000, fake, 16, None) == -4        # workspace
+    f = libdspark.dspark_fc_project_fp8
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int64, vp, vp, vp, ctypes.c_int,
+                  ctypes.c_int, vp, sz, vp]
+    taps = (vp * 2)(1 << 20, 1 << 21)
+    assert f(taps, 2, 256, fake, fake, fake, 4, 192, fake, 1 << 30, None) == -2   # H % 128
+    assert f(taps, 2, 256, fake, fake, fake, 4, 256, fake, 16, None) == -4
