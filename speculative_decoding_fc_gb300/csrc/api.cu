@@ -262,7 +262,7 @@ dspark_status_t dspark_greedy_sample(float *logits, const dspark_bf16_t *w1,
   if (st != DSPARK_OK) return st;
   if ((st = check_ws(ws, ws_bytes, chain_ws_bytes(B, k, V))) != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
-  st = prepare_workspace(ws, layout_signature({3, B, k, V}), {{0, kHeader + chain_counter_bytes(k)}},
+  st = prepare_workspace(ws, layout_signature({3, B, k, V}), {{0, kHeader + chain_counter_bytes(B, k)}},
                          as_stream(stream));
   if (st != DSPARK_OK) return st;
   return chain_launch(logits, w1, w2, w1 ? r : 0, prev_token, draft_tokens, q_stats, nullptr, B,
@@ -324,7 +324,7 @@ dspark_status_t dspark_draft_readout(const dspark_bf16_t *h, const dspark_bf16_t
   const size_t gemm_bytes = align_up(gemm_workspace_size(M, V, H), kWsAlign);
   st = prepare_workspace(ws, layout_signature({4, B, k, H, V}),
                          {{0, kHeader + gemm_counter_bytes(M, V, H)},
-                          {kHeader + gemm_bytes, chain_counter_bytes(k)}},
+                          {kHeader + gemm_bytes, chain_counter_bytes(B, k)}},
                          s);
   if (st != DSPARK_OK) return st;
   st = lm_head_enqueue(h, lm_w, logits, M, H, V, base + kHeader, gemm_bytes, status_word(ws), s);

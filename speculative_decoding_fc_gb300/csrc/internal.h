@@ -47,7 +47,7 @@ dspark_status_t gemm_launch(const GemmProblem &p, void *ws, size_t ws_bytes, int
 
 // ------------------------------------------------------------------ Markov chain
 size_t chain_workspace_size(int B, int k, int V);
-size_t chain_counter_bytes(int k);
+size_t chain_counter_bytes(int B, int k);
 dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *w2, int r,
                              const int32_t *prev_token, int32_t *draft_tokens, float *q_stats,
                              int32_t *draft_len_fill, int B, int k, int V, void *ws,

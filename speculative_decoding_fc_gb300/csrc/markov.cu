@@ -15,9 +15,11 @@
 //    positions and keeps its slice of markov_w2 in shared memory (XOR-swizzled
 //    16-byte chunks, bank-conflict free), so the weight is read from memory
 //    once per step instead of once per position.  Positions are separated by
-//    a grid barrier (atomic arrival counter, bounded spin); after it every CTA
-//    merges the per-CTA partials itself, in the same fixed order, so all CTAs
-//    agree on the draft token without a second barrier.
+//    tagged 64-bit words: every CTA publishes, per request, one word holding a
+//    tag of (call, position) and its slice's argmax key, and every CTA polls all
+//    CTAs' words until they carry the current tag.  The polled words are the data
+//    (their max is the draft token), so no fence is needed between positions;
+//    all CTAs take the same max and agree without a second barrier.
 //  * markov_chain_kernel (fallback when a cooperative launch is not possible):
 //    one launch per position; the last CTA to finish (atomic ticket, nobody
 //    waits) merges the slices and writes the token the next launch reads.
@@ -230,7 +232,6 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
 // ---------------------------------------------------------------- persistent chain
 constexpr int kPThreads = 256;
 constexpr int kPWarps = kPThreads / 32;
-constexpr int kPVPT = 4;                      // vocab rows per thread (slice <= 2048 rows)
 constexpr int kMaxPGrid = kMaxGemmCtas;       // CTAs of the persistent chain (<= SMs)
 constexpr long long kBarrierCycles = 2000000000LL;  // ~1 s at 2 GHz
 
@@ -242,9 +243,9 @@ struct ChainPArgs {
   int32_t *draft_tokens;
   float *q_stats;
   int32_t *draft_len_fill;
-  ChainPartial *partials;   // [k][B][grid]
-  int *flags;               // [k][grid]: CTA c has published its partials of position pos
-  int *epoch;               // call counter: the flags of call e carry tags of epoch e
+  ChainPartial *partials;   // [k][B][grid]: softmax statistics of each CTA's slice
+  unsigned long long *words;  // [k][B][grid]: tagged argmax word of each CTA's slice
+  int *epoch;               // call counter: the words of call e carry tags of epoch e
   int *done;                // exit counter (the last CTA advances the epoch)
   int *abort_flag;          // set when a wait gives up; later calls then do nothing
   int *status;
@@ -270,6 +271,20 @@ __device__ __forceinline__ void st_release(int *p, int v) {
   asm volatile("st.release.gpu.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.release.gpu.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // 16-byte chunk q of local row `row` of the shared-memory markov_w2 slice is
 // stored at chunk q ^ (row & mask): eight consecutive rows read at the same q
 // hit eight different bank groups.
@@ -278,11 +293,22 @@ __device__ __forceinline__ int w2_swizzle(int row, int q, int chunks_per_row) {
   return q ^ (row & mask);
 }
 
-// Tag a CTA writes into its flag once its partials of position `pos` are
-// visible; unique per (call, position) so flags never need clearing.
-__device__ __forceinline__ int flag_tag(int epoch, int pos) {
-  return 1 + static_cast<int>((static_cast<unsigned>(epoch) * 16u + static_cast<unsigned>(pos)) &
-                              0x3fffffffu);
+// Position words.  Bits 58-63: tag in [1, 63] of (call epoch, position); two
+// consecutive calls give a position different tags (16 or 15 apart mod 63), and 0
+// (a cleared workspace) is never a tag, so a word shows by itself whether it was
+// written in this call.  Bits 26-57: the ordered value bits of the slice's argmax
+// key; bits 0-25: 2^26 - 1 - index (V <= 2^26).  Among words of one tag a larger
+// word is a larger value, then a lower index, exactly as for argmax_key.
+__device__ __forceinline__ uint32_t word_tag(int epoch, int pos) {
+  return 1u + ((static_cast<uint32_t>(epoch) % 63u) * 16u + static_cast<uint32_t>(pos)) % 63u;
+}
+
+__device__ __forceinline__ unsigned long long pack_word(unsigned long long key, uint32_t tag) {
+  return (static_cast<unsigned long long>(tag) << 58) | ((key >> 32) << 26) | (key & 0x3ffffffull);
+}
+
+__device__ __forceinline__ int word_index(unsigned long long w) {
+  return static_cast<int>(0x3ffffffu - static_cast<uint32_t>(w & 0x3ffffffull));
 }
 
 // Rows of the vocabulary a thread of the persistent chain owns: 4 rows x up to 8
@@ -478,7 +504,16 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
         }
         warp_key_stats(key, m, sum);
         if (lane == 0) {
-          a.partials[(static_cast<long long>(pos) * B + g0 + g) * grid + cta] = ChainPartial{key, m, sum};
+          const long long at = (static_cast<long long>(pos) * B + g0 + g) * grid + cta;
+          a.partials[at] = ChainPartial{key, m, sum};
+          // This thread wrote every partial of this request (the combining warp of a
+          // request is fixed), so the release on the last position's word makes all
+          // of them visible to whoever sees that word.
+          const unsigned long long wd = pack_word(key, word_tag(epoch, pos));
+          if (pos + 1 < k)
+            st_relaxed_u64(a.words + at, wd);
+          else
+            st_release_u64(a.words + at, wd);
           // the global winner is one of the CTA winners: warm L2 with this one's
           // markov_w1 row for the next position's gather
           if (biased && pos + 1 < k)
@@ -497,11 +532,8 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
       __syncthreads();
     }
 
-    // Publish this CTA's partials of `pos` (the barrier above orders every thread's
-    // partial stores before the release), then wait until every CTA has: warp 0 polls
-    // the flags with relaxed loads and takes one acquire fence once all are seen.
-    const int tag = flag_tag(epoch, pos);
-    if (tid == 0) st_release(a.flags + pos * grid + cta, tag);
+    // This CTA's words of `pos` are published (above).  While the other CTAs finish,
+    // store the biased logits and load the next position's logits.
     if (biased && B <= G) {
 #pragma unroll
       for (int g = 0; g < G; ++g)
@@ -517,51 +549,55 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
         for (int g = 0; g < G; ++g)
           lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k + pos + 1) * V + vrow[j]] : 0.0f;
     }
-    if (warp == 0) {
-      const int *f = a.flags + pos * grid;
+    // Wait for every CTA's word of each request (warp w polls requests w, w + 8, ...);
+    // the max of the words is the draft token.  Relaxed loads suffice: nothing else is
+    // read on the strength of a word, except after the last position, where an acquire
+    // fence pairs with the words' release stores before the statistics are merged.
+    {
+      const uint32_t tg = word_tag(epoch, pos);
       const long long t0 = clock64();
-      int stop = 0;
-      while (true) {
-        // independent loads (no short-circuit): one round trip per pass
-        int seen = 0, want = 0;
-        for (int c = lane; c < grid; c += 32) {
-          seen += (ld_relaxed(f + c) == tag) ? 1 : 0;
-          ++want;
+      for (int b = warp; b < B; b += kPWarps) {
+        const unsigned long long *wb = a.words + (static_cast<long long>(pos) * B + b) * grid;
+        unsigned long long best = 0ull;
+        int stop = 0;
+        while (true) {
+          // independent loads (no short-circuit): one round trip per pass
+          unsigned long long mx = 0ull;
+          int missing = 0;
+          for (int c = lane; c < grid; c += 32) {
+            const unsigned long long w = ld_relaxed_u64(wb + c);
+            missing += (static_cast<uint32_t>(w >> 58) != tg) ? 1 : 0;
+            mx = w > mx ? w : mx;
+          }
+          if (__all_sync(0xffffffffu, missing == 0)) {
+            best = warp_max_u64(mx);
+            break;
+          }
+          int give_up = 0;
+          if (lane == 0)
+            give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > kBarrierCycles) ? 1 : 0;
+          if (__shfl_sync(0xffffffffu, give_up, 0)) {
+            if (lane == 0 && atomicExch(a.abort_flag, 1) == 0)
+              record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
+            stop = 1;
+            break;
+          }
+          __nanosleep(20);
         }
-        if (__all_sync(0xffffffffu, seen == want)) break;
-        int give_up = 0;
-        if (lane == 0)
-          give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > kBarrierCycles) ? 1 : 0;
-        if (__shfl_sync(0xffffffffu, give_up, 0)) {
-          if (lane == 0 && atomicExch(a.abort_flag, 1) == 0)
-            record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
-          stop = 1;
+        if (stop) {
+          if (lane == 0) stop_s = 1;
           break;
         }
-        __nanosleep(20);
+        if (lane == 0) {
+          const int d = word_index(best);
+          prev_s[b] = d;
+          if (cta == 0) a.draft_tokens[static_cast<long long>(b) * k + pos] = d;
+        }
       }
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      if (lane == 0) stop_s = stop;
+      if (pos + 1 == k) asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
     __syncthreads();
     if (stop_s) return;
-
-    // Every CTA merges all CTAs' argmax keys (same data, same order -> same token).
-    for (int b = warp; b < B; b += kPWarps) {
-      const ChainPartial *pb = a.partials + (static_cast<long long>(pos) * B + b) * grid;
-      unsigned long long kb = 0ull;
-      for (int c = lane; c < grid; c += 32) {
-        const unsigned long long key = __ldcg(reinterpret_cast<const unsigned long long *>(pb + c));
-        kb = key > kb ? key : kb;
-      }
-      kb = warp_max_u64(kb);
-      if (lane == 0) {
-        const int d = static_cast<int>(key_index(kb));
-        prev_s[b] = d;
-        if (cta == 0) a.draft_tokens[static_cast<long long>(b) * k + pos] = d;
-      }
-    }
-    __syncthreads();
   }
 
   // Off the critical path: softmax statistics of q for every (position, request),
@@ -659,19 +695,19 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(
 }  // namespace
 
 // Chain workspace: [0] ticket of the per-position kernel, [4] epoch, [8] exit
-// count, [12] abort flag; position flags from byte 256 (k x kMaxPGrid ints);
-// partials after them.
-size_t chain_flags_bytes(int k) {
-  return align_up(static_cast<size_t>(k) * kMaxPGrid * sizeof(int), kWsAlign);
+// count, [12] abort flag; position words from byte 256 (k x B x kMaxPGrid u64,
+// zero = not written); partials after them.
+size_t chain_words_bytes(int B, int k) {
+  return align_up(static_cast<size_t>(k) * B * kMaxPGrid * sizeof(unsigned long long), kWsAlign);
 }
 
-size_t chain_counter_bytes(int k) { return kWsAlign + chain_flags_bytes(k); }
+size_t chain_counter_bytes(int B, int k) { return kWsAlign + chain_words_bytes(B, k); }
 
 size_t chain_workspace_size(int B, int k, int V) {
   const int nchunks = (V + kChunk - 1) / kChunk;
   const size_t per_pos = static_cast<size_t>(B) * nchunks * sizeof(ChainPartial);
   const size_t persistent = static_cast<size_t>(k) * B * kMaxPGrid * sizeof(ChainPartial);
-  return kWsAlign + chain_flags_bytes(k) +
+  return kWsAlign + chain_words_bytes(B, k) +
          align_up(per_pos > persistent ? per_pos : persistent, kWsAlign);
 }
 
@@ -732,9 +768,10 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
                              int32_t *draft_len_fill, int B, int k, int V, void *ws,
                              int *status, cudaStream_t stream) {
   int *ctrl = reinterpret_cast<int *>(ws);
-  int *flags = reinterpret_cast<int *>(static_cast<char *>(ws) + kWsAlign);
+  unsigned long long *words =
+      reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kWsAlign);
   ChainPartial *partials = reinterpret_cast<ChainPartial *>(static_cast<char *>(ws) + kWsAlign +
-                                                           chain_flags_bytes(k));
+                                                           chain_words_bytes(B, k));
 
   ChainPArgs pa;
   pa.logits = logits;
@@ -745,7 +782,7 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
   pa.q_stats = q_stats;
   pa.draft_len_fill = draft_len_fill;
   pa.partials = partials;
-  pa.flags = flags;
+  pa.words = words;
   pa.epoch = ctrl + 1;
   pa.done = ctrl + 2;
   pa.abort_flag = ctrl + 3;
