@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sets", type=int, default=4, help="input sets rotated across steps")
     ap.add_argument("--no-graph", action="store_true", help="time un-captured steps only")
+    ap.add_argument("--q-stats", default="verify", choices=["verify", "chain"],
+                    help="where the softmax statistics of q are reduced: in verify's streaming "
+                         "pass over the draft logits, or in the Markov chain kernel")
     return ap.parse_args()
 
 
@@ -388,7 +391,8 @@ def run_ours(args, rank, local_rank, world):
     h_buf = torch.empty((M, H), dtype=torch.bfloat16, device=device)
     logits = torch.empty((B, k, V), dtype=torch.float32, device=device)
     drafts = torch.empty((B, k), dtype=torch.int32, device=device)
-    q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=device)
+    q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=device) \
+        if (args.q_stats == "chain" and mode == 1) else None
     dlen = torch.empty((B,), dtype=torch.int32, device=device) if cfg["conf"] else None
     K, W = args.steps, args.warmup
     acc_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
@@ -411,6 +415,7 @@ def run_ours(args, rank, local_rank, world):
         if ev is not None:
             ev[2].record(s)
         ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
+                         want_q_stats=q_stats is not None,
                          stream=s, workspaces=wsp)
         if conf_w is not None:
             ds.confidence_truncate(h_buf, conf_w, drafts, B, k, w_conf_b, w_conf_tau,
@@ -418,7 +423,7 @@ def run_ours(args, rank, local_rank, world):
         if ev is not None:
             ev[3].record(s)
         ds.verify(mode, st["target"], drafts, dlen_o if conf_w is not None else None,
-                  logits if mode == 1 else None, q_stats if mode == 1 else None, seed=12345,
+                  logits if mode == 1 else None, q_stats, seed=12345,
                   request_id=None, step=i, accepted_len=acc_o, next_token=nxt_o,
                   stream=s, workspaces=wsp)
         if ev is not None:
@@ -562,7 +567,7 @@ def run_ours(args, rank, local_rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": args.config, "B": B, "k": k, "H": H, "taps": T, "V": V, "r": r,
-                   "verify": "probabilistic" if mode == 1 else "greedy",
+                   "verify": "probabilistic" if mode == 1 else "greedy", "q_stats_in": args.q_stats,
                    "confidence_head": bool(conf_w is not None),
                    "weights": "e4m3 codes + fp32 row scales (fc, LM head)" if fp8 else "bf16",
                    "l2": "inputs larger than L2: %.2f GB of weights streamed per step"

@@ -212,9 +212,10 @@ def lm_head(h, lm_w, out=None, stream=None, workspaces=None):
 
 
 def greedy_sample(logits, w1, w2, prev_token, draft_tokens=None, q_stats=None, stream=None,
-                  workspaces=None):
+                  workspaces=None, want_q_stats=True):
     """Markov-biased greedy drafting.  logits fp32 [B, k, V] is biased in place; returns
-    (draft_tokens int32 [B, k], q_stats fp32 [B, k, 2])."""
+    (draft_tokens int32 [B, k], q_stats fp32 [B, k, 2]).  want_q_stats=False passes no
+    q_stats buffer (the kernel then reduces only the argmax) and returns None for it."""
     B, k, V = logits.shape
     _need(logits, "logits", torch.float32)
     r = 0
@@ -226,10 +227,13 @@ def greedy_sample(logits, w1, w2, prev_token, draft_tokens=None, q_stats=None, s
     dev = logits.device
     if draft_tokens is None:
         draft_tokens = torch.empty((B, k), dtype=torch.int32, device=dev)
-    if q_stats is None:
+    if not want_q_stats:
+        q_stats = None
+    elif q_stats is None:
         q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
-    _need(q_stats, "q_stats", torch.float32, (B, k, 2))
+    if q_stats is not None:
+        _need(q_stats, "q_stats", torch.float32, (B, k, 2))
     L = lib()
     ws = (workspaces or _default_ws).get("chain", dev, L.dspark_greedy_sample_workspace_size(B, k, V, r))
     _check(L.dspark_greedy_sample(_ptr(logits), _ptr(w1), _ptr(w2), r, _ptr(prev_token),

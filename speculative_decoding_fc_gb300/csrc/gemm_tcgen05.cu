@@ -492,9 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
     }
   }
 
+  // The producer and MMA warps ran their loops on one lane: converge each warp
+  // before the CTA barrier so that every warp arrives whole, and only then free
+  // the tensor memory the epilogue warps read.
+  __syncwarp();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(p.tmem_cols)

@@ -329,7 +329,9 @@ __device__ __forceinline__ void warp_key_stats(unsigned long long &key, float &m
   s = ss;
 }
 
-template <int G, int CPR>
+// kStats: also reduce the softmax statistics of q (max z, sum exp(z - max)) for
+// q_stats; without it only the argmax keys are reduced.
+template <int G, int CPR, bool kStats>
 __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const ChainPArgs a) {
   static_assert(G <= kPWarps, "one combining warp per request of a group");
   __shared__ ChainPartial red[kGroup][kPWarps];
@@ -464,31 +466,64 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
               for (int j = 0; j < kPRows; ++j) acc[j][g] = __fmaf_rn(w[j][t], e[g][t], acc[j][g]);
         }
       }
+      // Per thread: argmax key (and statistics) of its rows for every request of the
+      // group; then warp reductions, one shuffle round for all requests at a time so
+      // that the requests' shuffle latencies overlap.
+      unsigned long long key[G];
+      float mx[G], sm[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        if (g < gb) {
-          unsigned long long key = 0ull;
-          float m = -INFINITY, sum = 0.0f;
-          float zv[kPRows];
+        key[g] = 0ull;
+        mx[g] = -INFINITY;
+        sm[g] = 0.0f;
+        float zv[kPRows];
 #pragma unroll
-          for (int j = 0; j < kPRows; ++j) {
-            float z = lg_next[j][g];
-            if (biased) z = __fadd_rn(z, acc[j][g]);
-            zv[j] = z;
-            acc[j][g] = z;  // kept for the write-back after this position's release
-            if (valid[j]) {
-              const unsigned long long kj = argmax_key(z, static_cast<uint32_t>(vrow[j]));
-              key = kj > key ? kj : key;
-              if (z == z && z != -INFINITY) m = fmaxf(m, z);
-            }
+        for (int j = 0; j < kPRows; ++j) {
+          float z = lg_next[j][g];
+          if (biased) z = __fadd_rn(z, acc[j][g]);
+          zv[j] = z;
+          acc[j][g] = z;  // kept for the write-back after this position's words
+          if (valid[j] && g < gb) {
+            const unsigned long long kj = argmax_key(z, static_cast<uint32_t>(vrow[j]));
+            key[g] = kj > key[g] ? kj : key[g];
+            if (kStats && z == z && z != -INFINITY) mx[g] = fmaxf(mx[g], z);
           }
+        }
+        if (kStats) {
 #pragma unroll
           for (int j = 0; j < kPRows; ++j)
-            if (valid[j] && m != -INFINITY && zv[j] == zv[j] && zv[j] != -INFINITY)
-              sum += expf(zv[j] - m);
-          warp_key_stats(key, m, sum);
-          if (lane == 0) red[g][warp] = ChainPartial{key, m, sum};
+            if (valid[j] && g < gb && mx[g] != -INFINITY && zv[j] == zv[j] && zv[j] != -INFINITY)
+              sm[g] += expf(zv[j] - mx[g]);
         }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const unsigned long long other = __shfl_xor_sync(0xffffffffu, key[g], o);
+          key[g] = other > key[g] ? other : key[g];
+        }
+      if (kStats) {
+        float mm[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) mm[g] = mx[g];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) mm[g] = fmaxf(mm[g], __shfl_xor_sync(0xffffffffu, mm[g], o));
+#pragma unroll
+        for (int g = 0; g < G; ++g) sm[g] = (mx[g] == -INFINITY) ? 0.0f : sm[g] * expf(mx[g] - mm[g]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) sm[g] += __shfl_xor_sync(0xffffffffu, sm[g], o);
+#pragma unroll
+        for (int g = 0; g < G; ++g) mx[g] = mm[g];
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g < gb) red[g][warp] = ChainPartial{key[g], mx[g], sm[g]};
       }
       __syncthreads();
       // one warp per request of the group combines the 16 warp partials
@@ -502,10 +537,13 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
           m = c0.m;
           sum = c0.s;
         }
-        warp_key_stats(key, m, sum);
+        if (kStats)
+          warp_key_stats(key, m, sum);
+        else
+          key = warp_max_u64(key);
         if (lane == 0) {
           const long long at = (static_cast<long long>(pos) * B + g0 + g) * grid + cta;
-          a.partials[at] = ChainPartial{key, m, sum};
+          if (kStats) a.partials[at] = ChainPartial{key, m, sum};
           // This thread wrote every partial of this request (the combining warp of a
           // request is fixed), so the release on the last position's word makes all
           // of them visible to whoever sees that word.
@@ -600,9 +638,11 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
     if (stop_s) return;
   }
 
+  if (!kStats && a.draft_len_fill && cta == 0)
+    for (int b = tid; b < B; b += kPThreads) a.draft_len_fill[b] = k;
   // Off the critical path: softmax statistics of q for every (position, request),
   // spread over the CTAs, one warp each.
-  if (a.q_stats || a.draft_len_fill) {
+  if (kStats) {
     const int pairs = k * B;
     for (int pr = cta * kPWarps + warp; pr < pairs; pr += grid * kPWarps) {
       const int pos = pr / B, b = pr - pos * B;
@@ -713,7 +753,7 @@ size_t chain_workspace_size(int B, int k, int V) {
 
 namespace {
 
-template <int G, int CPR>
+template <int G, int CPR, bool kStats>
 bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
@@ -729,7 +769,7 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
   const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + static_cast<size_t>(B) * CPR * 32 +
                       static_cast<size_t>(B) * sizeof(int);
   if (smem > 200 * 1024) return false;
-  auto kern = markov_chain_persistent<G, CPR>;
+  auto kern = markov_chain_persistent<G, CPR, kStats>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
@@ -750,15 +790,21 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
   return true;
 }
 
-template <int G>
-bool try_persistent(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
+template <int G, bool kStats>
+bool try_persistent_s(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
   switch (r) {
-    case 0: return try_persistent_r<G, 1>(a, B, V, stream);  // no bias: rank unused
-    case 16: return try_persistent_r<G, 2>(a, B, V, stream);
-    case 32: return try_persistent_r<G, 4>(a, B, V, stream);
-    case 64: return try_persistent_r<G, 8>(a, B, V, stream);
+    case 0: return try_persistent_r<G, 1, kStats>(a, B, V, stream);  // no bias: rank unused
+    case 16: return try_persistent_r<G, 2, kStats>(a, B, V, stream);
+    case 32: return try_persistent_r<G, 4, kStats>(a, B, V, stream);
+    case 64: return try_persistent_r<G, 8, kStats>(a, B, V, stream);
     default: return false;  // other ranks: per-position kernels
   }
+}
+
+template <int G>
+bool try_persistent(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
+  return a.q_stats ? try_persistent_s<G, true>(a, r, B, V, stream)
+                   : try_persistent_s<G, false>(a, r, B, V, stream);
 }
 
 }  // namespace

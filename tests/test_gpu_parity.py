@@ -120,6 +120,27 @@ def test_greedy_sample_bit_exact(B, k, V, r):
     np.testing.assert_allclose(q[..., 1], ref["q_sumexp"], rtol=1e-5)
 
 
+@pytest.mark.parametrize("B,k,V,r", [(1, 7, 4096, 16), (3, 4, 5001, 16), (16, 7, 20000, 64),
+                                     (9, 16, 3001, 32), (1, 7, 20000, 0)])
+def test_greedy_sample_without_q_stats_bit_exact(B, k, V, r):
+    """Without a q_stats buffer the chain reduces only the argmax keys (another kernel
+    variant): z and the draft tokens stay bit-exact, and draft_len is not touched."""
+    logits = syn.uniform_logits(41 + V, (B, k, V), 1.5)
+    if r:
+        w1 = syn.normal_bf16(42, (V, r))
+        w2 = syn.normal_bf16(43, (V, r), (1.0 / r) ** 0.5)
+    else:
+        w1 = w2 = None
+    prev = (np.arange(B, dtype=np.int64) * 7919 % V).astype(np.int32)
+    ref = oracle.greedy_sample(logits, w1, w2, prev)
+    lg = dev(logits)
+    d, qs = ds.greedy_sample(lg, dev_bf16(w1) if r else None, dev_bf16(w2) if r else None,
+                             dev(prev), want_q_stats=False)
+    assert qs is None
+    np.testing.assert_array_equal(host(d), ref["draft_tokens"])
+    np.testing.assert_array_equal(host(lg), ref["z"])
+
+
 def test_greedy_sample_per_position_kernels_agree(monkeypatch):
     """The per-position kernels (used when a cooperative launch is not possible) give
     the same bits as the persistent kernel and the oracle."""
