@@ -3,6 +3,7 @@
 // memory or synchronises the host (except dspark_workspace_status, which is a
 // diagnostic read).
 #include <cuda_runtime.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <cmath>
@@ -20,6 +21,14 @@ std::atomic<long long> g_launches{0};
 }
 
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("DSPARK_NO_PDL");
+    return !(e && e[0] == '1');
+  }();
+  return on;
+}
 
 int device_sm_count() {
   static int cache[64] = {};

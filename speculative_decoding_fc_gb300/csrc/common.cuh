@@ -18,6 +18,17 @@ __device__ __forceinline__ void record_error(int *status, int code) {
 // descending): the maximum key is the largest value at its lowest index.
 // -0 is folded onto +0 so the two compare equal; NaN maps below every
 // number so it never wins.
+// Programmatic dependent launch.  Every kernel of the library is launched so that it
+// may start while the previous kernel on the stream is still finishing: it calls
+// pdl_wait() before its first access to global memory that an earlier kernel may
+// have written (and before any global write), and pdl_release() once the next
+// kernel may be scheduled.  Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t ordered_bits(float x) {
   uint32_t u = __float_as_uint(x);
   if ((u & 0x7fffffffu) == 0u) u = 0u;                       // -0 -> +0

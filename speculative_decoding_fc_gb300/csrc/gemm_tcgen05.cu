@@ -288,6 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Everything above touched only shared and tensor memory: from here on the
+  // previous kernel's results are needed.  One wave of persistent CTAs: the next
+  // kernel may be scheduled right away (its CTAs take SMs as these exit).
+  pdl_wait();
+  pdl_release();
 
   const Range rg = cta_range(p.units, cta, grid);
   const int kbt = p.kb_total;
@@ -653,8 +658,9 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
       return DSPARK_ERR_CUDA;
     if (dev >= 0 && dev < 64) configured[pr.fp8 ? 1 : 0][dev] = true;
   }
-  kern<<<static_cast<unsigned>(grid), kThreads, t.smem, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), t.smem, stream, p) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;
 }

@@ -73,6 +73,30 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
                               int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
                               void *ws, int *status, cudaStream_t stream);
 
+// ------------------------------------------------------------------ launches
+// Whether kernels are launched with programmatic dependent launch (default on;
+// DSPARK_NO_PDL=1 turns it off).
+bool pdl_enabled();
+
+// cudaLaunchKernelEx with programmatic stream serialization allowed (when enabled):
+// the kernel may start before the previous kernel on the stream completes and
+// orders itself with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ------------------------------------------------------------------ launch accounting
 // Counts every kernel this library enqueues (reported by dspark_launch_count).
 void count_launches(int n);

@@ -57,6 +57,8 @@ __global__ void __launch_bounds__(kThreads) markov_chain_kernel(
   __shared__ __align__(16) float e_s[kGroup * kMaxRank];
   __shared__ ChainPartial red[kGroup][kWarps];
   __shared__ int is_last;
+  pdl_wait();
+  pdl_release();  // one wave: the next position's kernel may be scheduled
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -362,6 +364,21 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
     vrow[j] = v_lo + (row < nrows ? row : (nrows > 0 ? nrows - 1 : 0));
   }
 
+  // Before the previous kernel has finished: warm L2 with this CTA's markov_w2
+  // slice (a prefetch reads nothing into the program, so it cannot observe data
+  // that is still being written).  Then wait for the previous kernel.
+  if (biased && nrows > 0) {
+    // 16 KB pieces, one per thread (the slice is at most 2048 rows x 512 bytes)
+    const char *src = reinterpret_cast<const char *>(a.w2 + static_cast<long long>(v_lo) * r);
+    const uint32_t bytes = static_cast<uint32_t>(nrows) * CPR * 16u;
+    const uint32_t off = static_cast<uint32_t>(tid) * 16384u;
+    if (off < bytes) {
+      const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + off), "r"(n) : "memory");
+    }
+  }
+  pdl_wait();
+  pdl_release();
   if (tid == 0) {
     stop_s = ld_acquire(a.abort_flag);
     epoch_s = ld_acquire(a.epoch);
@@ -692,6 +709,8 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(
     const uint16_t *__restrict__ h, const uint16_t *__restrict__ conf_w, float conf_b, float thr,
     int32_t *draft_tokens, int32_t *draft_len, float *conf_out, int k, int H) {
   __shared__ float red[kConfThreads / 32];
+  pdl_wait();
+  pdl_release();  // one CTA per request: one wave
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -781,6 +800,25 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
     }
     attr_set[dev] = true;
   }
+  // Cooperative (all CTAs resident together: they wait on each other), and, when
+  // enabled, with programmatic dependent launch; without the latter if the
+  // combination is refused.
+  if (pdl_enabled()) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, a) == cudaSuccess) return true;
+    cudaGetLastError();
+  }
   void *params[] = {const_cast<ChainPArgs *>(&a)};
   if (cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid),
                                   dim3(kPThreads), params, smem, stream) != cudaSuccess) {
@@ -861,10 +899,10 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
     auto kern = B >= 8 ? markov_chain_kernel<8>
                        : (B >= 4 ? markov_chain_kernel<4>
                                  : (B >= 2 ? markov_chain_kernel<2> : markov_chain_kernel<1>));
-    kern<<<nchunks, kThreads, 0, stream>>>(logits, w1, w2, r, prev_src, prev_stride, draft_tokens,
-                                           q_stats, draft_len_fill, B, k, V, pos, nchunks,
-                                           partials, counter, status);
-    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (launch_pdl(kern, dim3(nchunks), dim3(kThreads), 0, stream, logits, w1, w2, r, prev_src,
+                   prev_stride, draft_tokens, q_stats, draft_len_fill, B, k, V, pos, nchunks,
+                   partials, counter, status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
     count_launches(1);
   }
   return DSPARK_OK;
@@ -880,9 +918,9 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
     thr = INFINITY;
   else
     thr = static_cast<float>(log(static_cast<double>(conf_tau)) - log1p(-static_cast<double>(conf_tau)));
-  confidence_kernel<<<B, kConfThreads, 0, stream>>>(h, conf_w, conf_b, thr, draft_tokens,
-                                                    draft_len, conf_out, k, H);
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(confidence_kernel, dim3(B), dim3(kConfThreads), 0, stream, h, conf_w, conf_b, thr,
+                 draft_tokens, draft_len, conf_out, k, H) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;
 }

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const __grid_co
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const int c8 = a.seg_cols / 8;  // 16-byte chunks of a segment row
+  pdl_wait();
   float amax = 0.0f;
   for (int sgi = 0; sgi < a.nseg; ++sgi) {
     const uint4 *src = reinterpret_cast<const uint4 *>(a.segs[sgi] + row * a.seg_ld);
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const __grid_co
       dst[i] = make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
     }
   }
+  pdl_release();  // after this CTA's work: the grid may span many waves
 }
 
 }  // namespace
@@ -92,8 +94,8 @@ dspark_status_t quantize_fp8_launch(const uint16_t *const *segs, int nseg, int64
   a.seg_cols = seg_cols;
   a.codes = codes;
   a.scales = scales;
-  quantize_rows_kernel<<<rows, kThreads, 0, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(quantize_rows_kernel, dim3(rows), dim3(kThreads), 0, stream, a) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;
 }

@@ -481,7 +481,9 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
   const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
   const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
   const RowRef rr = row_ref(a, rho);
+  pdl_wait();
   if (row_needed(a, rr)) stats_item(a, rho, slice, red);
+  pdl_release();  // after this CTA's pass: the grid may span many waves
   const int rows_per_req = (a.k + 1) + (a.zrows ? a.k : 0);
   if (!last_arrival(a.req_ticket, rr.b, rows_per_req * a.nslices, &flag_s)) return;
   decide_request(a, rr.b, dec, true);
@@ -499,8 +501,10 @@ __global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArg
   __shared__ int flag_s;
   const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.ndraw));
   const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.ndraw));
+  pdl_wait();
   const SampleJob job = a.jobs[b];
   draw_item(a, job, b, slice, red_r, red_p);
+  pdl_release();
   if (!last_arrival(a.samp_ticket, b, a.ndraw, &flag_s)) return;
   if (threadIdx.x < 32) finish_draw(a, b);
 }
@@ -573,14 +577,16 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
   const long long nrows = static_cast<long long>(B) * (k + 1) + (a.zrows ? static_cast<long long>(B) * k : 0);
   const long long g1 = nrows * L.nslices;
 
-  verify_stats_kernel<<<static_cast<unsigned>(g1), kThreads, 0, stream>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(verify_stats_kernel, dim3(static_cast<unsigned>(g1)), dim3(kThreads), 0, stream,
+                 a) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   count_launches(1);
   if (mode == 1) {
     const long long g2 = static_cast<long long>(B) * L.ndraw;
     if (g2 > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
-    verify_sample_kernel<<<static_cast<unsigned>(g2), kThreads, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (launch_pdl(verify_sample_kernel, dim3(static_cast<unsigned>(g2)), dim3(kThreads), 0, stream,
+                   a) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
     count_launches(1);
   }
   return DSPARK_OK;
