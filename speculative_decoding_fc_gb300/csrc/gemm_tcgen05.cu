@@ -20,6 +20,8 @@
 //     weight bytes whatever the tile count.  A tile cut between CTAs is
 //     finished by the last CTA to arrive (atomic ticket, no spinning), which
 //     adds the fp32 partials in CTA order: results do not depend on timing.
+//     The fix-up keeps up to four pieces' loads in flight at once (one L2 round
+//     trip per 16 columns for up to four pieces).
 //   * Operands are 128-byte-swizzled K-major tiles (64 bf16 of K per row) as
 //     TMA writes them; the UMMA shared-memory descriptors describe exactly that
 //     layout.  Weights are loaded with an L2 evict-first policy, activations
@@ -466,24 +468,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
         if (ticket == nseg - 1) {
           __threadfence();
           const int mcount = min(p.BN, p.M - m_base);
-          // 16 columns at a time: the 16 loads of one piece are independent, so each
-          // piece costs one memory latency; pieces are added in CTA order.
+          // 16 columns at a time, the loads of up to four pieces issued together;
+          // pieces are added in CTA order.
           for (int c0 = 0; c0 < mcount; c0 += 16) {
             float acc[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-            for (int sg = 0; sg < nseg; ++sg) {
-              const int c2 = c_first + sg;
-              const int tile_c2 = static_cast<int>((p.units * c2 / grid) / kbt);
-              const int slot = (tile == tile_c2) ? 0 : 1;
-              const float *src = p.partials + (static_cast<size_t>(c2) * 2 + slot) *
-                                                  static_cast<size_t>(p.BN) * kBM;
-              float v[16];
+            for (int s0 = 0; s0 < nseg; s0 += 4) {
+              float v[4][16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                v[j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+              for (int q = 0; q < 4; ++q) {
+                if (s0 + q < nseg) {
+                  const int c2 = c_first + s0 + q;
+                  const int tile_c2 = static_cast<int>((p.units * c2 / grid) / kbt);
+                  const int slot = (tile == tile_c2) ? 0 : 1;
+                  const float *src = p.partials + (static_cast<size_t>(c2) * 2 + slot) *
+                                                      static_cast<size_t>(p.BN) * kBM;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) acc[j] += v[j];
+                  for (int j = 0; j < 16; ++j)
+                    v[q][j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+                }
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (s0 + q < nseg)
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) acc[j] += v[q][j];
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j)
