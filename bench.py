@@ -50,6 +50,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sets", type=int, default=4, help="input sets rotated across steps")
     ap.add_argument("--no-graph", action="store_true", help="time un-captured steps only")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the 27B sweep grid instead (one JSON line per cell, not the "
+                         "headline line): B x k x r x sigma, probabilistic verify")
+    ap.add_argument("--sweep-steps", type=int, default=200, help="timed steps per sweep cell")
     ap.add_argument("--q-stats", default="verify", choices=["verify", "chain"],
                     help="where the softmax statistics of q are reduced: in verify's streaming "
                          "pass over the draft logits, or in the Markov chain kernel")
@@ -560,6 +564,11 @@ def run_ours(args, rank, local_rank, world):
     lm_bytes = sb["lm_head"]
     achieved = lm_bytes / (lm_ms / 1000.0) / 1e9
     t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
+    # readout (fc + LM head + chain) and verify against their own rooflines
+    t_readout = max((sb["fc"] + sb["lm_head"] + sb["chain"]) / (peak_gbs * 1e9),
+                    step_flops(cfg) / (peak_tf * 1e12))
+    t_verify = sb["verify"] / (peak_gbs * 1e9)
+    readout_ms = stage_ms["fc_project"] + stage_ms["lm_head"] + stage_ms["greedy_sample"]
 
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
@@ -586,7 +595,10 @@ def run_ours(args, rank, local_rank, world):
                      "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
         "step_roofline": {"bytes": sb["total"], "flops": step_flops(cfg),
                           "t_roofline_ms": t_roof * 1000.0,
-                          "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src},
+                          "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src,
+                          "readout_frac": t_readout * 1000.0 / readout_ms,
+                          "verify_frac": t_verify * 1000.0 / stage_ms["verify"],
+                          "stage_times": "per-stage CUDA events of the staged loop"},
         "graph": graphs is not None,
         "graph_error": graph_error,
         "uncaptured": {"value": whole_job_rate(K, world, plain_ms / 1000.0), "unit": "steps/s",
@@ -617,11 +629,134 @@ def run_ours(args, rank, local_rank, world):
     return 0
 
 
+# ----------------------------------------------------------------------------- sweep
+
+SWEEP_B = (1, 2, 4, 8, 16, 32, 64)
+SWEEP_K = (4, 6, 7)
+SWEEP_R = (32, 128)
+SWEEP_SIGMA = (0.5, 2.0)
+
+
+def run_sweep(args):
+    """27B shapes over B x k x r x sigma (84 cells), probabilistic verify.  Per cell:
+    3 input sets (taps, prev tokens, target = own draft logits + sigma * N(0, 1)), one
+    CUDA graph per set, W = 3 warm-up and --sweep-steps timed replays rotating the sets
+    (1.8-2.2 GB of weights stream from HBM every step).  Prints one JSON line per cell:
+    steps/s, drafted tok/s, acceptance and the step's roofline fraction."""
+    import torch
+
+    import speculative_decoding_fc_gb300 as ds
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    H, T, V = 5120, 5, 151936
+    peak_gbs, peak_tf, peak_src = measured_peaks()
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    base = syn.weights(H, T, V, 8, with_markov=False)
+    fc_w, lm_w = d16(base["fc_w"]), d16(base["lm_w"])
+    del base
+    stream = torch.cuda.current_stream(device)
+    wsp = ds.Workspaces()
+    nsets = 3
+    for r in SWEEP_R:
+        mk = syn.weights(8, 1, V, r, with_markov=True)
+        w1, w2 = d16(mk["w1"]), d16(mk["w2"])
+        del mk
+        for B in SWEEP_B:
+            for k in SWEEP_K:
+                # unit-variance noise and taps per input set, shared by both sigmas
+                raw = [syn.step_inputs(replica_step_seed(si, 0), B, k, H, T, V, ("const", 1.0))
+                       for si in range(nsets)]
+                M = B * k
+                h_buf = torch.empty((M, H), dtype=torch.bfloat16, device=device)
+                logits = torch.empty((B, k, V), dtype=torch.float32, device=device)
+                drafts = torch.empty((B, k), dtype=torch.int32, device=device)
+                acc_o = torch.zeros((B,), dtype=torch.int32, device=device)
+                nxt_o = torch.zeros((B,), dtype=torch.int32, device=device)
+                dev_sets = []
+                for st in raw:
+                    taps = [d16(t) for t in st["taps"]]
+                    prev = torch.from_numpy(st["prev"]).to(device)
+                    h = ds.fc_project(taps, fc_w)
+                    lg = ds.lm_head(h, lm_w).view(B, k, V)
+                    ds.greedy_sample(lg, w1, w2, prev, want_q_stats=False)
+                    own = torch.cat([lg, lg[:, -1:]], dim=1)
+                    dev_sets.append({"taps": taps, "prev": prev, "own": own,
+                                     "noise": torch.from_numpy(st["noise"]).to(device)})
+                del raw
+                for sigma in SWEEP_SIGMA:
+                    for st in dev_sets:
+                        st["target"] = (st["own"] + st["noise"] * sigma).contiguous()
+
+                    def one_step(st, s):
+                        ds.fc_project(st["taps"], fc_w, out=h_buf, stream=s, workspaces=wsp)
+                        ds.lm_head(h_buf, lm_w, out=logits.view(M, V), stream=s, workspaces=wsp)
+                        ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts,
+                                         want_q_stats=False, stream=s, workspaces=wsp)
+                        ds.verify(1, st["target"], drafts, None, logits, None, seed=0,
+                                  request_id=None, step=0, accepted_len=acc_o, next_token=nxt_o,
+                                  stream=s, workspaces=wsp)
+
+                    for st in dev_sets:        # eager warm-up (workspaces, first launches)
+                        one_step(st, stream)
+                    torch.cuda.synchronize()
+                    cap = torch.cuda.Stream(device)
+                    cap.wait_stream(stream)
+                    graphs = []
+                    for st in dev_sets:
+                        g = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(g, stream=cap):
+                            one_step(st, cap)
+                        graphs.append(g)
+                    stream.wait_stream(cap)
+                    for i in range(3):
+                        graphs[i % nsets].replay()
+                    torch.cuda.synchronize()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    acc_sum = 0
+                    e0.record(stream)
+                    for i in range(args.sweep_steps):
+                        graphs[i % nsets].replay()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ms = e0.elapsed_time(e1) / args.sweep_steps
+                    # acceptance of one step on each set (outside the timed loop)
+                    for g in graphs:
+                        g.replay()
+                        torch.cuda.synchronize()
+                        acc_sum += int(acc_o.sum().item())
+                    cfg = dict(B=B, k=k, H=H, T=T, V=V, r=r)
+                    sb = step_bytes(cfg, 1)
+                    t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
+                    bound = "hbm" if sb["total"] / (peak_gbs * 1e9) >= step_flops(cfg) / (peak_tf * 1e12) \
+                        else "tensor"
+                    sps = 1000.0 / ms
+                    print(json.dumps({
+                        "sweep_cell": {"B": B, "k": k, "r": r, "sigma": sigma},
+                        "steps_per_s": sps, "ms_per_step": ms, "drafted_tok_s": sps * B * k,
+                        "mean_acceptance_length": acc_sum / (nsets * B) + 1.0,
+                        "roofline": {"bound": bound, "t_roofline_ms": t_roof * 1000.0,
+                                     "frac": t_roof * 1000.0 / ms, "peak_source": peak_src},
+                        "steps": args.sweep_steps, "warmup": 3, "input_sets": nsets,
+                        "dtype": "bf16", "data": "synthetic"}), flush=True)
+                    del graphs
+                del dev_sets, h_buf, logits
+                torch.cuda.empty_cache()
+        del w1, w2
+    return 0
+
+
 def main():
     args = parse_args()
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.sweep:
+        return run_sweep(args) if rank == 0 else 0
     return run_ours(args, rank, local_rank, world)
 
 
