@@ -14,7 +14,8 @@
 //    SM.  Each CTA owns a contiguous slice of the vocabulary for all k
 //    positions and keeps its slice of markov_w2 in shared memory (XOR-swizzled
 //    16-byte chunks, bank-conflict free), so the weight is read from memory
-//    once per step instead of once per position.  Positions are separated by
+//    once per step instead of once per position (r <= 64; at r = 128 the slice
+//    is prefetched into L2 and read from there at every position).  Positions are separated by
 //    tagged 64-bit words: every CTA publishes, per request, one word holding a
 //    tag of (call, position) and its slice's argmax key, and every CTA polls all
 //    CTAs' words until they carry the current tag.  The polled words are the data
@@ -333,7 +334,10 @@ __device__ __forceinline__ void warp_key_stats(unsigned long long &key, float &m
 
 // kStats: also reduce the softmax statistics of q (max z, sum exp(z - max)) for
 // q_stats; without it only the argmax keys are reduced.
-template <int G, int CPR, bool kStats>
+// kW2Smem: the CTA's markov_w2 slice is copied to shared memory once (r <= 64);
+// otherwise (r = 128: 38.9 MB, more than the SMs' shared memory together) the slice
+// is prefetched into L2 and read from there at every position.
+template <int G, int CPR, bool kStats, bool kW2Smem>
 __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const ChainPArgs a) {
   static_assert(G <= kPWarps, "one combining warp per request of a group");
   __shared__ ChainPartial red[kGroup][kPWarps];
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   // slice (a prefetch reads nothing into the program, so it cannot observe data
   // that is still being written).  Then wait for the previous kernel.
   if (biased && nrows > 0) {
-    // 16 KB pieces, one per thread (the slice is at most 2048 rows x 512 bytes)
+    // 16 KB pieces, one per thread (the slice is at most 1024 rows x 256 bytes)
     const char *src = reinterpret_cast<const char *>(a.w2 + static_cast<long long>(v_lo) * r);
     const uint32_t bytes = static_cast<uint32_t>(nrows) * CPR * 16u;
     const uint32_t off = static_cast<uint32_t>(tid) * 16384u;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   // markov_w2 slice -> shared memory (16-byte chunks XOR-swizzled by row so that 8
   // consecutive rows read at the same chunk hit 8 bank groups), asynchronous copies
   // all in flight together.
-  if (biased) {
+  if (biased && kW2Smem) {
     const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
     for (int i = tid; i < nrows * CPR; i += kPThreads) {
       const int row = i / CPR, q = i - row * CPR;
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
     }
     prev_s[b] = p;
   }
-  if (biased) asm volatile("cp.async.wait_all;" ::: "memory");
+  if (biased && kW2Smem) asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (stop_s) return;
   const int epoch = epoch_s;
@@ -453,11 +457,17 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
         for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
       if (biased) {
 #pragma unroll
+#pragma unroll
         for (int q = 0; q < CPR; ++q) {
           float w[kPRows][8];
 #pragma unroll
           for (int j = 0; j < kPRows; ++j) {
-            const uint4 c = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+            uint4 c;
+            if constexpr (kW2Smem) {
+              c = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+            } else {
+              c = __ldg(reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(vrow[j]) * r) + q);
+            }
             w[j][0] = bf16_lo(c.x); w[j][1] = bf16_hi(c.x);
             w[j][2] = bf16_lo(c.y); w[j][3] = bf16_hi(c.y);
             w[j][4] = bf16_lo(c.z); w[j][5] = bf16_hi(c.z);
@@ -702,25 +712,24 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 }
 
 // c[b, i] = sigmoid(w . h[b*k+i] + bias); draft_len[b] = first i whose logit
-// falls below thr = logit(tau); later drafts are replaced by -1.
-constexpr int kConfThreads = 256;
-
-__global__ void __launch_bounds__(kConfThreads) confidence_kernel(
+// falls below thr = logit(tau); later drafts are replaced by -1.  One CTA per
+// request, one warp per block position (all k dot products at once).
+__global__ void __launch_bounds__(32 * kMaxK) confidence_kernel(
     const uint16_t *__restrict__ h, const uint16_t *__restrict__ conf_w, float conf_b, float thr,
     int32_t *draft_tokens, int32_t *draft_len, float *conf_out, int k, int H) {
-  __shared__ float red[kConfThreads / 32];
+  __shared__ float zc_s[kMaxK];
+  __shared__ int len_s;
   pdl_wait();
   pdl_release();  // one CTA per request: one wave
   const int b = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  int len = k;
-  for (int i = 0; i < k; ++i) {
-    const uint4 *hrow = reinterpret_cast<const uint4 *>(h + (static_cast<long long>(b) * k + i) * H);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp < k) {
+    const uint4 *hrow = reinterpret_cast<const uint4 *>(h + (static_cast<long long>(b) * k + warp) * H);
     const uint4 *wrow = reinterpret_cast<const uint4 *>(conf_w);
     float acc = 0.0f;
-    for (int c = tid; c < H / 8; c += kConfThreads) {
+#pragma unroll 4
+    for (int c = lane; c < H / 8; c += 32) {
       const uint4 hv = __ldg(hrow + c);
       const uint4 wv = __ldg(wrow + c);
       acc = __fmaf_rn(bf16_lo(wv.x), bf16_lo(hv.x), acc);
@@ -734,21 +743,26 @@ __global__ void __launch_bounds__(kConfThreads) confidence_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) red[warp] = acc;
-    __syncthreads();
-    if (tid == 0) {
-      float zc = 0.0f;
-      for (int w = 0; w < kConfThreads / 32; ++w) zc += red[w];
-      zc += conf_b;
-      if (conf_out) conf_out[static_cast<long long>(b) * k + i] = 1.0f / (1.0f + expf(-zc));
-      if (len == k && !(zc >= thr)) len = i;
+    if (lane == 0) {
+      const float zc = acc + conf_b;
+      zc_s[warp] = zc;
+      if (conf_out) conf_out[static_cast<long long>(b) * k + warp] = 1.0f / (1.0f + expf(-zc));
     }
-    __syncthreads();
   }
-  if (tid == 0) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int len = k;
+    for (int i = 0; i < k; ++i)
+      if (!(zc_s[i] >= thr)) {
+        len = i;
+        break;
+      }
+    len_s = len;
     draft_len[b] = len;
-    for (int i = len; i < k; ++i) draft_tokens[static_cast<long long>(b) * k + i] = -1;
   }
+  __syncthreads();
+  if (threadIdx.x < k && threadIdx.x >= len_s)
+    draft_tokens[static_cast<long long>(b) * k + threadIdx.x] = -1;
 }
 
 }  // namespace
@@ -772,7 +786,7 @@ size_t chain_workspace_size(int B, int k, int V) {
 
 namespace {
 
-template <int G, int CPR, bool kStats>
+template <int G, int CPR, bool kStats, bool kW2Smem>
 bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
@@ -783,12 +797,13 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
   if (rows > kPRows * kPThreads) return false;
   ChainPArgs a = args0;
   a.rows_per_cta = rows;
-  a.w2_in_smem = 1;
-  a.w2_smem_bytes = static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024));
+  a.w2_in_smem = kW2Smem ? 1 : 0;
+  a.w2_smem_bytes =
+      kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
   const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + static_cast<size_t>(B) * CPR * 32 +
                       static_cast<size_t>(B) * sizeof(int);
   if (smem > 200 * 1024) return false;
-  auto kern = markov_chain_persistent<G, CPR, kStats>;
+  auto kern = markov_chain_persistent<G, CPR, kStats, kW2Smem>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
@@ -831,10 +846,11 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
 template <int G, bool kStats>
 bool try_persistent_s(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
   switch (r) {
-    case 0: return try_persistent_r<G, 1, kStats>(a, B, V, stream);  // no bias: rank unused
-    case 16: return try_persistent_r<G, 2, kStats>(a, B, V, stream);
-    case 32: return try_persistent_r<G, 4, kStats>(a, B, V, stream);
-    case 64: return try_persistent_r<G, 8, kStats>(a, B, V, stream);
+    case 0: return try_persistent_r<G, 1, kStats, true>(a, B, V, stream);  // no bias: rank unused
+    case 16: return try_persistent_r<G, 2, kStats, true>(a, B, V, stream);
+    case 32: return try_persistent_r<G, 4, kStats, true>(a, B, V, stream);
+    case 64: return try_persistent_r<G, 8, kStats, true>(a, B, V, stream);
+    case 128: return try_persistent_r<G, 16, kStats, false>(a, B, V, stream);
     default: return false;  // other ranks: per-position kernels
   }
 }
@@ -918,7 +934,7 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
     thr = INFINITY;
   else
     thr = static_cast<float>(log(static_cast<double>(conf_tau)) - log1p(-static_cast<double>(conf_tau)));
-  if (launch_pdl(confidence_kernel, dim3(B), dim3(kConfThreads), 0, stream, h, conf_w, conf_b, thr,
+  if (launch_pdl(confidence_kernel, dim3(B), dim3(32 * k), 0, stream, h, conf_w, conf_b, thr,
                  draft_tokens, draft_len, conf_out, k, H) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);

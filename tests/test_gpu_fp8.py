@@ -83,6 +83,23 @@ def test_quantize_fp8_segments_with_row_stride():
     np.testing.assert_array_equal(host(codes), ref_codes)
 
 
+@pytest.mark.parametrize("R,C,T,pad", [(7, 5120, 5, 64), (200, 4096, 2, 0), (3, 8192, 1, 16), (2, 1200, 3, 48)])
+def test_quantize_fp8_few_long_rows(R, C, T, pad):
+    """Few long rows (the activation rows of a step) are quantised by a cluster of CTAs
+    per row that combine their partial maxima; the codes stay bit-exact, also where a
+    CTA's range of the row crosses from one segment to the next."""
+    ld = C + pad
+    full = _rows_with_spread(90 + R, R, T * ld).reshape(R, T, ld)
+    segs = [full[:, j, :C] for j in range(T)]
+    x = np.concatenate(segs, axis=1)
+    ref_codes, ref_scales = oracle.quantize_fp8_rows(x)
+    base = dev_bf16(full.reshape(R, T * ld))
+    codes, scales = ds.quantize_fp8([base[:, j * ld: j * ld + C] for j in range(T)])
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(scales).view(np.uint32), ref_scales.view(np.uint32))
+    np.testing.assert_array_equal(host(codes), ref_codes)
+
+
 # ----------------------------------------------------------------------------- GEMMs
 
 @pytest.mark.parametrize("M,H,V", [(1, 256, 4096), (7, 256, 4097), (33, 512, 1000),

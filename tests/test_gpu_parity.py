@@ -104,7 +104,8 @@ def test_fc_project_strided_taps_and_integer_exact():
 # ----------------------------------------------------------------------------- Markov chain
 
 @pytest.mark.parametrize("B,k,V,r", [(1, 7, 4096, 16), (3, 4, 5001, 16), (16, 7, 20000, 64),
-                                     (9, 2, 513, 128), (2, 1, 1, 8)])
+                                     (9, 2, 513, 128), (2, 1, 1, 8), (1, 7, 40000, 128),
+                                     (12, 5, 30011, 128)])
 def test_greedy_sample_bit_exact(B, k, V, r):
     logits = syn.uniform_logits(31 + V, (B, k, V), 1.5)
     w1 = syn.normal_bf16(32, (V, r))
@@ -121,7 +122,7 @@ def test_greedy_sample_bit_exact(B, k, V, r):
 
 
 @pytest.mark.parametrize("B,k,V,r", [(1, 7, 4096, 16), (3, 4, 5001, 16), (16, 7, 20000, 64),
-                                     (9, 16, 3001, 32), (1, 7, 20000, 0)])
+                                     (9, 16, 3001, 32), (1, 7, 20000, 0), (20, 3, 20000, 128)])
 def test_greedy_sample_without_q_stats_bit_exact(B, k, V, r):
     """Without a q_stats buffer the chain reduces only the argmax keys (another kernel
     variant): z and the draft tokens stay bit-exact, and draft_len is not touched."""
