@@ -219,6 +219,18 @@ __device__ void decide_request(const VerifyArgs &a, int b, Decision &d, bool rec
   const bool want_stats = (a.mode == 1);
   const int n_t = L + 1;
   const int n_z = a.zrows ? L : 0;
+  // Loads that do not need the row statistics go first: each position's drafted
+  // token and its target / draft logit (thread j takes position j).
+  const long long drow = static_cast<long long>(b) * k;
+  int pre_dt = -1;
+  float pre_t = 0.0f, pre_z = 0.0f;
+  if (a.mode == 1 && tid < L) {
+    pre_dt = a.drafts[drow + tid];
+    if (pre_dt >= 0 && pre_dt < V) {
+      pre_t = a.target[(static_cast<long long>(b) * (k + 1) + tid) * V + pre_dt];
+      if (a.zlog) pre_z = a.zlog[(drow + tid) * V + pre_dt];
+    }
+  }
   for (int q = warp; q < n_t + n_z; q += kWarps) {
     const bool qz = q >= n_t;
     const int jj = qz ? q - n_t : q;
@@ -270,11 +282,10 @@ __device__ void decide_request(const VerifyArgs &a, int b, Decision &d, bool rec
 
   // Probabilistic: every position's ratio p(d)/q(d) and accept uniform, in parallel
   // (thread j takes position j); the sequential accept loop below only compares.
-  const long long drow = static_cast<long long>(b) * k;
   if (a.mode == 1 && tid < L) {
     const int jj = tid;
     const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
-    const int dt = a.drafts[drow + jj];
+    const int dt = pre_dt;
     double ua, us;
     verify_uniforms(a.seed, req, static_cast<uint32_t>(jj), a.step, ua, us);
     d.ua[jj] = ua;
@@ -283,12 +294,12 @@ __device__ void decide_request(const VerifyArgs &a, int b, Decision &d, bool rec
     if (!d.bad[jj]) {
       // p(d)/q(d) = exp((T_d - M) - (z_d - m)) * s / S: the exponent is formed
       // exactly in fp64, the exponential in fp32 (relative error ~1e-7)
-      const double tT = a.target[(static_cast<long long>(b) * (k + 1) + jj) * V + dt];
+      const double tT = pre_t;
       double ex = tT - d.tM[jj], sc = 1.0 / d.tS[jj];
       if (a.zlog) {
         const double qm = a.zrows ? d.zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
         const double qs = a.zrows ? d.zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
-        const double zd = a.zlog[(drow + jj) * V + dt];
+        const double zd = pre_z;
         ex -= zd - qm;
         sc *= qs;
       }
@@ -458,17 +469,22 @@ __device__ void finish_draw(const VerifyArgs &a, int b) {
 
 // Atomic ticket of request b in `tickets`: true for the CTA that arrives last
 // (of `count`), which then resets the ticket.  Block-wide.
+// The CTA's partial was stored by thread 0; thread 0's ticket increment is an
+// acquire-release atomic, so the partial is visible before the ticket moves, and the
+// last CTA's thread 0 sees every other CTA's partial; the CTA barrier then orders the
+// reads of the other threads after that acquire.  (A fence in every thread of every
+// CTA cost about a microsecond per CTA wave.)
 __device__ __forceinline__ bool last_arrival(int *tickets, int b, int count, int *flag_s) {
-  __threadfence();
-  __syncthreads();
   if (threadIdx.x == 0) {
-    const bool last = atomicAdd(&tickets[b], 1) == count - 1;
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(tickets + b) : "memory");
+    const bool last = (old == count - 1);
     if (last) tickets[b] = 0;
     *flag_s = last ? 1 : 0;
   }
   __syncthreads();
   const bool last = *flag_s != 0;
-  if (last) __threadfence();
+  if (last) __threadfence();  // the last CTA only: its threads read the others' partials
   return last;
 }
 
