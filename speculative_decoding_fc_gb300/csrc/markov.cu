@@ -713,23 +713,27 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 
 // c[b, i] = sigmoid(w . h[b*k+i] + bias); draft_len[b] = first i whose logit
 // falls below thr = logit(tau); later drafts are replaced by -1.  One CTA per
-// request, one warp per block position (all k dot products at once).
-__global__ void __launch_bounds__(32 * kMaxK) confidence_kernel(
+// request; wpp warps per block position (all k dot products at once, each split
+// over wpp warps, the warps' sums added in warp order).
+constexpr int kConfMaxWarps = 32;
+
+__global__ void __launch_bounds__(32 * kConfMaxWarps) confidence_kernel(
     const uint16_t *__restrict__ h, const uint16_t *__restrict__ conf_w, float conf_b, float thr,
-    int32_t *draft_tokens, int32_t *draft_len, float *conf_out, int k, int H) {
-  __shared__ float zc_s[kMaxK];
+    int32_t *draft_tokens, int32_t *draft_len, float *conf_out, int k, int H, int wpp) {
+  __shared__ float part_s[kConfMaxWarps];
   __shared__ int len_s;
   pdl_wait();
   pdl_release();  // one CTA per request: one wave
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp < k) {
-    const uint4 *hrow = reinterpret_cast<const uint4 *>(h + (static_cast<long long>(b) * k + warp) * H);
+  const int pos = warp / wpp, part = warp - pos * wpp;
+  if (pos < k) {
+    const uint4 *hrow = reinterpret_cast<const uint4 *>(h + (static_cast<long long>(b) * k + pos) * H);
     const uint4 *wrow = reinterpret_cast<const uint4 *>(conf_w);
     float acc = 0.0f;
 #pragma unroll 4
-    for (int c = lane; c < H / 8; c += 32) {
+    for (int c = part * 32 + lane; c < H / 8; c += 32 * wpp) {
       const uint4 hv = __ldg(hrow + c);
       const uint4 wv = __ldg(wrow + c);
       acc = __fmaf_rn(bf16_lo(wv.x), bf16_lo(hv.x), acc);
@@ -743,17 +747,22 @@ __global__ void __launch_bounds__(32 * kMaxK) confidence_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      const float zc = acc + conf_b;
-      zc_s[warp] = zc;
-      if (conf_out) conf_out[static_cast<long long>(b) * k + warp] = 1.0f / (1.0f + expf(-zc));
-    }
+    if (lane == 0) part_s[warp] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    const int i = threadIdx.x;
+    float zc = 0.0f;
+    for (int w = 0; w < wpp; ++w) zc += part_s[i * wpp + w];
+    zc += conf_b;
+    part_s[i * wpp] = zc;  // read back below by thread 0 (after the barrier)
+    if (conf_out) conf_out[static_cast<long long>(b) * k + i] = 1.0f / (1.0f + expf(-zc));
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int len = k;
     for (int i = 0; i < k; ++i)
-      if (!(zc_s[i] >= thr)) {
+      if (!(part_s[i * wpp] >= thr)) {
         len = i;
         break;
       }
@@ -934,8 +943,13 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
     thr = INFINITY;
   else
     thr = static_cast<float>(log(static_cast<double>(conf_tau)) - log1p(-static_cast<double>(conf_tau)));
-  if (launch_pdl(confidence_kernel, dim3(B), dim3(32 * k), 0, stream, h, conf_w, conf_b, thr,
-                 draft_tokens, draft_len, conf_out, k, H) != cudaSuccess)
+  // warps per position: as many as fit in 32 warps, no more than the 16-byte chunks of
+  // a row over 32 lanes
+  int wpp = kConfMaxWarps / k;
+  const int chunks_per_lane_min = 2;
+  while (wpp > 1 && (H / 8) / (32 * wpp) < chunks_per_lane_min) --wpp;
+  if (launch_pdl(confidence_kernel, dim3(B), dim3(32 * wpp * k), 0, stream, h, conf_w, conf_b,
+                 thr, draft_tokens, draft_len, conf_out, k, H, wpp) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;
