@@ -40,6 +40,11 @@
  *     fits.  Calls that share a workspace must not overlap in time (same
  *     stream, or ordered by events).  After a device-side error, zero the
  *     workspace again before reusing it.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the previous kernel on the stream is finishing and waits for
+ *     it (griddepcontrol.wait) before its first access to global memory, so
+ *     results are as with plain stream order.  DSPARK_NO_PDL=1 in the
+ *     environment launches them plainly.
  *   - Argument errors are detected on the host before anything is enqueued
  *     and returned as a negative dspark_status_t.  Errors the device finds
  *     (a token id outside [0, V), a bounded internal wait running out) are
@@ -71,7 +76,7 @@ typedef uint16_t dspark_bf16_t;
 #define DSPARK_ERR_CUDA (-5)              /* a CUDA runtime or driver call failed */
 #define DSPARK_ERR_DEVICE_TIMEOUT (-6)    /* (device) a bounded wait ran out; work skipped */
 #define DSPARK_ERR_BAD_TOKEN (-7)         /* (device) token id outside [0, V) */
-#define DSPARK_ERR_NO_DEVICE (-8)         /* no sm_100-family GPU is current */
+#define DSPARK_ERR_NO_DEVICE (-8)         /* the current GPU is not an sm_103 device */
 
 /* Human-readable name of a status code.  Never returns NULL. */
 const char *dspark_status_string(dspark_status_t status);
@@ -142,8 +147,10 @@ dspark_status_t dspark_lm_head(const dspark_bf16_t *h, const dspark_bf16_t *lm_w
  * w1 [V, r] and w2 [V, r] bf16 (w2 is the Linear(r -> V) weight); w1 == NULL
  * means no bias (plain argmax), then w2 and r are ignored.
  * prev_token [B] int32 in [0, V) (else DSPARK_ERR_BAD_TOKEN is recorded and
- * that request is drafted without bias).  Launches k kernels, one per
- * position.
+ * that request is drafted without bias).  One cooperative launch covers all k
+ * positions (one launch per position when a cooperative launch is refused or
+ * r is not 16, 32, 64 or 128).  q_stats == NULL selects a variant that reduces
+ * only the argmax (probabilistic verify then reduces q's statistics itself).
  * ---------------------------------------------------------------------- */
 size_t dspark_greedy_sample_workspace_size(int B, int k, int V, int r);
 dspark_status_t dspark_greedy_sample(float *logits, const dspark_bf16_t *w1,
