@@ -54,6 +54,9 @@ def parse_args():
                     help="run the 27B sweep grid instead (one JSON line per cell, not the "
                          "headline line): B x k x r x sigma, probabilistic verify")
     ap.add_argument("--sweep-steps", type=int, default=200, help="timed steps per sweep cell")
+    ap.add_argument("--fused-gemms", action="store_true",
+                    help="bf16 weights: run the fc and the LM head as one two-phase GEMM "
+                         "launch (dspark_fc_lm_head) instead of two launches")
     ap.add_argument("--q-stats", default="verify", choices=["verify", "chain"],
                     help="where the softmax statistics of q are reduced: in verify's streaming "
                          "pass over the draft logits, or in the Markov chain kernel")
@@ -114,11 +117,11 @@ def measured_peaks():
     return hbm, tflops, src
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, stem="gemm_tcgen05_lm_head"):
     """DRAM bytes per LM-head launch from the committed ncu summary of this workload,
     or None when there is none or the kernel source changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "gemm_tcgen05_lm_head_%s.md" % workload)
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (stem, workload))
     try:
         fields = {}
         with open(path) as f:
@@ -377,6 +380,10 @@ def run_ours(args, rank, local_rank, world):
             return ds.lm_head_fp8(h, lm_w8, lm_s, **kw)
         return ds.lm_head(h, lm_w, **kw)
 
+    # --fused-gemms (bf16 weights): fc and LM head as one two-phase launch (CTAs that
+    # finish their fc share stream LM-head weights while the others finish)
+    fused = (not fp8) and args.fused_gemms
+
     # input sets: taps, prev, target logits = own draft logits + noise (built once)
     sets = []
     for s in range(args.sets):
@@ -412,10 +419,16 @@ def run_ours(args, rank, local_rank, world):
         acc_o, nxt_o, dlen_o = hist if hist is not None else (acc_hist[i], nxt_hist[i], dlen_hist[i])
         if ev is not None:
             ev[0].record(s)
-        fc_call(st["taps"], out=h_buf, stream=s, workspaces=wsp)
-        if ev is not None:
-            ev[1].record(s)
-        lm_call(h_buf, out=logits.view(M, V), stream=s, workspaces=wsp)
+        if fused:
+            ds.fc_lm_head(st["taps"], fc_w, lm_w, h_out=h_buf, logits=logits.view(M, V), stream=s,
+                          workspaces=wsp)
+            if ev is not None:
+                ev[1].record(s)
+        else:
+            fc_call(st["taps"], out=h_buf, stream=s, workspaces=wsp)
+            if ev is not None:
+                ev[1].record(s)
+            lm_call(h_buf, out=logits.view(M, V), stream=s, workspaces=wsp)
         if ev is not None:
             ev[2].record(s)
         ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
@@ -507,10 +520,12 @@ def run_ours(args, rank, local_rank, world):
     # per-stage CUDA events on the launching stream (their host cost makes this loop
     # slower than the others; it is used for the per-kernel times only)
     staged_ms, _ = timed(run_staged)
-    stage_names = ["fc_project", "lm_head", "greedy_sample", "verify"]
+    stage_names = (["fc_lm_head", "(none)", "greedy_sample", "verify"] if fused
+                   else ["fc_project", "lm_head", "greedy_sample", "verify"])
     stage_ms = {nm: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev)
                 for j, nm in enumerate(stage_names)}
-    lm_ms = stage_ms["lm_head"]
+    stage_ms.pop("(none)", None)
+    lm_ms = stage_ms["fc_lm_head"] if fused else stage_ms["lm_head"]
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
@@ -561,14 +576,15 @@ def run_ours(args, rank, local_rank, world):
     steps_per_s = whole_job_rate(K, world, max_ms / 1000.0)
     peak_gbs, peak_tf, peak_src = measured_peaks()
     sb = step_bytes(cfg, mode)
-    lm_bytes = sb["lm_head"]
+    lm_bytes = sb["fc"] + sb["lm_head"] if fused else sb["lm_head"]
     achieved = lm_bytes / (lm_ms / 1000.0) / 1e9
     t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
     # readout (fc + LM head + chain) and verify against their own rooflines
     t_readout = max((sb["fc"] + sb["lm_head"] + sb["chain"]) / (peak_gbs * 1e9),
                     step_flops(cfg) / (peak_tf * 1e12))
     t_verify = sb["verify"] / (peak_gbs * 1e9)
-    readout_ms = stage_ms["fc_project"] + stage_ms["lm_head"] + stage_ms["greedy_sample"]
+    readout_ms = ((stage_ms["fc_lm_head"] if fused else stage_ms["fc_project"] + stage_ms["lm_head"])
+                  + stage_ms["greedy_sample"])
 
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
@@ -588,10 +604,13 @@ def run_ours(args, rank, local_rank, world):
         "per_position_acceptance": per_pos,
         "roofline": {"bound": "hbm",
                      "kernel": ("quantize_rows + gemm_tcgen05<fp8> (LM head stage)" if fp8
-                                else "gemm_tcgen05 (LM head)"),
+                                else "gemm_tcgen05, two phases: fc then LM head (one launch)"
+                                if fused else "gemm_tcgen05 (LM head)"),
                      "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
-                     "traffic": profiled_traffic(args.config), "peak_source": peak_src,
+                     "traffic": profiled_traffic(args.config, "gemm_tcgen05_fc_lm_head" if fused
+                                                 else "gemm_tcgen05_lm_head"),
+                     "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
         "step_roofline": {"bytes": sb["total"], "flops": step_flops(cfg),
                           "t_roofline_ms": t_roof * 1000.0,

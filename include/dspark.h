@@ -128,6 +128,25 @@ dspark_status_t dspark_lm_head(const dspark_bf16_t *h, const dspark_bf16_t *lm_w
                                size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * fc projection and LM head in ONE launch (as dspark_fc_project followed by
+ * dspark_lm_head on its output):
+ *   h[m, n]      = bf16_rne( sum_j sum_c taps[j][m, c] * fc_w[n, j*H + c] )
+ *   logits[m, v] = sum_c h[m, c] * lm_w[v, c]                (fp32)
+ * Same layouts as the two calls; h_out [M, H] bf16 (16-byte aligned) receives h.
+ * One persistent cooperative kernel: a CTA that has finished its share of the
+ * fc streams LM-head weight tiles while the other CTAs finish theirs; the LM
+ * head's reads of h wait until every fc output tile is stored.  Results are
+ * those of the two calls up to the fp32 summation order, and identical to them
+ * when both launches use the same number of CTAs (one per SM once each GEMM
+ * has at least 4 k-blocks of 128 bytes per SM, e.g. the 27B shapes).
+ * ---------------------------------------------------------------------- */
+size_t dspark_fc_lm_head_workspace_size(int M, int H, int T, int V);
+dspark_status_t dspark_fc_lm_head(const dspark_bf16_t *const *taps, int T, int64_t tap_ld,
+                                  const dspark_bf16_t *fc_w, const dspark_bf16_t *lm_w,
+                                  dspark_bf16_t *h_out, float *logits, int M, int H, int V,
+                                  void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Markov-biased semi-autoregressive greedy drafting ([PR620] VanillaMarkov;
  * _greedy_sample "applies the full-vocab bigram bias semi-autoregressively
  * across block positions (position i conditioned on position i-1's biased

@@ -19,7 +19,7 @@ import threading
 import torch
 
 __all__ = ["DSparkError", "lib", "fc_project", "lm_head", "greedy_sample", "confidence_truncate",
-           "draft_readout", "quantize_fp8", "fc_project_fp8", "lm_head_fp8",
+           "draft_readout", "quantize_fp8", "fc_project_fp8", "lm_head_fp8", "fc_lm_head",
            "verify", "workspace_status", "launch_count", "Workspaces", "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -89,6 +89,11 @@ def lib():
         L.dspark_verify.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_uint64, _vp,
                                     ctypes.c_uint32, _vp, _vp, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_fc_lm_head_workspace_size.restype = _sz
+        L.dspark_fc_lm_head_workspace_size.argtypes = [ctypes.c_int] * 4
+        L.dspark_fc_lm_head.restype = ctypes.c_int
+        L.dspark_fc_lm_head.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _i64, _vp, _vp, _vp, _vp,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _sz, _vp]
         L.dspark_quantize_fp8.restype = ctypes.c_int
         L.dspark_quantize_fp8.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, _i64, ctypes.c_int,
                                           ctypes.c_int, _vp, _vp, _vp]
@@ -191,6 +196,36 @@ def fc_project(taps, fc_w, out=None, stream=None, workspaces=None):
     _check(L.dspark_fc_project(arr, T, ld, _ptr(fc_w), _ptr(out), M, H, _ptr(ws), ws.numel(),
                                _stream(stream, dev)), "dspark_fc_project")
     return out
+
+
+def fc_lm_head(taps, fc_w, lm_w, h_out=None, logits=None, stream=None, workspaces=None):
+    """fc projection and LM head in one launch: returns (h [M, H] bf16, fp32 logits
+    [M, V]).  taps: T bf16 tensors [M, H] with a common row stride."""
+    T = len(taps)
+    M, H = taps[0].shape
+    V = lm_w.shape[0]
+    dev = fc_w.device
+    _need(fc_w, "fc_w", torch.bfloat16, (H, T * H))
+    _need(lm_w, "lm_w", torch.bfloat16, (V, H))
+    ld = taps[0].stride(0)
+    for j, t in enumerate(taps):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != (M, H) \
+                or t.stride(1) != 1 or t.stride(0) != ld:
+            raise ValueError("tap %d must be a CUDA bf16 [%d, %d] tensor with row stride %d" % (j, M, H, ld))
+    if h_out is None:
+        h_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    if logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    _need(h_out, "h_out", torch.bfloat16, (M, H))
+    _need(logits, "logits", torch.float32)
+    if logits.numel() != M * V:
+        raise ValueError("logits must hold M*V floats")
+    L = lib()
+    ws = (workspaces or _default_ws).get("fclm", dev, L.dspark_fc_lm_head_workspace_size(M, H, T, V))
+    arr = (_vp * T)(*[t.data_ptr() for t in taps])
+    _check(L.dspark_fc_lm_head(arr, T, ld, _ptr(fc_w), _ptr(lm_w), _ptr(h_out), _ptr(logits), M, H,
+                               V, _ptr(ws), ws.numel(), _stream(stream, dev)), "dspark_fc_lm_head")
+    return h_out, logits
 
 
 def lm_head(h, lm_w, out=None, stream=None, workspaces=None):

@@ -219,6 +219,67 @@ dspark_status_t dspark_fc_project(const dspark_bf16_t *const *taps, int T, int64
                      as_stream(stream));
 }
 
+// ---------------------------------------------------------------- fc + LM head, one launch
+size_t dspark_fc_lm_head_workspace_size(int M, int H, int T, int V) {
+  if (M < 1 || H < 64 || T < 1 || T > kMaxTaps || V < 1) return 0;
+  const size_t g = gemm2_workspace_size(M, H, T * H, V, H);
+  return g ? kHeader + g : 0;
+}
+
+dspark_status_t dspark_fc_lm_head(const dspark_bf16_t *const *taps, int T, int64_t tap_ld,
+                                  const dspark_bf16_t *fc_w, const dspark_bf16_t *lm_w,
+                                  dspark_bf16_t *h_out, float *logits, int M, int H, int V,
+                                  void *ws, size_t ws_bytes, void *stream) {
+  if (!taps || !fc_w || !lm_w || !h_out || !logits) return DSPARK_ERR_INVALID_ARG;
+  if (T < 1 || M < 1 || H < 1 || V < 1 || tap_ld < H) return DSPARK_ERR_INVALID_ARG;
+  if (T > kMaxTaps || H % 64 != 0 || M > kMaxM || H > (1 << 16) || V > kMaxV)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (tap_ld % 8 != 0 || !aligned16(fc_w) || !aligned16(lm_w) || !aligned16(h_out) ||
+      !aligned4(logits))
+    return DSPARK_ERR_MISALIGNED;
+  for (int j = 0; j < T; ++j) {
+    if (!taps[j]) return DSPARK_ERR_INVALID_ARG;
+    if (!aligned16(taps[j])) return DSPARK_ERR_MISALIGNED;
+  }
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_fc_lm_head_workspace_size(M, H, T, V));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  const size_t p1 = gemm2_phase1_offset(M, H, T * H);
+  st = prepare_workspace(ws, layout_signature({8, M, H, T, V}),
+                         {{0, kHeader + kWsAlign + gemm_counter_bytes(M, H, T * H)},
+                          {kHeader + p1, gemm_counter_bytes(M, V, H)}},
+                         s);
+  if (st != DSPARK_OK) return st;
+  GemmProblem fc, lm;
+  memset(&fc, 0, sizeof(fc));
+  memset(&lm, 0, sizeof(lm));
+  fc.w = fc_w;
+  for (int j = 0; j < T; ++j) {
+    fc.x[j] = taps[j];
+    fc.x_ld[j] = tap_ld;
+  }
+  fc.n_seg = T;
+  fc.seg_k = H;
+  fc.N = H;
+  fc.M = M;
+  fc.out = h_out;
+  fc.ldo = H;
+  fc.out_bf16 = true;
+  lm.w = lm_w;
+  lm.x[0] = h_out;
+  lm.x_ld[0] = H;
+  lm.n_seg = 1;
+  lm.seg_k = H;
+  lm.N = V;
+  lm.M = M;
+  lm.out = logits;
+  lm.ldo = V;
+  lm.out_bf16 = false;
+  return gemm_launch2(fc, lm, static_cast<char *>(ws) + kHeader, ws_bytes - kHeader,
+                      status_word(ws), s);
+}
+
 // ---------------------------------------------------------------- LM head
 size_t dspark_lm_head_workspace_size(int M, int H, int V) {
   if (M < 1 || H < 64 || V < 1) return 0;

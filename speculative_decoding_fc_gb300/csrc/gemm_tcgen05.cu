@@ -52,7 +52,10 @@ constexpr int kMaxStages = 12;
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 
-struct GemmParams {
+// One GEMM of a launch.  A launch runs one phase, or two (the fc projection, then
+// the LM head on its output h): the second phase's activation loads wait until
+// the first phase has stored every output tile, its weight loads do not.
+struct GemmPhase {
   CUtensorMap tm_w;
   CUtensorMap tm_x[kMaxTaps];
   const float *a_scale;   // FP8: scale of each activation row (else null)
@@ -60,17 +63,24 @@ struct GemmParams {
   void *out;
   float *partials;
   int *tickets;
-  int *status;
   long long ldo;
   long long units;
   int kb_per_seg;
   int kb_total;
   int N;
+  int out_bf16;
+  int tiles;              // output tiles of the phase
+};
+
+struct GemmParams {
+  GemmPhase ph[2];
+  int nphase;
+  int *sync;              // two phases: [0] phase-0 tiles stored, [1] CTAs finished
+  int *status;
   int M;
   int BN;
   int tiles_m;
   int stages;
-  int out_bf16;
   uint32_t tmem_cols;
   uint32_t idesc;
 };
@@ -224,14 +234,67 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long units, int gri
   return static_cast<int>(((x + 1) * grid - 1) / units);
 }
 
-__device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, float v) {
-  if (m >= p.M || n >= p.N) return;
-  if (p.w_scale) v *= __ldg(p.a_scale + m) * __ldg(p.w_scale + n);
-  const long long off = static_cast<long long>(m) * p.ldo + n;
-  if (p.out_bf16)
-    reinterpret_cast<__nv_bfloat16 *>(p.out)[off] = __float2bfloat16_rn(v);
+// The output side of a phase, copied into registers once per phase (fields read
+// through a reference into the parameter block would be re-read after every store).
+struct OutDesc {
+  void *out;
+  const float *a_scale;
+  const float *w_scale;
+  long long ldo;
+  int N;
+  int out_bf16;
+};
+
+__device__ __forceinline__ OutDesc out_desc(const GemmPhase &P) {
+  OutDesc o;
+  o.out = P.out;
+  o.a_scale = P.a_scale;
+  o.w_scale = P.w_scale;
+  o.ldo = P.ldo;
+  o.N = P.N;
+  o.out_bf16 = P.out_bf16;
+  return o;
+}
+
+__device__ __forceinline__ void store_out(const OutDesc &o, int M, int m, int n, float v) {
+  if (m >= M || n >= o.N) return;
+  if (o.w_scale) v *= __ldg(o.a_scale + m) * __ldg(o.w_scale + n);
+  const long long off = static_cast<long long>(m) * o.ldo + n;
+  if (o.out_bf16)
+    reinterpret_cast<__nv_bfloat16 *>(o.out)[off] = __float2bfloat16_rn(v);
   else
-    reinterpret_cast<float *>(p.out)[off] = v;
+    reinterpret_cast<float *>(o.out)[off] = v;
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int *ptr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// After observing (with a relaxed load) that phase 0 has stored all its tiles: an
+// acquire fence for those stores, then a proxy fence so that this thread's TMA
+// loads (async proxy) of h see them.
+__device__ __forceinline__ void acquire_for_tma() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Activation loads of n consecutive units from unit u (ring stages from `stage`).
+__device__ __noinline__ void issue_x_pending(const GemmParams &p, const CUtensorMap *tmx, int kps,
+                                             int kbt, int elem_k, long long u, int n, int stage,
+                                             uint32_t base, uint32_t stage_bytes, uint32_t full0,
+                                             int S, uint64_t pol_x) {
+  for (int i = 0; i < n; ++i, ++u) {
+    const int tile = static_cast<int>(u / kbt);
+    const int kb = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+    const int m_tile = tile % p.tiles_m;
+    const int seg = kb / kps;
+    const int xk = (kb - seg * kps) * elem_k;
+    tma_load_2d(base + stage * stage_bytes + kABytes, tmx + seg, xk, m_tile * p.BN,
+                full0 + 8u * stage, pol_x);
+    if (++stage == S) stage = 0;
+  }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -277,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
-    prefetch_map(&p.tm_w);
+    for (int ph = 0; ph < p.nphase; ++ph) prefetch_map(&p.ph[ph].tm_w);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -296,46 +359,99 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
   pdl_wait();
   pdl_release();
 
-  const Range rg = cta_range(p.units, cta, grid);
-  const int kbt = p.kb_total;
-  const int first_tile = static_cast<int>(rg.begin / kbt);
-
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const CUtensorMap *xmaps = &p.tm_x[0];
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (long long u = rg.begin; u < rg.end && ok;) {
-        const int tile = static_cast<int>(u / kbt);
-        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
-        const long long left = rg.end - u;
-        const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
-        const int n_tile = tile / p.tiles_m;
-        const int m_tile = tile - n_tile * p.tiles_m;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status)) {
+      for (int ph = 0; ph < p.nphase && ok; ++ph) {
+        const GemmPhase &P = p.ph[ph];
+        const CUtensorMap *tmw = &P.tm_w;
+        const CUtensorMap *tmx = &P.tm_x[0];
+        const int kps = P.kb_per_seg;
+        const Range rg = cta_range(P.units, cta, grid);
+        const int kbt = P.kb_total;
+        long long u = rg.begin;
+        if (ph == 1) {
+          // Phase 1 reads phase 0's output.  Until every phase-0 tile is stored,
+          // only weight tiles are loaded (up to one ring of stages); their
+          // activation loads follow once phase 0 is complete.
+          const int need = p.ph[0].tiles;
+          int seen = ld_relaxed_s32(p.sync);
+          const long long u0 = u;
+          const int stage0 = stage;
+          int nq = 0;
+          while (seen < need && nq < S && u < rg.end && ok) {
+            const int tile = static_cast<int>(u / kbt);
+            const int kb = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+            if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8u * stage;
+            mbar_expect_tx(fb, stage_bytes);
+            tma_load_2d(base + stage * stage_bytes, tmw, kb * kElemK, (tile / p.tiles_m) * kBM, fb,
+                        pol_w);
+            ++nq;
+            ++u;
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            if ((nq & 3) == 0) seen = ld_relaxed_s32(p.sync);  // a round trip every 4 tiles
+          }
+          const long long t0 = clock64();
+          while (seen < need) {
+            if (*abort_flag || clock64() - t0 > kWaitCycles) break;
+            __nanosleep(64);
+            seen = ld_relaxed_s32(p.sync);
+          }
+          if (seen < need) {
+            if (!*abort_flag) {
+              *abort_flag = 1;
+              record_error(p.status, DSPARK_ERR_DEVICE_TIMEOUT);
+            }
             ok = false;
-            break;
           }
-          const uint32_t fb = full0 + 8u * stage;
-          mbar_expect_tx(fb, stage_bytes);
-          const uint32_t sa = base + stage * stage_bytes;
-          tma_load_2d(sa, &p.tm_w, kb * kElemK, n_tile * kBM, fb, pol_w);
-          const int seg = kb / p.kb_per_seg;
-          const int xk = (kb - seg * p.kb_per_seg) * kElemK;
-          tma_load_2d(sa + kABytes, xmaps + seg, xk, m_tile * p.BN, fb, pol_x);
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          acquire_for_tma();
+          // (on failure the launch's status is set; the stages are still completed
+          // so that every issued copy lands)
+          issue_x_pending(p, tmx, kps, kbt, kElemK, u0, nq, stage0, base, stage_bytes, full0, S,
+                          pol_x);
+          if (!ok) break;
         }
-        u += kb1 - kb0;
+        for (; u < rg.end && ok;) {
+          const int tile = static_cast<int>(u / kbt);
+          const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+          const long long left = rg.end - u;
+          const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+          const int n_tile = tile / p.tiles_m;
+          const int m_tile = tile - n_tile * p.tiles_m;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = full0 + 8u * stage;
+            mbar_expect_tx(fb, stage_bytes);
+            const uint32_t sa = base + stage * stage_bytes;
+            tma_load_2d(sa, tmw, kb * kElemK, n_tile * kBM, fb, pol_w);
+            const int seg = kb / kps;
+            const int xk = (kb - seg * kps) * kElemK;
+            tma_load_2d(sa + kABytes, tmx + seg, xk, m_tile * p.BN, fb, pol_x);
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          u += kb1 - kb0;
+        }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA exits.
@@ -357,43 +473,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (long long u = rg.begin; u < rg.end && ok;) {
-        const int tile = static_cast<int>(u / kbt);
-        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
-        const long long left = rg.end - u;
-        const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
-        if (!wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bar(full0 + 8u * stage, phase, abort_flag, p.status)) {
+      for (int ph = 0; ph < p.nphase && ok; ++ph) {
+        const Range rg = cta_range(p.ph[ph].units, cta, grid);
+        const int kbt = p.ph[ph].kb_total;
+        for (long long u = rg.begin; u < rg.end && ok;) {
+          const int tile = static_cast<int>(u / kbt);
+          const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+          const long long left = rg.end - u;
+          const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+          if (!wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = base + stage * stage_bytes;
-          const uint32_t sb = sa + kABytes;
-          // 4 MMAs per stage, each over 32 bytes of K (16 bf16 or 32 E4M3)
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.BN);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bar(full0 + 8u * stage, phase, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = base + stage * stage_bytes;
+            const uint32_t sb = sa + kABytes;
+            // 4 MMAs per stage, each over 32 bytes of K (16 bf16 or 32 E4M3)
 #pragma unroll
-          for (int kk = 0; kk < kRowBytes / 32; ++kk) {
-            if constexpr (kFP8)
-              tc_mma_e4m3(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
-                          p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-            else
-              tc_mma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
-                          p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kRowBytes / 32; ++kk) {
+              if constexpr (kFP8)
+                tc_mma_e4m3(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
+                            p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+              else
+                tc_mma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
+                            p.idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(empty0 + 8u * stage);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit(empty0 + 8u * stage);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          tc_commit(tfull0 + 8u * acc);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+          u += kb1 - kb0;
         }
-        if (!ok) break;
-        tc_commit(tfull0 + 8u * acc);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-        u += kb1 - kb0;
       }
       // Every MMA issued by this thread has completed once this arrives.
       tc_commit(drain_bar);
@@ -408,102 +531,134 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (long long u = rg.begin; u < rg.end;) {
-      const int tile = static_cast<int>(u / kbt);
-      const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
-      const long long left = rg.end - u;
-      const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
-      const int n_tile = tile / p.tiles_m;
-      const int m_tile = tile - n_tile * p.tiles_m;
-      const int n = n_tile * kBM + row;
-      const int m_base = m_tile * p.BN;
-      const bool whole = (kb0 == 0 && kb1 == kbt);
+    bool alive = true;
+    for (int ph = 0; ph < p.nphase && alive; ++ph) {
+      const GemmPhase &P = p.ph[ph];
+      const OutDesc od = out_desc(P);
+      float *const partials = P.partials;
+      int *const tickets = P.tickets;
+      const long long units = P.units;
+      const Range rg = cta_range(units, cta, grid);
+      const int kbt = P.kb_total;
+      const int first_tile = static_cast<int>(rg.begin / kbt);
+      // phase 0 of a two-phase launch counts its stored tiles for phase 1
+      const bool signal = (p.nphase == 2 && ph == 0);
+      for (long long u = rg.begin; u < rg.end;) {
+        const int tile = static_cast<int>(u / kbt);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+        const long long left = rg.end - u;
+        const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+        const int n_tile = tile / p.tiles_m;
+        const int m_tile = tile - n_tile * p.tiles_m;
+        const int n = n_tile * kBM + row;
+        const int m_base = m_tile * p.BN;
+        const bool whole = (kb0 == 0 && kb1 == kbt);
 
-      // One thread waits for the accumulator; the decision is shared by all
-      // four epilogue warps so that they leave the loop together on abort.
-      if (threadIdx.x == 64)
-        *ok_slot = wait_bar(tfull0 + 8u * acc, acc_phase, abort_flag, p.status) ? 1 : 0;
-      epi_bar_sync();
-      const int ok = *ok_slot;
-      epi_bar_sync();
-      if (!ok) break;
-      tc_fence_after();
-
-      float *part = nullptr;
-      if (!whole) {
-        const int slot = (tile == first_tile) ? 0 : 1;
-        part = p.partials + (static_cast<size_t>(cta) * 2 + slot) * static_cast<size_t>(p.BN) * kBM;
-      }
-      for (int cc = 0; cc < p.BN; cc += 16) {
-        uint32_t r[16];
-        tmem_ld16(lane_addr + static_cast<uint32_t>(acc * p.BN + cc), r);
-        if (whole) {
-          if (m_base + cc < p.M) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) store_out(p, m_base + cc + j, n, __uint_as_float(r[j]));
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) part[(cc + j) * kBM + row] = __uint_as_float(r[j]);
+        // One thread waits for the accumulator; the decision is shared by all
+        // four epilogue warps so that they leave the loop together on abort.
+        if (threadIdx.x == 64)
+          *ok_slot = wait_bar(tfull0 + 8u * acc, acc_phase, abort_flag, p.status) ? 1 : 0;
+        epi_bar_sync();
+        const int ok = *ok_slot;
+        epi_bar_sync();
+        if (!ok) {
+          alive = false;
+          break;
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+        tc_fence_after();
 
-      if (!whole) {
-        // Stream-K fix-up: the last CTA to finish a piece of this tile adds the
-        // pieces in CTA order and stores the tile.
-        __threadfence();
-        epi_bar_sync();
-        if (threadIdx.x == 64) *ticket_slot = atomicAdd(&p.tickets[tile], 1);
-        epi_bar_sync();
-        const int ticket = *ticket_slot;
-        const long long t_first = static_cast<long long>(tile) * kbt;
-        const int c_first = cta_of_unit(t_first, p.units, grid);
-        const int c_last = cta_of_unit(t_first + kbt - 1, p.units, grid);
-        const int nseg = c_last - c_first + 1;
-        if (ticket == nseg - 1) {
+        float *part = nullptr;
+        if (!whole) {
+          const int slot = (tile == first_tile) ? 0 : 1;
+          part = partials + (static_cast<size_t>(cta) * 2 + slot) * static_cast<size_t>(p.BN) * kBM;
+        }
+        for (int cc = 0; cc < p.BN; cc += 16) {
+          uint32_t r[16];
+          tmem_ld16(lane_addr + static_cast<uint32_t>(acc * p.BN + cc), r);
+          if (whole) {
+            if (m_base + cc < p.M) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) store_out(od, p.M, m_base + cc + j, n, __uint_as_float(r[j]));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) part[(cc + j) * kBM + row] = __uint_as_float(r[j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+
+        if (whole && signal) {
+          // the tile is stored: publish it (the barrier orders the four warps'
+          // stores before thread 64's fence)
+          epi_bar_sync();
+          if (threadIdx.x == 64) {
+            __threadfence();
+            atomicAdd(p.sync, 1);
+          }
+        }
+        if (!whole) {
+          // Stream-K fix-up: the last CTA to finish a piece of this tile adds the
+          // pieces in CTA order and stores the tile.
           __threadfence();
-          const int mcount = min(p.BN, p.M - m_base);
-          // 16 columns at a time, the loads of up to four pieces issued together;
-          // pieces are added in CTA order.
-          for (int c0 = 0; c0 < mcount; c0 += 16) {
-            float acc[16];
+          epi_bar_sync();
+          if (threadIdx.x == 64) *ticket_slot = atomicAdd(&tickets[tile], 1);
+          epi_bar_sync();
+          const int ticket = *ticket_slot;
+          const long long t_first = static_cast<long long>(tile) * kbt;
+          const int c_first = cta_of_unit(t_first, units, grid);
+          const int c_last = cta_of_unit(t_first + kbt - 1, units, grid);
+          const int nseg = c_last - c_first + 1;
+          if (ticket == nseg - 1) {
+            __threadfence();
+            const int mcount = min(p.BN, p.M - m_base);
+            // 16 columns at a time, the loads of up to four pieces issued together;
+            // pieces are added in CTA order.
+            for (int c0 = 0; c0 < mcount; c0 += 16) {
+              float acc16[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-            for (int s0 = 0; s0 < nseg; s0 += 4) {
-              float v[4][16];
+              for (int j = 0; j < 16; ++j) acc16[j] = 0.0f;
+              for (int s0 = 0; s0 < nseg; s0 += 4) {
+                float v[4][16];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if (s0 + q < nseg) {
-                  const int c2 = c_first + s0 + q;
-                  const int tile_c2 = static_cast<int>((p.units * c2 / grid) / kbt);
-                  const int slot = (tile == tile_c2) ? 0 : 1;
-                  const float *src = p.partials + (static_cast<size_t>(c2) * 2 + slot) *
-                                                      static_cast<size_t>(p.BN) * kBM;
+                for (int q = 0; q < 4; ++q) {
+                  if (s0 + q < nseg) {
+                    const int c2 = c_first + s0 + q;
+                    const int tile_c2 = static_cast<int>((units * c2 / grid) / kbt);
+                    const int slot = (tile == tile_c2) ? 0 : 1;
+                    const float *src = partials + (static_cast<size_t>(c2) * 2 + slot) *
+                                                        static_cast<size_t>(p.BN) * kBM;
 #pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    v[q][j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+                    for (int j = 0; j < 16; ++j)
+                      v[q][j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+                  }
                 }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  if (s0 + q < nseg)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc16[j] += v[q][j];
               }
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (s0 + q < nseg)
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) acc[j] += v[q][j];
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < mcount) store_out(od, p.M, m_base + c0 + j, n, acc16[j]);
             }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < mcount) store_out(p, m_base + c0 + j, n, acc[j]);
+            if (threadIdx.x == 64) tickets[tile] = 0;
+            if (signal) {
+              epi_bar_sync();
+              if (threadIdx.x == 64) {
+                __threadfence();
+                atomicAdd(p.sync, 1);
+              }
+            }
           }
-          if (threadIdx.x == 64) p.tickets[tile] = 0;
+          epi_bar_sync();
         }
-        epi_bar_sync();
+        u += kb1 - kb0;
       }
-      u += kb1 - kb0;
     }
   }
 
@@ -517,6 +672,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(p.tmem_cols)
                  : "memory");
+  }
+  // A two-phase launch: the last CTA out clears the tile counter for the next one.
+  if (p.nphase == 2 && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sync + 1, 1) == grid - 1) {
+      p.sync[0] = 0;
+      p.sync[1] = 0;
+    }
   }
 }
 
@@ -609,6 +772,68 @@ size_t gemm_workspace_size(int M, int N, int K) {
 // The tile grid and the partial tiles do not depend on the element size.
 size_t gemm_workspace_size_fp8(int M, int N, int K) { return gemm_workspace_size(M, N, K); }
 
+namespace {
+
+// Tensor maps, scales, outputs and the stream-K schedule of one phase; ws holds the
+// phase's tile tickets then its partial tiles.
+bool fill_phase(GemmPhase &P, const GemmProblem &pr, const Tiling &t, void *ws) {
+  const int K = pr.n_seg * pr.seg_k;
+  const int esize = pr.fp8 ? 1 : 2;
+  if (!make_map(&P.tm_w, pr.w, static_cast<uint64_t>(K), static_cast<uint64_t>(pr.N),
+                static_cast<uint64_t>(K) * esize, kBM, pr.fp8))
+    return false;
+  for (int s = 0; s < pr.n_seg; ++s) {
+    if (!make_map(&P.tm_x[s], pr.x[s], static_cast<uint64_t>(pr.seg_k),
+                  static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.x_ld[s]) * esize,
+                  static_cast<uint32_t>(t.BN), pr.fp8))
+      return false;
+  }
+  P.a_scale = pr.a_scale;
+  P.w_scale = pr.w_scale;
+  const size_t tickets = align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
+  P.tickets = reinterpret_cast<int *>(ws);
+  P.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + tickets);
+  P.out = pr.out;
+  P.ldo = pr.ldo;
+  P.units = t.units;
+  P.kb_per_seg = pr.seg_k * esize / kRowBytes;
+  P.kb_total = t.kb_total;
+  P.N = pr.N;
+  P.out_bf16 = pr.out_bf16 ? 1 : 0;
+  P.tiles = t.tiles_m * t.tiles_n;
+  return true;
+}
+
+void fill_common(GemmParams &p, const Tiling &t, int M, bool fp8, int *status) {
+  p.status = status;
+  p.M = M;
+  p.BN = t.BN;
+  p.tiles_m = t.tiles_m;
+  p.stages = t.stages;
+  p.tmem_cols = t.tmem_cols;
+  // Instruction descriptor: D fp32 (bits 4-5 = 1); A and B format at bits 7-9 and
+  // 10-12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3); both K-major; N >> 3 at
+  // bits 17-22, M >> 4 at bits 24-28.
+  const uint32_t fmt = fp8 ? 0u : 1u;
+  p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(t.BN >> 3) << 17) |
+            (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+bool configure(bool fp8) {
+  static bool configured[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev >= 0 && dev < 64 && configured[fp8 ? 1 : 0][dev]) return true;
+  auto kern = fp8 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+      cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < 64) configured[fp8 ? 1 : 0][dev] = true;
+  return true;
+}
+
+}  // namespace
+
 dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, int *status,
                             cudaStream_t stream) {
   const int K = pr.n_seg * pr.seg_k;
@@ -620,57 +845,82 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
 
   GemmParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_map(&p.tm_w, pr.w, static_cast<uint64_t>(K), static_cast<uint64_t>(pr.N),
-                static_cast<uint64_t>(K) * esize, kBM, pr.fp8))
-    return DSPARK_ERR_CUDA;
-  for (int s = 0; s < pr.n_seg; ++s) {
-    if (!make_map(&p.tm_x[s], pr.x[s], static_cast<uint64_t>(pr.seg_k),
-                  static_cast<uint64_t>(pr.M), static_cast<uint64_t>(pr.x_ld[s]) * esize,
-                  static_cast<uint32_t>(t.BN), pr.fp8))
-      return DSPARK_ERR_CUDA;
-  }
-  p.a_scale = pr.a_scale;
-  p.w_scale = pr.w_scale;
-  const size_t tickets = align_up(static_cast<size_t>(t.tiles_m) * t.tiles_n * sizeof(int), kWsAlign);
-  p.tickets = reinterpret_cast<int *>(ws);
-  p.partials = reinterpret_cast<float *>(static_cast<char *>(ws) + tickets);
-  p.out = pr.out;
-  p.status = status;
-  p.ldo = pr.ldo;
-  p.units = t.units;
-  p.kb_per_seg = pr.seg_k * esize / kRowBytes;
-  p.kb_total = t.kb_total;
-  p.N = pr.N;
-  p.M = pr.M;
-  p.BN = t.BN;
-  p.tiles_m = t.tiles_m;
-  p.stages = t.stages;
-  p.out_bf16 = pr.out_bf16 ? 1 : 0;
-  p.tmem_cols = t.tmem_cols;
-  // Instruction descriptor: D fp32 (bits 4-5 = 1); A and B format at bits 7-9 and
-  // 10-12 (kind::f16: 1 = bf16; kind::f8f6f4: 0 = E4M3); both K-major; N >> 3 at
-  // bits 17-22, M >> 4 at bits 24-28.
-  const uint32_t fmt = pr.fp8 ? 0u : 1u;
-  p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(t.BN >> 3) << 17) |
-            (static_cast<uint32_t>(kBM >> 4) << 24);
+  if (!fill_phase(p.ph[0], pr, t, ws)) return DSPARK_ERR_CUDA;
+  p.nphase = 1;
+  fill_common(p, t, pr.M, pr.fp8, status);
 
   long long grid = sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
   const long long by_work = t.units / 4 > 0 ? t.units / 4 : 1;
   if (grid > by_work) grid = by_work;
-
-  static bool configured[2][64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (!configure(pr.fp8)) return DSPARK_ERR_CUDA;
   auto kern = pr.fp8 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
-  if (dev < 0 || dev >= 64 || !configured[pr.fp8 ? 1 : 0][dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-        cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    if (dev >= 0 && dev < 64) configured[pr.fp8 ? 1 : 0][dev] = true;
-  }
   if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), t.smem, stream, p) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
+  count_launches(1);
+  return DSPARK_OK;
+}
+
+// Two GEMMs in one launch: [256 B: tile counter, exit counter][phase 0][phase 1].
+size_t gemm2_workspace_size(int M, int N0, int K0, int N1, int K1) {
+  const size_t a = gemm_workspace_size(M, N0, K0), b = gemm_workspace_size(M, N1, K1);
+  if (!a || !b) return 0;
+  return kWsAlign + align_up(a, kWsAlign) + b;
+}
+
+size_t gemm2_phase1_offset(int M, int N0, int K0) {
+  return kWsAlign + align_up(gemm_workspace_size(M, N0, K0), kWsAlign);
+}
+
+dspark_status_t gemm_launch2(const GemmProblem &pr0, const GemmProblem &pr1, void *ws,
+                             size_t ws_bytes, int *status, cudaStream_t stream) {
+  const int K0 = pr0.n_seg * pr0.seg_k, K1 = pr1.n_seg * pr1.seg_k;
+  if (pr0.M != pr1.M || pr0.fp8 != pr1.fp8) return DSPARK_ERR_INVALID_ARG;
+  const int esize = pr0.fp8 ? 1 : 2;
+  Tiling t0 = plan(pr0.M, pr0.N, K0, esize), t1 = plan(pr1.M, pr1.N, K1, esize);
+  if (ws_bytes < gemm2_workspace_size(pr0.M, pr0.N, K0, pr1.N, K1)) return DSPARK_ERR_WORKSPACE;
+  const int sms = device_sm_count();
+  if (sms <= 0) return DSPARK_ERR_NO_DEVICE;
+
+  char *w = static_cast<char *>(ws);
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.sync = reinterpret_cast<int *>(w);
+  if (!fill_phase(p.ph[0], pr0, t0, w + kWsAlign)) return DSPARK_ERR_CUDA;
+  if (!fill_phase(p.ph[1], pr1, t1, w + gemm2_phase1_offset(pr0.M, pr0.N, K0)))
+    return DSPARK_ERR_CUDA;
+  p.nphase = 2;
+  fill_common(p, t0, pr0.M, pr0.fp8, status);  // same M: same tile width and ring
+
+  // every CTA must be resident (phase 1 waits for tiles stored by all CTAs): a
+  // cooperative launch, with programmatic dependent launch when enabled
+  long long grid = sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
+  const long long small = (t0.units < t1.units ? t0.units : t1.units) / 4;
+  if (grid > small) grid = small > 0 ? small : 1;
+  if (!configure(pr0.fp8)) return DSPARK_ERR_CUDA;
+  auto kern = pr0.fp8 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = t0.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess && cfg.numAttrs == 2) {
+    cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return DSPARK_ERR_CUDA;
+  }
   count_launches(1);
   return DSPARK_OK;
 }

@@ -44,6 +44,14 @@ size_t gemm_counter_bytes(int M, int N, int K);
 // Enqueues the GEMM.  ws must hold gemm_workspace_size bytes (zeroed once).
 dspark_status_t gemm_launch(const GemmProblem &p, void *ws, size_t ws_bytes, int *status,
                             cudaStream_t stream);
+// Two GEMMs in one cooperative launch, the second reading the first's output (same
+// M and element type): the second's activation loads wait until every output tile of
+// the first is stored.  Workspace: [256 B counters][first GEMM][second GEMM at
+// gemm2_phase1_offset]; the counters and both GEMMs' tickets must start at zero.
+size_t gemm2_workspace_size(int M, int N0, int K0, int N1, int K1);
+size_t gemm2_phase1_offset(int M, int N0, int K0);
+dspark_status_t gemm_launch2(const GemmProblem &p0, const GemmProblem &p1, void *ws,
+                             size_t ws_bytes, int *status, cudaStream_t stream);
 
 // ------------------------------------------------------------------ Markov chain
 size_t chain_workspace_size(int B, int k, int V);

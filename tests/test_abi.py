@@ -111,3 +111,25 @@ def test_fp8_argument_errors_are_caught_before_any_launch(libdspark):
     taps = (vp * 2)(1 << 20, 1 << 21)
     assert f(taps, 2, 256, fake, fake, fake, 4, 192, fake, 1 << 30, None) == -2   # H % 128
     assert f(taps, 2, 256, fake, fake, fake, 4, 256, fake, 16, None) == -4
+
+
+def test_fc_lm_head_sizes_and_argument_errors(libdspark):
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    libdspark.dspark_fc_lm_head_workspace_size.restype = sz
+    n = libdspark.dspark_fc_lm_head_workspace_size(7, 5120, 5, 151936)
+    libdspark.dspark_fc_project_workspace_size.restype = sz
+    libdspark.dspark_lm_head_workspace_size.restype = sz
+    assert n >= libdspark.dspark_fc_project_workspace_size(7, 5120, 5) + \
+        libdspark.dspark_lm_head_workspace_size(7, 5120, 151936) - 256
+    assert libdspark.dspark_fc_lm_head_workspace_size(7, 5120, 9, 151936) == 0
+    f = libdspark.dspark_fc_lm_head
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int64, vp, vp, vp, vp, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, vp, sz, vp]
+    fake = vp(1 << 20)
+    taps = (vp * 2)(1 << 20, 1 << 21)
+    assert f(taps, 2, 128, fake, fake, fake, None, 4, 128, 100, fake, 1 << 30, None) == -1
+    assert f(taps, 2, 128, fake, fake, fake, fake, 4, 96, 100, fake, 1 << 30, None) == -2
+    assert f(taps, 2, 128, fake, vp((1 << 20) + 8), fake, fake, 4, 128, 100, fake, 1 << 30,
+             None) == -3
+    assert f(taps, 2, 128, fake, fake, fake, fake, 4, 128, 100, fake, 16, None) == -4

@@ -85,6 +85,26 @@ def test_27b_lm_head_sampled_rows(w27, w27_dev, B):
 
 
 @pytest.mark.parametrize("B", [1, 16])
+def test_27b_fc_lm_head_one_launch(w27, w27_dev, B):
+    """The single-launch fc + LM head at the workload's shapes gives the bits of the two
+    separate launches (one CTA per SM in both), sampled against the oracle."""
+    k, H, T, V = 7, 5120, 5, 151936
+    st = syn.step_inputs(3, B, k, H, T, V, ("ramp", 0.5, 3.0))
+    taps = [dev_bf16(t) for t in st["taps"]]
+    h, logits = ds.fc_lm_head(taps, w27_dev["fc_w"], w27_dev["lm_w"])
+    h2 = ds.fc_project(taps, w27_dev["fc_w"])
+    l2 = ds.lm_head(h2, w27_dev["lm_w"])
+    torch.cuda.synchronize()
+    hb = host_bf16_bits(h)
+    np.testing.assert_array_equal(hb, host_bf16_bits(h2))
+    np.testing.assert_array_equal(host(logits), host(l2))
+    rows = np.random.default_rng(B + 7).choice(V, 1000, replace=False)
+    ref = oracle.lm_head(hb, w27["lm_w"][rows])
+    err = np.abs(host(logits)[:, rows].astype(np.float64) - ref)
+    assert np.all(err <= ATOL + RTOL * np.abs(ref))
+
+
+@pytest.mark.parametrize("B", [1, 16])
 def test_27b_markov_chain_bit_exact(w27, w27_dev, B):
     k, V = 7, 151936
     logits = syn.uniform_logits(500 + B, (B, k, V), 1.0)

@@ -103,6 +103,38 @@ def test_fc_project_strided_taps_and_integer_exact():
 
 # ----------------------------------------------------------------------------- Markov chain
 
+@pytest.mark.parametrize("M,H,T,V", [(7, 256, 5, 4096), (28, 512, 5, 20000), (130, 128, 3, 3001),
+                                     (300, 256, 2, 1000), (1, 64, 1, 7)])
+def test_fc_lm_head_one_launch_matches_oracle(M, H, T, V):
+    """fc and LM head in one cooperative launch: h within the fc bound of the oracle,
+    logits within the logit tolerance of the oracle's LM head on the GPU's h."""
+    taps = [syn.normal_bf16(700 + 10 * j + M, (M, H)) for j in range(T)]
+    fc_w = syn.normal_bf16(800 + H, (H, T * H), (1.0 / (T * H)) ** 0.5)
+    lm_w = syn.normal_bf16(900 + V, (V, H), (1.0 / H) ** 0.5)
+    h, logits = ds.fc_lm_head([dev_bf16(t) for t in taps], dev_bf16(fc_w), dev_bf16(lm_w))
+    torch.cuda.synchronize()
+    hb = host_bf16_bits(h)
+    _assert_fc_close(hb, oracle.fc_project(taps, fc_w), taps, fc_w)
+    _assert_logits_close(host(logits), oracle.lm_head(hb, lm_w))
+
+
+def test_fc_lm_head_one_launch_equals_two_calls_and_repeats():
+    """With one CTA per SM in both forms the single launch gives the two calls' bits,
+    and repeated launches (counter reset by the last CTA) give the same bits."""
+    M, H, T, V = 7, 1024, 5, 40000
+    taps = [dev_bf16(syn.normal_bf16(710 + j, (M, H))) for j in range(T)]
+    fc_w = dev_bf16(syn.normal_bf16(811, (H, T * H), (1.0 / (T * H)) ** 0.5))
+    lm_w = dev_bf16(syn.normal_bf16(912, (V, H), (1.0 / H) ** 0.5))
+    h2 = ds.fc_project(taps, fc_w)
+    l2 = ds.lm_head(h2, lm_w)
+    wsp = ds.Workspaces()
+    for _ in range(3):
+        h1, l1 = ds.fc_lm_head(taps, fc_w, lm_w, workspaces=wsp)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host_bf16_bits(h1), host_bf16_bits(h2))
+        np.testing.assert_array_equal(host(l1), host(l2))
+
+
 @pytest.mark.parametrize("B,k,V,r", [(1, 7, 4096, 16), (3, 4, 5001, 16), (16, 7, 20000, 64),
                                      (9, 2, 513, 128), (2, 1, 1, 8), (1, 7, 40000, 128),
                                      (12, 5, 30011, 128)])
