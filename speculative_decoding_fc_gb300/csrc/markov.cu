@@ -254,8 +254,7 @@ struct ChainPArgs {
   int *status;
   int r, B, k, V;
   int rows_per_cta;         // vocabulary rows owned by one CTA
-  int w2_in_smem;           // 1: the CTA's markov_w2 slice lives in shared memory
-  int w2_smem_bytes;        // bytes of shared memory reserved for that slice
+  int w2_smem_bytes;        // shared memory reserved for the markov_w2 slice (0: read via L2)
 };
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -806,7 +805,6 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
   if (rows > kPRows * kPThreads) return false;
   ChainPArgs a = args0;
   a.rows_per_cta = rows;
-  a.w2_in_smem = kW2Smem ? 1 : 0;
   a.w2_smem_bytes =
       kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
   const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + static_cast<size_t>(B) * CPR * 32 +
@@ -901,7 +899,6 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
   pa.k = k;
   pa.V = V;
   pa.rows_per_cta = 0;
-  pa.w2_in_smem = 0;
   pa.w2_smem_bytes = 0;
   // DSPARK_CHAIN_PER_POSITION=1 selects the per-position kernels (same results).
   const char *env = getenv("DSPARK_CHAIN_PER_POSITION");
