@@ -316,6 +316,33 @@ def test_verify_rejection_identity_on_gpu():
 
 # ----------------------------------------------------------------------------- readout
 
+@pytest.mark.parametrize("B,k,H,tau,bias", [(3, 1, 64, 0.5, 0.0), (5, 16, 5120, 0.5, 0.0),
+                                             (4, 7, 2560, 0.3, 0.2), (2, 5, 128, 0.7, -0.1),
+                                             (6, 4, 256, 0.0, 0.0), (6, 4, 256, 1.0, 0.0)])
+def test_confidence_truncate_matches_oracle(B, k, H, tau, bias):
+    """Confidence head alone at block sizes 1..16 (one to 32 warps per position): the
+    sigmoid within rtol 1e-5, draft_len and the -1 masking exact wherever no decision
+    is within 1e-4 of the threshold; tau <= 0 keeps all, tau >= 1 keeps none."""
+    h = syn.normal_bf16(40 + k, (B * k, H))
+    cw = syn.normal_bf16(41 + H, (H,), (4.0 / H) ** 0.5)
+    d0 = np.tile(np.arange(k, dtype=np.int32), (B, 1)) + 3
+    ref = oracle.confidence(h, B, k, cw, bias, tau, d0)
+    drafts = dev(d0)
+    dl, cf = ds.confidence_truncate(dev_bf16(h), dev_bf16(cw), drafts, B, k, bias, tau,
+                                    conf_out=torch.empty((B, k), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(host(cf), ref["conf"], rtol=1e-5, atol=1e-6)
+    import math
+    thr = -math.inf if tau <= 0 else (math.inf if tau >= 1 else math.log(tau) - math.log1p(-tau))
+    safe = np.all(np.abs(ref["zc"] - thr) >= 1e-4, axis=1) if np.isfinite(thr) else np.ones(B, bool)
+    np.testing.assert_array_equal(host(dl)[safe], ref["draft_len"][safe])
+    np.testing.assert_array_equal(host(drafts)[safe], ref["draft_tokens"][safe])
+    if tau <= 0:
+        assert (host(dl) == k).all()
+    if tau >= 1:
+        assert (host(dl) == 0).all() and (host(drafts) == -1).all()
+
+
 def test_draft_readout_with_confidence_matches_oracle():
     B, k, H, V, r = 4, 7, 256, 5000, 16
     h = syn.normal_bf16(61, (B * k, H))
