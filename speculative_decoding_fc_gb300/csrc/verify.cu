@@ -38,6 +38,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kPer = 16;                    // entries per thread per slice (pass 1)
 constexpr int kSlice = kThreads * kPer;     // 4096 entries per CTA (pass 1)
+constexpr int kPerWide = 64;                // many rows: 16384 entries per CTA (pass 1)
+constexpr int kSliceWide = kThreads * kPerWide;
 constexpr int kDrawSlice = kThreads * 4;    // 1024 entries per CTA (pass 2): one Philox block per thread
 
 struct __align__(16) RowPartial {
@@ -118,8 +120,9 @@ __device__ __forceinline__ bool row_needed(const VerifyArgs &a, const RowRef &r)
   return r.is_z ? (a.mode == 1 && r.j < L) : (r.j <= L);
 }
 
-// (argmax key, max, sum exp) of one 4096-entry slice of row rho -> rows partial.
-// Block-wide; `red` is shared scratch of kWarps entries.
+// (argmax key, max, sum exp) of one slice of row rho (KP entries per thread: 4096 or
+// 16384 per CTA) -> rows partial.  Block-wide; `red` is shared scratch of kWarps entries.
+template <int KP>
 __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *red) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k = a.k, V = a.V;
@@ -127,47 +130,49 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
   const bool want_stats = (a.mode == 1);
   const float *row = rr.is_z ? a.zlog + (static_cast<long long>(rr.b) * k + rr.j) * V
                              : a.target + (static_cast<long long>(rr.b) * (k + 1) + rr.j) * V;
-  const int base = slice * kSlice;
-  // This thread's 16 entries, in ascending index order: the argmax by strict float
-  // compare (first index wins ties, -0 == +0, NaN never wins), then the max and the
-  // sum of exp(x - max) from registers.
-  float x[kPer];
-  int xi[kPer];
+  const int base = slice * (kThreads * KP);
+  // This thread's KP entries, all loaded before any is used, in ascending index
+  // order: the argmax by strict float compare (first index wins ties, -0 == +0, NaN
+  // never wins), then the max and the sum of exp(x - max) from registers.  Entry e
+  // has index base + (e/4)*1024 + 4*tid + e%4 (vector loads) or base + e*256 + tid.
+  float x[KP];
   if (a.vec) {
 #pragma unroll
-    for (int it = 0; it < kPer / 4; ++it) {
+    for (int it = 0; it < KP / 4; ++it) {
       const int v = base + it * (kThreads * 4) + tid * 4;
       const float4 q = v < V ? __ldcs(reinterpret_cast<const float4 *>(row + v))
                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       x[4 * it] = q.x; x[4 * it + 1] = q.y; x[4 * it + 2] = q.z; x[4 * it + 3] = q.w;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) xi[4 * it + e] = v + e;
     }
   } else {
 #pragma unroll
-    for (int it = 0; it < kPer; ++it) {
+    for (int it = 0; it < KP; ++it) {
       const int v = base + it * kThreads + tid;
       x[it] = v < V ? __ldcs(row + v) : -INFINITY;
-      xi[it] = v;
     }
   }
+  auto index_of = [&](int e) {
+    return a.vec ? base + (e >> 2) * (kThreads * 4) + tid * 4 + (e & 3) : base + e * kThreads + tid;
+  };
   float bv = -INFINITY;
   int bi = -1;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    if (xi[e] < V && x[e] > bv) {
+  for (int e = 0; e < KP; ++e) {
+    const int xi = index_of(e);
+    if (xi < V && x[e] > bv) {
       bv = x[e];
-      bi = xi[e];
+      bi = xi;
     }
   }
+  const int x0 = index_of(0);
   unsigned long long best = bi >= 0 ? argmax_key(bv, static_cast<uint32_t>(bi))
-                                    : (xi[0] < V ? argmax_key(-INFINITY, static_cast<uint32_t>(xi[0])) : 0ull);
+                                    : (x0 < V ? argmax_key(-INFINITY, static_cast<uint32_t>(x0)) : 0ull);
   SoftStat st{-INFINITY, 0.0f};
   if (want_stats && bi >= 0 && bv != INFINITY) {
     float sum = 0.0f;
 #pragma unroll
-    for (int e = 0; e < kPer; ++e)
-      if (xi[e] < V && x[e] == x[e] && x[e] != -INFINITY) sum += __expf(x[e] - bv);
+    for (int e = 0; e < KP; ++e)
+      if (index_of(e) < V && x[e] == x[e] && x[e] != -INFINITY) sum += __expf(x[e] - bv);
     st = SoftStat{bv, sum};
   }
   best = warp_max_u64(best);
@@ -489,6 +494,7 @@ __device__ __forceinline__ bool last_arrival(int *tickets, int b, int count, int
 }
 
 // ------------------------------------------------------------------ two-launch path
+template <int KP>
 __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs a) {
   __shared__ RowPartial red[kWarps];
   __shared__ int flag_s;
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
   const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
   const RowRef rr = row_ref(a, rho);
   pdl_wait();
-  if (row_needed(a, rr)) stats_item(a, rho, slice, red);
+  if (row_needed(a, rr)) stats_item<KP>(a, rho, slice, red);
   pdl_release();  // after this CTA's pass: the grid may span many waves
   const int rows_per_req = (a.k + 1) + (a.zrows ? a.k : 0);
   if (!last_arrival(a.req_ticket, rr.b, rows_per_req * a.nslices, &flag_s)) return;
@@ -591,10 +597,15 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
               ? 1
               : 0;
   const long long nrows = static_cast<long long>(B) * (k + 1) + (a.zrows ? static_cast<long long>(B) * k : 0);
-  const long long g1 = nrows * L.nslices;
-
-  if (launch_pdl(verify_stats_kernel, dim3(static_cast<unsigned>(g1)), dim3(kThreads), 0, stream,
-                 a) != cudaSuccess)
+  // Many rows (more than about four waves of 4096-entry CTAs): 16384 entries per CTA,
+  // so that each CTA's fixed cost (launch, reduction, ticket) covers 64 KB of reads.
+  // The workspace holds the partials of the 4096-entry slicing, the larger count.
+  const int sms = device_sm_count();
+  const bool wide = sms > 0 && nrows * L.nslices > 4LL * sms * 8;
+  if (wide) a.nslices = (V + kSliceWide - 1) / kSliceWide;
+  const long long g1 = nrows * a.nslices;
+  if (launch_pdl(wide ? verify_stats_kernel<kPerWide> : verify_stats_kernel<kPer>,
+                 dim3(static_cast<unsigned>(g1)), dim3(kThreads), 0, stream, a) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);
   if (mode == 1) {

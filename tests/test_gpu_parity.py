@@ -231,7 +231,9 @@ def _verify_inputs(B, k, V, seed):
     return z, drafts, target.astype(np.float32)
 
 
-@pytest.mark.parametrize("B,k,V", [(1, 7, 4096), (5, 3, 4097), (16, 7, 9000), (4, 16, 301)])
+# the last two cases have enough rows for the 16384-entry slicing of the stats pass
+@pytest.mark.parametrize("B,k,V", [(1, 7, 4096), (5, 3, 4097), (16, 7, 9000), (4, 16, 301),
+                                   (64, 7, 50000), (96, 7, 30001)])
 def test_verify_greedy_bit_exact(B, k, V):
     z, drafts, target = _verify_inputs(B, k, V, 41 + V)
     # make some requests accept a long prefix: copy the target argmax into the drafts
@@ -258,7 +260,9 @@ def _excluded(ref, B):
 
 
 @pytest.mark.parametrize("with_q_stats", [False, True])
-@pytest.mark.parametrize("B,k,V", [(1, 7, 4096), (6, 5, 4099), (16, 7, 20000), (64, 2, 128)])
+# (64, 7, 50001) and (48, 7, 40000) without q stats take the 16384-entry slicing
+@pytest.mark.parametrize("B,k,V", [(1, 7, 4096), (6, 5, 4099), (16, 7, 20000), (64, 2, 128),
+                                   (64, 7, 50001), (48, 7, 40000)])
 def test_verify_probabilistic_bit_exact(B, k, V, with_q_stats):
     z, drafts, target = _verify_inputs(B, k, V, 51 + V + B)
     t = target.argmax(axis=-1).astype(np.int32)
