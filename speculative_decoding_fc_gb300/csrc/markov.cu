@@ -316,6 +316,54 @@ __device__ __forceinline__ int word_index(unsigned long long w) {
 // Rows of the vocabulary a thread of the persistent chain owns: 4 rows x up to 8
 // requests = 32 independent fma chains per thread.
 constexpr int kPRows = 4;
+constexpr int kGather = 8;    // markov_w1 elements a thread loads at once
+constexpr int kPollReq = 4;   // requests a warp polls at once
+constexpr int kPSmemMax = 225 * 1024;  // dynamic shared memory of the persistent chain
+constexpr int kPollWords = (kMaxPGrid + 31) / 32;  // words of one request per lane
+
+// Two fp32 fused multiply-adds in one instruction: lane i of d = a_i * b_i + c_i,
+// each rounded to nearest once (the same IEEE operation as fmaf on each lane).
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                       unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// Asynchronous copies of this thread's logits of requests g0 .. g0 + G - 1 (those
+// below B) at position pos into lg_s[(g * kPRows + j) * kPThreads + tid]: issued a
+// group ahead, they land while the fma chains run and hold no registers meanwhile.
+template <int G>
+__device__ __forceinline__ void issue_logits_copy(float *lg_s, const float *logits,
+                                                  const int (&vrow)[kPRows], int g0, int pos,
+                                                  int B, int k, int V, int tid) {
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (g0 + g < B) {
+      const float *src = logits + (static_cast<long long>(g0 + g) * k + pos) * V;
+#pragma unroll
+      for (int j = 0; j < kPRows; ++j) {
+        const uint32_t dst =
+            static_cast<uint32_t>(__cvta_generic_to_shared(&lg_s[(g * kPRows + j) * kPThreads + tid]));
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src + vrow[j])
+                     : "memory");
+      }
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Warp-wide (key max, softmax stats) of one value pair per thread, with one exp per
 // thread: the max first, then the sum of s * exp(m - max).
@@ -343,10 +391,15 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   __shared__ int stop_s, epoch_s;
   extern __shared__ __align__(16) uint8_t psmem[];
   // dynamic shared memory: markov_w2 slice [rows][CPR] (1024-byte aligned), then the
-  // contexts e of all requests [B][r], then prev tokens [B]
+  // contexts e of all requests (G = 1: [B][r]; G >= 2: request pairs interleaved,
+  // [B/2][r][2], the odd request's partner zero), then prev tokens [B] (padded to 16
+  // bytes), then (G = 8) one request group's logits [G][kPRows][kPThreads]
   uint4 *w2_s = reinterpret_cast<uint4 *>(psmem);
+  const size_t e_bytes = static_cast<size_t>((a.B + 1) & ~1) * CPR * 32;
   float *e_s = reinterpret_cast<float *>(psmem + a.w2_smem_bytes);
-  int *prev_s = reinterpret_cast<int *>(psmem + a.w2_smem_bytes + static_cast<size_t>(a.B) * CPR * 32);
+  int *prev_s = reinterpret_cast<int *>(psmem + a.w2_smem_bytes + e_bytes);
+  float *lg_s = reinterpret_cast<float *>(psmem + a.w2_smem_bytes + e_bytes +
+                                          ((static_cast<size_t>(a.B) * 4 + 15) & ~static_cast<size_t>(15)));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
@@ -417,31 +470,52 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 #pragma unroll
   for (int j = 0; j < kPRows; ++j) lrow[j] = vrow[j] - v_lo;
 
-  // Logits of the first request group at the coming position, loaded ahead of the
-  // wait for the other CTAs (they do not depend on it).
+  // Logits of the first request group at position 0.  Groups of 8 requests stage
+  // them in shared memory through asynchronous copies issued a group ahead; smaller
+  // groups (latency-bound) hold them in registers, loaded a group ahead.
+  constexpr bool kStage = (G >= 8);
   float lg_next[kPRows][G];
+  if constexpr (kStage) {
+    issue_logits_copy<G>(lg_s, a.logits, vrow, 0, 0, B, k, V, tid);
+  } else {
 #pragma unroll
-  for (int j = 0; j < kPRows; ++j)
+    for (int j = 0; j < kPRows; ++j)
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k) * V + vrow[j]] : 0.0f;
+      for (int g = 0; g < G; ++g)
+        lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k) * V + vrow[j]] : 0.0f;
+  }
+
+  // e_b = markov_w1[prev_b] of every request for position 0 (the poll below gathers
+  // those of the later positions): each thread's loads (up to kGather) are all issued
+  // before its stores, one round trip
+  if (biased) {
+    const int bpad = (G >= 2) ? ((B + 1) & ~1) : B;
+    for (int i0 = 0; i0 < bpad * r; i0 += kPThreads * kGather) {
+      uint32_t ev[kGather];
+#pragma unroll
+      for (int u = 0; u < kGather; ++u) {
+        const int idx = i0 + u * kPThreads + tid;
+        const int b = idx / r, t = idx - b * r;
+        const int p = (idx < bpad * r && b < B) ? prev_s[b] : -1;
+        ev[u] = p >= 0 ? static_cast<uint32_t>(a.w1[static_cast<long long>(p) * r + t]) << 16 : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kGather; ++u) {
+        const int idx = i0 + u * kPThreads + tid;
+        const int b = idx / r, t = idx - b * r;
+        if (idx < bpad * r)
+          e_s[(G >= 2) ? (((b >> 1) * r + t) << 1) + (b & 1) : idx] = __uint_as_float(ev[u]);
+      }
+    }
+    __syncthreads();
+  }
 
   float acc[kPRows][G];  // bias, then the biased logit, of this thread's rows
   for (int pos = 0; pos < k; ++pos) {
-    if (biased) {
-      // e_b = markov_w1[prev_b] for every request, once per position
-      for (int idx = tid; idx < B * r; idx += kPThreads) {
-        const int b = idx / r, t = idx - b * r;
-        const int p = prev_s[b];
-        e_s[idx] = p >= 0 ? __uint_as_float(static_cast<uint32_t>(a.w1[static_cast<long long>(p) * r + t]) << 16)
-                          : 0.0f;
-      }
-      __syncthreads();
-    }
     for (int g0 = 0; g0 < B; g0 += G) {
       const int gb = min(G, B - g0);
-      // later groups: their logits, loaded before the fma loop hides the latency
-      if (g0 > 0) {
+      if (!kStage && g0 > 0) {
+        // later groups: their logits, loaded before the fma loop hides the latency
 #pragma unroll
         for (int j = 0; j < kPRows; ++j)
 #pragma unroll
@@ -454,8 +528,57 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
       for (int j = 0; j < kPRows; ++j)
 #pragma unroll
         for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
-      if (biased) {
+      if (biased && G >= 2) {
+        // The chains of requests 2i and 2i+1 advance together in one fma.rn.f32x2:
+        // each lane is the same fp32 fma, in the same t order, as the chain alone.
+        unsigned long long acc2[kPRows][(G + 1) / 2];
 #pragma unroll
+        for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+          for (int gp = 0; gp < G / 2; ++gp) acc2[j][gp] = 0ull;  // +0.0f in both lanes
+#pragma unroll
+        for (int q = 0; q < CPR; ++q) {
+          float w[kPRows][8];
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) {
+            uint4 c;
+            if constexpr (kW2Smem) {
+              c = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+            } else {
+              c = __ldg(reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(vrow[j]) * r) + q);
+            }
+            w[j][0] = bf16_lo(c.x); w[j][1] = bf16_hi(c.x);
+            w[j][2] = bf16_lo(c.y); w[j][3] = bf16_hi(c.y);
+            w[j][4] = bf16_lo(c.z); w[j][5] = bf16_hi(c.z);
+            w[j][6] = bf16_lo(c.w); w[j][7] = bf16_hi(c.w);
+          }
+          unsigned long long e2[(G + 1) / 2][8];
+#pragma unroll
+          for (int gp = 0; gp < G / 2; ++gp) {
+            // pairs past the batch end read pair 0 (results unused)
+            const int pair = (2 * gp < gb) ? (g0 >> 1) + gp : 0;
+            const float4 *ep = reinterpret_cast<const float4 *>(&e_s[(pair * r + q * 8) * 2]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float4 v = ep[h];
+              e2[gp][2 * h] = pack_f32x2(v.x, v.y);
+              e2[gp][2 * h + 1] = pack_f32x2(v.z, v.w);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int j = 0; j < kPRows; ++j) {
+              const unsigned long long wd = pack_f32x2(w[j][t], w[j][t]);
+#pragma unroll
+              for (int gp = 0; gp < G / 2; ++gp) acc2[j][gp] = fma_f32x2(wd, e2[gp][t], acc2[j][gp]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+          for (int gp = 0; gp < G / 2; ++gp) unpack_f32x2(acc2[j][gp], acc[j][2 * gp], acc[j][2 * gp + 1]);
+      } else if (biased) {
 #pragma unroll
         for (int q = 0; q < CPR; ++q) {
           float w[kPRows][8];
@@ -495,23 +618,32 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
       // Per thread: argmax key (and statistics) of its rows for every request of the
       // group; then warp reductions, one shuffle round for all requests at a time so
       // that the requests' shuffle latencies overlap.
+      // The key of a row is (ordered value, inverted index): per thread the best
+      // ordered value with the lowest index holding it (rows ascend), then per warp
+      // the max ordered value and the lowest index among the lanes holding it.
       unsigned long long key[G];
       float mx[G], sm[G];
+      uint32_t bo[G], bi[G];
+      if (kStage) cp_async_wait_all();  // this thread's logits of the group are in lg_s
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        key[g] = 0ull;
+        bo[g] = 0u;             // NaN and "no row" order lowest
+        bi[g] = 0xffffffffu;
         mx[g] = -INFINITY;
         sm[g] = 0.0f;
         float zv[kPRows];
 #pragma unroll
         for (int j = 0; j < kPRows; ++j) {
-          float z = lg_next[j][g];
+          float z = kStage ? lg_s[(g * kPRows + j) * kPThreads + tid] : lg_next[j][g];
           if (biased) z = __fadd_rn(z, acc[j][g]);
           zv[j] = z;
           acc[j][g] = z;  // kept for the write-back after this position's words
           if (valid[j] && g < gb) {
-            const unsigned long long kj = argmax_key(z, static_cast<uint32_t>(vrow[j]));
-            key[g] = kj > key[g] ? kj : key[g];
+            const uint32_t o = ordered_bits(z);
+            if (o > bo[g] || bi[g] == 0xffffffffu) {
+              bo[g] = o;
+              bi[g] = static_cast<uint32_t>(vrow[j]);
+            }
             if (kStats && z == z && z != -INFINITY) mx[g] = fmaxf(mx[g], z);
           }
         }
@@ -522,13 +654,19 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
               sm[g] += expf(zv[j] - mx[g]);
         }
       }
+      // lg_s is consumed: the next group's logits (this position's, else the next's)
+      if (kStage) {
+        if (g0 + G < B)
+          issue_logits_copy<G>(lg_s, a.logits, vrow, g0 + G, pos, B, k, V, tid);
+        else if (pos + 1 < k)
+          issue_logits_copy<G>(lg_s, a.logits, vrow, 0, pos + 1, B, k, V, tid);
+      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const unsigned long long other = __shfl_xor_sync(0xffffffffu, key[g], o);
-          key[g] = other > key[g] ? other : key[g];
-        }
+      for (int g = 0; g < G; ++g) {
+        const uint32_t mo = __reduce_max_sync(0xffffffffu, bo[g]);
+        const uint32_t mi = __reduce_min_sync(0xffffffffu, bo[g] == mo ? bi[g] : 0xffffffffu);
+        key[g] = (static_cast<unsigned long long>(mo) << 32) | (0xffffffffu - mi);
+      }
       if (kStats) {
         float mm[G];
 #pragma unroll
@@ -597,7 +735,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
     }
 
     // This CTA's words of `pos` are published (above).  While the other CTAs finish,
-    // store the biased logits and load the next position's logits.
+    // store the biased logits and load the next position's logits (register path).
     if (biased && B <= G) {
 #pragma unroll
       for (int g = 0; g < G; ++g)
@@ -606,37 +744,65 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
           for (int j = 0; j < kPRows; ++j)
             if (valid[j]) a.logits[(static_cast<long long>(g) * k + pos) * V + vrow[j]] = acc[j][g];
     }
-    if (pos + 1 < k) {
+    if (!kStage && pos + 1 < k) {
 #pragma unroll
       for (int j = 0; j < kPRows; ++j)
 #pragma unroll
         for (int g = 0; g < G; ++g)
           lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k + pos + 1) * V + vrow[j]] : 0.0f;
     }
-    // Wait for every CTA's word of each request (warp w polls requests w, w + 8, ...);
+    // Wait for every CTA's word of each request (warp w polls requests w, w + 8, ...,
+    // up to kPollReq of them at once);
     // the max of the words is the draft token.  Relaxed loads suffice: nothing else is
     // read on the strength of a word, except after the last position, where an acquire
     // fence pairs with the words' release stores before the statistics are merged.
     {
       const uint32_t tg = word_tag(epoch, pos);
       const long long t0 = clock64();
-      for (int b = warp; b < B; b += kPWarps) {
-        const unsigned long long *wb = a.words + (static_cast<long long>(pos) * B + b) * grid;
-        unsigned long long best = 0ull;
+      for (int b0 = warp; b0 < B; b0 += kPWarps * kPollReq) {
+        // requests b0 + i * kPWarps (i < kPollReq): their words are loaded together,
+        // one round trip per pass for all of them
+        unsigned long long best[kPollReq];
+        bool done[kPollReq];  // warp-uniform
+#pragma unroll
+        for (int i = 0; i < kPollReq; ++i) {
+          best[i] = 0ull;
+          done[i] = b0 + i * kPWarps >= B;
+        }
         int stop = 0;
         while (true) {
-          // independent loads (no short-circuit): one round trip per pass
-          unsigned long long mx = 0ull;
-          int missing = 0;
-          for (int c = lane; c < grid; c += 32) {
-            const unsigned long long w = ld_relaxed_u64(wb + c);
-            missing += (static_cast<uint32_t>(w >> 58) != tg) ? 1 : 0;
-            mx = w > mx ? w : mx;
+          unsigned long long w[kPollReq][kPollWords];
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const unsigned long long *wb =
+                a.words + (static_cast<long long>(pos) * B + b0 + i * kPWarps) * grid;
+#pragma unroll
+            for (int c = 0; c < kPollWords; ++c) {
+              const int cc = lane + 32 * c;
+              w[i][c] = (!done[i] && cc < grid) ? ld_relaxed_u64(wb + cc) : 0ull;
+            }
           }
-          if (__all_sync(0xffffffffu, missing == 0)) {
-            best = warp_max_u64(mx);
-            break;
+          bool all_done = true;
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            if (done[i]) continue;
+            unsigned long long mx = 0ull;
+            int missing = 0;
+#pragma unroll
+            for (int c = 0; c < kPollWords; ++c) {
+              if (lane + 32 * c < grid) {
+                missing += (static_cast<uint32_t>(w[i][c] >> 58) != tg) ? 1 : 0;
+                mx = w[i][c] > mx ? w[i][c] : mx;
+              }
+            }
+            if (__all_sync(0xffffffffu, missing == 0)) {
+              best[i] = warp_max_u64(mx);
+              done[i] = true;
+            } else {
+              all_done = false;
+            }
           }
+          if (all_done) break;
           int give_up = 0;
           if (lane == 0)
             give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > kBarrierCycles) ? 1 : 0;
@@ -653,15 +819,52 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
           break;
         }
         if (lane == 0) {
-          const int d = word_index(best);
-          prev_s[b] = d;
-          if (cta == 0) a.draft_tokens[static_cast<long long>(b) * k + pos] = d;
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const int b = b0 + i * kPWarps;
+            if (b < B) {
+              const int d = word_index(best[i]);
+              prev_s[b] = d;
+              if (cta == 0) a.draft_tokens[static_cast<long long>(b) * k + pos] = d;
+            }
+          }
+        }
+        // the next position's context of these requests: markov_w1[draft], gathered
+        // by the warp that found it (loads first, then stores)
+        if (biased && pos + 1 < k) {
+          constexpr int kPerLane = (r + 31) / 32;
+          uint32_t ev[kPollReq][kPerLane];
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const int b = b0 + i * kPWarps;
+            const int d = word_index(best[i]);
+            const bool ok = b < B && d >= 0 && d < V;
+#pragma unroll
+            for (int u = 0; u < kPerLane; ++u) {
+              const int t = lane + 32 * u;
+              ev[i][u] = (ok && t < r) ? static_cast<uint32_t>(a.w1[static_cast<long long>(d) * r + t]) << 16 : 0u;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const int b = b0 + i * kPWarps;
+            if (b < B) {
+#pragma unroll
+              for (int u = 0; u < kPerLane; ++u) {
+                const int t = lane + 32 * u;
+                if (t < r) e_s[(G >= 2) ? (((b >> 1) * r + t) << 1) + (b & 1) : b * r + t] = __uint_as_float(ev[i][u]);
+              }
+            }
+          }
         }
       }
       if (pos + 1 == k) asm volatile("fence.acq_rel.gpu;" ::: "memory");
     }
     __syncthreads();
-    if (stop_s) return;
+    if (stop_s) {
+      cp_async_wait_all();  // the next group's logits copies land before the CTA exits
+      return;
+    }
   }
 
   if (!kStats && a.draft_len_fill && cta == 0)
@@ -807,15 +1010,17 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
   a.rows_per_cta = rows;
   a.w2_smem_bytes =
       kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
-  const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + static_cast<size_t>(B) * CPR * 32 +
-                      static_cast<size_t>(B) * sizeof(int);
-  if (smem > 200 * 1024) return false;
+  const size_t smem = static_cast<size_t>(a.w2_smem_bytes) +
+                      static_cast<size_t>((B + 1) & ~1) * CPR * 32 +
+                      ((static_cast<size_t>(B) * sizeof(int) + 15) & ~static_cast<size_t>(15)) +
+                      (G >= 8 ? static_cast<size_t>(G) * kPRows * kPThreads * sizeof(float) : 0);
+  if (smem > kPSmemMax) return false;
   auto kern = markov_chain_persistent<G, CPR, kStats, kW2Smem>;
   static bool attr_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemMax) !=
         cudaSuccess) {
       cudaGetLastError();
       return false;
