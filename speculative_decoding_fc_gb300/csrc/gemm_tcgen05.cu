@@ -25,7 +25,7 @@
 //   * Operands are 128-byte-swizzled K-major tiles (64 bf16 of K per row) as
 //     TMA writes them; the UMMA shared-memory descriptors describe exactly that
 //     layout.  Weights are loaded with an L2 evict-first policy, activations
-//     with evict-last.
+//     with evict-last, and so are the outputs (the next kernel reads them).
 //   * FP8 variant (kind::f8f6f4, E4M3 x E4M3): the same 128-byte rows hold 128
 //     codes, each MMA consumes K = 32, and the epilogue multiplies by the
 //     activation-row and weight-row scales.
@@ -243,6 +243,7 @@ struct OutDesc {
   long long ldo;
   int N;
   int out_bf16;
+  uint64_t pol;  // L2 policy of the output stores (evict-last: the next kernel reads them)
 };
 
 __device__ __forceinline__ OutDesc out_desc(const GemmPhase &P) {
@@ -253,6 +254,7 @@ __device__ __forceinline__ OutDesc out_desc(const GemmPhase &P) {
   o.ldo = P.ldo;
   o.N = P.N;
   o.out_bf16 = P.out_bf16;
+  o.pol = policy_evict_last();
   return o;
 }
 
@@ -260,10 +262,16 @@ __device__ __forceinline__ void store_out(const OutDesc &o, int M, int m, int n,
   if (m >= M || n >= o.N) return;
   if (o.w_scale) v *= __ldg(o.a_scale + m) * __ldg(o.w_scale + n);
   const long long off = static_cast<long long>(m) * o.ldo + n;
-  if (o.out_bf16)
-    reinterpret_cast<__nv_bfloat16 *>(o.out)[off] = __float2bfloat16_rn(v);
-  else
-    reinterpret_cast<float *>(o.out)[off] = v;
+  if (o.out_bf16) {
+    const unsigned short b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(reinterpret_cast<unsigned short *>(o.out) + off),
+                 "h"(b), "l"(o.pol)
+                 : "memory");
+  } else {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(reinterpret_cast<float *>(o.out) + off), "f"(v),
+                 "l"(o.pol)
+                 : "memory");
+  }
 }
 
 __device__ __forceinline__ int ld_relaxed_s32(const int *ptr) {
