@@ -11,7 +11,7 @@
 //
 // Phase 1 (row statistics): one streaming read of every needed row (target
 // rows 0..draft_len, and the draft-logit rows when their softmax statistics
-// were not supplied) with 128-bit loads; each CTA reduces a 4096-entry slice to
+// were not supplied) with 128-bit loads; each CTA reduces a 16384-entry slice to
 // (argmax key, max, sum exp).
 // Decision: the slices of a request are merged in a fixed order, then the
 // accept/reject tests run with Philox uniforms.
@@ -36,10 +36,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPer = 16;                    // entries per thread per slice (pass 1)
-constexpr int kSlice = kThreads * kPer;     // 4096 entries per CTA (pass 1)
-constexpr int kPerWide = 64;                // many rows: 16384 entries per CTA (pass 1)
-constexpr int kSliceWide = kThreads * kPerWide;
+constexpr int kPer = 64;                    // entries per thread per slice (pass 1), all
+                                            // loaded before any is used
+constexpr int kSlice = kThreads * kPer;     // 16384 entries per CTA (pass 1)
 constexpr int kDrawSlice = kThreads * 4;    // 1024 entries per CTA (pass 2): one Philox block per thread
 
 struct __align__(16) RowPartial {
@@ -120,8 +119,8 @@ __device__ __forceinline__ bool row_needed(const VerifyArgs &a, const RowRef &r)
   return r.is_z ? (a.mode == 1 && r.j < L) : (r.j <= L);
 }
 
-// (argmax key, max, sum exp) of one slice of row rho (KP entries per thread: 4096 or
-// 16384 per CTA) -> rows partial.  Block-wide; `red` is shared scratch of kWarps entries.
+// (argmax key, max, sum exp) of one slice of row rho (KP entries per thread) -> rows
+// partial.  Block-wide; `red` is shared scratch of kWarps entries.
 template <int KP>
 __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *red) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -494,7 +493,6 @@ __device__ __forceinline__ bool last_arrival(int *tickets, int b, int count, int
 }
 
 // ------------------------------------------------------------------ two-launch path
-template <int KP>
 __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs a) {
   __shared__ RowPartial red[kWarps];
   __shared__ int flag_s;
@@ -504,7 +502,7 @@ __global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs
   const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
   const RowRef rr = row_ref(a, rho);
   pdl_wait();
-  if (row_needed(a, rr)) stats_item<KP>(a, rho, slice, red);
+  if (row_needed(a, rr)) stats_item<kPer>(a, rho, slice, red);
   pdl_release();  // after this CTA's pass: the grid may span many waves
   const int rows_per_req = (a.k + 1) + (a.zrows ? a.k : 0);
   if (!last_arrival(a.req_ticket, rr.b, rows_per_req * a.nslices, &flag_s)) return;
@@ -597,15 +595,12 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
               ? 1
               : 0;
   const long long nrows = static_cast<long long>(B) * (k + 1) + (a.zrows ? static_cast<long long>(B) * k : 0);
-  // Many rows (more than about four waves of 4096-entry CTAs): 16384 entries per CTA,
-  // so that each CTA's fixed cost (launch, reduction, ticket) covers 64 KB of reads.
-  // The workspace holds the partials of the 4096-entry slicing, the larger count.
-  const int sms = device_sm_count();
-  const bool wide = sms > 0 && nrows * L.nslices > 4LL * sms * 8;
-  if (wide) a.nslices = (V + kSliceWide - 1) / kSliceWide;
+  // 16384 entries (64 KB) per CTA: each CTA's fixed cost (scheduling, reduction,
+  // ticket) is spread over 64 loads in flight per thread; at batch 1 the 27B rows
+  // make one wave of CTAs.
   const long long g1 = nrows * a.nslices;
-  if (launch_pdl(wide ? verify_stats_kernel<kPerWide> : verify_stats_kernel<kPer>,
-                 dim3(static_cast<unsigned>(g1)), dim3(kThreads), 0, stream, a) != cudaSuccess)
+  if (launch_pdl(verify_stats_kernel, dim3(static_cast<unsigned>(g1)), dim3(kThreads), 0, stream, a) !=
+      cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);
   if (mode == 1) {

@@ -231,7 +231,7 @@ def _verify_inputs(B, k, V, seed):
     return z, drafts, target.astype(np.float32)
 
 
-# the last two cases have enough rows for the 16384-entry slicing of the stats pass
+# the last two cases: many requests, rows of several 16384-entry slices with a ragged tail
 @pytest.mark.parametrize("B,k,V", [(1, 7, 4096), (5, 3, 4097), (16, 7, 9000), (4, 16, 301),
                                    (64, 7, 50000), (96, 7, 30001)])
 def test_verify_greedy_bit_exact(B, k, V):
@@ -260,7 +260,7 @@ def _excluded(ref, B):
 
 
 @pytest.mark.parametrize("with_q_stats", [False, True])
-# (64, 7, 50001) and (48, 7, 40000) without q stats take the 16384-entry slicing
+# (64, 7, 50001) and (48, 7, 40000): many requests, rows of several slices, ragged tails
 @pytest.mark.parametrize("B,k,V", [(1, 7, 4096), (6, 5, 4099), (16, 7, 20000), (64, 2, 128),
                                    (64, 7, 50001), (48, 7, 40000)])
 def test_verify_probabilistic_bit_exact(B, k, V, with_q_stats):
