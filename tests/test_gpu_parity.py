@@ -153,8 +153,10 @@ def test_greedy_sample_bit_exact(B, k, V, r):
     np.testing.assert_allclose(q[..., 1], ref["q_sumexp"], rtol=1e-5)
 
 
+# (13, 7, 20011, 64): a second 8-request group of 5 (an odd request pair, staged logits)
 @pytest.mark.parametrize("B,k,V,r", [(1, 7, 4096, 16), (3, 4, 5001, 16), (16, 7, 20000, 64),
-                                     (9, 16, 3001, 32), (1, 7, 20000, 0), (20, 3, 20000, 128)])
+                                     (9, 16, 3001, 32), (1, 7, 20000, 0), (20, 3, 20000, 128),
+                                     (13, 7, 20011, 64)])
 def test_greedy_sample_without_q_stats_bit_exact(B, k, V, r):
     """Without a q_stats buffer the chain reduces only the argmax keys (another kernel
     variant): z and the draft tokens stay bit-exact, and draft_len is not touched."""
