@@ -167,9 +167,11 @@ dspark_status_t dspark_fc_lm_head(const dspark_bf16_t *const *taps, int T, int64
  * means no bias (plain argmax), then w2 and r are ignored.
  * prev_token [B] int32 in [0, V) (else DSPARK_ERR_BAD_TOKEN is recorded and
  * that request is drafted without bias).  One cooperative launch covers all k
- * positions (one launch per position when a cooperative launch is refused or
- * r is not 16, 32, 64 or 128).  q_stats == NULL selects a variant that reduces
- * only the argmax (probabilistic verify then reduces q's statistics itself).
+ * positions (one launch per position when a cooperative launch is refused, r is
+ * not 16, 32, 64 or 128, V exceeds 1024 rows per SM, or the batch's contexts do
+ * not fit in shared memory: B above 266 at V = 151936, r = 64 on 152 SMs).
+ * q_stats == NULL selects a variant that reduces only the argmax (probabilistic
+ * verify then reduces q's statistics itself).
  * ---------------------------------------------------------------------- */
 size_t dspark_greedy_sample_workspace_size(int B, int k, int V, int r);
 dspark_status_t dspark_greedy_sample(float *logits, const dspark_bf16_t *w1,
