@@ -153,14 +153,33 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
   auto index_of = [&](int e) {
     return a.vec ? base + (e >> 2) * (kThreads * 4) + tid * 4 + (e & 3) : base + e * kThreads + tid;
   };
+  // A slice wholly inside the row (every slice but a row's last): the max by fmaxf
+  // (which passes over NaN like the strict compare), then the first entry holding it
+  // (ascending index); the same value and index as the strict-compare scan below.
+  const bool full = base + kThreads * KP <= V;
   float bv = -INFINITY;
   int bi = -1;
+  if (full) {
+    float m = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < KP; ++e) {
-    const int xi = index_of(e);
-    if (xi < V && x[e] > bv) {
-      bv = x[e];
-      bi = xi;
+    for (int e = 0; e < KP; ++e) m = fmaxf(m, x[e]);
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int e = KP - 1; e >= 0; --e) {
+        if (x[e] == m) {  // the last hit is the lowest index
+          bv = x[e];
+          bi = index_of(e);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < KP; ++e) {
+      const int xi = index_of(e);
+      if (xi < V && x[e] > bv) {
+        bv = x[e];
+        bi = xi;
+      }
     }
   }
   const int x0 = index_of(0);
@@ -169,9 +188,16 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
   SoftStat st{-INFINITY, 0.0f};
   if (want_stats && bi >= 0 && bv != INFINITY) {
     float sum = 0.0f;
+    if (full) {
+      // every entry in range; -inf adds exp(-inf) = +0 and NaN adds +0, both exact
+      // no-ops on a sum that starts at +0, so the sum is the one of the scan below
 #pragma unroll
-    for (int e = 0; e < KP; ++e)
-      if (index_of(e) < V && x[e] == x[e] && x[e] != -INFINITY) sum += __expf(x[e] - bv);
+      for (int e = 0; e < KP; ++e) sum += (x[e] == x[e]) ? __expf(x[e] - bv) : 0.0f;
+    } else {
+#pragma unroll
+      for (int e = 0; e < KP; ++e)
+        if (index_of(e) < V && x[e] == x[e] && x[e] != -INFINITY) sum += __expf(x[e] - bv);
+    }
     st = SoftStat{bv, sum};
   }
   best = warp_max_u64(best);
