@@ -283,6 +283,31 @@ def test_verify_probabilistic_bit_exact(B, k, V, with_q_stats):
     np.testing.assert_array_equal(host(n)[~ex], ref["next_token"][~ex])
 
 
+def test_verify_with_masked_vocabulary_bit_exact():
+    """A vocabulary mask (about 30% of the entries -inf in the target and draft-logit
+    rows, as a sampler's token mask leaves them) over rows of two whole 16384-entry
+    slices and a ragged one: greedy and probabilistic decisions match the oracle."""
+    B, k, V = 4, 5, 40000
+    z, drafts, target = _verify_inputs(B, k, V, 97)
+    mask = np.random.default_rng(98).random(V) < 0.3
+    z[:, :, mask] = -np.inf
+    target[:, :, mask] = -np.inf
+    drafts = z.argmax(axis=-1).astype(np.int32)
+    t = target.argmax(axis=-1).astype(np.int32)
+    drafts[::2, :2] = t[::2, :2]
+    ref0 = oracle.verify(0, target, drafts, None)
+    a, n = ds.verify(0, dev(target), dev(drafts), None)
+    np.testing.assert_array_equal(host(a), ref0["accepted_len"])
+    np.testing.assert_array_equal(host(n), ref0["next_token"])
+    ref = oracle.verify(1, target, drafts, None, z, seed=0xABCDEF, step=9)
+    a, n = ds.verify(1, dev(target), dev(drafts), None, dev(z), None, seed=0xABCDEF, step=9)
+    ex = _excluded(ref, B)
+    assert ex.mean() < 0.5
+    np.testing.assert_array_equal(host(a)[~ex], ref["accepted_len"][~ex])
+    np.testing.assert_array_equal(host(n)[~ex], ref["next_token"][~ex])
+    assert not mask[host(n)[~ex]].any()  # no draw lands on a masked token
+
+
 def test_verify_probabilistic_one_hot_and_request_ids():
     B, k, V = 12, 4, 3000
     z, drafts, target = _verify_inputs(B, k, V, 77)
