@@ -414,7 +414,7 @@ def run_ours(args, rank, local_rank, world):
     stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     wsp = ds.Workspaces()
 
-    def one_step(i, st, ev=None, s=None, hist=None):
+    def one_step(i, st, ev=None, s=None, hist=None, side_copy=None, target_ready=None):
         s = s if s is not None else stream
         acc_o, nxt_o, dlen_o = hist if hist is not None else (acc_hist[i], nxt_hist[i], dlen_hist[i])
         if ev is not None:
@@ -429,6 +429,8 @@ def run_ours(args, rank, local_rank, world):
             if ev is not None:
                 ev[1].record(s)
             lm_call(h_buf, out=logits.view(M, V), stream=s, workspaces=wsp)
+        if side_copy is not None:  # (both branches) once the GEMMs are queued: the
+            side_copy()            # copy's host time overlaps them
         if ev is not None:
             ev[2].record(s)
         ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
@@ -439,6 +441,8 @@ def run_ours(args, rank, local_rank, world):
                                    draft_len=dlen_o, stream=s)
         if ev is not None:
             ev[3].record(s)
+        if target_ready is not None:
+            s.wait_event(target_ready)  # the target logits were copied on a side stream
         ds.verify(mode, st["target"], drafts, dlen_o if conf_w is not None else None,
                   logits if mode == 1 else None, q_stats, seed=12345,
                   request_id=None, step=i, accepted_len=acc_o, next_token=nxt_o,
@@ -545,6 +549,15 @@ def run_ours(args, rank, local_rank, world):
     e2e_set = {"taps": [dev_taps[j] for j in range(T)], "prev": dev_prev, "target": dev_target}
     h2d = pin_taps.numel() * 2 + pin_prev.numel() * 4 + pin_target.numel() * 4
     d2h = (2 * B + B * k) * 4
+    # Only verify reads the target logits: their copy runs on a side stream, under the
+    # readout, and verify waits for it (the taps and prev tokens go first, in order).
+    copy_stream = torch.cuda.Stream(device)
+    target_ready = torch.cuda.Event()
+
+    def copy_target():
+        with torch.cuda.stream(copy_stream):  # the previous step's verify is done
+            dev_target.copy_(pin_target, non_blocking=True)
+            target_ready.record(copy_stream)
     for rep in range(2):
         if world > 1:
             dist.barrier()
@@ -554,8 +567,7 @@ def run_ours(args, rank, local_rank, world):
         for i in range(n):
             dev_taps.copy_(pin_taps, non_blocking=True)
             dev_prev.copy_(pin_prev, non_blocking=True)
-            dev_target.copy_(pin_target, non_blocking=True)
-            one_step(i, e2e_set)
+            one_step(i, e2e_set, side_copy=copy_target, target_ready=target_ready)
             out_acc.copy_(acc_hist[i], non_blocking=True)
             out_nxt.copy_(nxt_hist[i], non_blocking=True)
             out_drafts.copy_(drafts, non_blocking=True)
