@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   const int v_lo = cta * a.rows_per_cta;
   const int v_hi = min(V, v_lo + a.rows_per_cta);
   const int nrows = max(0, v_hi - v_lo);
-  // this thread's rows: tid and tid + 512 of the slice (clamped; results of the
-  // clamped copies are discarded)
+  // this thread's rows: tid + j * kPThreads of the slice, j < kPRows (clamped;
+  // results of the clamped copies are discarded)
   bool valid[kPRows];
   int vrow[kPRows];
 #pragma unroll
@@ -690,7 +690,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
           if (g < gb) red[g][warp] = ChainPartial{key[g], mx[g], sm[g]};
       }
       __syncthreads();
-      // one warp per request of the group combines the 16 warp partials
+      // one warp per request of the group combines the kPWarps warp partials
       if (warp < gb) {
         const int g = warp;
         unsigned long long key = 0ull;
