@@ -78,3 +78,34 @@ def test_measured_peaks_fall_back_when_no_file(tmp_path, monkeypatch):
 @pytest.mark.parametrize("units,world,secs,rate", [(100, 1, 2.0, 50.0), (100, 4, 2.0, 200.0)])
 def test_whole_job_rate_counts_every_rank(units, world, secs, rate):
     assert bench.whole_job_rate(units, world, secs) == rate
+
+
+class _FakeProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler_with(tmp_path, lines):
+    cs = bench.ClockSampler(0)
+    cs.path = str(tmp_path / "clocks.csv")
+    with open(cs.path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    cs.fh = open(cs.path, "a")
+    cs.proc = _FakeProc()
+    return cs
+
+
+def test_clock_sampler_reports_median_clock_and_throttle_reasons(tmp_path):
+    rows = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1980, 2070, 1390.2, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 1001.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbage line",
+            "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    out = _sampler_with(tmp_path, rows).stop()
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    hot = ["0, 1500, 2070, 1400.0, 0x48, Active, Not Active, Active, Not Active"] * 3
+    assert _sampler_with(tmp_path, hot).stop()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert _sampler_with(tmp_path, ["nothing parseable"]).stop() is None
