@@ -53,6 +53,13 @@ def lib():
                                     ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, _u32p,
                                     ctypes.c_uint32, _i32p, _i32p, _f64p, _f64p, _i32p]
         L.oracle_f32_to_bf16_n.argtypes = [_f32p, ctypes.c_int64, _u16p]
+        L.oracle_confidence_markov.restype = ctypes.c_int
+        L.oracle_confidence_markov.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p,
+                                               ctypes.c_float, ctypes.c_float, ctypes.c_int, _u16p,
+                                               ctypes.c_int, ctypes.c_int64, _i32p, _i32p, _f64p,
+                                               _f64p, _f64p, _i32p]
+        L.oracle_row_stats.restype = ctypes.c_int
+        L.oracle_row_stats.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, _i32p]
         L.oracle_e4m3_to_f32.restype = ctypes.c_float
         L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
         L.oracle_f32_to_e4m3.restype = ctypes.c_uint8
@@ -179,6 +186,21 @@ def greedy_sample(logits, w1, w2, prev):
     return {"z": z, "draft_tokens": d, "q_max": qm, "q_sumexp": qs, "top2_gap": gap}
 
 
+def row_stats(x):
+    """fp32 rows [..., V] -> dict max (fp64), sumexp (fp64 sum of exp(x - max)), argmax
+    (int32, lowest index of the max), each of shape [...]."""
+    x = _c(np.asarray(x), np.float32)
+    V = x.shape[-1]
+    lead = x.shape[:-1]
+    n = int(np.prod(lead)) if lead else 1
+    mx = np.empty(n, np.float64)
+    se = np.empty(n, np.float64)
+    arg = np.empty(n, np.int32)
+    _check(lib().oracle_row_stats(_p(x, _f32p), n, V, _p(mx, _f64p), _p(se, _f64p), _p(arg, _i32p)),
+           "oracle_row_stats")
+    return {"max": mx.reshape(lead), "sumexp": se.reshape(lead), "argmax": arg.reshape(lead)}
+
+
 def confidence(h, B, k, conf_w, conf_b, tau, draft_tokens=None):
     """h uint16 [B*k, H]; returns dict zc, conf, draft_len, draft_tokens (masked copy)."""
     h = _c(h, np.uint16)
@@ -192,6 +214,35 @@ def confidence(h, B, k, conf_w, conf_b, tau, draft_tokens=None):
                                    float(tau), _p(zc, _f64p), _p(cf, _f64p), _p(L, _i32p),
                                    _p(dt, _i32p)), "oracle_confidence")
     return {"zc": zc, "conf": cf, "draft_len": L, "draft_tokens": dt}
+
+
+def confidence_markov(h, B, k, conf_w, conf_b, tau, draft_tokens, cumulative=False, w1=None,
+                      prev=None):
+    """Confidence head over [h ; markov_w1[context]] (w1 given: conf_w has H + r entries)
+    or over h alone, with the per-position or cumulative truncation rule.  draft_tokens
+    [B, k] are the chain's drafts (contexts of positions 1..k-1); returns dict zc, conf,
+    cum (running sum of log sigmoid), draft_len, draft_tokens (masked copy)."""
+    h = _c(h, np.uint16)
+    H = h.shape[1]
+    conf_w = _c(conf_w, np.uint16)
+    r, V = 0, 0
+    if w1 is not None:
+        w1 = _c(w1, np.uint16)
+        V, r = w1.shape
+        assert conf_w.shape == (H + r,)
+        prev = _c(np.asarray(prev, np.int32), np.int32)
+    else:
+        assert conf_w.shape[0] >= H
+    dt = np.array(draft_tokens, dtype=np.int32, copy=True)
+    zc = np.empty((B, k), np.float64)
+    cf = np.empty((B, k), np.float64)
+    cum = np.empty((B, k), np.float64)
+    L = np.empty((B,), np.int32)
+    _check(lib().oracle_confidence_markov(_p(h, _u16p), B, k, H, _p(conf_w, _u16p), float(conf_b),
+                                          float(tau), int(bool(cumulative)), _p(w1, _u16p), r, V,
+                                          _p(prev, _i32p), _p(dt, _i32p), _p(zc, _f64p), _p(cf, _f64p),
+                                          _p(cum, _f64p), _p(L, _i32p)), "oracle_confidence_markov")
+    return {"zc": zc, "conf": cf, "cum": cum, "draft_len": L, "draft_tokens": dt}
 
 
 def verify(mode, target, drafts, draft_len=None, z=None, seed=0, request_id=None, step=0):

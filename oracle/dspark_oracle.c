@@ -286,6 +286,49 @@ int oracle_greedy_sample(float *logits, int B, int k, int64_t V,
 }
 
 /* ------------------------------------------------------------------ */
+/* Softmax statistics and argmax of rows                               */
+/* ------------------------------------------------------------------ */
+/*
+ * The per-row quantities verify needs from one distribution's logits (p from
+ * the target rows, q from the draft-logit rows; [PR128] "verified by
+ * rejection sampling", [CARD] "draft_sample_method": "probabilistic"):
+ *   mx[r]  = max_v x[r, v]                    (-inf when every entry is -inf)
+ *   se[r]  = sum_v exp(x[r, v] - mx[r])       (fp64; 0 when mx is -inf)
+ *   arg[r] = smallest v with x[r, v] == mx[r] (0 when every entry is -inf)
+ * NaN entries are skipped (they neither win nor add).  -0 == +0.
+ */
+int oracle_row_stats(const float *x, int64_t nrows, int64_t V, double *mx, double *se,
+                     int32_t *arg) {
+    if (nrows < 0 || V < 1 || !x) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const float *row = x + r * V;
+        double m = -INFINITY;
+        int64_t best = 0;
+        int found = 0;
+        for (int64_t v = 0; v < V; ++v) {
+            const double xv = (double)row[v];
+            if (xv != xv) continue;
+            if (!found || xv > m) {
+                m = xv;
+                best = v;
+                found = 1;
+            }
+        }
+        double s = 0.0;
+        if (m != -INFINITY)
+            for (int64_t v = 0; v < V; ++v) {
+                const double xv = (double)row[v];
+                if (xv == xv) s += exp(xv - m);
+            }
+        if (mx) mx[r] = m;
+        if (se) se[r] = s;
+        if (arg) arg[r] = (int32_t)best;
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------ */
 /* Confidence head and adaptive truncation                             */
 /* ------------------------------------------------------------------ */
 /*
@@ -327,6 +370,77 @@ int oracle_confidence(const uint16_t *h, int B, int k, int H,
             for (int i = L; i < k; ++i) draft_tokens[(int64_t)b * k + i] = -1;
     }
     return ORACLE_OK;
+}
+
+/* log(sigmoid(z)) without overflow: -log1p(exp(-z)) for z >= 0, z - log1p(exp(z))
+ * below. */
+static double log_sigmoid(double z) {
+    return z >= 0.0 ? -log1p(exp(-z)) : z - log1p(exp(z));
+}
+
+/*
+ * Confidence head with the Markov context, and the cumulative truncation rule.
+ * [PR620] / [CARD] name the draft config field confidence_head_with_markov
+ * next to enable_confidence_head and markov_rank, and the AcceptRatePredictor
+ * head; the pages give no formula.  Reading taken: with the field set, the
+ * head sees the Markov context of the position besides its hidden state, as
+ * one linear layer over the concatenation [h_i ; e_i]:
+ *   e_i      = markov_w1[c_i, :]   (r values; c_0 = the bonus token prev[b],
+ *                                   c_i = the draft token of position i-1)
+ *   zc[b,i]  = sum_c w[c] h_i[c] + sum_t w[H + t] e_i[t] + b        (fp64)
+ *   conf     = sigmoid(zc)
+ * (w1 == NULL: the plain head, w has H entries.)  Truncation:
+ *   per position (cumulative == 0): L = first i with zc < logit(tau);
+ *   cumulative   (cumulative != 0): L = first i with
+ *       sum_{j <= i} log sigmoid(zc_j) < log(tau),
+ *     i.e. the product of the acceptance confidences of the prefix falls
+ *     below tau (the head predicts per-position acceptance, and the whole
+ *     prefix must be accepted for position i to count).
+ * tau <= 0 keeps every position, tau >= 1 keeps none.  draft_tokens (in/out,
+ * [B, k], the chain's drafts) supply the contexts and get -1 from L on.
+ * Also returns cum[b,i] = sum_{j<=i} log sigmoid(zc_j) (may be NULL).
+ */
+int oracle_confidence_markov(const uint16_t *h, int B, int k, int H, const uint16_t *conf_w,
+                             float conf_b, float tau, int cumulative, const uint16_t *w1, int r,
+                             int64_t V, const int32_t *prev, int32_t *draft_tokens, double *zc,
+                             double *conf, double *cum, int32_t *draft_len) {
+    if (B < 0 || k < 1 || H < 1 || !h || !conf_w || !draft_len || !draft_tokens) return ORACLE_ERR_ARG;
+    if (w1 && (r < 1 || V < 1 || !prev)) return ORACLE_ERR_ARG;
+    int status = ORACLE_OK;
+    for (int b = 0; b < B; ++b) {
+        double s = 0.0;
+        int32_t L = k;
+        for (int i = 0; i < k; ++i) {
+            const uint16_t *hrow = h + ((int64_t)b * k + i) * H;
+            double acc = 0.0;
+            for (int c = 0; c < H; ++c)
+                acc += (double)bf16_bits_to_float(conf_w[c]) * (double)bf16_bits_to_float(hrow[c]);
+            if (w1) {
+                const int32_t ctx = i == 0 ? prev[b] : draft_tokens[(int64_t)b * k + i - 1];
+                if (ctx < 0 || (int64_t)ctx >= V) {
+                    status = ORACLE_ERR_TOKEN;
+                } else {
+                    for (int t = 0; t < r; ++t)
+                        acc += (double)bf16_bits_to_float(conf_w[H + t]) *
+                               (double)bf16_bits_to_float(w1[(int64_t)ctx * r + t]);
+                }
+            }
+            acc += (double)conf_b;
+            s += log_sigmoid(acc);
+            if (zc) zc[(int64_t)b * k + i] = acc;
+            if (conf) conf[(int64_t)b * k + i] = 1.0 / (1.0 + exp(-acc));
+            if (cum) cum[(int64_t)b * k + i] = s;
+            int keep;
+            if (tau <= 0.0f) keep = 1;
+            else if (tau >= 1.0f) keep = 0;
+            else if (cumulative) keep = s >= log((double)tau);
+            else keep = acc >= log((double)tau) - log1p(-(double)tau);
+            if (L == k && !keep) L = i;
+        }
+        draft_len[b] = L;
+        for (int i = L; i < k; ++i) draft_tokens[(int64_t)b * k + i] = -1;
+    }
+    return status;
 }
 
 /* ------------------------------------------------------------------ */

@@ -458,3 +458,177 @@ def test_fp8_gemm_matches_numpy_on_decoded_operands():
 def test_bf16_array_rounding_matches_torch():
     x = np.random.default_rng(9).standard_normal(5000).astype(np.float32) * 7
     np.testing.assert_array_equal(oracle.f32_to_bf16_array(x), syn.to_bf16_bits(x))
+
+
+# ----------------------------------------------------------------------------- row statistics
+
+def test_row_stats_matches_library_definitions():
+    """max, first argmax and the fp64 sum of exp(x - max) of each row equal numpy's on
+    rows with ties, -0/+0, -inf entries, an all -inf row and large values (no overflow:
+    the max is subtracted before the exponential)."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((6, 257)).astype(np.float32)
+    x[0, [5, 200]] = 9.0                       # tie -> index 5
+    x[1, :] = -np.inf
+    x[2, 10] = -0.0
+    x[2, 11] = 0.0
+    x[2, :10] = -5.0
+    x[2, 12:] = -5.0                           # -0 == +0: the first of the two wins
+    x[3, ::3] = -np.inf
+    x[4] *= 1000.0                              # exp(x) alone would overflow
+    x[5, 256] = 50.0                            # the max in the last entry
+    got = oracle.row_stats(x)
+    xd = x.astype(np.float64)
+    for r in range(x.shape[0]):
+        m = xd[r].max()
+        assert got["max"][r] == m
+        assert got["argmax"][r] == int(np.argmax(xd[r]))
+        ref = 0.0 if m == -np.inf else float(np.exp(xd[r] - m).sum())
+        assert got["sumexp"][r] == pytest.approx(ref, rel=1e-14, abs=0.0)
+    assert got["argmax"][0] == 5 and got["argmax"][2] == 10 and got["argmax"][1] == 0
+    assert got["sumexp"][1] == 0.0 and got["max"][1] == -np.inf
+
+
+# ----------------------------------------------------------------------------- draw margins
+
+def _gumbel32(seed, req, row, step, V):
+    """The same noise evaluated in binary32 (numpy float32 logarithms)."""
+    g = np.empty(V, np.float32)
+    for v in range(V):
+        w = oracle.philox4x32_10((req, row, step, 1 + v // 4), (seed & 0xFFFFFFFF, seed >> 32))
+        u = np.float32((2 * (w[v % 4] >> 9) + 1) * 2.0 ** -24)
+        g[v] = -np.log(-np.log(u))
+    return g
+
+
+def _float32_draw(t, z, row, seed, b, step, kind):
+    """Binary32 evaluation of a draw's keys with numpy float32 (normalisers rounded to
+    fp32; residual log(p - q) as (t - cp) + log1p(-exp((z - cq) - (t - cp))); noise
+    -log(-log U)) -> the argmax."""
+    V = t.shape[-1]
+    tr = t[b, row]
+    fin = tr[np.isfinite(tr)].astype(np.float64)
+    cp = np.float32(fin.max() + math.log(np.exp(fin - fin.max()).sum()))
+    g = _gumbel32(seed, b, row, step, V)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        if kind == "residual":
+            zr = z[b, row]
+            cq = np.float32(float(zr.max()) + math.log(float(np.exp(zr.astype(np.float64) - zr.max()).sum())))
+            av = (tr - cp).astype(np.float32)
+            bv = (zr - cq).astype(np.float32)
+            kr = np.where(av > bv, av + np.log1p(-np.exp(bv - av)) + g, -np.inf)
+        else:
+            kr = tr + g
+    return int(np.argmax(kr.astype(np.float32)))
+
+
+def test_draw_margin_bounds_a_binary32_evaluation():
+    """Where the oracle reports a positive draw margin, an independent binary32 evaluation
+    of the draw keys picks the oracle's token.  Two families: random rows (residual draws
+    after a rejection, and bonus draws), and bonus draws built so that the top two keys
+    lie 1e-7 .. 1e-3 apart, which puts many margins just above zero; a margin formula
+    that under-counted the binary32 error would let the two sides disagree there."""
+    seed, step = 77, 5
+    # family 1: random rows, residual draws (q = softmax of z, draft = argmax z)
+    N, V = 400, 24
+    rng = np.random.default_rng(9)
+    t = (rng.standard_normal((N, 2, V)) * 0.05).astype(np.float32)
+    z = (t[:, :1] + rng.standard_normal((N, 1, V)).astype(np.float32) * 0.05).astype(np.float32)
+    d = z[:, 0].argmax(axis=-1).astype(np.int32)[:, None]
+    out = oracle.verify(1, t, d, None, z, seed=seed, step=step)
+    checked = 0
+    for b in range(N):
+        if out["sample_margin"][b] > 0:
+            row = out["sample_row"][b]
+            kind = "residual" if row == 0 else "bonus"
+            assert _float32_draw(t, z, row, seed, b, step, kind) == out["next_token"][b]
+            checked += 1
+    assert checked > N // 2
+    # family 2: built close pairs at the bonus row (the draft has p = 1, so it is accepted)
+    deltas = np.logspace(-7, -3, 200)
+    M, V2, a, c = len(deltas), 8, 1, 6
+    tb = np.full((M, 2, V2), -np.inf, np.float32)
+    tb[:, 0, 3] = 0.0                                   # p(3) = 1 at row 0
+    for b, dl in enumerate(deltas):
+        g = _gumbel(seed, b, 1, step, V2)
+        tb[b, 1, a] = 0.0
+        tb[b, 1, c] = np.float32(g[a] - g[c] + (dl if b % 2 else -dl))
+    outb = oracle.verify(1, tb, np.full((M, 1), 3, np.int32), None, None, seed=seed, step=step)
+    assert np.all(outb["accepted_len"] == 1) and np.all(outb["sample_row"] == 1)
+    pos = 0
+    for b in range(M):
+        if outb["sample_margin"][b] > 0:
+            assert _float32_draw(tb, None, 1, seed, b, step, "bonus") == outb["next_token"][b], b
+            pos += 1
+    neg = int((outb["sample_margin"] < 0).sum())
+    assert pos > 50 and neg > 20                         # both sides of the bound exercised
+    # the bound sits between 1e-6 and 1e-4 for keys of this size
+    assert np.all(outb["sample_margin"][deltas > 1e-4] > 0)
+    assert np.all(outb["sample_margin"][deltas < 1e-6] < 0)
+
+
+def test_draw_margin_is_negative_on_a_built_near_tie():
+    """Two candidates whose keys log p + G differ by about one fp32 ulp: the oracle must
+    flag the draw (negative margin), since binary32 evaluations may order them either way."""
+    seed, step, V = 5, 3, 8
+    a, c = 2, 6                              # the two candidates; every other weight is zero
+    g = _gumbel(seed, 0, 0, step, V)
+    t = np.full((1, 2, V), -np.inf, np.float32)
+    t[0, 0, a] = 0.0
+    t[0, 0, c] = np.float32(g[a] - g[c])     # t_c + G_c = t_a + G_a up to fp32 rounding
+    t[0, 1] = 0.0
+    drafts = np.array([[0]], np.int32)       # p(0) = 0: rejected; residual = p without 0
+    out = oracle.verify(1, t, drafts, None, None, seed=seed, step=step)
+    assert out["accepted_len"][0] == 0 and out["sample_row"][0] == 0
+    assert out["next_token"][0] in (a, c)
+    assert out["sample_margin"][0] < 0
+
+
+# ----------------------------------------------------------------------------- confidence with the Markov context
+
+def test_confidence_markov_hand_case():
+    """H = 2, r = 2, V = 4, integer weights, worked by hand.
+    h rows (1, 2), (0, 1), (2, -1); conf_w = (1, -1 | 2, 1); markov_w1 rows
+    (0, 0), (1, 0), (0, 1), (-1, 1); bonus token 1; drafts (2, 3, 0).
+      position 0: h.w = 1 - 2 = -1, context 1 -> e = (1, 0) -> 2;  zc = 1
+      position 1: h.w = 0 - 1 = -1, context 2 -> e = (0, 1) -> 1;  zc = 0
+      position 2: h.w = 2 + 1 =  3, context 3 -> e = (-1, 1) -> -1; zc = 2
+    Per position at tau = 0.5 (keep iff zc >= 0): all three kept.
+    Cumulative at tau = 0.5: sigmoid(1) = 0.731 kept; 0.731 * sigmoid(0) = 0.366 < 0.5 ->
+    draft_len 1.  At tau = 0.3: 0.366 kept; 0.366 * sigmoid(2) = 0.322 kept -> 3."""
+    bf = syn.to_bf16_bits
+    h = bf(np.array([[1, 2], [0, 1], [2, -1]], np.float32))
+    w = bf(np.array([1, -1, 2, 1], np.float32))
+    w1 = bf(np.array([[0, 0], [1, 0], [0, 1], [-1, 1]], np.float32))
+    prev = np.array([1], np.int32)
+    drafts = np.array([[2, 3, 0]], np.int32)
+    per = oracle.confidence_markov(h, 1, 3, w, 0.0, 0.5, drafts, False, w1, prev)
+    assert per["zc"][0].tolist() == [1.0, 0.0, 2.0]
+    assert per["draft_len"][0] == 3 and per["draft_tokens"][0].tolist() == [2, 3, 0]
+    cum = oracle.confidence_markov(h, 1, 3, w, 0.0, 0.5, drafts, True, w1, prev)
+    assert cum["draft_len"][0] == 1 and cum["draft_tokens"][0].tolist() == [2, -1, -1]
+    cum3 = oracle.confidence_markov(h, 1, 3, w, 0.0, 0.3, drafts, True, w1, prev)
+    assert cum3["draft_len"][0] == 3
+    # a bias shifts every position: b = -1.5 fails position 0 under either rule
+    low = oracle.confidence_markov(h, 1, 3, w, -1.5, 0.5, drafts, False, w1, prev)
+    assert low["draft_len"][0] == 0 and low["draft_tokens"][0].tolist() == [-1, -1, -1]
+
+
+def test_confidence_markov_reduces_to_the_plain_head_and_product_rule():
+    """Without markov_w1 the head is the plain one (same zc and draft lengths); the
+    cumulative rule cuts where numpy's running product of sigmoids first drops below tau."""
+    B, k, H = 6, 7, 64
+    h = syn.normal_bf16(81, (B * k, H))
+    w = syn.normal_bf16(82, (H,), (4.0 / H) ** 0.5)
+    drafts = np.tile(np.arange(k, dtype=np.int32), (B, 1))
+    plain = oracle.confidence(h, B, k, w, 0.1, 0.5, drafts)
+    mk = oracle.confidence_markov(h, B, k, w, 0.1, 0.5, drafts, False)
+    np.testing.assert_array_equal(mk["zc"], plain["zc"])
+    np.testing.assert_array_equal(mk["draft_len"], plain["draft_len"])
+    for tau in (0.05, 0.2, 0.5, 0.8):
+        cum = oracle.confidence_markov(h, B, k, w, 0.1, tau, drafts, True)
+        prod = np.cumprod(1.0 / (1.0 + np.exp(-mk["zc"])), axis=1)
+        want = np.array([int(np.argmax(row < tau)) if (row < tau).any() else k for row in prod])
+        np.testing.assert_array_equal(cum["draft_len"], want)
+    assert (oracle.confidence_markov(h, B, k, w, 0.1, 0.0, drafts, True)["draft_len"] == k).all()
+    assert (oracle.confidence_markov(h, B, k, w, 0.1, 1.0, drafts, True)["draft_len"] == 0).all()
