@@ -48,7 +48,18 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sets", type=int, default=4, help="input sets rotated across steps")
+    ap.add_argument("--sets", type=int, default=3,
+                    help="minimum input sets rotated across steps (more are used when needed "
+                         "to exceed 2x the L2 cache)")
+    ap.add_argument("--min-time", type=float, default=1.0,
+                    help="seconds of repeated K-step timed loops (the median loop is reported)")
+    ap.add_argument("--no-b16", action="store_true",
+                    help="27b_b1: skip the batch-16 sub-record")
+    ap.add_argument("--verify", default="inline", choices=["split", "inline"],
+                    help="inline: the whole verify (target-row statistics, decision, draw) on "
+                         "the step's stream after drafting; split: the target-row statistics "
+                         "on a side stream beside the GEMMs (their CTAs then compete with the "
+                         "persistent GEMM CTAs for registers), one decision kernel after drafting")
     ap.add_argument("--no-graph", action="store_true", help="time un-captured steps only")
     ap.add_argument("--sweep", action="store_true",
                     help="run the 27B sweep grid instead (one JSON line per cell, not the "
@@ -57,9 +68,9 @@ def parse_args():
     ap.add_argument("--fused-gemms", action="store_true",
                     help="bf16 weights: run the fc and the LM head as one two-phase GEMM "
                          "launch (dspark_fc_lm_head) instead of two launches")
-    ap.add_argument("--q-stats", default="verify", choices=["verify", "chain"],
-                    help="where the softmax statistics of q are reduced: in verify's streaming "
-                         "pass over the draft logits, or in the Markov chain kernel")
+    ap.add_argument("--q-stats", default="chain", choices=["verify", "chain"],
+                    help="where the softmax statistics of q are reduced: in the Markov chain "
+                         "kernel, or by a row-statistics pass over the draft logits")
     return ap.parse_args()
 
 
@@ -327,8 +338,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / sps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "wall_s": wall,
-        "config": {"workload": args.config, **{kk: cfg[kk] for kk in ("B", "k", "H", "T", "V", "r")},
-                   "verify": "probabilistic" if mode == 1 else "greedy"},
+        "config": config_of(args.config, cfg, mode, args, world),
         "cpu_baseline": {"value": sps, "unit": "steps/s", "cores": ora.num_threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": sps, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -339,146 +349,242 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- our arm
 
-def run_ours(args, rank, local_rank, world):
+def n_input_sets(cfg, min_sets, l2_bytes):
+    """Input sets rotated across steps: at least min_sets and enough that their per-step
+    inputs (taps, prev tokens, target logits) exceed 2.2x the L2 cache, so no step finds
+    its inputs in L2 (the 1.8-2.2 GB of weights stream from HBM every step anyway)."""
+    B, k, H, T, V = (cfg[x] for x in ("B", "k", "H", "T", "V"))
+    per_set = T * B * k * H * 2 + B * 4 + B * (k + 1) * V * 4
+    need = -(-int(2.2 * l2_bytes) // per_set)
+    return int(min(256, max(min_sets, need))), per_set
+
+
+def timing_events_supported(torch):
+    """Timing events that become event-record nodes when captured in a CUDA graph."""
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+class Pipeline:
+    """One draft+verify step through the C ABI on given streams.
+
+    main stream: fc -> LM head -> Markov chain (+ q statistics) [-> confidence] ->
+    [wait for the target statistics] -> verify decision + draw.
+    side stream: statistics of the target rows (depend only on the target logits, so
+    they run beside the GEMMs).  verify="inline" instead runs the whole verify (row
+    statistics included) on the main stream after the chain."""
+
+    def __init__(self, ds, torch, device, cfg, mode, w, args):
+        self.ds, self.torch, self.dev = ds, torch, device
+        self.cfg, self.mode, self.w = cfg, mode, w
+        B, k, H, V = cfg["B"], cfg["k"], cfg["H"], cfg["V"]
+        M = B * k
+        self.fp8 = bool(cfg.get("fp8"))
+        self.fused = (not self.fp8) and args.fused_gemms
+        self.split = args.verify == "split"
+        self.q_in = args.q_stats
+        f32, i32 = torch.float32, torch.int32
+        self.h = torch.empty((M, H), dtype=torch.bfloat16, device=device)
+        self.logits = torch.empty((B, k, V), dtype=f32, device=device)
+        self.drafts = torch.empty((B, k), dtype=i32, device=device)
+        self.q_stats = torch.empty((B, k, 2), dtype=f32, device=device) if mode == 1 else None
+        self.t_ms = torch.empty((B, k + 1, 2), dtype=f32, device=device)
+        self.t_arg = torch.empty((B, k + 1), dtype=i32, device=device)
+        self.wsp = ds.Workspaces()          # main-stream calls
+        self.wsp_side = ds.Workspaces()     # the side stream's row statistics
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
+
+    def target_stats(self, target, s):
+        self.ds.row_stats(target, ms=self.t_ms, argmax=self.t_arg, stream=s, workspaces=self.wsp_side)
+
+    def step(self, st, s, side, hist, step_id, ev=None, side_ev=None, target_ready=None):
+        """ev: 5 timing events on s (start, after fc, after LM head, after chain, end);
+        side_ev: 2 timing events on the side stream around the target statistics.
+        target_ready: the target statistics are issued elsewhere (end-to-end leg) and
+        this event marks them done."""
+        ds, w, cfg = self.ds, self.w, self.cfg
+        B, k, V = cfg["B"], cfg["k"], cfg["V"]
+        M = B * k
+        acc_o, nxt_o, dlen_o = hist
+        if ev is not None:
+            ev[0].record(s)
+        if self.split and target_ready is None:
+            self.fork.record(s)
+            side.wait_event(self.fork)
+            if side_ev is not None:
+                side_ev[0].record(side)
+            self.target_stats(st["target"], side)
+            if side_ev is not None:
+                side_ev[1].record(side)
+            self.join.record(side)
+        if self.fused:
+            ds.fc_lm_head(st["taps"], w["fc_w"], w["lm_w"], h_out=self.h, logits=self.logits.view(M, V),
+                          stream=s, workspaces=self.wsp)
+            if ev is not None:
+                ev[1].record(s)
+        else:
+            if self.fp8:
+                ds.fc_project_fp8(st["taps"], w["fc_w8"], w["fc_s"], out=self.h, stream=s, workspaces=self.wsp)
+            else:
+                ds.fc_project(st["taps"], w["fc_w"], out=self.h, stream=s, workspaces=self.wsp)
+            if ev is not None:
+                ev[1].record(s)
+            if self.fp8:
+                ds.lm_head_fp8(self.h, w["lm_w8"], w["lm_s"], out=self.logits.view(M, V), stream=s,
+                               workspaces=self.wsp)
+            else:
+                ds.lm_head(self.h, w["lm_w"], out=self.logits.view(M, V), stream=s, workspaces=self.wsp)
+        if ev is not None:
+            ev[2].record(s)
+        chain_q = self.mode == 1 and self.q_in == "chain"
+        ds.greedy_sample(self.logits, w["w1"], w["w2"], st["prev"], draft_tokens=self.drafts,
+                         q_stats=self.q_stats if chain_q else None, want_q_stats=chain_q,
+                         stream=s, workspaces=self.wsp)
+        if w.get("conf_w") is not None:
+            ds.confidence_truncate(self.h, w["conf_w"], self.drafts, B, k, 0.0, 0.5,
+                                   draft_len=dlen_o, stream=s)
+        if ev is not None:
+            ev[3].record(s)
+        dl = dlen_o if w.get("conf_w") is not None else None
+        if self.split:
+            if self.mode == 1 and not chain_q:
+                ds.row_stats(self.logits, ms=self.q_stats, want_argmax=False, stream=s,
+                             workspaces=self.wsp)
+            s.wait_event(target_ready if target_ready is not None else self.join)
+            ds.verify_from_stats(self.mode, st["target"], self.t_ms, self.t_arg, self.drafts, dl,
+                                 self.logits if self.mode == 1 else None, self.q_stats, seed=12345,
+                                 request_id=None, step=step_id, accepted_len=acc_o, next_token=nxt_o,
+                                 stream=s, workspaces=self.wsp)
+        else:
+            if target_ready is not None:
+                s.wait_event(target_ready)
+            ds.verify(self.mode, st["target"], self.drafts, dl, self.logits if self.mode == 1 else None,
+                      self.q_stats if chain_q else None, seed=12345, request_id=None, step=step_id,
+                      accepted_len=acc_o, next_token=nxt_o, stream=s, workspaces=self.wsp)
+        if ev is not None:
+            ev[4].record(s)
+
+
+def load_weights(ds, torch, device, cfg, host_cache):
+    """Device weights of a workload (bf16, or E4M3 codes + row scales), from seeded host
+    draws shared between workloads of the same shapes."""
+    H, T, V, r = cfg["H"], cfg["T"], cfg["V"], cfg["r"]
+    key = (H, T, V, r)
+    if key not in host_cache:
+        host_cache.clear()
+        host_cache[key] = syn.weights(H, T, V, r, with_conf=True)
+    hw = host_cache[key]
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    w = {"w1": d16(hw["w1"]), "w2": d16(hw["w2"]), "conf_w": d16(hw["conf_w"]) if cfg["conf"] else None}
+    fc_w, lm_w = d16(hw["fc_w"]), d16(hw["lm_w"])
+    if cfg.get("fp8"):
+        w["fc_w8"], w["fc_s"] = ds.quantize_fp8(fc_w)
+        w["lm_w8"], w["lm_s"] = ds.quantize_fp8(lm_w)
+        torch.cuda.synchronize()
+        del fc_w, lm_w
+    else:
+        w["fc_w"], w["lm_w"] = fc_w, lm_w
+    return w
+
+
+def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_baseline):
+    """Times one workload: K-step loops of CUDA-graph replays repeated for at least
+    --min-time seconds (median reported), stage times from replays of graphs carrying
+    timing events, the un-captured loop, and the end-to-end leg with host buffers."""
     import torch
     import torch.distributed as dist
 
     import speculative_decoding_fc_gb300 as ds
 
-    torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=device)
-    cfg = dict(syn.CONFIGS[args.config])
+    cfg = dict(syn.CONFIGS[name])
     mode = cfg["mode"] if args.mode is None else args.mode
     B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
     M = B * k
-
-    def d16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
-
-    w = syn.weights(H, T, V, r, with_conf=cfg["conf"])
-    fc_w, lm_w, w1, w2 = d16(w["fc_w"]), d16(w["lm_w"]), d16(w["w1"]), d16(w["w2"])
-    conf_w = d16(w["conf_w"]) if cfg["conf"] else None
-    host_w = w if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
-    del w
-    fp8 = bool(cfg.get("fp8"))
-    if fp8:
-        # weights quantised once (E4M3 codes + row scales); the bf16 copies are dropped
-        fc_w8, fc_s = ds.quantize_fp8(fc_w)
-        lm_w8, lm_s = ds.quantize_fp8(lm_w)
-        torch.cuda.synchronize()
-        del fc_w, lm_w
-
-    def fc_call(taps, **kw):
-        if fp8:
-            return ds.fc_project_fp8(taps, fc_w8, fc_s, **kw)
-        return ds.fc_project(taps, fc_w, **kw)
-
-    def lm_call(h, **kw):
-        if fp8:
-            return ds.lm_head_fp8(h, lm_w8, lm_s, **kw)
-        return ds.lm_head(h, lm_w, **kw)
-
-    # --fused-gemms (bf16 weights): fc and LM head as one two-phase launch (CTAs that
-    # finish their fc share stream LM-head weights while the others finish)
-    fused = (not fp8) and args.fused_gemms
+    w = load_weights(ds, torch, device, cfg, host_cache)
+    pipe = Pipeline(ds, torch, device, cfg, mode, w, args)
+    stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 << 20) or (129 << 20))
+    nsets, set_bytes = n_input_sets(cfg, args.sets, l2)
 
     # input sets: taps, prev, target logits = own draft logits + noise (built once)
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
     sets = []
-    for s in range(args.sets):
-        st = syn.step_inputs(replica_step_seed(s, rank), B, k, H, T, V, cfg["sigma"])
-        taps = [d16(t) for t in st["taps"]]
-        prev = torch.from_numpy(st["prev"]).to(device)
-        h = fc_call(taps)
-        logits = lm_call(h).view(B, k, V)
-        ds.greedy_sample(logits, w1, w2, prev)
+    tmp_hist = tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
+    for si in range(nsets):
+        st = syn.step_inputs(replica_step_seed(si, rank), B, k, H, T, V, cfg["sigma"])
+        dev_set = {"taps": [d16(t) for t in st["taps"]], "prev": torch.from_numpy(st["prev"]).to(device)}
+        # the drafter's own biased logits on this set, then the target = those + noise
+        if pipe.fp8:
+            h = ds.fc_project_fp8(dev_set["taps"], w["fc_w8"], w["fc_s"])
+            lg = ds.lm_head_fp8(h, w["lm_w8"], w["lm_s"]).view(B, k, V)
+        else:
+            h = ds.fc_project(dev_set["taps"], w["fc_w"])
+            lg = ds.lm_head(h, w["lm_w"]).view(B, k, V)
+        ds.greedy_sample(lg, w["w1"], w["w2"], dev_set["prev"], want_q_stats=False)
         noise = torch.from_numpy(st["noise"]).to(device)
-        target = torch.cat([logits, logits[:, -1:]], dim=1) + noise
-        sets.append({"taps": taps, "prev": prev, "target": target.contiguous(),
-                     "host": st if s == 0 else None})
+        dev_set["target"] = (torch.cat([lg, lg[:, -1:]], dim=1) + noise).contiguous()
+        dev_set["host"] = st if si == 0 else None
+        del h, lg, noise
+        sets.append(dev_set)
     torch.cuda.synchronize()
 
-    h_buf = torch.empty((M, H), dtype=torch.bfloat16, device=device)
-    logits = torch.empty((B, k, V), dtype=torch.float32, device=device)
-    drafts = torch.empty((B, k), dtype=torch.int32, device=device)
-    q_stats = torch.empty((B, k, 2), dtype=torch.float32, device=device) \
-        if (args.q_stats == "chain" and mode == 1) else None
-    dlen = torch.empty((B,), dtype=torch.int32, device=device) if cfg["conf"] else None
     K, W = args.steps, args.warmup
     acc_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
     nxt_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
     dlen_hist = torch.zeros((K + W, B), dtype=torch.int32, device=device)
-    stream = torch.cuda.current_stream(device)
-    # events at the stage boundaries of every timed step: fc | LM head | chain | verify
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    wsp = ds.Workspaces()
 
-    def one_step(i, st, ev=None, s=None, hist=None, side_copy=None, target_ready=None):
-        s = s if s is not None else stream
-        acc_o, nxt_o, dlen_o = hist if hist is not None else (acc_hist[i], nxt_hist[i], dlen_hist[i])
-        if ev is not None:
-            ev[0].record(s)
-        if fused:
-            ds.fc_lm_head(st["taps"], fc_w, lm_w, h_out=h_buf, logits=logits.view(M, V), stream=s,
-                          workspaces=wsp)
-            if ev is not None:
-                ev[1].record(s)
-        else:
-            fc_call(st["taps"], out=h_buf, stream=s, workspaces=wsp)
-            if ev is not None:
-                ev[1].record(s)
-            lm_call(h_buf, out=logits.view(M, V), stream=s, workspaces=wsp)
-        if side_copy is not None:  # (both branches) once the GEMMs are queued: the
-            side_copy()            # copy's host time overlaps them
-        if ev is not None:
-            ev[2].record(s)
-        ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts, q_stats=q_stats,
-                         want_q_stats=q_stats is not None,
-                         stream=s, workspaces=wsp)
-        if conf_w is not None:
-            ds.confidence_truncate(h_buf, conf_w, drafts, B, k, w_conf_b, w_conf_tau,
-                                   draft_len=dlen_o, stream=s)
-        if ev is not None:
-            ev[3].record(s)
-        if target_ready is not None:
-            s.wait_event(target_ready)  # the target logits were copied on a side stream
-        ds.verify(mode, st["target"], drafts, dlen_o if conf_w is not None else None,
-                  logits if mode == 1 else None, q_stats, seed=12345,
-                  request_id=None, step=i, accepted_len=acc_o, next_token=nxt_o,
-                  stream=s, workspaces=wsp)
-        if ev is not None:
-            ev[4].record(s)
+    def hist(i):
+        return acc_hist[i], nxt_hist[i], dlen_hist[i]
 
-    w_conf_b, w_conf_tau = 0.0, 0.5
     for i in range(W):
-        one_step(K + i, sets[i % len(sets)])
+        pipe.step(sets[i % nsets], stream, side, hist(K + i), K + i)
     torch.cuda.synchronize()
 
-    # One CUDA graph per input set: a replay re-runs every kernel of the step on that
-    # set (nothing is cached); graphs remove the per-step host launch cost.
+    # One CUDA graph per input set (a replay re-runs every kernel of the step on that
+    # set; nothing is cached); graphs remove the per-step host launch cost.
     graphs, graph_error, launches_per_step = None, None, None
+    staged, stage_src = None, None
+    ev_ok = timing_events_supported(torch)
     if not args.no_graph:
         try:
             cap = torch.cuda.Stream(device)
+            cap_side = torch.cuda.Stream(device)
             cap.wait_stream(stream)
-            ghist = (torch.zeros((B,), dtype=torch.int32, device=device),
-                     torch.zeros((B,), dtype=torch.int32, device=device),
-                     torch.zeros((B,), dtype=torch.int32, device=device))
+            ghist = tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
             graphs = []
-            for si, st in enumerate(sets):
+            for st in sets:
                 g = torch.cuda.CUDAGraph()
                 n0 = ds.launch_count()
                 with torch.cuda.graph(g, stream=cap):
-                    one_step(si, st, s=cap, hist=ghist)
+                    pipe.step(st, cap, cap_side, ghist, 0)
                 launches_per_step = ds.launch_count() - n0
                 graphs.append(g)
+            if ev_ok:
+                # the same steps with timing events at the stage boundaries (event-record
+                # nodes), for the per-stage times of graph replays
+                staged = []
+                for st in sets:
+                    g = torch.cuda.CUDAGraph()
+                    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+                    sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                    with torch.cuda.graph(g, stream=cap):
+                        pipe.step(st, cap, cap_side, ghist, 0, ev=ev, side_ev=sev if pipe.split else None)
+                    staged.append((g, ev, sev))
             stream.wait_stream(cap)
             for g in graphs:      # one untimed replay each
                 g.replay()
             torch.cuda.synchronize()
         except Exception as exc:  # noqa: BLE001 - fall back to un-captured timing
-            graphs, graph_error = None, str(exc).splitlines()[0][:200]
+            graphs, staged, graph_error = None, None, str(exc).splitlines()[0][:200]
             torch.cuda.synchronize()
 
     def timed(run_steps):
@@ -487,52 +593,79 @@ def run_ours(args, rank, local_rank, world):
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        n0 = ds.launch_count()
         t0.record(stream)
         run_steps()
         t1.record(stream)
-        n = ds.launch_count() - n0
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        return max_over_ranks(t0.elapsed_time(t1), world, device), n
+        return max_over_ranks(t0.elapsed_time(t1), world, device)
 
     def run_graphs():
         for i in range(K):
-            graphs[i % len(graphs)].replay()
+            graphs[i % nsets].replay()
 
     def run_plain():
         for i in range(K):
-            one_step(i, sets[i % len(sets)])
+            pipe.step(sets[i % nsets], stream, side, hist(i), i)
 
-    def run_staged():
-        for i in range(K):
-            one_step(i, sets[i % len(sets)], stage_ev[i])
-
+    # the headline: K-step timed loops repeated until --min-time has elapsed
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.1)
-    if graphs is not None:
-        max_ms, _ = timed(run_graphs)
-        launches = launches_per_step * K
-    else:
-        max_ms, launches = timed(run_plain)
+    rep_ms = []
+    t_start = time.perf_counter()
+    while True:
+        n0 = ds.launch_count()
+        rep_ms.append(timed(run_graphs if graphs is not None else run_plain))
+        launches = launches_per_step * K if graphs is not None else ds.launch_count() - n0
+        done = time.perf_counter() - t_start >= args.min_time and len(rep_ms) >= 3
+        if world > 1:
+            done = max_over_ranks(1.0 if done else 0.0, world, device) > 0.5
+        if done:
+            break
     clk = clocks.stop()
-    plain_ms, plain_launches = timed(run_plain)
-    if graphs is None:
-        launches = plain_launches
-    # per-stage CUDA events on the launching stream (their host cost makes this loop
-    # slower than the others; it is used for the per-kernel times only)
-    staged_ms, _ = timed(run_staged)
-    stage_names = (["fc_lm_head", "(none)", "greedy_sample", "verify"] if fused
-                   else ["fc_project", "lm_head", "greedy_sample", "verify"])
-    stage_ms = {nm: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in stage_ev)
-                for j, nm in enumerate(stage_names)}
-    stage_ms.pop("(none)", None)
-    lm_ms = stage_ms["fc_lm_head"] if fused else stage_ms["lm_head"]
+    max_ms = statistics.median(rep_ms)
+    plain_ms = timed(run_plain)
+
+    # per-stage times: replays of the graphs with timing events (passes over all input
+    # sets, back to back, read after each pass); else the un-captured loop with events
+    stage_names = ["fc_lm_head", "(none)", "greedy_sample", "verify"] if pipe.fused \
+        else ["fc_project", "lm_head", "greedy_sample", "verify"]
+    samples = {nm: [] for nm in stage_names}
+    samples["target_stats"] = []
+    samples["step"] = []
+    if staged is not None:
+        stage_src = "CUDA-graph replays (event-record nodes at the stage boundaries)"
+        t_s = time.perf_counter()
+        while len(samples["step"]) < 200 or time.perf_counter() - t_s < 0.3:
+            for g, _, _ in staged:
+                g.replay()
+            torch.cuda.synchronize()
+            for _, ev, sev in staged:
+                for j, nm in enumerate(stage_names):
+                    samples[nm].append(ev[j].elapsed_time(ev[j + 1]))
+                samples["step"].append(ev[0].elapsed_time(ev[4]))
+                if pipe.split:
+                    samples["target_stats"].append(sev[0].elapsed_time(sev[1]))
+            if time.perf_counter() - t_s > 5.0:
+                break
+    else:
+        stage_src = "un-captured loop with CUDA events (host launch cost included)"
+        for i in range(K):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            sev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            pipe.step(sets[i % nsets], stream, side, hist(i), i, ev=ev, side_ev=sev if pipe.split else None)
+            torch.cuda.synchronize()
+            for j, nm in enumerate(stage_names):
+                samples[nm].append(ev[j].elapsed_time(ev[j + 1]))
+            samples["step"].append(ev[0].elapsed_time(ev[4]))
+            if pipe.split:
+                samples["target_stats"].append(sev[0].elapsed_time(sev[1]))
+    stage_ms = {nm: statistics.median(v) for nm, v in samples.items() if v and nm != "(none)"}
+    lm_ms = stage_ms["fc_lm_head"] if pipe.fused else stage_ms["lm_head"]
 
     # ---------------------------------------------------------------- end to end (host buffers)
-    e2e = None
     Ke = min(args.e2e_steps, K)
     st0 = sets[0]
     pin_taps = torch.empty((T, M, H), dtype=torch.bfloat16).pin_memory()
@@ -549,14 +682,16 @@ def run_ours(args, rank, local_rank, world):
     e2e_set = {"taps": [dev_taps[j] for j in range(T)], "prev": dev_prev, "target": dev_target}
     h2d = pin_taps.numel() * 2 + pin_prev.numel() * 4 + pin_target.numel() * 4
     d2h = (2 * B + B * k) * 4
-    # Only verify reads the target logits: their copy runs on a side stream, under the
-    # readout, and verify waits for it (the taps and prev tokens go first, in order).
+    # The target logits go to the device on a side stream and their row statistics run
+    # there too, under the readout; verify waits for them.
     copy_stream = torch.cuda.Stream(device)
     target_ready = torch.cuda.Event()
 
     def copy_target():
-        with torch.cuda.stream(copy_stream):  # the previous step's verify is done
+        with torch.cuda.stream(copy_stream):  # the previous step's verify is done (host sync)
             dev_target.copy_(pin_target, non_blocking=True)
+            if pipe.split:
+                pipe.target_stats(dev_target, copy_stream)
             target_ready.record(copy_stream)
     for rep in range(2):
         if world > 1:
@@ -565,12 +700,13 @@ def run_ours(args, rank, local_rank, world):
         n = 3 if rep == 0 else Ke
         t0 = time.perf_counter()
         for i in range(n):
+            copy_target()
             dev_taps.copy_(pin_taps, non_blocking=True)
             dev_prev.copy_(pin_prev, non_blocking=True)
-            one_step(i, e2e_set, side_copy=copy_target, target_ready=target_ready)
+            pipe.step(e2e_set, stream, side, hist(i), i, target_ready=target_ready)
             out_acc.copy_(acc_hist[i], non_blocking=True)
             out_nxt.copy_(nxt_hist[i], non_blocking=True)
-            out_drafts.copy_(drafts, non_blocking=True)
+            out_drafts.copy_(pipe.drafts, non_blocking=True)
             stream.synchronize()  # the host reads this step's result
         wall = time.perf_counter() - t0
     e2e = {"value": whole_job_rate(Ke, world, max_over_ranks(wall, world, device)), "unit": "steps/s",
@@ -578,60 +714,65 @@ def run_ours(args, rank, local_rank, world):
 
     # ---------------------------------------------------------------- acceptance statistics
     acc = acc_hist[:K].cpu().numpy()
-    if conf_w is not None:
-        drafted = float(dlen_hist[:K].cpu().numpy().sum()) / K
-    else:
-        drafted = float(B * k)
+    drafted = float(dlen_hist[:K].cpu().numpy().sum()) / K if cfg["conf"] else float(B * k)
     mean_acc_len = float(acc.mean()) + 1.0   # accepted drafts + the bonus/corrected token
     per_pos = [float((acc > j).mean()) for j in range(k)]
 
     steps_per_s = whole_job_rate(K, world, max_ms / 1000.0)
     peak_gbs, peak_tf, peak_src = measured_peaks()
     sb = step_bytes(cfg, mode)
-    lm_bytes = sb["fc"] + sb["lm_head"] if fused else sb["lm_head"]
+    lm_bytes = sb["fc"] + sb["lm_head"] if pipe.fused else sb["lm_head"]
     achieved = lm_bytes / (lm_ms / 1000.0) / 1e9
     t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
-    # readout (fc + LM head + chain) and verify against their own rooflines
     t_readout = max((sb["fc"] + sb["lm_head"] + sb["chain"]) / (peak_gbs * 1e9),
                     step_flops(cfg) / (peak_tf * 1e12))
     t_verify = sb["verify"] / (peak_gbs * 1e9)
-    readout_ms = ((stage_ms["fc_lm_head"] if fused else stage_ms["fc_project"] + stage_ms["lm_head"])
+    t_tstats = B * (k + 1) * V * 4 / (peak_gbs * 1e9)
+    readout_ms = ((stage_ms["fc_lm_head"] if pipe.fused else stage_ms["fc_project"] + stage_ms["lm_head"])
                   + stage_ms["greedy_sample"])
-
+    traffic_file = "gemm_tcgen05_fc_lm_head" if pipe.fused else "gemm_tcgen05_lm_head"
+    traffic = profiled_traffic(name, traffic_file)
+    step_roof = {"bytes": sb["total"], "flops": step_flops(cfg), "t_roofline_ms": t_roof * 1000.0,
+                 "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src,
+                 "readout_frac": t_readout * 1000.0 / readout_ms,
+                 "verify_frac": t_verify * 1000.0 / stage_ms["verify"],
+                 "verify_frac_is": ("critical-path verify time: from the end of the drafting "
+                                    "kernels to the end of verify on the step's stream; the "
+                                    "target-row statistics run beside the GEMMs"
+                                    if pipe.split else "the whole verify on the step's stream"),
+                 "stage_times": stage_src}
+    if pipe.split and "target_stats" in stage_ms:
+        step_roof["target_stats_frac"] = t_tstats * 1000.0 / stage_ms["target_stats"]
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": max_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if pipe.fp8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": args.config, "B": B, "k": k, "H": H, "taps": T, "V": V, "r": r,
-                   "verify": "probabilistic" if mode == 1 else "greedy", "q_stats_in": args.q_stats,
-                   "confidence_head": bool(conf_w is not None),
-                   "weights": "e4m3 codes + fp32 row scales (fc, LM head)" if fp8 else "bf16",
-                   "l2": "inputs larger than L2: %.2f GB of weights streamed per step"
-                         % ((sb["fc"] + sb["lm_head"]) / 1e9),
-                   "parallelism": "replicas%d" % world},
+        "config": config_of(name, cfg, mode, args, world, nsets, set_bytes, l2,
+                            weights_bytes=sb["fc"] + sb["lm_head"]),
         "drafted_tok_s": steps_per_s * drafted,
         "accepted_tok_s": steps_per_s * B * mean_acc_len,
         "mean_acceptance_length": mean_acc_len,
         "per_position_acceptance": per_pos,
         "roofline": {"bound": "hbm",
-                     "kernel": ("quantize_rows + gemm_tcgen05<fp8> (LM head stage)" if fp8
+                     "kernel": ("quantize_rows + gemm_tcgen05<fp8> (LM head stage)" if pipe.fp8
                                 else "gemm_tcgen05, two phases: fc then LM head (one launch)"
-                                if fused else "gemm_tcgen05 (LM head)"),
+                                if pipe.fused else "gemm_tcgen05 (LM head)"),
                      "achieved": achieved,
                      "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
-                     "traffic": profiled_traffic(args.config, "gemm_tcgen05_fc_lm_head" if fused
-                                                 else "gemm_tcgen05_lm_head"),
+                     "traffic": traffic,
+                     "traffic_source": ("profiled: dram__bytes_read.sum + dram__bytes_write.sum "
+                                        "per launch from profiles/%s_%s.md (ncu capture of the same "
+                                        "kernel source), not measured in this run"
+                                        % (traffic_file, name)) if traffic is not None else None,
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
-        "step_roofline": {"bytes": sb["total"], "flops": step_flops(cfg),
-                          "t_roofline_ms": t_roof * 1000.0,
-                          "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src,
-                          "readout_frac": t_readout * 1000.0 / readout_ms,
-                          "verify_frac": t_verify * 1000.0 / stage_ms["verify"],
-                          "stage_times": "per-stage CUDA events of the staged loop"},
+        "step_roofline": step_roof,
         "graph": graphs is not None,
         "graph_error": graph_error,
+        "timed_reps": {"reps": len(rep_ms), "steps_per_rep": K, "median_ms": max_ms,
+                       "min_ms": min(rep_ms), "max_ms": max(rep_ms),
+                       "seconds": sum(rep_ms) / 1000.0},
         "uncaptured": {"value": whole_job_rate(K, world, plain_ms / 1000.0), "unit": "steps/s",
                        "ms_per_step": plain_ms / K},
         "stage_ms": stage_ms,
@@ -640,18 +781,59 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clk,
     }
 
-    # ---------------------------------------------------------------- CPU oracle baseline
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if with_cpu_baseline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as ora
+        hw = host_cache[(H, T, V, r)]
         st = sets[0]["host"]
-        host = {"taps": st["taps"], "fc_w": host_w["fc_w"], "lm_w": host_w["lm_w"],
-                "w1": host_w["w1"], "w2": host_w["w2"], "prev": st["prev"],
+        host = {"taps": st["taps"], "fc_w": hw["fc_w"], "lm_w": hw["lm_w"],
+                "w1": hw["w1"], "w2": hw["w2"], "prev": st["prev"],
                 "target": np.ascontiguousarray(sets[0]["target"].cpu().numpy())}
         add_host_fp8(ora, host, cfg)
         host["h"] = oracle_h(ora, host, cfg)
         sps, cores, desc, _ = cpu_oracle_baseline(host, cfg, mode, args.cpu_budget)
         line["cpu_baseline"] = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
+    del graphs, staged, sets, pipe
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def config_of(name, cfg, mode, args, world, nsets=None, set_bytes=None, l2=None, weights_bytes=None):
+    """The workload description shared by both arms' JSON lines."""
+    c = {"workload": name, "B": cfg["B"], "k": cfg["k"], "H": cfg["H"], "taps": cfg["T"],
+         "V": cfg["V"], "r": cfg["r"], "verify": "probabilistic" if mode == 1 else "greedy",
+         "confidence_head": bool(cfg["conf"]),
+         "weights": "e4m3 codes + fp32 row scales (fc, LM head)" if cfg.get("fp8") else "bf16",
+         "parallelism": "replicas%d" % world}
+    if nsets is not None:
+        c["q_stats_in"] = args.q_stats
+        c["verify_path"] = args.verify
+        c["l2"] = ("inputs larger than L2: %.2f GB of weights streamed per step; %d input sets of "
+                   "%.1f MB rotated (%.0f MB > 2x the %.0f MB L2)"
+                   % (weights_bytes / 1e9, nsets, set_bytes / 1e6, nsets * set_bytes / 1e6, l2 / 1e6))
+    return c
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    host_cache = {}
+    line = measure_workload(args, args.config, rank, local_rank, world, host_cache, True)
+    if args.config == "27b_b1" and not args.no_b16:
+        # the metric names batch 1 and batch 16: the 27B batch-16 workload (confidence
+        # head on) with the same steps, warm-up and timing rules
+        sub = measure_workload(args, "27b_b16", rank, local_rank, world, host_cache, False)
+        line["batch16"] = {kk: sub[kk] for kk in (
+            "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "drafted_tok_s",
+            "accepted_tok_s", "mean_acceptance_length", "per_position_acceptance", "roofline",
+            "step_roofline", "graph", "timed_reps", "uncaptured", "stage_ms", "gpu_launches",
+            "e2e", "clocks")}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -669,8 +851,8 @@ SWEEP_SIGMA = (0.5, 2.0)
 
 
 def run_sweep(args):
-    """27B shapes over B x k x r x sigma (84 cells), probabilistic verify.  Per cell:
-    3 input sets (taps, prev tokens, target = own draft logits + sigma * N(0, 1)), one
+    """27B shapes over B x k x r x sigma (84 cells), probabilistic verify, the same step
+    pipeline as the headline (--verify, --q-stats).  Per cell: 3 input sets (taps, prev tokens, target = own draft logits + sigma * N(0, 1)), one
     CUDA graph per set, W = 3 warm-up and --sweep-steps timed replays rotating the sets
     (1.8-2.2 GB of weights stream from HBM every step).  Prints one JSON line per cell:
     steps/s, drafted tok/s, acceptance and the step's roofline fraction."""
@@ -690,7 +872,6 @@ def run_sweep(args):
     fc_w, lm_w = d16(base["fc_w"]), d16(base["lm_w"])
     del base
     stream = torch.cuda.current_stream(device)
-    wsp = ds.Workspaces()
     nsets = 3
     for r in SWEEP_R:
         mk = syn.weights(8, 1, V, r, with_markov=True)
@@ -701,12 +882,12 @@ def run_sweep(args):
                 # unit-variance noise and taps per input set, shared by both sigmas
                 raw = [syn.step_inputs(replica_step_seed(si, 0), B, k, H, T, V, ("const", 1.0))
                        for si in range(nsets)]
-                M = B * k
-                h_buf = torch.empty((M, H), dtype=torch.bfloat16, device=device)
-                logits = torch.empty((B, k, V), dtype=torch.float32, device=device)
-                drafts = torch.empty((B, k), dtype=torch.int32, device=device)
-                acc_o = torch.zeros((B,), dtype=torch.int32, device=device)
-                nxt_o = torch.zeros((B,), dtype=torch.int32, device=device)
+                cell = dict(B=B, k=k, H=H, T=T, V=V, r=r, conf=False)
+                pipe = Pipeline(ds, torch, device, cell, 1,
+                                {"fc_w": fc_w, "lm_w": lm_w, "w1": w1, "w2": w2, "conf_w": None}, args)
+                hist = tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
+                acc_o = hist[0]
+                side = torch.cuda.Stream(device)
                 dev_sets = []
                 for st in raw:
                     taps = [d16(t) for t in st["taps"]]
@@ -722,25 +903,17 @@ def run_sweep(args):
                     for st in dev_sets:
                         st["target"] = (st["own"] + st["noise"] * sigma).contiguous()
 
-                    def one_step(st, s):
-                        ds.fc_project(st["taps"], fc_w, out=h_buf, stream=s, workspaces=wsp)
-                        ds.lm_head(h_buf, lm_w, out=logits.view(M, V), stream=s, workspaces=wsp)
-                        ds.greedy_sample(logits, w1, w2, st["prev"], draft_tokens=drafts,
-                                         want_q_stats=False, stream=s, workspaces=wsp)
-                        ds.verify(1, st["target"], drafts, None, logits, None, seed=0,
-                                  request_id=None, step=0, accepted_len=acc_o, next_token=nxt_o,
-                                  stream=s, workspaces=wsp)
-
                     for st in dev_sets:        # eager warm-up (workspaces, first launches)
-                        one_step(st, stream)
+                        pipe.step(st, stream, side, hist, 0)
                     torch.cuda.synchronize()
                     cap = torch.cuda.Stream(device)
+                    cap_side = torch.cuda.Stream(device)
                     cap.wait_stream(stream)
                     graphs = []
                     for st in dev_sets:
                         g = torch.cuda.CUDAGraph()
                         with torch.cuda.graph(g, stream=cap):
-                            one_step(st, cap)
+                            pipe.step(st, cap, cap_side, hist, 0)
                         graphs.append(g)
                     stream.wait_stream(cap)
                     for i in range(3):
@@ -775,7 +948,7 @@ def run_sweep(args):
                         "steps": args.sweep_steps, "warmup": 3, "input_sets": nsets,
                         "dtype": "bf16", "data": "synthetic"}), flush=True)
                     del graphs
-                del dev_sets, h_buf, logits
+                del dev_sets, pipe
                 torch.cuda.empty_cache()
         del w1, w2
     return 0

@@ -197,6 +197,42 @@ dspark_status_t dspark_confidence_truncate(const dspark_bf16_t *h, const dspark_
                                            int H, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Confidence head that also sees the Markov context, and cumulative
+ * truncation ([PR620] draft config fields enable_confidence_head,
+ * confidence_head_with_markov, markov_rank; AcceptRatePredictor,
+ * _truncate_by_confidence, DSPARK_ADAPTIVE_BLOCK).  The pages name
+ * confidence_head_with_markov without a formula; the reading implemented:
+ * one linear layer over the concatenation [h_i ; e_i], where e_i =
+ * w1[ctx_i, :] is the Markov embedding of the token position i is
+ * conditioned on (ctx_0 = prev_token[b], the bonus token; ctx_i = the draft
+ * of position i-1):
+ *   zc[b, i] = sum_c conf_w[c] h[b*k+i, c] + sum_t conf_w[H + t] w1[ctx_i, t]
+ *              + conf_b,            c[b, i] = sigmoid(zc[b, i])
+ * conf_w is [H + r] bf16 (16-byte aligned); w1 == NULL gives the plain head
+ * (conf_w [H], prev_token and V unused).  Truncation rule:
+ *   cumulative == 0: draft_len[b] = first i with c[b, i] < conf_tau (as
+ *     dspark_confidence_truncate);
+ *   cumulative != 0: draft_len[b] = first i with
+ *     prod_{j <= i} c[b, j] < conf_tau  (evaluated as the running sum of
+ *     log sigmoid(zc) against log conf_tau): the predicted probability that
+ *     the whole prefix up to i is accepted.
+ * conf_tau <= 0 keeps every position, conf_tau >= 1 keeps none.
+ * draft_tokens [B, k] int32 (in: the chain's drafts, which give the
+ * contexts; out: -1 from draft_len on), draft_len [B] int32, conf_out [B, k]
+ * fp32 or NULL.  status: a device int32 (or NULL) where a context token
+ * outside [0, V) is recorded as DSPARK_ERR_BAD_TOKEN (its Markov term is
+ * then left out).  One kernel; needs no workspace.
+ * ---------------------------------------------------------------------- */
+dspark_status_t dspark_confidence_truncate_markov(const dspark_bf16_t *h,
+                                                  const dspark_bf16_t *conf_w, float conf_b,
+                                                  float conf_tau, int cumulative,
+                                                  const dspark_bf16_t *w1, int r, int V,
+                                                  const int32_t *prev_token,
+                                                  int32_t *draft_tokens, int32_t *draft_len,
+                                                  float *conf_out, int B, int k, int H,
+                                                  int32_t *status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Whole drafter readout: LM head (as dspark_lm_head) + Markov greedy
  * drafting (as dspark_greedy_sample) + optional confidence truncation
  * ([PR620] AcceptRatePredictor "optional per-position acceptance-confidence
@@ -254,6 +290,10 @@ dspark_status_t dspark_draft_readout(const dspark_bf16_t *h, const dspark_bf16_t
  *   request_id [B] uint32 or NULL (= b),
  *   accepted_len [B] int32, next_token [B] int32 (outputs).
  * Mode 0 ignores draft_logits, q_stats, seed, request_id and step.
+ * Enqueues dspark_row_stats over the target rows 0..draft_len[b] (and over the
+ * draft-logit rows 0..draft_len[b]-1 when q_stats is NULL), then the decision
+ * kernel of dspark_verify_from_stats: two or three kernels.
+ * q_stats, when given, must be 8-byte aligned.
  * ---------------------------------------------------------------------- */
 size_t dspark_verify_workspace_size(int B, int k, int V);
 dspark_status_t dspark_verify(int mode, const float *target_logits,
@@ -262,6 +302,50 @@ dspark_status_t dspark_verify(int mode, const float *target_logits,
                               const uint32_t *request_id, uint32_t step,
                               int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
                               void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Softmax statistics and argmax of fp32 rows: the part of verify that needs
+ * only the logits of one distribution (p from the target rows, or q from the
+ * draft-logit rows).  For each row r of rows [nrows, V] (row-major):
+ *   ms_out[r]     = (max_v x[r, v], sum_v exp(x[r, v] - max))   fp32 pair
+ *   argmax_out[r] = smallest v with x[r, v] == max               int32
+ * (-0 == +0; NaN entries never win and add nothing; an all -inf row gives
+ * (-inf, 0) and argmax 0).  Either output may be NULL (not both); with
+ * ms_out == NULL only the argmax is reduced.  ms_out must be 8-byte aligned.
+ * 1 <= nrows <= 2^24, 1 <= V <= 2^26.  One kernel: every CTA reduces a
+ * 16384-entry slice of one row, the last CTA of a row merges the slices
+ * (sum in fp64, rounded once to fp32).
+ * Applied to the target logits [B, k+1, V] (nrows = B*(k+1)) this depends
+ * on nothing the drafter computes, so it may run as soon as the target
+ * logits exist, concurrently with drafting work on another stream.
+ * ---------------------------------------------------------------------- */
+size_t dspark_row_stats_workspace_size(int64_t nrows, int V);
+dspark_status_t dspark_row_stats(const float *rows, int64_t nrows, int V, float *ms_out,
+                                 int32_t *argmax_out, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Verify with the row statistics already computed: the same decisions and
+ * draws as dspark_verify, in ONE kernel.
+ *   target_ms [B, k+1, 2] fp32 and target_argmax [B, k+1] int32: the
+ *     dspark_row_stats outputs of target_logits (mode 0 needs target_argmax,
+ *     mode 1 target_ms; rows past draft_len[b] are never read);
+ *   q_stats [B, k, 2] fp32: required in mode 1 when draft_logits is given
+ *     (from dspark_greedy_sample, or dspark_row_stats of the draft logits);
+ * every other argument as for dspark_verify.  Mode 0: one warp per request
+ * compares the drafts with the target argmaxes.  Mode 1: every CTA of a
+ * request takes the request's accept/reject decisions (its drafted tokens,
+ * the target and draft logits at them, the row statistics), then reduces one
+ * 1024-entry slice of the Gumbel-max draw; the request's last CTA merges the
+ * draw.
+ * ---------------------------------------------------------------------- */
+size_t dspark_verify_from_stats_workspace_size(int B, int k, int V);
+dspark_status_t dspark_verify_from_stats(int mode, const float *target_logits,
+                                         const float *target_ms, const int32_t *target_argmax,
+                                         const int32_t *draft_tokens, const int32_t *draft_len,
+                                         const float *draft_logits, const float *q_stats,
+                                         uint64_t seed, const uint32_t *request_id, uint32_t step,
+                                         int32_t *accepted_len, int32_t *next_token, int B, int k,
+                                         int V, void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free verify.  No counterpart in the pages: a library
@@ -276,9 +360,10 @@ dspark_status_t dspark_verify(int mode, const float *target_logits,
  *
  * Scratch: one fixed array of DSPARK_VERIFY_NOALLOC_MAX_BYTES inside the
  * library's device image, held by every GPU that loads the library until the
- * process exits.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Each call first clears the part of the
+ * process exits.  Every call looks up the array's device address
+ * (cudaGetSymbolAddress) with the current device; the first lookup on a
+ * device may load the library's device code there, so make the first call on
+ * each device before any stream capture.  Each call first clears the part of the
  * array it uses (cudaMemsetAsync on `stream`), then enqueues the same kernels
  * as dspark_verify.  Nothing is allocated: no cudaMalloc, no cudaFree.
  * All calls share the one array, so calls whose GPU work overlaps (streams
@@ -287,6 +372,8 @@ dspark_status_t dspark_verify(int mode, const float *target_logits,
  * Limit: dspark_verify_workspace_size(B, k, V) must not exceed
  * DSPARK_VERIFY_NOALLOC_MAX_BYTES (4 MiB; e.g. B = 64, k = 16, V = 262144
  * fits), otherwise DSPARK_ERR_WORKSPACE is returned and nothing is enqueued.
+ * Arguments are checked as for dspark_verify before anything is enqueued: a
+ * rejected call queues no GPU work and leaves the array untouched.
  * Device-side errors are recorded in the array's status word, which the next
  * call clears; this variant does not report them.
  * ---------------------------------------------------------------------- */

@@ -11,6 +11,8 @@ Functions follow the pages' notation:
   greedy_sample   Markov-biased, semi-autoregressive argmax drafting (in place)
   draft_readout   lm_head + greedy_sample + optional confidence truncation
   verify          greedy exact match or probabilistic rejection sampling
+  row_stats       (max, sum exp) and argmax of fp32 rows (target or draft logits)
+  verify_from_stats  verify's decisions and draw from precomputed row statistics
 """
 import ctypes
 import os
@@ -19,8 +21,9 @@ import threading
 import torch
 
 __all__ = ["DSparkError", "lib", "fc_project", "lm_head", "greedy_sample", "confidence_truncate",
-           "draft_readout", "quantize_fp8", "fc_project_fp8", "lm_head_fp8", "fc_lm_head",
-           "verify", "workspace_status", "launch_count", "Workspaces", "library_path"]
+           "draft_readout", "confidence_truncate_markov", "quantize_fp8", "fc_project_fp8", "lm_head_fp8", "fc_lm_head",
+           "verify", "row_stats", "verify_from_stats", "workspace_status", "launch_count",
+           "Workspaces", "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libdspark.so")
@@ -77,6 +80,11 @@ def lib():
         L.dspark_confidence_truncate.restype = ctypes.c_int
         L.dspark_confidence_truncate.argtypes = [_vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp,
                                                  _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
+        L.dspark_confidence_truncate_markov.restype = ctypes.c_int
+        L.dspark_confidence_truncate_markov.argtypes = [_vp, _vp, ctypes.c_float, ctypes.c_float,
+                                                        ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int,
+                                                        _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                                        ctypes.c_int, _vp, _vp]
         L.dspark_draft_readout_workspace_size.restype = _sz
         L.dspark_draft_readout_workspace_size.argtypes = [ctypes.c_int] * 5
         L.dspark_draft_readout.restype = ctypes.c_int
@@ -89,6 +97,16 @@ def lib():
         L.dspark_verify.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, ctypes.c_uint64, _vp,
                                     ctypes.c_uint32, _vp, _vp, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _vp, _sz, _vp]
+        L.dspark_row_stats_workspace_size.restype = _sz
+        L.dspark_row_stats_workspace_size.argtypes = [_i64, ctypes.c_int]
+        L.dspark_row_stats.restype = ctypes.c_int
+        L.dspark_row_stats.argtypes = [_vp, _i64, ctypes.c_int, _vp, _vp, _vp, _sz, _vp]
+        L.dspark_verify_from_stats_workspace_size.restype = _sz
+        L.dspark_verify_from_stats_workspace_size.argtypes = [ctypes.c_int] * 3
+        L.dspark_verify_from_stats.restype = ctypes.c_int
+        L.dspark_verify_from_stats.argtypes = [ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                               ctypes.c_uint64, _vp, ctypes.c_uint32, _vp, _vp,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _sz, _vp]
         L.dspark_fc_lm_head_workspace_size.restype = _sz
         L.dspark_fc_lm_head_workspace_size.argtypes = [ctypes.c_int] * 4
         L.dspark_fc_lm_head.restype = ctypes.c_int
@@ -148,6 +166,14 @@ class Workspaces:
 
     def __init__(self):
         self._bufs = {}
+
+    def buffer(self, kind, device):
+        """The workspace tensor of a call kind on a device (None before its first call);
+        pass it to workspace_status() to read the device-side status word."""
+        idx = torch.device(device).index
+        if idx is None:
+            idx = torch.cuda.current_device()
+        return self._bufs.get((kind, idx))
 
     def get(self, kind, device, nbytes):
         key = (kind, torch.device(device).index)
@@ -300,6 +326,37 @@ def confidence_truncate(h, conf_w, draft_tokens, B, k, conf_b=0.0, conf_tau=0.5,
     return draft_len, conf_out
 
 
+def confidence_truncate_markov(h, conf_w, draft_tokens, B, k, conf_b=0.0, conf_tau=0.5,
+                               cumulative=False, w1=None, prev_token=None, draft_len=None,
+                               conf_out=None, status=None, stream=None):
+    """Confidence head over [h ; markov_w1[context]] (w1 given: conf_w has H + r entries)
+    or over h alone, with the per-position or the cumulative (product of confidences)
+    truncation rule.  Returns (draft_len int32 [B], conf fp32 [B, k] or None)."""
+    M, H = h.shape
+    if M != B * k:
+        raise ValueError("h must have B*k rows")
+    _need(h, "h", torch.bfloat16)
+    r, V = 0, 0
+    if w1 is not None:
+        V, r = w1.shape
+        _need(w1, "w1", torch.bfloat16, (V, r))
+        _need(prev_token, "prev_token", torch.int32, (B,))
+    _need(conf_w, "conf_w", torch.bfloat16, (H + r,))
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    if draft_len is None:
+        draft_len = torch.empty((B,), dtype=torch.int32, device=h.device)
+    _need(draft_len, "draft_len", torch.int32, (B,))
+    if conf_out is not None:
+        _need(conf_out, "conf_out", torch.float32, (B, k))
+    if status is not None:
+        _need(status, "status", torch.int32, (1,))
+    _check(lib().dspark_confidence_truncate_markov(
+        _ptr(h), _ptr(conf_w), float(conf_b), float(conf_tau), int(bool(cumulative)), _ptr(w1), r, V,
+        _ptr(prev_token), _ptr(draft_tokens), _ptr(draft_len), _ptr(conf_out), B, k, H,
+        _ptr(status), _stream(stream, h.device)), "dspark_confidence_truncate_markov")
+    return draft_len, conf_out
+
+
 def draft_readout(h, lm_w, w1, w2, prev_token, B, k, conf_w=None, conf_b=0.0, conf_tau=0.5,
                   out=None, stream=None, workspaces=None):
     """LM head + Markov greedy drafting + optional confidence truncation.
@@ -386,6 +443,77 @@ def verify(mode, target_logits, draft_tokens, draft_len=None, draft_logits=None,
                            _ptr(request_id), int(step) & 0xFFFFFFFF, _ptr(accepted_len),
                            _ptr(next_token), B, k, V, _ptr(ws), ws.numel(), _stream(stream, dev)),
            "dspark_verify")
+    return accepted_len, next_token
+
+
+def _request_ids(request_id, B):
+    if request_id is not None:
+        if request_id.dtype not in (torch.int32, torch.uint32):
+            raise TypeError("request_id must be int32/uint32")
+        if not request_id.is_cuda or not request_id.is_contiguous() or tuple(request_id.shape) != (B,):
+            raise ValueError("request_id must be a contiguous CUDA [B] tensor")
+
+
+def row_stats(rows, ms=None, argmax=None, want_ms=True, want_argmax=True, stream=None,
+              workspaces=None):
+    """Softmax statistics and argmax of every row of an fp32 tensor [..., V]:
+    returns (ms fp32 [..., 2] = (max, sum exp(x - max)) or None, argmax int32 [...] or None)."""
+    _need(rows, "rows", torch.float32)
+    V = rows.shape[-1]
+    lead = tuple(rows.shape[:-1])
+    n = rows.numel() // V
+    dev = rows.device
+    if want_ms and ms is None:
+        ms = torch.empty(lead + (2,), dtype=torch.float32, device=dev)
+    if want_argmax and argmax is None:
+        argmax = torch.empty(lead, dtype=torch.int32, device=dev)
+    if ms is not None:
+        _need(ms, "ms", torch.float32, lead + (2,))
+    if argmax is not None:
+        _need(argmax, "argmax", torch.int32, lead)
+    L = lib()
+    ws = (workspaces or _default_ws).get("rows", dev, L.dspark_row_stats_workspace_size(n, V))
+    _check(L.dspark_row_stats(_ptr(rows), n, V, _ptr(ms), _ptr(argmax), _ptr(ws), ws.numel(),
+                              _stream(stream, dev)), "dspark_row_stats")
+    return ms, argmax
+
+
+def verify_from_stats(mode, target_logits, target_ms, target_argmax, draft_tokens, draft_len=None,
+                      draft_logits=None, q_stats=None, seed=0, request_id=None, step=0,
+                      accepted_len=None, next_token=None, stream=None, workspaces=None):
+    """verify() with the target rows' statistics already computed (row_stats of the target
+    logits): one kernel.  Returns (accepted_len int32 [B], next_token int32 [B])."""
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    _need(target_logits, "target_logits", torch.float32)
+    if target_ms is not None:
+        _need(target_ms, "target_ms", torch.float32, (B, k1, 2))
+    if target_argmax is not None:
+        _need(target_argmax, "target_argmax", torch.int32, (B, k1))
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    if draft_len is not None:
+        _need(draft_len, "draft_len", torch.int32, (B,))
+    if draft_logits is not None:
+        _need(draft_logits, "draft_logits", torch.float32, (B, k, V))
+    if q_stats is not None:
+        _need(q_stats, "q_stats", torch.float32, (B, k, 2))
+    _request_ids(request_id, B)
+    if accepted_len is None:
+        accepted_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(accepted_len, "accepted_len", torch.int32, (B,))
+    _need(next_token, "next_token", torch.int32, (B,))
+    L = lib()
+    ws = (workspaces or _default_ws).get("verify_fs", dev,
+                                         L.dspark_verify_from_stats_workspace_size(B, k, V))
+    _check(L.dspark_verify_from_stats(int(mode), _ptr(target_logits), _ptr(target_ms),
+                                      _ptr(target_argmax), _ptr(draft_tokens), _ptr(draft_len),
+                                      _ptr(draft_logits), _ptr(q_stats), int(seed) & (2 ** 64 - 1),
+                                      _ptr(request_id), int(step) & 0xFFFFFFFF, _ptr(accepted_len),
+                                      _ptr(next_token), B, k, V, _ptr(ws), ws.numel(),
+                                      _stream(stream, dev)), "dspark_verify_from_stats")
     return accepted_len, next_token
 
 

@@ -61,13 +61,14 @@ using namespace dspark;
 
 namespace {
 
-constexpr size_t kHeader = kWsAlign;  // status word + padding at the start of every workspace
 constexpr int kMaxM = 1 << 20;
-constexpr int kMaxV = 1 << 26;
+
+constexpr size_t kHeader = kWsAlign;  // status word + padding at the start of every workspace
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool aligned2(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 int *status_word(void *ws) { return reinterpret_cast<int *>(ws); }
 
@@ -106,6 +107,33 @@ dspark_status_t check_chain_args(const void *logits, const void *w1, const void 
   if (q_stats && !aligned4(q_stats)) return DSPARK_ERR_MISALIGNED;
   return DSPARK_OK;
 }
+
+}  // namespace
+
+namespace dspark {
+
+dspark_status_t verify_check_args(int mode, const float *target_logits,
+                                  const int32_t *draft_tokens, const int32_t *draft_len,
+                                  const float *draft_logits, const float *q_stats,
+                                  const uint32_t *request_id, const int32_t *accepted_len,
+                                  const int32_t *next_token, int B, int k, int V) {
+  if (mode != 0 && mode != 1) return DSPARK_ERR_INVALID_ARG;
+  if (!target_logits || !draft_tokens || !accepted_len || !next_token) return DSPARK_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (k > kMaxK || V > kMaxV || B > (1 << 20)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (mode == 1 && draft_logits && q_stats && !aligned8(q_stats)) return DSPARK_ERR_MISALIGNED;
+  if (!aligned4(target_logits) || !aligned4(draft_tokens) || !aligned4(accepted_len) ||
+      !aligned4(next_token))
+    return DSPARK_ERR_MISALIGNED;
+  if ((draft_len && !aligned4(draft_len)) || (draft_logits && !aligned4(draft_logits)) ||
+      (request_id && !aligned4(request_id)))
+    return DSPARK_ERR_MISALIGNED;
+  return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+namespace {
 
 size_t chain_ws_bytes(int B, int k, int V) { return kHeader + chain_workspace_size(B, k, V); }
 
@@ -353,8 +381,32 @@ dspark_status_t dspark_confidence_truncate(const dspark_bf16_t *h, const dspark_
     return DSPARK_ERR_MISALIGNED;
   dspark_status_t st = check_device();
   if (st != DSPARK_OK) return st;
-  return confidence_launch(h, conf_w, conf_b, conf_tau, draft_tokens, draft_len, conf_out, B, k,
-                           H, as_stream(stream));
+  return confidence_launch(h, conf_w, conf_b, conf_tau, 0, nullptr, 0, 0, nullptr, draft_tokens,
+                           draft_len, conf_out, B, k, H, nullptr, as_stream(stream));
+}
+
+// ---------------------------------------------------------------- confidence with the Markov context
+dspark_status_t dspark_confidence_truncate_markov(const dspark_bf16_t *h, const dspark_bf16_t *conf_w,
+                                                  float conf_b, float conf_tau, int cumulative,
+                                                  const dspark_bf16_t *w1, int r, int V,
+                                                  const int32_t *prev_token, int32_t *draft_tokens,
+                                                  int32_t *draft_len, float *conf_out, int B, int k,
+                                                  int H, int32_t *status, void *stream) {
+  if (!h || !conf_w || !draft_tokens || !draft_len) return DSPARK_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || H < 1) return DSPARK_ERR_INVALID_ARG;
+  if (w1 && (!prev_token || V < 1)) return DSPARK_ERR_INVALID_ARG;
+  if (k > kMaxK || B > (1 << 20) || H % 64 != 0 || V > kMaxV) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (w1 && (r < 1 || r > kMaxRank)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (std::isnan(conf_tau) || std::isnan(conf_b)) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(conf_w) || !aligned4(draft_tokens) || !aligned4(draft_len) ||
+      (conf_out && !aligned4(conf_out)) || (w1 && !aligned2(w1)) ||
+      (prev_token && !aligned4(prev_token)) || (status && !aligned4(status)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return confidence_launch(h, conf_w, conf_b, conf_tau, cumulative, w1, w1 ? r : 0, V,
+                           prev_token, draft_tokens, draft_len, conf_out, B, k, H, status,
+                           as_stream(stream));
 }
 
 // ---------------------------------------------------------------- whole readout
@@ -404,8 +456,8 @@ dspark_status_t dspark_draft_readout(const dspark_bf16_t *h, const dspark_bf16_t
                     status_word(ws), s);
   if (st != DSPARK_OK) return st;
   if (conf_w)
-    st = confidence_launch(h, conf_w, conf_b, conf_tau, draft_tokens, draft_len, conf_out, B, k,
-                           H, s);
+    st = confidence_launch(h, conf_w, conf_b, conf_tau, 0, nullptr, 0, 0, nullptr, draft_tokens,
+                           draft_len, conf_out, B, k, H, status_word(ws), s);
   return st;
 }
 
@@ -420,19 +472,11 @@ dspark_status_t dspark_verify(int mode, const float *target_logits, const int32_
                               const float *q_stats, uint64_t seed, const uint32_t *request_id,
                               uint32_t step, int32_t *accepted_len, int32_t *next_token, int B,
                               int k, int V, void *ws, size_t ws_bytes, void *stream) {
-  if (mode != 0 && mode != 1) return DSPARK_ERR_INVALID_ARG;
-  if (!target_logits || !draft_tokens || !accepted_len || !next_token) return DSPARK_ERR_INVALID_ARG;
-  if (B < 1 || k < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
-  if (k > kMaxK || V > kMaxV || B > (1 << 20)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
-  if (mode == 1 && draft_logits && q_stats && !aligned4(q_stats)) return DSPARK_ERR_MISALIGNED;
-  if (!aligned4(target_logits) || !aligned4(draft_tokens) || !aligned4(accepted_len) ||
-      !aligned4(next_token))
-    return DSPARK_ERR_MISALIGNED;
-  if ((draft_len && !aligned4(draft_len)) || (draft_logits && !aligned4(draft_logits)) ||
-      (request_id && !aligned4(request_id)))
-    return DSPARK_ERR_MISALIGNED;
-  dspark_status_t st = check_ws(ws, ws_bytes, dspark_verify_workspace_size(B, k, V));
+  dspark_status_t st = verify_check_args(mode, target_logits, draft_tokens, draft_len,
+                                         draft_logits, q_stats, request_id, accepted_len,
+                                         next_token, B, k, V);
   if (st != DSPARK_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, dspark_verify_workspace_size(B, k, V))) != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
   st = prepare_workspace(ws, layout_signature({5, B, k, V}), {{0, verify_counter_bytes(B, k, V)}},
                          as_stream(stream));
@@ -440,6 +484,62 @@ dspark_status_t dspark_verify(int mode, const float *target_logits, const int32_
   return verify_launch(mode, target_logits, draft_tokens, draft_len, draft_logits, q_stats, seed,
                        request_id, step, accepted_len, next_token, B, k, V, ws, status_word(ws),
                        as_stream(stream));
+}
+
+// ---------------------------------------------------------------- row statistics
+size_t dspark_row_stats_workspace_size(int64_t nrows, int V) {
+  if (nrows < 1 || nrows > (1LL << 24) || V < 1 || V > kMaxV) return 0;
+  return row_stats_workspace_size(nrows, V);
+}
+
+dspark_status_t dspark_row_stats(const float *rows, int64_t nrows, int V, float *ms_out,
+                                 int32_t *argmax_out, void *ws, size_t ws_bytes, void *stream) {
+  if (!rows || (!ms_out && !argmax_out)) return DSPARK_ERR_INVALID_ARG;
+  if (nrows < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (nrows > (1LL << 24) || V > kMaxV) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned4(rows) || (ms_out && !aligned8(ms_out)) || (argmax_out && !aligned4(argmax_out)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_row_stats_workspace_size(nrows, V));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({9, nrows, V}), {{0, row_stats_counter_bytes(nrows, V)}},
+                         as_stream(stream));
+  if (st != DSPARK_OK) return st;
+  return row_stats_launch(rows, nrows, V, ms_out, argmax_out, ws, status_word(ws), as_stream(stream));
+}
+
+// ---------------------------------------------------------------- verify from row statistics
+size_t dspark_verify_from_stats_workspace_size(int B, int k, int V) {
+  if (B < 1 || k < 1 || k > kMaxK || V < 1) return 0;
+  return verify_from_stats_workspace_size(B, V);
+}
+
+dspark_status_t dspark_verify_from_stats(int mode, const float *target_logits,
+                                         const float *target_ms, const int32_t *target_argmax,
+                                         const int32_t *draft_tokens, const int32_t *draft_len,
+                                         const float *draft_logits, const float *q_stats,
+                                         uint64_t seed, const uint32_t *request_id, uint32_t step,
+                                         int32_t *accepted_len, int32_t *next_token, int B, int k,
+                                         int V, void *ws, size_t ws_bytes, void *stream) {
+  dspark_status_t st = verify_check_args(mode, target_logits, draft_tokens, draft_len,
+                                         draft_logits, q_stats, request_id, accepted_len,
+                                         next_token, B, k, V);
+  if (st != DSPARK_OK) return st;
+  if (mode == 0 && !target_argmax) return DSPARK_ERR_INVALID_ARG;
+  if (mode == 1 && (!target_ms || (draft_logits && !q_stats))) return DSPARK_ERR_INVALID_ARG;
+  if ((target_ms && !aligned8(target_ms)) || (target_argmax && !aligned4(target_argmax)) ||
+      (mode == 1 && q_stats && !aligned8(q_stats)))
+    return DSPARK_ERR_MISALIGNED;
+  if ((st = check_ws(ws, ws_bytes, dspark_verify_from_stats_workspace_size(B, k, V))) != DSPARK_OK)
+    return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({10, B, k, V}),
+                         {{0, verify_from_stats_counter_bytes(B, V)}}, as_stream(stream));
+  if (st != DSPARK_OK) return st;
+  return verify_from_stats_launch(mode, target_logits, target_ms, target_argmax, draft_tokens,
+                                  draft_len, draft_logits, q_stats, seed, request_id, step,
+                                  accepted_len, next_token, B, k, V, ws, status_word(ws),
+                                  as_stream(stream));
 }
 
 // ---------------------------------------------------------------- FP8 (E4M3) drafter weights

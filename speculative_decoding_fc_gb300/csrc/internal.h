@@ -14,6 +14,7 @@ constexpr int kMaxTaps = 8;
 constexpr int kMaxK = 16;
 constexpr int kMaxRank = 256;
 constexpr int kMaxGemmCtas = 160;  // upper bound of the persistent GEMM grid
+constexpr int kMaxV = 1 << 26;     // vocabulary cap (argmax words keep 26 index bits)
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -60,9 +61,13 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
                              const int32_t *prev_token, int32_t *draft_tokens, float *q_stats,
                              int32_t *draft_len_fill, int B, int k, int V, void *ws,
                              int *status, cudaStream_t stream);
+// Confidence head + truncation: over h alone (w1 == null) or over [h ; markov_w1[ctx]]
+// (conf_w then has H + r entries); per-position or cumulative rule.
 dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, float conf_b,
-                                  float conf_tau, int32_t *draft_tokens, int32_t *draft_len,
-                                  float *conf_out, int B, int k, int H, cudaStream_t stream);
+                                  float conf_tau, int cumulative, const uint16_t *w1, int r, int V,
+                                  const int32_t *prev_token, int32_t *draft_tokens,
+                                  int32_t *draft_len, float *conf_out, int B, int k, int H,
+                                  int *status, cudaStream_t stream);
 
 // ------------------------------------------------------------------ FP8 quantisation
 // codes[r, :] = E4M3(x[r, :] / scale[r]), scale = amax(row) / 448 (1 if zero); the
@@ -73,6 +78,30 @@ dspark_status_t quantize_fp8_launch(const uint16_t *const *segs, int nseg, int64
                                     cudaStream_t stream);
 
 // ------------------------------------------------------------------ verify
+// Row statistics of nrows fp32 rows of V entries: ms[r] = (max, sum exp(x - max)),
+// argmax[r] = lowest index of the max (either output may be null; without ms only
+// the argmax is reduced).
+size_t row_stats_workspace_size(long long nrows, int V);
+size_t row_stats_counter_bytes(long long nrows, int V);
+dspark_status_t row_stats_launch(const float *rows, long long nrows, int V, float *ms,
+                                 int32_t *argmax, void *ws, int *status, cudaStream_t stream);
+// Decisions (and the draw) of verify from precomputed target-row statistics.
+size_t verify_from_stats_workspace_size(int B, int V);
+size_t verify_from_stats_counter_bytes(int B, int V);
+dspark_status_t verify_from_stats_launch(int mode, const float *target, const float *t_ms,
+                                         const int32_t *t_arg, const int32_t *drafts,
+                                         const int32_t *draft_len, const float *zlog,
+                                         const float *q_ms, uint64_t seed,
+                                         const uint32_t *request_id, uint32_t step,
+                                         int32_t *accepted_len, int32_t *next_token, int B, int k,
+                                         int V, void *ws, int *status, cudaStream_t stream);
+// Host-side argument checks shared by every verify entry point (nothing enqueued).
+dspark_status_t verify_check_args(int mode, const float *target_logits,
+                                  const int32_t *draft_tokens, const int32_t *draft_len,
+                                  const float *draft_logits, const float *q_stats,
+                                  const uint32_t *request_id, const int32_t *accepted_len,
+                                  const int32_t *next_token, int B, int k, int V);
+// The whole verify (row statistics, then decisions) in one workspace.
 size_t verify_workspace_size(int B, int k, int V);
 size_t verify_counter_bytes(int B, int k, int V);
 dspark_status_t verify_launch(int mode, const float *target, const int32_t *drafts,

@@ -255,6 +255,7 @@ struct ChainPArgs {
   int r, B, k, V;
   int rows_per_cta;         // vocabulary rows owned by one CTA
   int w2_smem_bytes;        // shared memory reserved for the markov_w2 slice (0: read via L2)
+  long long wait_cycles;    // budget of one wait for the other CTAs' words (clock64 cycles)
 };
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -651,7 +652,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 #pragma unroll
           for (int j = 0; j < kPRows; ++j)
             if (valid[j] && g < gb && mx[g] != -INFINITY && zv[j] == zv[j] && zv[j] != -INFINITY)
-              sm[g] += expf(zv[j] - mx[g]);
+              sm[g] += __expf(zv[j] - mx[g]);  // x <= 0: relative error ~2^-21
         }
       }
       // lg_s is consumed: the next group's logits (this position's, else the next's)
@@ -805,7 +806,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
           if (all_done) break;
           int give_up = 0;
           if (lane == 0)
-            give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > kBarrierCycles) ? 1 : 0;
+            give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > a.wait_cycles) ? 1 : 0;
           if (__shfl_sync(0xffffffffu, give_up, 0)) {
             if (lane == 0 && atomicExch(a.abort_flag, 1) == 0)
               record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
@@ -913,29 +914,46 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   }
 }
 
-// c[b, i] = sigmoid(w . h[b*k+i] + bias); draft_len[b] = first i whose logit
-// falls below thr = logit(tau); later drafts are replaced by -1.  One CTA per
-// request; wpp warps per block position (all k dot products at once, each split
-// over wpp warps, the warps' sums added in warp order).
+// c[b, i] = sigmoid(zc[b, i]), zc = w . h[b*k+i] (+ w_m . markov_w1[ctx_i] when the head
+// sees the Markov context) + bias; draft_len[b] = first i that fails the truncation rule
+// (per position: zc < thr = logit(tau); cumulative: the running sum of log sigmoid(zc)
+// falls below log tau); later drafts are replaced by -1.  One CTA per request; wpp warps
+// per block position (all k dot products at once, each split over wpp warps, the warps'
+// sums added in warp order; the first warp of a position also takes the Markov term).
 constexpr int kConfMaxWarps = 32;
 
-__global__ void __launch_bounds__(32 * kConfMaxWarps) confidence_kernel(
-    const uint16_t *__restrict__ h, const uint16_t *__restrict__ conf_w, float conf_b, float thr,
-    int32_t *draft_tokens, int32_t *draft_len, float *conf_out, int k, int H, int wpp) {
+struct ConfArgs {
+  const uint16_t *h, *conf_w;
+  const uint16_t *w1;         // markov_w1 [V, r] or null (plain head)
+  const int32_t *prev_token;  // context of position 0 (with w1)
+  int32_t *draft_tokens, *draft_len;
+  float *conf_out;
+  int *status;
+  float conf_b, thr;          // thr: logit(tau) (per position) or log(tau) (cumulative)
+  int cumulative, r, V, k, H, wpp;
+};
+
+__device__ __forceinline__ float log_sigmoid_f(float z) {
+  return z >= 0.0f ? -log1pf(expf(-z)) : z - log1pf(expf(z));
+}
+
+__global__ void __launch_bounds__(32 * kConfMaxWarps) confidence_kernel(const ConfArgs a) {
   __shared__ float part_s[kConfMaxWarps];
+  __shared__ float zc_s[kMaxK];
   __shared__ int len_s;
   pdl_wait();
   pdl_release();  // one CTA per request: one wave
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int pos = warp / wpp, part = warp - pos * wpp;
+  const int k = a.k, H = a.H;
+  const int pos = warp / a.wpp, part = warp - pos * a.wpp;
   if (pos < k) {
-    const uint4 *hrow = reinterpret_cast<const uint4 *>(h + (static_cast<long long>(b) * k + pos) * H);
-    const uint4 *wrow = reinterpret_cast<const uint4 *>(conf_w);
+    const uint4 *hrow = reinterpret_cast<const uint4 *>(a.h + (static_cast<long long>(b) * k + pos) * H);
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(a.conf_w);
     float acc = 0.0f;
 #pragma unroll 4
-    for (int c = part * 32 + lane; c < H / 8; c += 32 * wpp) {
+    for (int c = part * 32 + lane; c < H / 8; c += 32 * a.wpp) {
       const uint4 hv = __ldg(hrow + c);
       const uint4 wv = __ldg(wrow + c);
       acc = __fmaf_rn(bf16_lo(wv.x), bf16_lo(hv.x), acc);
@@ -947,6 +965,18 @@ __global__ void __launch_bounds__(32 * kConfMaxWarps) confidence_kernel(
       acc = __fmaf_rn(bf16_lo(wv.w), bf16_lo(hv.w), acc);
       acc = __fmaf_rn(bf16_hi(wv.w), bf16_hi(hv.w), acc);
     }
+    if (a.w1 && part == 0) {
+      // the Markov context of this position: the bonus token for position 0, else the
+      // draft of the position before (read before any draft is overwritten below)
+      const int ctx = pos == 0 ? a.prev_token[b] : a.draft_tokens[static_cast<long long>(b) * k + pos - 1];
+      if (ctx >= 0 && ctx < a.V) {
+        for (int t = lane; t < a.r; t += 32)
+          acc = __fmaf_rn(bf16_lo(static_cast<uint32_t>(a.conf_w[H + t])),
+                          bf16_lo(static_cast<uint32_t>(a.w1[static_cast<long long>(ctx) * a.r + t])), acc);
+      } else if (lane == 0) {
+        record_error(a.status, DSPARK_ERR_BAD_TOKEN);
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) part_s[warp] = acc;
@@ -955,25 +985,34 @@ __global__ void __launch_bounds__(32 * kConfMaxWarps) confidence_kernel(
   if (threadIdx.x < k) {
     const int i = threadIdx.x;
     float zc = 0.0f;
-    for (int w = 0; w < wpp; ++w) zc += part_s[i * wpp + w];
-    zc += conf_b;
-    part_s[i * wpp] = zc;  // read back below by thread 0 (after the barrier)
-    if (conf_out) conf_out[static_cast<long long>(b) * k + i] = 1.0f / (1.0f + expf(-zc));
+    for (int w = 0; w < a.wpp; ++w) zc += part_s[i * a.wpp + w];
+    zc += a.conf_b;
+    zc_s[i] = zc;
+    if (a.conf_out) a.conf_out[static_cast<long long>(b) * k + i] = 1.0f / (1.0f + expf(-zc));
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int len = k;
-    for (int i = 0; i < k; ++i)
-      if (!(part_s[i * wpp] >= thr)) {
+    float cum = 0.0f;
+    for (int i = 0; i < k; ++i) {
+      bool keep;
+      if (a.cumulative) {
+        cum += log_sigmoid_f(zc_s[i]);
+        keep = cum >= a.thr;
+      } else {
+        keep = zc_s[i] >= a.thr;
+      }
+      if (!keep) {
         len = i;
         break;
       }
+    }
     len_s = len;
-    draft_len[b] = len;
+    a.draft_len[b] = len;
   }
   __syncthreads();
   if (threadIdx.x < k && threadIdx.x >= len_s)
-    draft_tokens[static_cast<long long>(b) * k + threadIdx.x] = -1;
+    a.draft_tokens[static_cast<long long>(b) * k + threadIdx.x] = -1;
 }
 
 }  // namespace
@@ -1108,6 +1147,13 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
   // DSPARK_CHAIN_PER_POSITION=1 selects the per-position kernels (same results).
   const char *env = getenv("DSPARK_CHAIN_PER_POSITION");
   const bool per_position = env && env[0] == '1';
+  // DSPARK_CHAIN_WAIT_CYCLES: budget of each wait for the other CTAs' words (default
+  // about a second); a tiny budget makes the waits give up (a failure-path test).
+  pa.wait_cycles = kBarrierCycles;
+  if (const char *wc = getenv("DSPARK_CHAIN_WAIT_CYCLES")) {
+    const long long v = atoll(wc);
+    if (v >= 0) pa.wait_cycles = v;
+  }
   const bool ok = per_position ? false
                   : B >= 8 ? try_persistent<8>(pa, pa.r, B, V, stream)
                   : B >= 4 ? try_persistent<4>(pa, pa.r, B, V, stream)
@@ -1136,22 +1182,41 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
 }
 
 dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, float conf_b,
-                                  float conf_tau, int32_t *draft_tokens, int32_t *draft_len,
-                                  float *conf_out, int B, int k, int H, cudaStream_t stream) {
-  float thr;
+                                  float conf_tau, int cumulative, const uint16_t *w1, int r, int V,
+                                  const int32_t *prev_token, int32_t *draft_tokens,
+                                  int32_t *draft_len, float *conf_out, int B, int k, int H,
+                                  int *status, cudaStream_t stream) {
+  ConfArgs a;
+  a.h = h;
+  a.conf_w = conf_w;
+  a.w1 = w1;
+  a.prev_token = prev_token;
+  a.draft_tokens = draft_tokens;
+  a.draft_len = draft_len;
+  a.conf_out = conf_out;
+  a.status = status;
+  a.conf_b = conf_b;
+  a.cumulative = cumulative ? 1 : 0;
+  a.r = w1 ? r : 0;
+  a.V = V;
+  a.k = k;
+  a.H = H;
+  // thresholds: tau <= 0 keeps every position, tau >= 1 keeps none
   if (conf_tau <= 0.0f)
-    thr = -INFINITY;
+    a.thr = -INFINITY;
   else if (conf_tau >= 1.0f)
-    thr = INFINITY;
+    a.thr = INFINITY;
+  else if (cumulative)
+    a.thr = static_cast<float>(log(static_cast<double>(conf_tau)));
   else
-    thr = static_cast<float>(log(static_cast<double>(conf_tau)) - log1p(-static_cast<double>(conf_tau)));
+    a.thr = static_cast<float>(log(static_cast<double>(conf_tau)) - log1p(-static_cast<double>(conf_tau)));
   // warps per position: as many as fit in 32 warps, no more than the 16-byte chunks of
   // a row over 32 lanes
   int wpp = kConfMaxWarps / k;
   const int chunks_per_lane_min = 2;
   while (wpp > 1 && (H / 8) / (32 * wpp) < chunks_per_lane_min) --wpp;
-  if (launch_pdl(confidence_kernel, dim3(B), dim3(32 * wpp * k), 0, stream, h, conf_w, conf_b,
-                 thr, draft_tokens, draft_len, conf_out, k, H, wpp) != cudaSuccess)
+  a.wpp = wpp;
+  if (launch_pdl(confidence_kernel, dim3(B), dim3(32 * wpp * k), 0, stream, a) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;

@@ -9,22 +9,29 @@
 // first rejection draw from max(0, p - q) normalised; after a fully accepted
 // block draw the bonus token from p.
 //
-// Phase 1 (row statistics): one streaming read of every needed row (target
-// rows 0..draft_len, and the draft-logit rows when their softmax statistics
-// were not supplied) with 128-bit loads; each CTA reduces a 16384-entry slice to
-// (argmax key, max, sum exp).
-// Decision: the slices of a request are merged in a fixed order, then the
-// accept/reject tests run with Philox uniforms.
-// Phase 2 (draw, probabilistic only): the one row per request that needs a draw
-// is re-read.  The draw is the Gumbel-max rule: the index maximising
+// Two stages.
+//
+// Row statistics (row_stats_kernel): one streaming read of a set of fp32 rows
+// with 128-bit loads.  Each CTA reduces a 16384-entry slice of one row to
+// (argmax key, max, sum exp(x - max)); the last CTA of a row (atomic ticket,
+// nobody waits) merges the slices in a fixed order and stores the row's
+// (max, sum) and argmax.  Applied to the target rows it depends on nothing but
+// the target logits, so it can run as soon as they exist (in a serving loop:
+// right after the target forward, beside the next block's fc and LM head, which
+// also need only the target forward's outputs).  Applied to the draft-logit
+// rows it yields q's statistics when the drafting kernel did not supply them.
+//
+// Decision and draw (verify_draw_kernel, probabilistic; verify_greedy_kernel,
+// greedy): with the row statistics known, the accept/reject tests of a request
+// need only its drafted tokens and two gathered logits per position.  Every CTA
+// of the draw grid takes its request's decision itself (a handful of loads,
+// identical in every CTA), then reduces one slice (1024 entries per Philox block
+// per thread; 1 to 4 blocks per thread, fewer CTAs for larger batches) of the row
+// that needs a draw.  The draw is the Gumbel-max rule: the index maximising
 // log w_v + G_v, G_v = -log(-log U_v) with U_v from Philox counter (request,
 // row, step, 1 + v/4).  That samples exactly from w normalised and makes the
 // draw an argmax, reduced like every other argmax here (per-CTA 64-bit keys,
-// merged by the request's last CTA).
-//
-// verify_stats_kernel does phase 1 and its last CTA per request (atomic
-// ticket, nobody waits) takes the decisions; verify_sample_kernel does phase 2
-// and its last CTA per request merges the draw.
+// merged by the request's last CTA).  One launch after the drafts exist.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -36,10 +43,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPer = 64;                    // entries per thread per slice (pass 1), all
-                                            // loaded before any is used
-constexpr int kSlice = kThreads * kPer;     // 16384 entries per CTA (pass 1)
-constexpr int kDrawSlice = kThreads * 4;    // 1024 entries per CTA (pass 2): one Philox block per thread
+constexpr int kPer = 64;                    // entries per thread per slice (row statistics),
+                                            // all loaded before any is used
+constexpr int kSlice = kThreads * kPer;     // 16384 entries (64 KB) per CTA (row statistics)
+constexpr int kDrawSlice = kThreads * 4;    // 1024 entries per draw block: one Philox block per thread
 
 struct __align__(16) RowPartial {
   unsigned long long key;
@@ -53,7 +60,7 @@ struct __align__(16) SampleJob {
   int row;     // block row of the target (and draft) logits to draw from
   int kind;
   int d;       // draft token removed by the one-hot residual
-  int pad;
+  int acc_len;
   double cp;   // log-normaliser of the target row: max + log(sum exp)
   double cq;   // log-normaliser of the draft row (kResidual)
 };
@@ -63,79 +70,58 @@ struct __align__(16) SamplePartial {
   unsigned long long best_p;  // argmax key of log p + G (fallback: residual all zero)
 };
 
-struct VerifyArgs {
-  const float *target;
-  const int32_t *drafts;
-  const int32_t *draft_len;
-  const float *zlog;
-  const float *q_stats;
-  const uint32_t *request_id;
-  int32_t *accepted_len;
-  int32_t *next_token;
-  RowPartial *rows;
-  SampleJob *jobs;
-  SamplePartial *sparts;
-  int *req_ticket;
-  int *samp_ticket;
-  int *status;
-  unsigned long long seed;
-  unsigned int step;
-  int mode;
-  int B, k, V;
-  int nslices;
-  int ndraw;      // slices of the draw pass
-  int zrows;      // 1 when draft-logit statistics are computed here
-  int vec;        // 1 when every row starts on a 16-byte boundary (128-bit loads)
-};
+// Atomic ticket `t`: true for the CTA that arrives last (of `count`), which then
+// resets the ticket.  Block-wide.
+// The CTA's partial was stored by thread 0; thread 0's ticket increment is an
+// acquire-release atomic, so the partial is visible before the ticket moves, and the
+// last CTA's thread 0 sees every other CTA's partial; the CTA barrier then orders the
+// reads of the other threads after that acquire.  (A fence in every thread of every
+// CTA cost about a microsecond per CTA wave.)
+__device__ __forceinline__ bool last_arrival(int *t, int count, int *flag_s) {
+  if (threadIdx.x == 0) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+    const bool last = (old == count - 1);
+    if (last) *t = 0;
+    *flag_s = last ? 1 : 0;
+  }
+  __syncthreads();
+  const bool last = *flag_s != 0;
+  if (last) __threadfence();  // the last CTA only: its threads read the others' partials
+  return last;
+}
 
-__device__ __forceinline__ int request_len(const VerifyArgs &a, int b, bool record) {
-  int L = a.draft_len ? a.draft_len[b] : a.k;
-  if (L < 0 || L > a.k) {
-    if (record) record_error(a.status, DSPARK_ERR_INVALID_ARG);
-    L = L < 0 ? 0 : a.k;
+__device__ __forceinline__ int clamp_len(const int32_t *draft_len, int b, int k, int *status) {
+  int L = draft_len ? draft_len[b] : k;
+  if (L < 0 || L > k) {
+    if (status) record_error(status, DSPARK_ERR_INVALID_ARG);
+    L = L < 0 ? 0 : k;
   }
   return L;
 }
 
-// ------------------------------------------------------------------ shared pieces
-
-// Row index rho -> (request, block row, draft-logit row?).
-struct RowRef {
-  int b, j;
-  bool is_z;
+// ------------------------------------------------------------------ row statistics
+struct RowStatsArgs {
+  const float *rows;      // [nrows, V]
+  float *ms;              // [nrows, 2]: (max, sum exp(x - max)); may be null
+  int32_t *argmax;        // [nrows]; may be null
+  RowPartial *parts;      // [nrows, nslices]
+  int *tickets;           // [nrows]
+  const int32_t *len;     // optional: row rho = g * group + j is read only if j <= len[g] + len_off
+  int group, len_off, k;  // (k: the cap of len, for the clamp)
+  long long nrows;
+  int V;
+  int nslices;
+  int vec;                // 1 when rows start on 16-byte boundaries (128-bit loads)
 };
 
-__device__ __forceinline__ RowRef row_ref(const VerifyArgs &a, int rho) {
-  const int trows = a.B * (a.k + 1);
-  RowRef r;
-  r.is_z = rho >= trows;
-  r.b = r.is_z ? (rho - trows) / a.k : rho / (a.k + 1);
-  r.j = r.is_z ? (rho - trows) - r.b * a.k : rho - r.b * (a.k + 1);
-  return r;
-}
-
-__device__ __forceinline__ bool row_needed(const VerifyArgs &a, const RowRef &r) {
-  const int L = request_len(a, r.b, false);
-  return r.is_z ? (a.mode == 1 && r.j < L) : (r.j <= L);
-}
-
-// (argmax key, max, sum exp) of one slice of row rho (KP entries per thread) -> rows
-// partial.  Block-wide; `red` is shared scratch of kWarps entries.
+// This thread's KP entries of slice `slice` of `row`: entry e has index
+// base + (e/4)*1024 + 4*tid + e%4 (vector loads) or base + e*256 + tid; -inf past V.
 template <int KP>
-__device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *red) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int k = a.k, V = a.V;
-  const RowRef rr = row_ref(a, rho);
-  const bool want_stats = (a.mode == 1);
-  const float *row = rr.is_z ? a.zlog + (static_cast<long long>(rr.b) * k + rr.j) * V
-                             : a.target + (static_cast<long long>(rr.b) * (k + 1) + rr.j) * V;
+__device__ __forceinline__ void load_slice(const float *row, int V, int slice, int vec, float (&x)[KP]) {
+  const int tid = threadIdx.x;
   const int base = slice * (kThreads * KP);
-  // This thread's KP entries, all loaded before any is used, in ascending index
-  // order: the argmax by strict float compare (first index wins ties, -0 == +0, NaN
-  // never wins), then the max and the sum of exp(x - max) from registers.  Entry e
-  // has index base + (e/4)*1024 + 4*tid + e%4 (vector loads) or base + e*256 + tid.
-  float x[KP];
-  if (a.vec) {
+  if (vec) {
 #pragma unroll
     for (int it = 0; it < KP / 4; ++it) {
       const int v = base + it * (kThreads * 4) + tid * 4;
@@ -150,8 +136,17 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
       x[it] = v < V ? __ldcs(row + v) : -INFINITY;
     }
   }
+}
+
+// (argmax key, max, sum exp) of one slice whose entries this thread holds in x; thread
+// 0 stores it in *dst.  Block-wide; `red` is shared scratch of kWarps entries.
+template <int KP, bool kSums>
+__device__ void slice_stats(const float (&x)[KP], int V, int slice, int vec, RowPartial *red,
+                            RowPartial *dst) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int base = slice * (kThreads * KP);
   auto index_of = [&](int e) {
-    return a.vec ? base + (e >> 2) * (kThreads * 4) + tid * 4 + (e & 3) : base + e * kThreads + tid;
+    return vec ? base + (e >> 2) * (kThreads * 4) + tid * 4 + (e & 3) : base + e * kThreads + tid;
   };
   // A slice wholly inside the row (every slice but a row's last): the max by fmaxf
   // (which passes over NaN like the strict compare), then the first entry holding it
@@ -186,7 +181,7 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
   unsigned long long best = bi >= 0 ? argmax_key(bv, static_cast<uint32_t>(bi))
                                     : (x0 < V ? argmax_key(-INFINITY, static_cast<uint32_t>(x0)) : 0ull);
   SoftStat st{-INFINITY, 0.0f};
-  if (want_stats && bi >= 0 && bv != INFINITY) {
+  if (kSums && bi >= 0 && bv != INFINITY) {
     float sum = 0.0f;
     if (full) {
       // every entry in range; -inf adds exp(-inf) = +0 and NaN adds +0, both exact
@@ -201,7 +196,7 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
     st = SoftStat{bv, sum};
   }
   best = warp_max_u64(best);
-  if (want_stats) {
+  if (kSums) {
     // warp (max, sum): the max first, then the sum of s * exp(m - max)
     float mm = st.m;
 #pragma unroll
@@ -222,168 +217,164 @@ __device__ void stats_item(const VerifyArgs &a, int rho, int slice, RowPartial *
     }
     acc.m = sacc.m;
     acc.s = sacc.s;
-    a.rows[static_cast<long long>(rho) * a.nslices + slice] = acc;
+    *dst = acc;
   }
-  __syncthreads();
 }
 
-// Decision state of one request, in shared memory.
-struct Decision {
-  unsigned long long tkey[kMaxK + 1];
-  double tM[kMaxK + 1], tS[kMaxK + 1];
-  double zM[kMaxK], zS[kMaxK];
-  double ratio[kMaxK], ua[kMaxK];
-  int bad[kMaxK];
-  SampleJob job;
-  int acc_len;
-  int next;  // greedy: the next token
-};
-
-// Merges the row partials of request b and takes its decisions (block-wide).
-// Greedy: acc_len and next.  Probabilistic: acc_len and the draw job.
-__device__ void decide_request(const VerifyArgs &a, int b, Decision &d, bool record) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int k = a.k, V = a.V;
-  const int trows = a.B * (k + 1);
-  const int L = request_len(a, b, record);
-  const bool want_stats = (a.mode == 1);
-  const int n_t = L + 1;
-  const int n_z = a.zrows ? L : 0;
-  // Loads that do not need the row statistics go first: each position's drafted
-  // token and its target / draft logit (thread j takes position j).
-  const long long drow = static_cast<long long>(b) * k;
-  int pre_dt = -1;
-  float pre_t = 0.0f, pre_z = 0.0f;
-  if (a.mode == 1 && tid < L) {
-    pre_dt = a.drafts[drow + tid];
-    if (pre_dt >= 0 && pre_dt < V) {
-      pre_t = a.target[(static_cast<long long>(b) * (k + 1) + tid) * V + pre_dt];
-      if (a.zlog) pre_z = a.zlog[(drow + tid) * V + pre_dt];
-    }
-  }
-  for (int q = warp; q < n_t + n_z; q += kWarps) {
-    const bool qz = q >= n_t;
-    const int jj = qz ? q - n_t : q;
-    const int r_idx = qz ? trows + b * k + jj : b * (k + 1) + jj;
-    const RowPartial *pr = a.rows + static_cast<long long>(r_idx) * a.nslices;
-    // one pass: each lane merges its slices online (fp64 sums), then the warp
-    unsigned long long kb = 0ull;
-    float mm = -INFINITY;
-    double s = 0.0;
-    for (int c = lane; c < a.nslices; c += 32) {
-      const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
-      kb = raw.x > kb ? raw.x : kb;
-      const float cm = __uint_as_float(static_cast<uint32_t>(raw.y));
-      const float cs = __uint_as_float(static_cast<uint32_t>(raw.y >> 32));
-      if (want_stats && cm != -INFINITY) {
-        if (cm > mm) {
-          s = (mm == -INFINITY) ? static_cast<double>(cs)
-                                : s * static_cast<double>(expf(mm - cm)) + static_cast<double>(cs);
-          mm = cm;
-        } else {
-          s += static_cast<double>(cs) * static_cast<double>(expf(cm - mm));
-        }
-      } else if (!want_stats) {
-        mm = fmaxf(mm, cm);
+// Warp 0 of a row's last CTA: merges the slice partials (max first, then the sum of
+// s * exp(m - max) in fp64, one pass with online rescaling) and stores the row's
+// statistics.
+template <bool kSums>
+__device__ void merge_row(const RowStatsArgs &a, long long rho) {
+  const int lane = threadIdx.x & 31;
+  const RowPartial *pr = a.parts + rho * a.nslices;
+  unsigned long long kb = 0ull;
+  float mm = -INFINITY;
+  double s = 0.0;
+  for (int c = lane; c < a.nslices; c += 32) {
+    const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
+    kb = raw.x > kb ? raw.x : kb;
+    const float cm = __uint_as_float(static_cast<uint32_t>(raw.y));
+    const float cs = __uint_as_float(static_cast<uint32_t>(raw.y >> 32));
+    if (kSums && cm != -INFINITY) {
+      if (cm > mm) {
+        s = (mm == -INFINITY) ? static_cast<double>(cs)
+                              : s * static_cast<double>(expf(mm - cm)) + static_cast<double>(cs);
+        mm = cm;
+      } else {
+        s += static_cast<double>(cs) * static_cast<double>(expf(cm - mm));
       }
     }
-    kb = warp_max_u64(kb);
+  }
+  kb = warp_max_u64(kb);
+  if (kSums) {
     float wm = mm;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-    if (want_stats) {
-      s = (mm == -INFINITY) ? 0.0 : s * static_cast<double>(expf(mm - wm));
+    s = (mm == -INFINITY) ? 0.0 : s * static_cast<double>(expf(mm - wm));
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    }
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     mm = wm;
-    if (lane == 0) {
-      if (qz) {
-        d.zM[jj] = mm;
-        d.zS[jj] = s;
-      } else {
-        d.tkey[jj] = kb;
-        d.tM[jj] = mm;
-        d.tS[jj] = s;
-      }
+  }
+  if (lane == 0) {
+    if (a.ms) {
+      a.ms[2 * rho] = mm;
+      a.ms[2 * rho + 1] = static_cast<float>(s);
+    }
+    if (a.argmax) a.argmax[rho] = static_cast<int32_t>(key_index(kb));
+  }
+}
+
+// One CTA per (row, slice): the slice's KP entries per thread are loaded together,
+// reduced, and the row's last CTA to arrive merges the slices.  Rows past a request's
+// draft length are skipped (every slice of such a row returns at once, so its ticket
+// never moves).
+template <int KP, bool kSums>
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(const RowStatsArgs a) {
+  __shared__ RowPartial red[kWarps];
+  __shared__ int flag_s;
+  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice
+  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
+  const long long rho = static_cast<long long>(blockIdx.x / static_cast<unsigned>(a.nslices));
+  pdl_wait();
+  if (a.len) {
+    const int g = static_cast<int>(rho / a.group), j = static_cast<int>(rho - static_cast<long long>(g) * a.group);
+    if (j > clamp_len(a.len, g, a.k, nullptr) + a.len_off) {
+      pdl_release();
+      return;
     }
   }
-  __syncthreads();
+  float x[KP];
+  load_slice<KP>(a.rows + rho * a.V, a.V, slice, a.vec, x);
+  slice_stats<KP, kSums>(x, a.V, slice, a.vec, red, a.parts + rho * a.nslices + slice);
+  pdl_release();  // after this CTA's pass: the grid may span many waves
+  if (!last_arrival(a.tickets + rho, a.nslices, &flag_s)) return;
+  if (threadIdx.x < 32) merge_row<kSums>(a, rho);
+}
 
-  // Probabilistic: every position's ratio p(d)/q(d) and accept uniform, in parallel
-  // (thread j takes position j); the sequential accept loop below only compares.
-  if (a.mode == 1 && tid < L) {
-    const int jj = tid;
-    const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
-    const int dt = pre_dt;
-    double ua, us;
-    verify_uniforms(a.seed, req, static_cast<uint32_t>(jj), a.step, ua, us);
-    d.ua[jj] = ua;
-    d.bad[jj] = (dt < 0 || dt >= V) ? 1 : 0;
+// ------------------------------------------------------------------ decision and draw
+struct DrawArgs {
+  const float *target;      // [B, k+1, V]
+  const float *t_ms;        // [B, k+1, 2] target row (max, sum exp)
+  const int32_t *t_arg;     // [B, k+1] target row argmax (greedy)
+  const int32_t *drafts;    // [B, k]
+  const int32_t *draft_len; // [B] or null (= k)
+  const float *zlog;        // [B, k, V] draft logits, or null (one-hot q)
+  const float *q_ms;        // [B, k, 2] draft row (max, sum exp) when zlog is given
+  const uint32_t *request_id;
+  int32_t *accepted_len;
+  int32_t *next_token;
+  SamplePartial *sparts;    // [B, ndraw]
+  int *tickets;             // [B]
+  int *status;
+  unsigned long long seed;
+  unsigned int step;
+  int B, k, V;
+  int ndraw;
+  int vec;
+};
+
+// Warp 0: the accept/reject decisions of request b (lane j takes block position j)
+// and the draw job they leave.  Every CTA of the request computes the same job.
+// p(d)/q(d) = exp((T_d - M) - (z_d - m)) * s / S: the exponent is formed exactly in
+// fp64, the exponential in fp32 (relative error ~1e-7).
+__device__ void decide_request(const DrawArgs &a, int b, SampleJob *job_s, bool record) {
+  const int lane = threadIdx.x & 31;
+  const int k = a.k, V = a.V;
+  const int L = clamp_len(a.draft_len, b, k, record ? a.status : nullptr);
+  const long long drow = static_cast<long long>(b) * k;
+  const long long trow = static_cast<long long>(b) * (k + 1);
+  const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
+  int dt = -1;
+  bool bad = false, stop = false;
+  if (lane < L) {
+    dt = a.drafts[drow + lane];
+    bad = (dt < 0 || dt >= V);
     double ratio = 0.0;
-    if (!d.bad[jj]) {
-      // p(d)/q(d) = exp((T_d - M) - (z_d - m)) * s / S: the exponent is formed
-      // exactly in fp64, the exponential in fp32 (relative error ~1e-7)
-      const double tT = pre_t;
-      double ex = tT - d.tM[jj], sc = 1.0 / d.tS[jj];
+    if (!bad) {
+      const float tT = a.target[(trow + lane) * V + dt];
+      const float2 tm = *reinterpret_cast<const float2 *>(a.t_ms + 2 * (trow + lane));
+      double ex = static_cast<double>(tT) - static_cast<double>(tm.x);
+      double sc = 1.0 / static_cast<double>(tm.y);
       if (a.zlog) {
-        const double qm = a.zrows ? d.zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
-        const double qs = a.zrows ? d.zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
-        const double zd = pre_z;
-        ex -= zd - qm;
-        sc *= qs;
+        const float zd = a.zlog[(drow + lane) * V + dt];
+        const float2 qm = *reinterpret_cast<const float2 *>(a.q_ms + 2 * (drow + lane));
+        ex -= static_cast<double>(zd) - static_cast<double>(qm.x);
+        sc *= static_cast<double>(qm.y);
       }
       ratio = static_cast<double>(expf(static_cast<float>(ex))) * sc;
     }
-    d.ratio[jj] = ratio;
+    double ua, us;
+    verify_uniforms(a.seed, req, static_cast<uint32_t>(lane), a.step, ua, us);
+    stop = bad || !(ua < ratio);
   }
-  __syncthreads();
-
-  if (tid == 0) {
-    int acc_len = 0;
-    if (a.mode == 0) {
-      while (acc_len < L &&
-             a.drafts[drow + acc_len] == static_cast<int32_t>(key_index(d.tkey[acc_len])))
-        ++acc_len;
-      d.next = static_cast<int32_t>(key_index(d.tkey[acc_len]));
+  const unsigned stops = __ballot_sync(0xffffffffu, stop);
+  const int acc = stops ? __ffs(stops) - 1 : L;
+  const int stop_bad = __shfl_sync(0xffffffffu, bad ? 1 : 0, acc & 31);
+  const int dsel = __shfl_sync(0xffffffffu, dt, acc & 31);
+  if (lane == 0) {
+    SampleJob job;
+    job.row = acc;
+    job.acc_len = acc;
+    job.d = -1;
+    job.cq = 0.0;
+    if (acc < L && stop_bad) {
+      if (record) record_error(a.status, DSPARK_ERR_BAD_TOKEN);
+      job.kind = kFromP;
+    } else if (acc < L) {
+      job.kind = a.zlog ? kResidual : kResidualOneHot;
+      job.d = dsel;
+      if (a.zlog) {
+        const float2 qm = *reinterpret_cast<const float2 *>(a.q_ms + 2 * (drow + acc));
+        job.cq = static_cast<double>(qm.x) + log(static_cast<double>(qm.y));
+      }
     } else {
-      SampleJob job;
-      job.kind = kNone;
-      job.d = -1;
-      job.pad = 0;
-      job.cq = 0.0;
-      for (; acc_len < L; ++acc_len) {
-        const int jj = acc_len;
-        if (d.bad[jj]) {
-          if (record) record_error(a.status, DSPARK_ERR_BAD_TOKEN);
-          job.row = jj;
-          job.kind = kFromP;
-          job.cp = d.tM[jj] + log(d.tS[jj]);
-          break;
-        }
-        if (d.ua[jj] < d.ratio[jj]) continue;
-        double qm = 0.0, qs = 1.0;
-        if (a.zlog) {
-          qm = a.zrows ? d.zM[jj] : static_cast<double>(a.q_stats[2 * (drow + jj)]);
-          qs = a.zrows ? d.zS[jj] : static_cast<double>(a.q_stats[2 * (drow + jj) + 1]);
-        }
-        job.row = jj;
-        job.kind = a.zlog ? kResidual : kResidualOneHot;
-        job.d = a.drafts[drow + jj];
-        job.cp = d.tM[jj] + log(d.tS[jj]);
-        job.cq = qm + log(qs);
-        break;
-      }
-      if (job.kind == kNone) {
-        job.row = L;
-        job.kind = kFromP;
-        job.cp = d.tM[L] + log(d.tS[L]);
-      }
-      d.job = job;
+      job.kind = kFromP;
     }
-    d.acc_len = acc_len;
+    const float2 tm = *reinterpret_cast<const float2 *>(a.t_ms + 2 * (trow + acc));
+    job.cp = static_cast<double>(tm.x) + log(static_cast<double>(tm.y));
+    *job_s = job;
   }
-  __syncthreads();
 }
 
 // Noise of entry v of a draw at block row `row`: Philox4x32-10 counter
@@ -397,10 +388,12 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
   return -__logf(-logf(u));
 }
 
-// Gumbel-max keys of one 1024-entry slice of the draw row of request b ->
-// draw partial (block-wide).  `red_r`, `red_p` are shared scratch of kWarps.
-__device__ void draw_item(const VerifyArgs &a, const SampleJob &job, int b, int slice,
-                          unsigned long long *red_r, unsigned long long *red_p) {
+// Gumbel-max keys of one slice (NB blocks of 1024 entries, one Philox block of 4 entries
+// per thread in each) of the draw row of request b -> draw partial (block-wide).
+// `red_r`, `red_p` are shared scratch of kWarps.
+template <int NB>
+__device__ void draw_slice(const DrawArgs &a, const SampleJob &job, int b, int slice,
+                           unsigned long long *red_r, unsigned long long *red_p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k = a.k, V = a.V;
   const uint32_t req = a.request_id ? a.request_id[b] : static_cast<uint32_t>(b);
@@ -414,48 +407,58 @@ __device__ void draw_item(const VerifyArgs &a, const SampleJob &job, int b, int 
   const float cqf = static_cast<float>(job.cq);
 
   unsigned long long best_r = 0ull, best_p = 0ull;
-  const int vg = slice * kDrawSlice + tid * 4;   // this thread's 4 entries: one Philox block
-  if (vg < V) {
-    const U4 w = philox4x32_10(U4{req, static_cast<uint32_t>(job.row), a.step,
-                                  1u + static_cast<uint32_t>(vg >> 2)},
-                               k0, k1);
-    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-    float tv[4], zv[4];
+  // every block's row values first (loads in flight together), then the arithmetic
+  float tv[NB][4], zv[NB][4];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int vg = (slice * NB + nb) * kDrawSlice + tid * 4;
     if (a.vec && vg + 4 <= V) {
       const float4 t4 = __ldcs(reinterpret_cast<const float4 *>(trow + vg));
-      tv[0] = t4.x; tv[1] = t4.y; tv[2] = t4.z; tv[3] = t4.w;
+      tv[nb][0] = t4.x; tv[nb][1] = t4.y; tv[nb][2] = t4.z; tv[nb][3] = t4.w;
       if (zrow) {
         const float4 z4 = __ldcs(reinterpret_cast<const float4 *>(zrow + vg));
-        zv[0] = z4.x; zv[1] = z4.y; zv[2] = z4.z; zv[3] = z4.w;
+        zv[nb][0] = z4.x; zv[nb][1] = z4.y; zv[nb][2] = z4.z; zv[nb][3] = z4.w;
+      } else {
+        zv[nb][0] = zv[nb][1] = zv[nb][2] = zv[nb][3] = 0.0f;
       }
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        tv[e] = vg + e < V ? trow[vg + e] : 0.0f;
-        zv[e] = (zrow && vg + e < V) ? zrow[vg + e] : 0.0f;
+        tv[nb][e] = vg + e < V ? trow[vg + e] : 0.0f;
+        zv[nb][e] = (zrow && vg + e < V) ? zrow[vg + e] : 0.0f;
       }
     }
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int v = vg + e;
-      if (v < V) {
-        const float g = gumbel_from_word(words[e]);
-        const float t = tv[e];
-        const float kp = t + g;
-        float kr;
-        if (job.kind == kResidual) {
-          const float av = t - cpf;
-          const float bv = zv[e] - cqf;
-          kr = (av > bv) ? av + log1pf(-expf(bv - av)) + g : -INFINITY;
-        } else if (job.kind == kResidualOneHot) {
-          kr = (v == job.d) ? -INFINITY : kp;
-        } else {
-          kr = kp;
+  for (int nb = 0; nb < NB; ++nb) {
+    const int vg = (slice * NB + nb) * kDrawSlice + tid * 4;
+    if (vg < V) {
+      const U4 w = philox4x32_10(U4{req, static_cast<uint32_t>(job.row), a.step,
+                                    1u + static_cast<uint32_t>(vg >> 2)},
+                                 k0, k1);
+      const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int v = vg + e;
+        if (v < V) {
+          const float g = gumbel_from_word(words[e]);
+          const float t = tv[nb][e];
+          const float kp = t + g;
+          float kr;
+          if (job.kind == kResidual) {
+            const float av = t - cpf;
+            const float bv = zv[nb][e] - cqf;
+            kr = (av > bv) ? av + log1pf(-expf(bv - av)) + g : -INFINITY;
+          } else if (job.kind == kResidualOneHot) {
+            kr = (v == job.d) ? -INFINITY : kp;
+          } else {
+            kr = kp;
+          }
+          const unsigned long long keyr = argmax_key(kr, static_cast<uint32_t>(v));
+          const unsigned long long keyp = argmax_key(kp, static_cast<uint32_t>(v));
+          best_r = keyr > best_r ? keyr : best_r;
+          best_p = keyp > best_p ? keyp : best_p;
         }
-        const unsigned long long keyr = argmax_key(kr, static_cast<uint32_t>(v));
-        const unsigned long long keyp = argmax_key(kp, static_cast<uint32_t>(v));
-        best_r = keyr > best_r ? keyr : best_r;
-        best_p = keyp > best_p ? keyp : best_p;
       }
     }
   }
@@ -474,11 +477,10 @@ __device__ void draw_item(const VerifyArgs &a, const SampleJob &job, int b, int 
     }
     a.sparts[static_cast<long long>(b) * a.ndraw + slice] = SamplePartial{br, bp};
   }
-  __syncthreads();
 }
 
-// Warp 0 merges the draw partials of request b and stores the next token.
-__device__ void finish_draw(const VerifyArgs &a, int b) {
+// Warp 0 of a request's last CTA: merges the draw partials and stores the results.
+__device__ void finish_draw(const DrawArgs &a, const SampleJob &job, int b) {
   const int lane = threadIdx.x & 31;
   const SamplePartial *sp = a.sparts + static_cast<long long>(b) * a.ndraw;
   unsigned long long br = 0ull, bp = 0ull;
@@ -494,150 +496,277 @@ __device__ void finish_draw(const VerifyArgs &a, int b) {
     const float vr = key_value(br);
     const bool has_r = br != 0ull && vr != -INFINITY && vr == vr;
     a.next_token[b] = static_cast<int32_t>(key_index(has_r ? br : bp));
+    a.accepted_len[b] = job.acc_len;
   }
 }
 
-// Atomic ticket of request b in `tickets`: true for the CTA that arrives last
-// (of `count`), which then resets the ticket.  Block-wide.
-// The CTA's partial was stored by thread 0; thread 0's ticket increment is an
-// acquire-release atomic, so the partial is visible before the ticket moves, and the
-// last CTA's thread 0 sees every other CTA's partial; the CTA barrier then orders the
-// reads of the other threads after that acquire.  (A fence in every thread of every
-// CTA cost about a microsecond per CTA wave.)
-__device__ __forceinline__ bool last_arrival(int *tickets, int b, int count, int *flag_s) {
-  if (threadIdx.x == 0) {
-    int old;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(tickets + b) : "memory");
-    const bool last = (old == count - 1);
-    if (last) tickets[b] = 0;
-    *flag_s = last ? 1 : 0;
-  }
-  __syncthreads();
-  const bool last = *flag_s != 0;
-  if (last) __threadfence();  // the last CTA only: its threads read the others' partials
-  return last;
-}
-
-// ------------------------------------------------------------------ two-launch path
-__global__ void __launch_bounds__(kThreads) verify_stats_kernel(const VerifyArgs a) {
-  __shared__ RowPartial red[kWarps];
-  __shared__ int flag_s;
-  __shared__ Decision dec;
-  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice
-  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
-  const int rho = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.nslices));
-  const RowRef rr = row_ref(a, rho);
-  pdl_wait();
-  if (row_needed(a, rr)) stats_item<kPer>(a, rho, slice, red);
-  pdl_release();  // after this CTA's pass: the grid may span many waves
-  const int rows_per_req = (a.k + 1) + (a.zrows ? a.k : 0);
-  if (!last_arrival(a.req_ticket, rr.b, rows_per_req * a.nslices, &flag_s)) return;
-  decide_request(a, rr.b, dec, true);
-  if (threadIdx.x == 0) {
-    a.accepted_len[rr.b] = dec.acc_len;
-    if (a.mode == 0)
-      a.next_token[rr.b] = dec.next;
-    else
-      a.jobs[rr.b] = dec.job;
-  }
-}
-
-__global__ void __launch_bounds__(kThreads) verify_sample_kernel(const VerifyArgs a) {
+template <int NB>
+__global__ void __launch_bounds__(kThreads) verify_draw_kernel(const DrawArgs a) {
   __shared__ unsigned long long red_r[kWarps], red_p[kWarps];
+  __shared__ SampleJob job_s;
   __shared__ int flag_s;
   const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.ndraw));
   const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.ndraw));
   pdl_wait();
-  const SampleJob job = a.jobs[b];
-  draw_item(a, job, b, slice, red_r, red_p);
+  if (threadIdx.x < 32) decide_request(a, b, &job_s, slice == 0);
+  __syncthreads();
+  const SampleJob job = job_s;
+  draw_slice<NB>(a, job, b, slice, red_r, red_p);
   pdl_release();
-  if (!last_arrival(a.samp_ticket, b, a.ndraw, &flag_s)) return;
-  if (threadIdx.x < 32) finish_draw(a, b);
+  if (!last_arrival(a.tickets + b, a.ndraw, &flag_s)) return;
+  if (threadIdx.x < 32) finish_draw(a, job, b);
 }
 
-struct VerifyLayout {
-  size_t req_ticket, samp_ticket, rows, jobs, sparts, total;
-  int nslices, ndraw;
+// Greedy: one warp per request; lane j compares draft j with the target argmax of
+// row j.  accepted_len = first mismatch (draft_len if none), next = argmax of that row.
+__global__ void __launch_bounds__(kThreads) verify_greedy_kernel(const DrawArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_release();
+  if (b >= a.B) return;
+  const int k = a.k;
+  const int L = clamp_len(a.draft_len, b, k, a.status);
+  const long long trow = static_cast<long long>(b) * (k + 1);
+  const int t = lane <= L ? a.t_arg[trow + lane] : -1;
+  const bool miss = lane < L && a.drafts[static_cast<long long>(b) * k + lane] != t;
+  const unsigned m = __ballot_sync(0xffffffffu, miss);
+  const int acc = m ? __ffs(m) - 1 : L;
+  const int next = __shfl_sync(0xffffffffu, t, acc & 31);
+  if (lane == 0) {
+    a.accepted_len[b] = acc;
+    a.next_token[b] = next;
+  }
+}
+
+int nslices_of(int V) { return (V + kSlice - 1) / kSlice; }
+int ndraw_of(int V) { return (V + kDrawSlice - 1) / kDrawSlice; }
+
+bool rows_vec(const float *p, int V) { return (V & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dspark_status_t launch_row_stats(const float *rows, long long nrows, int V, float *ms,
+                                 int32_t *argmax, RowPartial *parts, int *tickets,
+                                 const int32_t *len, int group, int len_off, int k, bool sums,
+                                 cudaStream_t stream) {
+  RowStatsArgs a;
+  a.rows = rows;
+  a.ms = ms;
+  a.argmax = argmax;
+  a.parts = parts;
+  a.tickets = tickets;
+  a.len = len;
+  a.group = group;
+  a.len_off = len_off;
+  a.k = k;
+  a.nrows = nrows;
+  a.V = V;
+  a.nslices = nslices_of(V);
+  a.vec = rows_vec(rows, V) ? 1 : 0;
+  // 16384 entries (64 KB) per CTA: each CTA's fixed cost (scheduling, reduction,
+  // ticket) is spread over 64 loads in flight per thread.
+  const long long g = nrows * a.nslices;
+  if (g > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  const cudaError_t e =
+      sums ? launch_pdl(row_stats_kernel<kPer, true>, dim3(static_cast<unsigned>(g)), dim3(kThreads), 0, stream, a)
+           : launch_pdl(row_stats_kernel<kPer, false>, dim3(static_cast<unsigned>(g)), dim3(kThreads), 0, stream, a);
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  count_launches(1);
+  return DSPARK_OK;
+}
+
+dspark_status_t launch_decision(const DrawArgs &a, int mode, cudaStream_t stream) {
+  if (mode == 0) {
+    if (launch_pdl(verify_greedy_kernel, dim3((a.B + kWarps - 1) / kWarps), dim3(kThreads), 0, stream,
+                   a) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  } else {
+    // Philox blocks per thread: 1 while the grid stays within about four CTAs per SM,
+    // else 2 or 4 (fewer CTAs, each with its decision taken once, at larger batches)
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    DrawArgs d = a;
+    int nb = 1;
+    while (nb < 4 && static_cast<long long>(a.B) * ((a.V + kDrawSlice * nb - 1) / (kDrawSlice * nb)) > 4LL * sms)
+      nb *= 2;
+    d.ndraw = (a.V + kDrawSlice * nb - 1) / (kDrawSlice * nb);
+    const long long g = static_cast<long long>(a.B) * d.ndraw;
+    if (g > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    cudaError_t e;
+    if (nb == 1)
+      e = launch_pdl(verify_draw_kernel<1>, dim3(static_cast<unsigned>(g)), dim3(kThreads), 0, stream, d);
+    else if (nb == 2)
+      e = launch_pdl(verify_draw_kernel<2>, dim3(static_cast<unsigned>(g)), dim3(kThreads), 0, stream, d);
+    else
+      e = launch_pdl(verify_draw_kernel<4>, dim3(static_cast<unsigned>(g)), dim3(kThreads), 0, stream, d);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+  count_launches(1);
+  return DSPARK_OK;
+}
+
+// Workspace layouts (offsets from the start of the caller's workspace, whose first
+// kWsAlign bytes hold the status word).
+struct RowStatsLayout {
+  size_t tickets, parts, total;
 };
 
-VerifyLayout layout(int B, int k, int V) {
-  VerifyLayout L;
-  L.nslices = (V + kSlice - 1) / kSlice;
-  L.ndraw = (V + kDrawSlice - 1) / kDrawSlice;
+RowStatsLayout row_stats_layout(long long nrows, int V) {
+  RowStatsLayout L;
   size_t off = kWsAlign;
-  L.req_ticket = off;
-  off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
-  L.samp_ticket = off;
-  off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
-  L.rows = off;
-  off += align_up(static_cast<size_t>(B) * (2 * k + 1) * L.nslices * sizeof(RowPartial), kWsAlign);
-  L.jobs = off;
-  off += align_up(static_cast<size_t>(B) * sizeof(SampleJob), kWsAlign);
-  L.sparts = off;
-  off += align_up(static_cast<size_t>(B) * L.ndraw * sizeof(SamplePartial), kWsAlign);
+  L.tickets = off;
+  off += align_up(static_cast<size_t>(nrows) * sizeof(int), kWsAlign);
+  L.parts = off;
+  off += align_up(static_cast<size_t>(nrows) * nslices_of(V) * sizeof(RowPartial), kWsAlign);
   L.total = off;
   return L;
 }
 
+struct DrawLayout {
+  size_t tickets, sparts, total;
+};
+
+DrawLayout draw_layout(int B, int V, size_t start) {
+  DrawLayout L;
+  size_t off = start;
+  L.tickets = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
+  L.sparts = off;
+  off += align_up(static_cast<size_t>(B) * ndraw_of(V) * sizeof(SamplePartial), kWsAlign);
+  L.total = off;
+  return L;
+}
+
+// The whole verify in one workspace: [status | target-row tickets | draft-row tickets
+// | draw tickets | target partials | draft partials | target (max, sum) | target
+// argmax | draft (max, sum) | draw partials].
+struct VerifyLayout {
+  size_t t_tickets, z_tickets, d_tickets, t_parts, z_parts, t_ms, t_arg, q_ms, sparts, total;
+};
+
+VerifyLayout verify_layout(int B, int k, int V) {
+  VerifyLayout L;
+  const size_t tr = static_cast<size_t>(B) * (k + 1), zr = static_cast<size_t>(B) * k;
+  const size_t ns = nslices_of(V);
+  size_t off = kWsAlign;
+  L.t_tickets = off;
+  off += align_up(tr * sizeof(int), kWsAlign);
+  L.z_tickets = off;
+  off += align_up(zr * sizeof(int), kWsAlign);
+  L.d_tickets = off;
+  off += align_up(static_cast<size_t>(B) * sizeof(int), kWsAlign);
+  L.t_parts = off;
+  off += align_up(tr * ns * sizeof(RowPartial), kWsAlign);
+  L.z_parts = off;
+  off += align_up(zr * ns * sizeof(RowPartial), kWsAlign);
+  L.t_ms = off;
+  off += align_up(tr * 2 * sizeof(float), kWsAlign);
+  L.t_arg = off;
+  off += align_up(tr * sizeof(int32_t), kWsAlign);
+  L.q_ms = off;
+  off += align_up(zr * 2 * sizeof(float), kWsAlign);
+  L.sparts = off;
+  off += align_up(static_cast<size_t>(B) * ndraw_of(V) * sizeof(SamplePartial), kWsAlign);
+  L.total = off;
+  return L;
+}
+
+DrawArgs draw_args(int mode, const float *target, const float *t_ms, const int32_t *t_arg,
+                   const int32_t *drafts, const int32_t *draft_len, const float *zlog,
+                   const float *q_ms, uint64_t seed, const uint32_t *request_id, uint32_t step,
+                   int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
+                   SamplePartial *sparts, int *tickets, int *status) {
+  DrawArgs a;
+  a.target = target;
+  a.t_ms = t_ms;
+  a.t_arg = t_arg;
+  a.drafts = drafts;
+  a.draft_len = draft_len;
+  a.zlog = (mode == 1) ? zlog : nullptr;
+  a.q_ms = q_ms;
+  a.request_id = request_id;
+  a.accepted_len = accepted_len;
+  a.next_token = next_token;
+  a.sparts = sparts;
+  a.tickets = tickets;
+  a.status = status;
+  a.seed = seed;
+  a.step = step;
+  a.B = B;
+  a.k = k;
+  a.V = V;
+  a.ndraw = ndraw_of(V);
+  a.vec = (rows_vec(target, V) && (a.zlog == nullptr || rows_vec(a.zlog, V))) ? 1 : 0;
+  return a;
+}
+
 }  // namespace
 
-size_t verify_workspace_size(int B, int k, int V) { return layout(B, k, V).total; }
+size_t row_stats_workspace_size(long long nrows, int V) { return row_stats_layout(nrows, V).total; }
+size_t row_stats_counter_bytes(long long nrows, int V) { return row_stats_layout(nrows, V).parts; }
 
-size_t verify_counter_bytes(int B, int k, int V) { return layout(B, k, V).rows; }
+dspark_status_t row_stats_launch(const float *rows, long long nrows, int V, float *ms,
+                                 int32_t *argmax, void *ws, int *status, cudaStream_t stream) {
+  (void)status;
+  const RowStatsLayout L = row_stats_layout(nrows, V);
+  char *w = static_cast<char *>(ws);
+  return launch_row_stats(rows, nrows, V, ms, argmax, reinterpret_cast<RowPartial *>(w + L.parts),
+                          reinterpret_cast<int *>(w + L.tickets), nullptr, 1, 0, 0, ms != nullptr,
+                          stream);
+}
+
+size_t verify_from_stats_workspace_size(int B, int V) { return draw_layout(B, V, kWsAlign).total; }
+size_t verify_from_stats_counter_bytes(int B, int V) { return draw_layout(B, V, kWsAlign).sparts; }
+
+dspark_status_t verify_from_stats_launch(int mode, const float *target, const float *t_ms,
+                                         const int32_t *t_arg, const int32_t *drafts,
+                                         const int32_t *draft_len, const float *zlog,
+                                         const float *q_ms, uint64_t seed,
+                                         const uint32_t *request_id, uint32_t step,
+                                         int32_t *accepted_len, int32_t *next_token, int B, int k,
+                                         int V, void *ws, int *status, cudaStream_t stream) {
+  const DrawLayout L = draw_layout(B, V, kWsAlign);
+  char *w = static_cast<char *>(ws);
+  const DrawArgs a = draw_args(mode, target, t_ms, t_arg, drafts, draft_len, zlog, q_ms, seed,
+                               request_id, step, accepted_len, next_token, B, k, V,
+                               reinterpret_cast<SamplePartial *>(w + L.sparts),
+                               reinterpret_cast<int *>(w + L.tickets), status);
+  return launch_decision(a, mode, stream);
+}
+
+size_t verify_workspace_size(int B, int k, int V) { return verify_layout(B, k, V).total; }
+
+size_t verify_counter_bytes(int B, int k, int V) { return verify_layout(B, k, V).t_parts; }
 
 dspark_status_t verify_launch(int mode, const float *target, const int32_t *drafts,
                               const int32_t *draft_len, const float *zlog, const float *q_stats,
                               uint64_t seed, const uint32_t *request_id, uint32_t step,
                               int32_t *accepted_len, int32_t *next_token, int B, int k, int V,
                               void *ws, int *status, cudaStream_t stream) {
-  const VerifyLayout L = layout(B, k, V);
+  const VerifyLayout L = verify_layout(B, k, V);
   char *w = static_cast<char *>(ws);
-  VerifyArgs a;
-  a.target = target;
-  a.drafts = drafts;
-  a.draft_len = draft_len;
-  a.zlog = (mode == 1) ? zlog : nullptr;
-  a.q_stats = q_stats;
-  a.request_id = request_id;
-  a.accepted_len = accepted_len;
-  a.next_token = next_token;
-  a.rows = reinterpret_cast<RowPartial *>(w + L.rows);
-  a.jobs = reinterpret_cast<SampleJob *>(w + L.jobs);
-  a.sparts = reinterpret_cast<SamplePartial *>(w + L.sparts);
-  a.req_ticket = reinterpret_cast<int *>(w + L.req_ticket);
-  a.samp_ticket = reinterpret_cast<int *>(w + L.samp_ticket);
-  a.status = status;
-  a.seed = seed;
-  a.step = step;
-  a.mode = mode;
-  a.B = B;
-  a.k = k;
-  a.V = V;
-  a.nslices = L.nslices;
-  a.ndraw = L.ndraw;
-  a.zrows = (mode == 1 && zlog != nullptr && q_stats == nullptr) ? 1 : 0;
-  a.vec = ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(target) & 15u) == 0 &&
-           (a.zlog == nullptr || (reinterpret_cast<uintptr_t>(a.zlog) & 15u) == 0))
-              ? 1
-              : 0;
-  const long long nrows = static_cast<long long>(B) * (k + 1) + (a.zrows ? static_cast<long long>(B) * k : 0);
-  // 16384 entries (64 KB) per CTA: each CTA's fixed cost (scheduling, reduction,
-  // ticket) is spread over 64 loads in flight per thread; at batch 1 the 27B rows
-  // make one wave of CTAs.
-  const long long g1 = nrows * a.nslices;
-  if (launch_pdl(verify_stats_kernel, dim3(static_cast<unsigned>(g1)), dim3(kThreads), 0, stream, a) !=
-      cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  count_launches(1);
-  if (mode == 1) {
-    const long long g2 = static_cast<long long>(B) * L.ndraw;
-    if (g2 > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
-    if (launch_pdl(verify_sample_kernel, dim3(static_cast<unsigned>(g2)), dim3(kThreads), 0, stream,
-                   a) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    count_launches(1);
+  float *t_ms = reinterpret_cast<float *>(w + L.t_ms);
+  int32_t *t_arg = reinterpret_cast<int32_t *>(w + L.t_arg);
+  // target rows 0 .. draft_len of every request (greedy needs only their argmax)
+  dspark_status_t st = launch_row_stats(
+      target, static_cast<long long>(B) * (k + 1), V, t_ms, t_arg,
+      reinterpret_cast<RowPartial *>(w + L.t_parts), reinterpret_cast<int *>(w + L.t_tickets),
+      draft_len, k + 1, 0, k, mode == 1, stream);
+  if (st != DSPARK_OK) return st;
+  const float *q_ms = q_stats;
+  if (mode == 1 && zlog != nullptr && q_stats == nullptr) {
+    // q's statistics from the draft-logit rows 0 .. draft_len - 1
+    float *qw = reinterpret_cast<float *>(w + L.q_ms);
+    st = launch_row_stats(zlog, static_cast<long long>(B) * k, V, qw, nullptr,
+                          reinterpret_cast<RowPartial *>(w + L.z_parts),
+                          reinterpret_cast<int *>(w + L.z_tickets), draft_len, k, -1, k, true,
+                          stream);
+    if (st != DSPARK_OK) return st;
+    q_ms = qw;
   }
-  return DSPARK_OK;
+  const DrawArgs a = draw_args(mode, target, t_ms, t_arg, drafts, draft_len, zlog, q_ms, seed,
+                               request_id, step, accepted_len, next_token, B, k, V,
+                               reinterpret_cast<SamplePartial *>(w + L.sparts),
+                               reinterpret_cast<int *>(w + L.d_tickets), status);
+  return launch_decision(a, mode, stream);
 }
 
 }  // namespace dspark

@@ -8,8 +8,6 @@
 // because the process works to a fixed memory budget.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "internal.h"
 
 namespace {
@@ -21,23 +19,16 @@ constexpr size_t kScratchBytes = DSPARK_VERIFY_NOALLOC_MAX_BYTES;
 // host code it is only a stand-in for the device symbol.
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
-std::mutex g_mutex;
-void *g_scratch_ptr[64] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current).
+// Device address of the scratch array on the current device.  Looked up on every
+// call (a host-side query): an address cached across calls could outlive the
+// context it belongs to (after cudaDeviceReset the module is loaded afresh).
 dspark_status_t scratch_for_current_device(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return DSPARK_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr)
-      return DSPARK_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return DSPARK_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return DSPARK_OK;
 }
 
@@ -51,13 +42,18 @@ extern "C" dspark_status_t dspark_verify_noalloc(int mode, const float *target_l
                                                  uint32_t step, int32_t *accepted_len,
                                                  int32_t *next_token, int B, int k, int V,
                                                  void *stream) {
-  if (B < 1 || k < 1 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  // Every check dspark_verify makes, before anything is enqueued: a rejected call
+  // leaves the shared array and the stream untouched.
+  dspark_status_t st = dspark::verify_check_args(mode, target_logits, draft_tokens, draft_len,
+                                                 draft_logits, q_stats, request_id, accepted_len,
+                                                 next_token, B, k, V);
+  if (st != DSPARK_OK) return st;
   const size_t need = dspark_verify_workspace_size(B, k, V);
   if (need == 0) return DSPARK_ERR_UNSUPPORTED_SHAPE;
   if (need > kScratchBytes) return DSPARK_ERR_WORKSPACE;  // beyond the fixed scratch
+  if (!dspark::device_is_blackwell()) return DSPARK_ERR_NO_DEVICE;
   void *ws = nullptr;
-  dspark_status_t st = scratch_for_current_device(&ws);
-  if (st != DSPARK_OK) return st;
+  if ((st = scratch_for_current_device(&ws)) != DSPARK_OK) return st;
   // The array keeps the previous call's contents: clear the part this call uses
   // (status word, tickets, partials) before the kernels run, on the same stream.
   if (cudaMemsetAsync(ws, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -6,10 +6,19 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
 
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libdspark.so")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    import parity_log
+    for line in parity_log.summary_lines():
+        terminalreporter.write_line(line)
 
 
 @pytest.fixture(scope="session")

@@ -133,3 +133,53 @@ def test_fc_lm_head_sizes_and_argument_errors(libdspark):
     assert f(taps, 2, 128, fake, vp((1 << 20) + 8), fake, fake, 4, 128, 100, fake, 1 << 30,
              None) == -3
     assert f(taps, 2, 128, fake, fake, fake, fake, 4, 128, 100, fake, 16, None) == -4
+
+
+def test_row_stats_and_verify_from_stats_argument_errors(libdspark):
+    vp, sz, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
+    libdspark.dspark_row_stats_workspace_size.restype = sz
+    libdspark.dspark_row_stats_workspace_size.argtypes = [i64, ctypes.c_int]
+    libdspark.dspark_verify_from_stats_workspace_size.restype = sz
+    assert libdspark.dspark_row_stats_workspace_size(128, 151936) > 128 * 10 * 16
+    assert libdspark.dspark_row_stats_workspace_size(0, 151936) == 0
+    assert libdspark.dspark_row_stats_workspace_size(8, (1 << 26) + 1) == 0
+    assert libdspark.dspark_verify_from_stats_workspace_size(16, 7, 151936) > 16 * 149 * 16
+    assert libdspark.dspark_verify_from_stats_workspace_size(16, 17, 151936) == 0
+    fake = vp(1 << 20)
+    r = libdspark.dspark_row_stats
+    r.restype = ctypes.c_int
+    r.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, sz, vp]
+    assert r(fake, 8, 100, None, None, fake, 1 << 30, None) == -1              # no output
+    assert r(fake, 0, 100, fake, None, fake, 1 << 30, None) == -1              # no rows
+    assert r(fake, 8, 100, vp((1 << 20) + 4), None, fake, 1 << 30, None) == -3  # ms not 8-B aligned
+    assert r(fake, 8, 100, fake, fake, fake, 16, None) == -4                    # workspace too small
+    f = libdspark.dspark_verify_from_stats
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, ctypes.c_uint64, vp, ctypes.c_uint32,
+                  vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, sz, vp]
+    big = 1 << 30
+    # greedy needs the target argmax; probabilistic the target (max, sum) and, with draft
+    # logits, q's statistics
+    assert f(0, fake, fake, None, fake, None, None, None, 0, None, 0, fake, fake, 2, 7, 100, fake, big, None) == -1
+    assert f(1, fake, None, fake, fake, None, None, None, 0, None, 0, fake, fake, 2, 7, 100, fake, big, None) == -1
+    assert f(1, fake, fake, fake, fake, None, fake, None, 0, None, 0, fake, fake, 2, 7, 100, fake, big, None) == -1
+    assert f(1, fake, fake, fake, fake, None, fake, vp((1 << 20) + 4), 0, None, 0, fake, fake, 2, 7,
+             100, fake, big, None) == -3
+    assert f(0, fake, fake, fake, fake, None, None, None, 0, None, 0, fake, fake, 2, 17, 100, fake, big, None) == -2
+    assert f(0, fake, fake, fake, fake, None, None, None, 0, None, 0, fake, fake, 2, 7, 100, fake, 16, None) == -4
+
+
+def test_verify_noalloc_rejects_before_enqueueing(libdspark):
+    """Argument and size errors of the allocation-free verify come back before any GPU
+    work is queued (the checks run on the host; no device is needed to reach them)."""
+    vp = ctypes.c_void_p
+    f = libdspark.dspark_verify_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, ctypes.c_uint64, vp, ctypes.c_uint32, vp, vp,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+    fake = vp(1 << 20)
+    assert f(3, fake, fake, None, None, None, 0, None, 0, fake, fake, 2, 7, 100, None) == -1
+    assert f(0, fake, fake, None, None, None, 0, None, 0, fake, fake, 2, 17, 100, None) == -2
+    assert f(0, vp((1 << 20) + 2), fake, None, None, None, 0, None, 0, fake, fake, 2, 7, 100, None) == -3
+    # beyond the fixed scratch: 1024 requests of 16 positions over 2^20 entries
+    assert f(0, fake, fake, None, None, None, 0, None, 0, fake, fake, 1024, 16, 1 << 20, None) == -4

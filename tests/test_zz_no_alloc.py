@@ -1,6 +1,7 @@
 """The allocation-free verify entry point, called through the C ABI, gives the same
-accepted lengths and next tokens as dspark_verify with a caller workspace, on two calls
-in a row (the second call finds the first call's leftovers in the shared scratch).
+accepted lengths and next tokens as dspark_verify with a caller workspace, on calls of
+different shapes in a row (each later call finds the earlier call's leftovers in the
+shared scratch).
 
 For callers that are handed only input and output buffers by a framework that owns all
 other device memory, or that must not call cudaMalloc while they run.  Outputs are
@@ -46,21 +47,42 @@ def _inputs(B, k, V, seed):
             torch.from_numpy(z).cuda())
 
 
-@pytest.mark.parametrize("mode", [1, 0])
-def test_noalloc_verify_matches_workspace_verify_twice(mode):
-    f = _entry()
-    B, k, V = 16, 7, 20000
+def _call(f, mode, target, drafts, dlen, z, qs, seed, step, B, k, V):
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    nxt = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
-    for call in range(2):
-        target, drafts, z = _inputs(B, k, V, 900 + 10 * call + mode)
+    rc = f(mode, _p(target), _p(drafts), _p(dlen), _p(z), _p(qs), seed, None, step, _p(acc),
+           _p(nxt), B, k, V, _vp(stream.cuda_stream))
+    assert rc == 0, ds.lib().dspark_status_string(rc)
+    return acc, nxt
+
+
+def test_noalloc_verify_matches_workspace_verify_on_calls_in_a_row():
+    """Calls of different shapes in a row share the one scratch array: the first call
+    (64 requests, 16 positions, 65536 entries) leaves tickets and partial sums laid out
+    for its shape where the next call (3 requests, 5 positions, a ragged 20001-entry
+    vocabulary, draft lengths, q statistics from the drafting kernel) keeps other data;
+    a greedy call of a third shape follows.  Each must equal dspark_verify with its own
+    workspace."""
+    f = _entry()
+    cases = [(1, 64, 16, 65536, False, False), (1, 3, 5, 20001, True, True),
+             (0, 9, 7, 4099, True, False)]
+    for call, (mode, B, k, V, with_len, chain_q) in enumerate(cases):
+        target, drafts, z = _inputs(B, k, V, 900 + 10 * call)
+        dlen = torch.tensor([(k - b) % (k + 1) for b in range(B)], dtype=torch.int32,
+                            device="cuda") if with_len else None
+        qs = None
+        if chain_q:
+            # q's statistics as the drafting kernel writes them (unbiased chain here)
+            z2 = z.clone()
+            prev = torch.zeros((B,), dtype=torch.int32, device="cuda")
+            d2, qs = ds.greedy_sample(z2, None, None, prev)
+            drafts = d2
         seed, step = 0xABCDEF + call, 3 + call
-        ref_a, ref_n = ds.verify(mode, target, drafts, None, z if mode == 1 else None, None,
-                                 seed=seed, step=step)
-        acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
-        nxt = torch.full((B,), -7, dtype=torch.int32, device="cuda")
-        rc = f(mode, _p(target), _p(drafts), None, _p(z) if mode == 1 else None, None, seed, None,
-               step, _p(acc), _p(nxt), B, k, V, _vp(stream.cuda_stream))
-        assert rc == 0, ds.lib().dspark_status_string(rc)
+        ref_a, ref_n = ds.verify(mode, target, drafts, dlen, z if mode == 1 else None, qs,
+                                 seed=seed, step=step, workspaces=ds.Workspaces())
+        acc, nxt = _call(f, mode, target, drafts, dlen, z if mode == 1 else None, qs, seed, step,
+                         B, k, V)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(acc.cpu().numpy(), ref_a.cpu().numpy())
         np.testing.assert_array_equal(nxt.cpu().numpy(), ref_n.cpu().numpy())
