@@ -68,9 +68,9 @@ def parse_args():
     ap.add_argument("--fused-gemms", action="store_true",
                     help="bf16 weights: run the fc and the LM head as one two-phase GEMM "
                          "launch (dspark_fc_lm_head) instead of two launches")
-    ap.add_argument("--q-stats", default="chain", choices=["verify", "chain"],
-                    help="where the softmax statistics of q are reduced: in the Markov chain "
-                         "kernel, or by a row-statistics pass over the draft logits")
+    ap.add_argument("--q-stats", default="verify", choices=["verify", "chain"],
+                    help="where the softmax statistics of q are reduced: in verify's row-"
+                         "statistics launch (with the target rows), or in the Markov chain kernel")
     return ap.parse_args()
 
 

@@ -256,6 +256,7 @@ struct ChainPArgs {
   int rows_per_cta;         // vocabulary rows owned by one CTA
   int w2_smem_bytes;        // shared memory reserved for the markov_w2 slice (0: read via L2)
   long long wait_cycles;    // budget of one wait for the other CTAs' words (clock64 cycles)
+  int vec;                  // logits rows 16-byte aligned and slices multiples of 4 rows
 };
 
 __device__ __forceinline__ int ld_acquire(const int *p) {
@@ -289,11 +290,12 @@ __device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned l
 }
 
 // 16-byte chunk q of local row `row` of the shared-memory markov_w2 slice is
-// stored at chunk q ^ (row & mask): eight consecutive rows read at the same q
-// hit eight different bank groups.
+// stored at chunk q ^ ((row / 4) & mask): a thread owns four consecutive rows, so
+// the eight threads of a shared-memory phase read rows 4 apart at the same q and hit
+// eight different bank groups (128-byte rows; shorter rows share bank groups).
 __device__ __forceinline__ int w2_swizzle(int row, int q, int chunks_per_row) {
   const int mask = chunks_per_row < 8 ? chunks_per_row - 1 : 7;
-  return q ^ (row & mask);
+  return q ^ ((row >> 2) & mask);
 }
 
 // Position words.  Bits 58-63: tag in [1, 63] of (call epoch, position); two
@@ -342,26 +344,63 @@ __device__ __forceinline__ void unpack_f32x2(unsigned long long v, float &lo, fl
 }
 
 // Asynchronous copies of this thread's logits of requests g0 .. g0 + G - 1 (those
-// below B) at position pos into lg_s[(g * kPRows + j) * kPThreads + tid]: issued a
+// below B) at position pos into lg_s[(g * kPThreads + tid) * kPRows + j]: issued a
 // group ahead, they land while the fma chains run and hold no registers meanwhile.
+// vec4: the thread's four rows are consecutive, in range and 16-byte aligned (one
+// 16-byte copy per request).
 template <int G>
 __device__ __forceinline__ void issue_logits_copy(float *lg_s, const float *logits,
-                                                  const int (&vrow)[kPRows], int g0, int pos,
-                                                  int B, int k, int V, int tid) {
+                                                  const int (&vrow)[kPRows], bool vec4, int g0,
+                                                  int pos, int B, int k, int V, int tid) {
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (g0 + g < B) {
       const float *src = logits + (static_cast<long long>(g0 + g) * k + pos) * V;
-#pragma unroll
-      for (int j = 0; j < kPRows; ++j) {
-        const uint32_t dst =
-            static_cast<uint32_t>(__cvta_generic_to_shared(&lg_s[(g * kPRows + j) * kPThreads + tid]));
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src + vrow[j])
+      float *dst0 = &lg_s[(g * kPThreads + tid) * kPRows];
+      if (vec4) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                         __cvta_generic_to_shared(dst0))),
+                     "l"(src + vrow[0])
                      : "memory");
+      } else {
+#pragma unroll
+        for (int j = 0; j < kPRows; ++j)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(
+                           __cvta_generic_to_shared(dst0 + j))),
+                       "l"(src + vrow[j])
+                       : "memory");
       }
     }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Stores this thread's biased logits of one request row: one 16-byte store when vec4,
+// else one per row in range.
+__device__ __forceinline__ void store_row4(float *row, const int (&vrow)[kPRows],
+                                           const bool (&valid)[kPRows], bool vec4, float z0,
+                                           float z1, float z2, float z3) {
+  if (vec4) {
+    *reinterpret_cast<float4 *>(row + vrow[0]) = make_float4(z0, z1, z2, z3);
+  } else {
+    if (valid[0]) row[vrow[0]] = z0;
+    if (valid[1]) row[vrow[1]] = z1;
+    if (valid[2]) row[vrow[2]] = z2;
+    if (valid[3]) row[vrow[3]] = z3;
+  }
+}
+
+// This thread's logits of one request row (four rows of the vocabulary): one 16-byte
+// load when vec4, else four.
+__device__ __forceinline__ void load_row4(const float *row, const int (&vrow)[kPRows], bool vec4,
+                                          float (&out)[kPRows]) {
+  if (vec4) {
+    const float4 v = *reinterpret_cast<const float4 *>(row + vrow[0]);
+    out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kPRows; ++j) out[j] = row[vrow[j]];
+  }
 }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
@@ -410,28 +449,46 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   const int v_lo = cta * a.rows_per_cta;
   const int v_hi = min(V, v_lo + a.rows_per_cta);
   const int nrows = max(0, v_hi - v_lo);
-  // this thread's rows: tid + j * kPThreads of the slice, j < kPRows (clamped;
-  // results of the clamped copies are discarded)
+  // this thread's rows: kPRows * tid + j of the slice, j < kPRows (clamped; results
+  // of the clamped copies are discarded).  vec4: all four in range, and the logits
+  // rows 16-byte aligned (the slice starts on a multiple of 4, V % 4 == 0): logits
+  // move as one 16-byte access per request.
   bool valid[kPRows];
   int vrow[kPRows];
 #pragma unroll
   for (int j = 0; j < kPRows; ++j) {
-    const int row = j * kPThreads + tid;
+    const int row = kPRows * tid + j;
     valid[j] = row < nrows;
     vrow[j] = v_lo + (row < nrows ? row : (nrows > 0 ? nrows - 1 : 0));
   }
+  const bool vec4 = a.vec != 0 && kPRows * tid + kPRows <= nrows;
 
-  // Before the previous kernel has finished: warm L2 with this CTA's markov_w2
-  // slice (a prefetch reads nothing into the program, so it cannot observe data
-  // that is still being written).  Then wait for the previous kernel.
+  // markov_w2 is a weight that no kernel of the step writes, so the CTA's slice is
+  // fetched before the wait for the previous kernel (this CTA runs as soon as the
+  // previous kernel's CTA on its SM has exited): into shared memory by asynchronous
+  // copies (16-byte chunks XOR-swizzled by row so that 8 consecutive rows read at the
+  // same chunk hit 8 bank groups), all in flight together; or, when the slice is read
+  // through L2 at every position, as a bulk prefetch into L2.
   if (biased && nrows > 0) {
-    // 16 KB pieces, one per thread (the slice is at most 1024 rows x 256 bytes)
-    const char *src = reinterpret_cast<const char *>(a.w2 + static_cast<long long>(v_lo) * r);
-    const uint32_t bytes = static_cast<uint32_t>(nrows) * CPR * 16u;
-    const uint32_t off = static_cast<uint32_t>(tid) * 16384u;
-    if (off < bytes) {
-      const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + off), "r"(n) : "memory");
+    if constexpr (kW2Smem) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
+      for (int i = tid; i < nrows * CPR; i += kPThreads) {
+        const int row = i / CPR, q = i - row * CPR;
+        const uint32_t dst = static_cast<uint32_t>(
+            __cvta_generic_to_shared(&w2_s[row * CPR + w2_swizzle(row, q, CPR)]));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + i)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    } else {
+      // 16 KB pieces, one per thread (the slice is at most 1024 rows x 256 bytes)
+      const char *src = reinterpret_cast<const char *>(a.w2 + static_cast<long long>(v_lo) * r);
+      const uint32_t bytes = static_cast<uint32_t>(nrows) * CPR * 16u;
+      const uint32_t off = static_cast<uint32_t>(tid) * 16384u;
+      if (off < bytes) {
+        const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + off), "r"(n) : "memory");
+      }
     }
   }
   pdl_wait();
@@ -440,20 +497,6 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
     stop_s = ld_acquire(a.abort_flag);
     epoch_s = ld_acquire(a.epoch);
     if (stop_s && cta == 0) record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
-  }
-  // markov_w2 slice -> shared memory (16-byte chunks XOR-swizzled by row so that 8
-  // consecutive rows read at the same chunk hit 8 bank groups), asynchronous copies
-  // all in flight together.
-  if (biased && kW2Smem) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
-    for (int i = tid; i < nrows * CPR; i += kPThreads) {
-      const int row = i / CPR, q = i - row * CPR;
-      const uint32_t dst = static_cast<uint32_t>(
-          __cvta_generic_to_shared(&w2_s[row * CPR + w2_swizzle(row, q, CPR)]));
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + i)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   }
   for (int b = tid; b < B; b += kPThreads) {
     int p = a.prev_token[b];
@@ -477,13 +520,15 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   constexpr bool kStage = (G >= 8);
   float lg_next[kPRows][G];
   if constexpr (kStage) {
-    issue_logits_copy<G>(lg_s, a.logits, vrow, 0, 0, B, k, V, tid);
+    issue_logits_copy<G>(lg_s, a.logits, vrow, vec4, 0, 0, B, k, V, tid);
   } else {
 #pragma unroll
-    for (int j = 0; j < kPRows; ++j)
+    for (int g = 0; g < G; ++g) {
+      float t4[kPRows] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (g < B) load_row4(a.logits + (static_cast<long long>(g) * k) * V, vrow, vec4, t4);
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-        lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k) * V + vrow[j]] : 0.0f;
+      for (int j = 0; j < kPRows; ++j) lg_next[j][g] = t4[j];
+    }
   }
 
   // e_b = markov_w1[prev_b] of every request for position 0 (the poll below gathers
@@ -518,10 +563,12 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
       if (!kStage && g0 > 0) {
         // later groups: their logits, loaded before the fma loop hides the latency
 #pragma unroll
-        for (int j = 0; j < kPRows; ++j)
+        for (int g = 0; g < G; ++g) {
+          float t4[kPRows] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (g < gb) load_row4(a.logits + (static_cast<long long>(g0 + g) * k + pos) * V, vrow, vec4, t4);
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-            lg_next[j][g] = (g < gb) ? a.logits[(static_cast<long long>(g0 + g) * k + pos) * V + vrow[j]] : 0.0f;
+          for (int j = 0; j < kPRows; ++j) lg_next[j][g] = t4[j];
+        }
       }
       // bias[v] = sequential fp32 fma chain over t = 0..r-1 (the chain of each
       // (row, request) is one thread's, in t order; chains interleave for ILP)
@@ -633,19 +680,47 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
         mx[g] = -INFINITY;
         sm[g] = 0.0f;
         float zv[kPRows];
+        float lg4[kPRows];
+        if (kStage) {
+          const float4 v = *reinterpret_cast<const float4 *>(&lg_s[(g * kPThreads + tid) * kPRows]);
+          lg4[0] = v.x; lg4[1] = v.y; lg4[2] = v.z; lg4[3] = v.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) lg4[j] = lg_next[j][g];
+        }
 #pragma unroll
         for (int j = 0; j < kPRows; ++j) {
-          float z = kStage ? lg_s[(g * kPRows + j) * kPThreads + tid] : lg_next[j][g];
+          float z = lg4[j];
           if (biased) z = __fadd_rn(z, acc[j][g]);
           zv[j] = z;
           acc[j][g] = z;  // kept for the write-back after this position's words
-          if (valid[j] && g < gb) {
-            const uint32_t o = ordered_bits(z);
-            if (o > bo[g] || bi[g] == 0xffffffffu) {
-              bo[g] = o;
-              bi[g] = static_cast<uint32_t>(vrow[j]);
+        }
+        if (kPRows * tid + kPRows <= nrows) {
+          // all four rows in range: the max by fmaxf (which passes over NaN like the
+          // strict compare), then the first row holding it; the value and index of the
+          // ordered-key scan below.  All NaN: the first row with the lowest key.
+          const float m = fmaxf(fmaxf(zv[0], zv[1]), fmaxf(zv[2], zv[3]));
+          int jj = 0;
+#pragma unroll
+          for (int j = kPRows - 1; j >= 0; --j)
+            if (zv[j] == m) jj = j;
+          if (g < gb) {
+            bo[g] = ordered_bits(m);
+            bi[g] = static_cast<uint32_t>(vrow[0] + jj);  // the four rows are consecutive
+            if (kStats && m == m && m != -INFINITY) mx[g] = m;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) {
+            const float z = zv[j];
+            if (valid[j] && g < gb) {
+              const uint32_t o = ordered_bits(z);
+              if (o > bo[g] || bi[g] == 0xffffffffu) {
+                bo[g] = o;
+                bi[g] = static_cast<uint32_t>(vrow[j]);
+              }
+              if (kStats && z == z && z != -INFINITY) mx[g] = fmaxf(mx[g], z);
             }
-            if (kStats && z == z && z != -INFINITY) mx[g] = fmaxf(mx[g], z);
           }
         }
         if (kStats) {
@@ -658,9 +733,9 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
       // lg_s is consumed: the next group's logits (this position's, else the next's)
       if (kStage) {
         if (g0 + G < B)
-          issue_logits_copy<G>(lg_s, a.logits, vrow, g0 + G, pos, B, k, V, tid);
+          issue_logits_copy<G>(lg_s, a.logits, vrow, vec4, g0 + G, pos, B, k, V, tid);
         else if (pos + 1 < k)
-          issue_logits_copy<G>(lg_s, a.logits, vrow, 0, pos + 1, B, k, V, tid);
+          issue_logits_copy<G>(lg_s, a.logits, vrow, vec4, 0, pos + 1, B, k, V, tid);
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -728,9 +803,8 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 #pragma unroll
         for (int g = 0; g < G; ++g)
           if (g < gb)
-#pragma unroll
-            for (int j = 0; j < kPRows; ++j)
-              if (valid[j]) a.logits[(static_cast<long long>(g0 + g) * k + pos) * V + vrow[j]] = acc[j][g];
+            store_row4(a.logits + (static_cast<long long>(g0 + g) * k + pos) * V, vrow, valid, vec4,
+                       acc[0][g], acc[1][g], acc[2][g], acc[3][g]);
       }
       __syncthreads();
     }
@@ -741,16 +815,17 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 #pragma unroll
       for (int g = 0; g < G; ++g)
         if (g < B)
-#pragma unroll
-          for (int j = 0; j < kPRows; ++j)
-            if (valid[j]) a.logits[(static_cast<long long>(g) * k + pos) * V + vrow[j]] = acc[j][g];
+          store_row4(a.logits + (static_cast<long long>(g) * k + pos) * V, vrow, valid, vec4,
+                     acc[0][g], acc[1][g], acc[2][g], acc[3][g]);
     }
     if (!kStage && pos + 1 < k) {
 #pragma unroll
-      for (int j = 0; j < kPRows; ++j)
+      for (int g = 0; g < G; ++g) {
+        float t4[kPRows] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (g < B) load_row4(a.logits + (static_cast<long long>(g) * k + pos + 1) * V, vrow, vec4, t4);
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          lg_next[j][g] = (g < B) ? a.logits[(static_cast<long long>(g) * k + pos + 1) * V + vrow[j]] : 0.0f;
+        for (int j = 0; j < kPRows; ++j) lg_next[j][g] = t4[j];
+      }
     }
     // Wait for every CTA's word of each request (warp w polls requests w, w + 8, ...,
     // up to kPollReq of them at once);
@@ -1043,10 +1118,12 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
   int grid = sms < kMaxPGrid ? sms : kMaxPGrid;
   const int by_rows = (V + 255) / 256;
   if (grid > by_rows) grid = by_rows;
-  const int rows = (V + grid - 1) / grid;
+  // slices of a multiple of kPRows rows (a thread's rows stay within one 16-byte run)
+  const int rows = ((V + grid - 1) / grid + kPRows - 1) / kPRows * kPRows;
   if (rows > kPRows * kPThreads) return false;
   ChainPArgs a = args0;
   a.rows_per_cta = rows;
+  a.vec = ((V % kPRows) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
   a.w2_smem_bytes =
       kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
   const size_t smem = static_cast<size_t>(a.w2_smem_bytes) +

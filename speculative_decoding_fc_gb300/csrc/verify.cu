@@ -101,18 +101,26 @@ __device__ __forceinline__ int clamp_len(const int32_t *draft_len, int b, int k,
 }
 
 // ------------------------------------------------------------------ row statistics
-struct RowStatsArgs {
+// One set of rows reduced by a row-statistics launch (a launch reduces one or two sets,
+// e.g. the target rows and the draft-logit rows of a verify).
+struct RowSet {
   const float *rows;      // [nrows, V]
   float *ms;              // [nrows, 2]: (max, sum exp(x - max)); may be null
   int32_t *argmax;        // [nrows]; may be null
   RowPartial *parts;      // [nrows, nslices]
   int *tickets;           // [nrows]
   const int32_t *len;     // optional: row rho = g * group + j is read only if j <= len[g] + len_off
-  int group, len_off, k;  // (k: the cap of len, for the clamp)
+  int group, len_off;
   long long nrows;
+  int vec;                // 1 when rows start on 16-byte boundaries (128-bit loads)
+};
+
+struct RowStatsArgs {
+  RowSet set[2];
+  long long blocks0;      // CTAs of set 0 (nrows * nslices); set 1's follow
+  int k;                  // the cap of len, for the clamp
   int V;
   int nslices;
-  int vec;                // 1 when rows start on 16-byte boundaries (128-bit loads)
 };
 
 // This thread's KP entries of slice `slice` of `row`: entry e has index
@@ -225,13 +233,13 @@ __device__ void slice_stats(const float (&x)[KP], int V, int slice, int vec, Row
 // s * exp(m - max) in fp64, one pass with online rescaling) and stores the row's
 // statistics.
 template <bool kSums>
-__device__ void merge_row(const RowStatsArgs &a, long long rho) {
+__device__ void merge_row(const RowSet &a, int nslices, long long rho) {
   const int lane = threadIdx.x & 31;
-  const RowPartial *pr = a.parts + rho * a.nslices;
+  const RowPartial *pr = a.parts + rho * nslices;
   unsigned long long kb = 0ull;
   float mm = -INFINITY;
   double s = 0.0;
-  for (int c = lane; c < a.nslices; c += 32) {
+  for (int c = lane; c < nslices; c += 32) {
     const ulonglong2 raw = __ldcg(reinterpret_cast<const ulonglong2 *>(pr + c));
     kb = raw.x > kb ? raw.x : kb;
     const float cm = __uint_as_float(static_cast<uint32_t>(raw.y));
@@ -270,26 +278,30 @@ __device__ void merge_row(const RowStatsArgs &a, long long rho) {
 // draft length are skipped (every slice of such a row returns at once, so its ticket
 // never moves).
 template <int KP, bool kSums>
-__global__ void __launch_bounds__(kThreads) row_stats_kernel(const RowStatsArgs a) {
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(const __grid_constant__ RowStatsArgs a) {
   __shared__ RowPartial red[kWarps];
   __shared__ int flag_s;
-  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice
-  const int slice = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.nslices));
-  const long long rho = static_cast<long long>(blockIdx.x / static_cast<unsigned>(a.nslices));
+  // 1-D grid (rows can exceed the 65535 limit of gridDim.y): block = row * nslices + slice,
+  // set 0's blocks first
+  const bool second = blockIdx.x >= a.blocks0;
+  const RowSet &rs = second ? a.set[1] : a.set[0];
+  const long long bid = second ? blockIdx.x - a.blocks0 : blockIdx.x;
+  const int slice = static_cast<int>(bid % a.nslices);
+  const long long rho = bid / a.nslices;
   pdl_wait();
-  if (a.len) {
-    const int g = static_cast<int>(rho / a.group), j = static_cast<int>(rho - static_cast<long long>(g) * a.group);
-    if (j > clamp_len(a.len, g, a.k, nullptr) + a.len_off) {
+  if (rs.len) {
+    const int g = static_cast<int>(rho / rs.group), j = static_cast<int>(rho - static_cast<long long>(g) * rs.group);
+    if (j > clamp_len(rs.len, g, a.k, nullptr) + rs.len_off) {
       pdl_release();
       return;
     }
   }
   float x[KP];
-  load_slice<KP>(a.rows + rho * a.V, a.V, slice, a.vec, x);
-  slice_stats<KP, kSums>(x, a.V, slice, a.vec, red, a.parts + rho * a.nslices + slice);
+  load_slice<KP>(rs.rows + rho * a.V, a.V, slice, rs.vec, x);
+  slice_stats<KP, kSums>(x, a.V, slice, rs.vec, red, rs.parts + rho * a.nslices + slice);
   pdl_release();  // after this CTA's pass: the grid may span many waves
-  if (!last_arrival(a.tickets + rho, a.nslices, &flag_s)) return;
-  if (threadIdx.x < 32) merge_row<kSums>(a, rho);
+  if (!last_arrival(rs.tickets + rho, a.nslices, &flag_s)) return;
+  if (threadIdx.x < 32) merge_row<kSums>(rs, a.nslices, rho);
 }
 
 // ------------------------------------------------------------------ decision and draw
@@ -544,27 +556,35 @@ int ndraw_of(int V) { return (V + kDrawSlice - 1) / kDrawSlice; }
 
 bool rows_vec(const float *p, int V) { return (V & 3) == 0 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-dspark_status_t launch_row_stats(const float *rows, long long nrows, int V, float *ms,
-                                 int32_t *argmax, RowPartial *parts, int *tickets,
-                                 const int32_t *len, int group, int len_off, int k, bool sums,
+RowSet row_set(const float *rows, long long nrows, int V, float *ms, int32_t *argmax,
+               RowPartial *parts, int *tickets, const int32_t *len, int group, int len_off) {
+  RowSet r;
+  r.rows = rows;
+  r.ms = ms;
+  r.argmax = argmax;
+  r.parts = parts;
+  r.tickets = tickets;
+  r.len = len;
+  r.group = group;
+  r.len_off = len_off;
+  r.nrows = nrows;
+  r.vec = rows_vec(rows, V) ? 1 : 0;
+  return r;
+}
+
+// One launch over one or two row sets (n = 1 or 2).
+dspark_status_t launch_row_stats(const RowSet *sets, int n, int V, int k, bool sums,
                                  cudaStream_t stream) {
   RowStatsArgs a;
-  a.rows = rows;
-  a.ms = ms;
-  a.argmax = argmax;
-  a.parts = parts;
-  a.tickets = tickets;
-  a.len = len;
-  a.group = group;
-  a.len_off = len_off;
+  a.set[0] = sets[0];
+  a.set[1] = n > 1 ? sets[1] : sets[0];
   a.k = k;
-  a.nrows = nrows;
   a.V = V;
   a.nslices = nslices_of(V);
-  a.vec = rows_vec(rows, V) ? 1 : 0;
+  a.blocks0 = sets[0].nrows * a.nslices;
   // 16384 entries (64 KB) per CTA: each CTA's fixed cost (scheduling, reduction,
   // ticket) is spread over 64 loads in flight per thread.
-  const long long g = nrows * a.nslices;
+  const long long g = a.blocks0 + (n > 1 ? sets[1].nrows * a.nslices : 0);
   if (g > 0x7fffffffLL) return DSPARK_ERR_UNSUPPORTED_SHAPE;
   const cudaError_t e =
       sums ? launch_pdl(row_stats_kernel<kPer, true>, dim3(static_cast<unsigned>(g)), dim3(kThreads), 0, stream, a)
@@ -708,9 +728,9 @@ dspark_status_t row_stats_launch(const float *rows, long long nrows, int V, floa
   (void)status;
   const RowStatsLayout L = row_stats_layout(nrows, V);
   char *w = static_cast<char *>(ws);
-  return launch_row_stats(rows, nrows, V, ms, argmax, reinterpret_cast<RowPartial *>(w + L.parts),
-                          reinterpret_cast<int *>(w + L.tickets), nullptr, 1, 0, 0, ms != nullptr,
-                          stream);
+  const RowSet rs = row_set(rows, nrows, V, ms, argmax, reinterpret_cast<RowPartial *>(w + L.parts),
+                            reinterpret_cast<int *>(w + L.tickets), nullptr, 1, 0);
+  return launch_row_stats(&rs, 1, V, 0, ms != nullptr, stream);
 }
 
 size_t verify_from_stats_workspace_size(int B, int V) { return draw_layout(B, V, kWsAlign).total; }
@@ -745,23 +765,25 @@ dspark_status_t verify_launch(int mode, const float *target, const int32_t *draf
   char *w = static_cast<char *>(ws);
   float *t_ms = reinterpret_cast<float *>(w + L.t_ms);
   int32_t *t_arg = reinterpret_cast<int32_t *>(w + L.t_arg);
-  // target rows 0 .. draft_len of every request (greedy needs only their argmax)
-  dspark_status_t st = launch_row_stats(
-      target, static_cast<long long>(B) * (k + 1), V, t_ms, t_arg,
-      reinterpret_cast<RowPartial *>(w + L.t_parts), reinterpret_cast<int *>(w + L.t_tickets),
-      draft_len, k + 1, 0, k, mode == 1, stream);
-  if (st != DSPARK_OK) return st;
+  // One launch over the target rows 0 .. draft_len of every request (greedy needs only
+  // their argmax) and, when q's statistics are not given, the draft-logit rows
+  // 0 .. draft_len - 1.
+  RowSet sets[2];
+  sets[0] = row_set(target, static_cast<long long>(B) * (k + 1), V, t_ms, t_arg,
+                    reinterpret_cast<RowPartial *>(w + L.t_parts),
+                    reinterpret_cast<int *>(w + L.t_tickets), draft_len, k + 1, 0);
+  int nsets = 1;
   const float *q_ms = q_stats;
   if (mode == 1 && zlog != nullptr && q_stats == nullptr) {
-    // q's statistics from the draft-logit rows 0 .. draft_len - 1
     float *qw = reinterpret_cast<float *>(w + L.q_ms);
-    st = launch_row_stats(zlog, static_cast<long long>(B) * k, V, qw, nullptr,
-                          reinterpret_cast<RowPartial *>(w + L.z_parts),
-                          reinterpret_cast<int *>(w + L.z_tickets), draft_len, k, -1, k, true,
-                          stream);
-    if (st != DSPARK_OK) return st;
+    sets[1] = row_set(zlog, static_cast<long long>(B) * k, V, qw, nullptr,
+                      reinterpret_cast<RowPartial *>(w + L.z_parts),
+                      reinterpret_cast<int *>(w + L.z_tickets), draft_len, k, -1);
+    nsets = 2;
     q_ms = qw;
   }
+  dspark_status_t st = launch_row_stats(sets, nsets, V, k, mode == 1, stream);
+  if (st != DSPARK_OK) return st;
   const DrawArgs a = draw_args(mode, target, t_ms, t_arg, drafts, draft_len, zlog, q_ms, seed,
                                request_id, step, accepted_len, next_token, B, k, V,
                                reinterpret_cast<SamplePartial *>(w + L.sparts),
