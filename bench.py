@@ -55,11 +55,6 @@ def parse_args():
                     help="seconds of repeated K-step timed loops (the median loop is reported)")
     ap.add_argument("--no-b16", action="store_true",
                     help="27b_b1: skip the batch-16 sub-record")
-    ap.add_argument("--verify", default="inline", choices=["split", "inline"],
-                    help="inline: the whole verify (target-row statistics, decision, draw) on "
-                         "the step's stream after drafting; split: the target-row statistics "
-                         "on a side stream beside the GEMMs (their CTAs then compete with the "
-                         "persistent GEMM CTAs for registers), one decision kernel after drafting")
     ap.add_argument("--no-graph", action="store_true", help="time un-captured steps only")
     ap.add_argument("--sweep", action="store_true",
                     help="run the 27B sweep grid instead (one JSON line per cell, not the "
@@ -369,13 +364,14 @@ def timing_events_supported(torch):
 
 
 class Pipeline:
-    """One draft+verify step through the C ABI on given streams.
+    """One draft+verify step through the C ABI.
 
-    main stream: fc -> LM head -> Markov chain (+ q statistics) [-> confidence] ->
-    [wait for the target statistics] -> verify decision + draw.
-    side stream: statistics of the target rows (depend only on the target logits, so
-    they run beside the GEMMs).  verify="inline" instead runs the whole verify (row
-    statistics included) on the main stream after the chain."""
+    draft(): fc -> LM head -> Markov chain [-> confidence] on one stream.
+    verify(): the verify of those drafts (row statistics of the target rows, and of the
+    draft-logit rows unless the chain reduced q's statistics, then the decision/draw
+    kernel) on a given stream.  A serial step runs both on one stream; the decode loop
+    of `measure_workload` runs the verify of step i on a second stream beside the fc
+    and LM head of step i + 1 (two Pipelines, alternating buffers)."""
 
     def __init__(self, ds, torch, device, cfg, mode, w, args):
         self.ds, self.torch, self.dev = ds, torch, device
@@ -384,43 +380,27 @@ class Pipeline:
         M = B * k
         self.fp8 = bool(cfg.get("fp8"))
         self.fused = (not self.fp8) and args.fused_gemms
-        self.split = args.verify == "split"
         self.q_in = args.q_stats
         f32, i32 = torch.float32, torch.int32
         self.h = torch.empty((M, H), dtype=torch.bfloat16, device=device)
         self.logits = torch.empty((B, k, V), dtype=f32, device=device)
         self.drafts = torch.empty((B, k), dtype=i32, device=device)
         self.q_stats = torch.empty((B, k, 2), dtype=f32, device=device) if mode == 1 else None
-        self.t_ms = torch.empty((B, k + 1, 2), dtype=f32, device=device)
-        self.t_arg = torch.empty((B, k + 1), dtype=i32, device=device)
-        self.wsp = ds.Workspaces()          # main-stream calls
-        self.wsp_side = ds.Workspaces()     # the side stream's row statistics
-        self.fork = torch.cuda.Event()
-        self.join = torch.cuda.Event()
+        self.wsp = ds.Workspaces()          # drafting calls
+        self.wsp_v = ds.Workspaces()        # verify calls (may run beside the next drafting)
 
-    def target_stats(self, target, s):
-        self.ds.row_stats(target, ms=self.t_ms, argmax=self.t_arg, stream=s, workspaces=self.wsp_side)
+    def chain_q(self):
+        return self.mode == 1 and self.q_in == "chain"
 
-    def step(self, st, s, side, hist, step_id, ev=None, side_ev=None, target_ready=None):
-        """ev: 5 timing events on s (start, after fc, after LM head, after chain, end);
-        side_ev: 2 timing events on the side stream around the target statistics.
-        target_ready: the target statistics are issued elsewhere (end-to-end leg) and
-        this event marks them done."""
+    def draft(self, st, s, hist, ev=None, chain_after=None):
+        """ev: 4 timing events on s (start, after fc, after LM head, after chain).
+        chain_after: an event the chain waits for (the previous step's verify)."""
         ds, w, cfg = self.ds, self.w, self.cfg
         B, k, V = cfg["B"], cfg["k"], cfg["V"]
         M = B * k
-        acc_o, nxt_o, dlen_o = hist
+        dlen_o = hist[2]
         if ev is not None:
             ev[0].record(s)
-        if self.split and target_ready is None:
-            self.fork.record(s)
-            side.wait_event(self.fork)
-            if side_ev is not None:
-                side_ev[0].record(side)
-            self.target_stats(st["target"], side)
-            if side_ev is not None:
-                side_ev[1].record(side)
-            self.join.record(side)
         if self.fused:
             ds.fc_lm_head(st["taps"], w["fc_w"], w["lm_w"], h_out=self.h, logits=self.logits.view(M, V),
                           stream=s, workspaces=self.wsp)
@@ -440,33 +420,31 @@ class Pipeline:
                 ds.lm_head(self.h, w["lm_w"], out=self.logits.view(M, V), stream=s, workspaces=self.wsp)
         if ev is not None:
             ev[2].record(s)
-        chain_q = self.mode == 1 and self.q_in == "chain"
+        if chain_after is not None:
+            s.wait_event(chain_after)
         ds.greedy_sample(self.logits, w["w1"], w["w2"], st["prev"], draft_tokens=self.drafts,
-                         q_stats=self.q_stats if chain_q else None, want_q_stats=chain_q,
+                         q_stats=self.q_stats if self.chain_q() else None, want_q_stats=self.chain_q(),
                          stream=s, workspaces=self.wsp)
         if w.get("conf_w") is not None:
             ds.confidence_truncate(self.h, w["conf_w"], self.drafts, B, k, 0.0, 0.5,
                                    draft_len=dlen_o, stream=s)
         if ev is not None:
             ev[3].record(s)
-        dl = dlen_o if w.get("conf_w") is not None else None
-        if self.split:
-            if self.mode == 1 and not chain_q:
-                ds.row_stats(self.logits, ms=self.q_stats, want_argmax=False, stream=s,
-                             workspaces=self.wsp)
-            s.wait_event(target_ready if target_ready is not None else self.join)
-            ds.verify_from_stats(self.mode, st["target"], self.t_ms, self.t_arg, self.drafts, dl,
-                                 self.logits if self.mode == 1 else None, self.q_stats, seed=12345,
-                                 request_id=None, step=step_id, accepted_len=acc_o, next_token=nxt_o,
-                                 stream=s, workspaces=self.wsp)
-        else:
-            if target_ready is not None:
-                s.wait_event(target_ready)
-            ds.verify(self.mode, st["target"], self.drafts, dl, self.logits if self.mode == 1 else None,
-                      self.q_stats if chain_q else None, seed=12345, request_id=None, step=step_id,
-                      accepted_len=acc_o, next_token=nxt_o, stream=s, workspaces=self.wsp)
+
+    def verify(self, st, s, hist, step_id, ev=None):
+        acc_o, nxt_o, dlen_o = hist
+        dl = dlen_o if self.w.get("conf_w") is not None else None
+        self.ds.verify(self.mode, st["target"], self.drafts, dl, self.logits if self.mode == 1 else None,
+                       self.q_stats if self.chain_q() else None, seed=12345, request_id=None,
+                       step=step_id, accepted_len=acc_o, next_token=nxt_o, stream=s,
+                       workspaces=self.wsp_v)
         if ev is not None:
-            ev[4].record(s)
+            ev.record(s)
+
+    def step(self, st, s, hist, step_id, ev=None):
+        """A serial step: draft and verify on stream s (ev: 5 timing events)."""
+        self.draft(st, s, hist, ev)
+        self.verify(st, s, hist, step_id, ev[4] if ev is not None else None)
 
 
 def load_weights(ds, torch, device, cfg, host_cache):
@@ -494,9 +472,16 @@ def load_weights(ds, torch, device, cfg, host_cache):
 
 
 def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_baseline):
-    """Times one workload: K-step loops of CUDA-graph replays repeated for at least
-    --min-time seconds (median reported), stage times from replays of graphs carrying
-    timing events, the un-captured loop, and the end-to-end leg with host buffers."""
+    """Times one workload.
+
+    Headline: a decode loop of K steps captured in one CUDA graph, where the verify of
+    step i runs on a second stream beside the fc and LM head of step i + 1 (which need
+    only the target forward's outputs) and the Markov chain of step i + 1 waits for
+    that verify (its context is the verified token).  The K-step loop is replayed for
+    at least --min-time seconds and the median loop is reported.  Also: serial steps
+    (draft and verify on one stream, one CUDA graph per step), per-stage times from
+    serial graphs carrying timing events, the un-captured serial loop, and the
+    end-to-end leg with host buffers."""
     import torch
     import torch.distributed as dist
 
@@ -508,9 +493,10 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
     M = B * k
     w = load_weights(ds, torch, device, cfg, host_cache)
-    pipe = Pipeline(ds, torch, device, cfg, mode, w, args)
+    pipes = [Pipeline(ds, torch, device, cfg, mode, w, args) for _ in range(2)]
+    pipe = pipes[0]
     stream = torch.cuda.current_stream(device)
-    side = torch.cuda.Stream(device)
+    vstream = torch.cuda.Stream(device)
     l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 << 20) or (129 << 20))
     nsets, set_bytes = n_input_sets(cfg, args.sets, l2)
 
@@ -518,7 +504,6 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     def d16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
     sets = []
-    tmp_hist = tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
     for si in range(nsets):
         st = syn.step_inputs(replica_step_seed(si, rank), B, k, H, T, V, cfg["sigma"])
         dev_set = {"taps": [d16(t) for t in st["taps"]], "prev": torch.from_numpy(st["prev"]).to(device)}
@@ -546,45 +531,78 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
         return acc_hist[i], nxt_hist[i], dlen_hist[i]
 
     for i in range(W):
-        pipe.step(sets[i % nsets], stream, side, hist(K + i), K + i)
+        pipe.step(sets[i % nsets], stream, hist(K + i), K + i)
     torch.cuda.synchronize()
 
-    # One CUDA graph per input set (a replay re-runs every kernel of the step on that
-    # set; nothing is cached); graphs remove the per-step host launch cost.
-    graphs, graph_error, launches_per_step = None, None, None
-    staged, stage_src = None, None
+    def decode_loop(s, sv, first, nsteps, hist_of):
+        """nsteps consecutive steps from input set `first`: step i drafts on s with the
+        buffers of pipes[i % 2]; its verify runs on sv once its drafts exist; the chain
+        of step i + 1 waits for it, the fc and LM head of step i + 1 do not (they only
+        wait, before overwriting the buffers of step i - 1, for that step's verify)."""
+        done_d = [torch.cuda.Event(), torch.cuda.Event()]
+        done_v = [torch.cuda.Event(), torch.cuda.Event()]
+        for i in range(nsteps):
+            p = pipes[i % 2]
+            st = sets[(first + i) % nsets]
+            if i >= 2:
+                s.wait_event(done_v[i % 2])      # step i - 2's verify read these buffers
+            h_ = hist_of(i)
+            # fc + LM head, then the chain once the previous step's verify is done
+            p.draft(st, s, h_, chain_after=done_v[(i - 1) % 2] if i >= 1 else None)
+            done_d[i % 2].record(s)
+            sv.wait_event(done_d[i % 2])
+            p.verify(st, sv, h_, i)
+            done_v[i % 2].record(sv)
+        s.wait_event(done_v[(nsteps - 1) % 2])   # the loop ends with its last verify
+        if nsteps >= 2:
+            s.wait_event(done_v[(nsteps - 2) % 2])
+
+    # ---------------------------------------------------------------- CUDA graphs
+    graphs, loops, staged, graph_error = None, None, None, None
+    launches_per_step = None
     ev_ok = timing_events_supported(torch)
+    nloops = max(1, -(-nsets // K))
     if not args.no_graph:
         try:
             cap = torch.cuda.Stream(device)
-            cap_side = torch.cuda.Stream(device)
+            capv = torch.cuda.Stream(device)
             cap.wait_stream(stream)
             ghist = tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
+            # serial: one graph per input set
             graphs = []
             for st in sets:
                 g = torch.cuda.CUDAGraph()
                 n0 = ds.launch_count()
                 with torch.cuda.graph(g, stream=cap):
-                    pipe.step(st, cap, cap_side, ghist, 0)
+                    pipe.step(st, cap, ghist, 0)
                 launches_per_step = ds.launch_count() - n0
                 graphs.append(g)
+            # decode loop: K steps per graph, consecutive graphs start at later sets
+            lhist = [tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
+                     for _ in range(2)]
+            loops = []
+            for li in range(nloops):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    capv.wait_stream(cap)
+                    decode_loop(cap, capv, li * K, K, lambda i: lhist[i % 2])
+                loops.append(g)
             if ev_ok:
-                # the same steps with timing events at the stage boundaries (event-record
+                # serial steps with timing events at the stage boundaries (event-record
                 # nodes), for the per-stage times of graph replays
                 staged = []
                 for st in sets:
                     g = torch.cuda.CUDAGraph()
                     ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-                    sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
                     with torch.cuda.graph(g, stream=cap):
-                        pipe.step(st, cap, cap_side, ghist, 0, ev=ev, side_ev=sev if pipe.split else None)
-                    staged.append((g, ev, sev))
+                        pipe.step(st, cap, ghist, 0, ev=ev)
+                    staged.append((g, ev))
             stream.wait_stream(cap)
-            for g in graphs:      # one untimed replay each
+            for g in graphs + loops:      # one untimed replay each
                 g.replay()
             torch.cuda.synchronize()
         except Exception as exc:  # noqa: BLE001 - fall back to un-captured timing
-            graphs, staged, graph_error = None, None, str(exc).splitlines()[0][:200]
+            graphs, loops, staged, graph_error = None, None, None, str(exc).splitlines()[0][:200]
             torch.cuda.synchronize()
 
     def timed(run_steps):
@@ -601,67 +619,76 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
             dist.barrier()
         return max_over_ranks(t0.elapsed_time(t1), world, device)
 
+    def repeat(run_steps, seconds):
+        """K-step timed loops until `seconds` have elapsed (at least 3): their times."""
+        out = []
+        t_start = time.perf_counter()
+        while True:
+            out.append(timed(run_steps))
+            done = time.perf_counter() - t_start >= seconds and len(out) >= 3
+            if world > 1:
+                done = max_over_ranks(1.0 if done else 0.0, world, device) > 0.5
+            if done:
+                return out
+
+    rep_no = [0]
+
+    def run_loop():
+        loops[rep_no[0] % len(loops)].replay()
+        rep_no[0] += 1
+
     def run_graphs():
         for i in range(K):
             graphs[i % nsets].replay()
 
     def run_plain():
         for i in range(K):
-            pipe.step(sets[i % nsets], stream, side, hist(i), i)
+            pipe.step(sets[i % nsets], stream, hist(i), i)
 
-    # the headline: K-step timed loops repeated until --min-time has elapsed
+    # the headline: the decode loop (K steps per replay), repeated for --min-time
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.1)
-    rep_ms = []
-    t_start = time.perf_counter()
-    while True:
+    if loops is not None:
+        rep_ms = repeat(run_loop, args.min_time)
+        launches = launches_per_step * K
+    else:
         n0 = ds.launch_count()
-        rep_ms.append(timed(run_graphs if graphs is not None else run_plain))
-        launches = launches_per_step * K if graphs is not None else ds.launch_count() - n0
-        done = time.perf_counter() - t_start >= args.min_time and len(rep_ms) >= 3
-        if world > 1:
-            done = max_over_ranks(1.0 if done else 0.0, world, device) > 0.5
-        if done:
-            break
+        rep_ms = repeat(run_plain, args.min_time)
+        launches = (ds.launch_count() - n0) // len(rep_ms)
     clk = clocks.stop()
     max_ms = statistics.median(rep_ms)
+    serial_ms = statistics.median(repeat(run_graphs, 0.25)) if graphs is not None else max_ms
     plain_ms = timed(run_plain)
 
-    # per-stage times: replays of the graphs with timing events (passes over all input
-    # sets, back to back, read after each pass); else the un-captured loop with events
+    # per-stage times: replays of the serial graphs with timing events (passes over all
+    # input sets, back to back, read after each pass); else the un-captured loop
     stage_names = ["fc_lm_head", "(none)", "greedy_sample", "verify"] if pipe.fused \
         else ["fc_project", "lm_head", "greedy_sample", "verify"]
     samples = {nm: [] for nm in stage_names}
-    samples["target_stats"] = []
     samples["step"] = []
     if staged is not None:
-        stage_src = "CUDA-graph replays (event-record nodes at the stage boundaries)"
+        stage_src = "serial CUDA-graph replays (event-record nodes at the stage boundaries)"
         t_s = time.perf_counter()
         while len(samples["step"]) < 200 or time.perf_counter() - t_s < 0.3:
-            for g, _, _ in staged:
+            for g, _ in staged:
                 g.replay()
             torch.cuda.synchronize()
-            for _, ev, sev in staged:
+            for _, ev in staged:
                 for j, nm in enumerate(stage_names):
                     samples[nm].append(ev[j].elapsed_time(ev[j + 1]))
                 samples["step"].append(ev[0].elapsed_time(ev[4]))
-                if pipe.split:
-                    samples["target_stats"].append(sev[0].elapsed_time(sev[1]))
             if time.perf_counter() - t_s > 5.0:
                 break
     else:
-        stage_src = "un-captured loop with CUDA events (host launch cost included)"
+        stage_src = "un-captured serial loop with CUDA events (host launch cost included)"
         for i in range(K):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-            sev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            pipe.step(sets[i % nsets], stream, side, hist(i), i, ev=ev, side_ev=sev if pipe.split else None)
+            pipe.step(sets[i % nsets], stream, hist(i), i, ev=ev)
             torch.cuda.synchronize()
             for j, nm in enumerate(stage_names):
                 samples[nm].append(ev[j].elapsed_time(ev[j + 1]))
             samples["step"].append(ev[0].elapsed_time(ev[4]))
-            if pipe.split:
-                samples["target_stats"].append(sev[0].elapsed_time(sev[1]))
     stage_ms = {nm: statistics.median(v) for nm, v in samples.items() if v and nm != "(none)"}
     lm_ms = stage_ms["fc_lm_head"] if pipe.fused else stage_ms["lm_head"]
 
@@ -682,17 +709,10 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     e2e_set = {"taps": [dev_taps[j] for j in range(T)], "prev": dev_prev, "target": dev_target}
     h2d = pin_taps.numel() * 2 + pin_prev.numel() * 4 + pin_target.numel() * 4
     d2h = (2 * B + B * k) * 4
-    # The target logits go to the device on a side stream and their row statistics run
-    # there too, under the readout; verify waits for them.
+    # The target logits go to the device on a side stream, under the readout; verify
+    # waits for them.  The host reads every step's result before the next step.
     copy_stream = torch.cuda.Stream(device)
     target_ready = torch.cuda.Event()
-
-    def copy_target():
-        with torch.cuda.stream(copy_stream):  # the previous step's verify is done (host sync)
-            dev_target.copy_(pin_target, non_blocking=True)
-            if pipe.split:
-                pipe.target_stats(dev_target, copy_stream)
-            target_ready.record(copy_stream)
     for rep in range(2):
         if world > 1:
             dist.barrier()
@@ -700,10 +720,14 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
         n = 3 if rep == 0 else Ke
         t0 = time.perf_counter()
         for i in range(n):
-            copy_target()
+            with torch.cuda.stream(copy_stream):  # the previous step's verify is done (host sync)
+                dev_target.copy_(pin_target, non_blocking=True)
+                target_ready.record(copy_stream)
             dev_taps.copy_(pin_taps, non_blocking=True)
             dev_prev.copy_(pin_prev, non_blocking=True)
-            pipe.step(e2e_set, stream, side, hist(i), i, target_ready=target_ready)
+            pipe.draft(e2e_set, stream, hist(i))
+            stream.wait_event(target_ready)
+            pipe.verify(e2e_set, stream, hist(i), i)
             out_acc.copy_(acc_hist[i], non_blocking=True)
             out_nxt.copy_(nxt_hist[i], non_blocking=True)
             out_drafts.copy_(pipe.drafts, non_blocking=True)
@@ -727,22 +751,18 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     t_readout = max((sb["fc"] + sb["lm_head"] + sb["chain"]) / (peak_gbs * 1e9),
                     step_flops(cfg) / (peak_tf * 1e12))
     t_verify = sb["verify"] / (peak_gbs * 1e9)
-    t_tstats = B * (k + 1) * V * 4 / (peak_gbs * 1e9)
     readout_ms = ((stage_ms["fc_lm_head"] if pipe.fused else stage_ms["fc_project"] + stage_ms["lm_head"])
                   + stage_ms["greedy_sample"])
     traffic_file = "gemm_tcgen05_fc_lm_head" if pipe.fused else "gemm_tcgen05_lm_head"
     traffic = profiled_traffic(name, traffic_file)
     step_roof = {"bytes": sb["total"], "flops": step_flops(cfg), "t_roofline_ms": t_roof * 1000.0,
                  "frac": (t_roof * 1000.0) / (max_ms / K), "peak_source": peak_src,
+                 "serial_frac": (t_roof * 1000.0) / (serial_ms / K),
                  "readout_frac": t_readout * 1000.0 / readout_ms,
                  "verify_frac": t_verify * 1000.0 / stage_ms["verify"],
-                 "verify_frac_is": ("critical-path verify time: from the end of the drafting "
-                                    "kernels to the end of verify on the step's stream; the "
-                                    "target-row statistics run beside the GEMMs"
-                                    if pipe.split else "the whole verify on the step's stream"),
+                 "verify_frac_is": "the serial step's verify (row statistics, decision, draw) "
+                                   "against its own algorithmic bytes",
                  "stage_times": stage_src}
-    if pipe.split and "target_stats" in stage_ms:
-        step_roof["target_stats_frac"] = t_tstats * 1000.0 / stage_ms["target_stats"]
     line = {
         "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": max_ms / K, "higher_is_better": True,
@@ -768,11 +788,17 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": lm_bytes, "ms_per_launch": lm_ms},
         "step_roofline": step_roof,
-        "graph": graphs is not None,
+        "graph": loops is not None,
         "graph_error": graph_error,
+        "timing": ("decode loop: K steps per CUDA-graph replay; verify of step i on a second "
+                   "stream beside the fc and LM head of step i+1; the chain of step i+1 waits "
+                   "for it" if loops is not None else "un-captured serial steps"),
         "timed_reps": {"reps": len(rep_ms), "steps_per_rep": K, "median_ms": max_ms,
                        "min_ms": min(rep_ms), "max_ms": max(rep_ms),
                        "seconds": sum(rep_ms) / 1000.0},
+        "serial": {"value": whole_job_rate(K, world, serial_ms / 1000.0), "unit": "steps/s",
+                   "ms_per_step": serial_ms / K,
+                   "what": "one CUDA graph per step, draft and verify on one stream"},
         "uncaptured": {"value": whole_job_rate(K, world, plain_ms / 1000.0), "unit": "steps/s",
                        "ms_per_step": plain_ms / K},
         "stage_ms": stage_ms,
@@ -793,7 +819,7 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
         sps, cores, desc, _ = cpu_oracle_baseline(host, cfg, mode, args.cpu_budget)
         line["cpu_baseline"] = {"value": sps, "unit": "steps/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
-    del graphs, staged, sets, pipe
+    del graphs, loops, staged, sets, pipes, pipe
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return line
@@ -808,7 +834,6 @@ def config_of(name, cfg, mode, args, world, nsets=None, set_bytes=None, l2=None,
          "parallelism": "replicas%d" % world}
     if nsets is not None:
         c["q_stats_in"] = args.q_stats
-        c["verify_path"] = args.verify
         c["l2"] = ("inputs larger than L2: %.2f GB of weights streamed per step; %d input sets of "
                    "%.1f MB rotated (%.0f MB > 2x the %.0f MB L2)"
                    % (weights_bytes / 1e9, nsets, set_bytes / 1e6, nsets * set_bytes / 1e6, l2 / 1e6))
@@ -832,8 +857,8 @@ def run_ours(args, rank, local_rank, world):
         line["batch16"] = {kk: sub[kk] for kk in (
             "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "drafted_tok_s",
             "accepted_tok_s", "mean_acceptance_length", "per_position_acceptance", "roofline",
-            "step_roofline", "graph", "timed_reps", "uncaptured", "stage_ms", "gpu_launches",
-            "e2e", "clocks")}
+            "step_roofline", "graph", "timing", "timed_reps", "serial", "uncaptured", "stage_ms",
+            "gpu_launches", "e2e", "clocks")}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -887,7 +912,6 @@ def run_sweep(args):
                                 {"fc_w": fc_w, "lm_w": lm_w, "w1": w1, "w2": w2, "conf_w": None}, args)
                 hist = tuple(torch.zeros((B,), dtype=torch.int32, device=device) for _ in range(3))
                 acc_o = hist[0]
-                side = torch.cuda.Stream(device)
                 dev_sets = []
                 for st in raw:
                     taps = [d16(t) for t in st["taps"]]
@@ -904,16 +928,15 @@ def run_sweep(args):
                         st["target"] = (st["own"] + st["noise"] * sigma).contiguous()
 
                     for st in dev_sets:        # eager warm-up (workspaces, first launches)
-                        pipe.step(st, stream, side, hist, 0)
+                        pipe.step(st, stream, hist, 0)
                     torch.cuda.synchronize()
                     cap = torch.cuda.Stream(device)
-                    cap_side = torch.cuda.Stream(device)
                     cap.wait_stream(stream)
                     graphs = []
                     for st in dev_sets:
                         g = torch.cuda.CUDAGraph()
                         with torch.cuda.graph(g, stream=cap):
-                            pipe.step(st, cap, cap_side, hist, 0)
+                            pipe.step(st, cap, hist, 0)
                         graphs.append(g)
                     stream.wait_stream(cap)
                     for i in range(3):
