@@ -427,7 +427,7 @@ __device__ __forceinline__ void warp_key_stats(unsigned long long &key, float &m
 template <int G, int CPR, bool kStats, bool kW2Smem>
 __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const ChainPArgs a) {
   static_assert(G <= kPWarps, "one combining warp per request of a group");
-  __shared__ ChainPartial red[kGroup][kPWarps];
+  __shared__ ChainPartial red[G][kPWarps];
   __shared__ int stop_s, epoch_s;
   extern __shared__ __align__(16) uint8_t psmem[];
   // dynamic shared memory: markov_w2 slice [rows][CPR] (1024-byte aligned), then the
@@ -766,9 +766,9 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
           if (g < gb) red[g][warp] = ChainPartial{key[g], mx[g], sm[g]};
       }
       __syncthreads();
-      // one warp per request of the group combines the kPWarps warp partials
-      if (warp < gb) {
-        const int g = warp;
+      // one warp per request of the group combines the kPWarps warp partials (warp w
+      // takes requests w and w + kPWarps of the group)
+      for (int g = warp; g < gb; g += kPWarps) {
         unsigned long long key = 0ull;
         float m = -INFINITY, sum = 0.0f;
         if (lane < kPWarps) {
@@ -1132,16 +1132,19 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
                       (G >= 8 ? static_cast<size_t>(G) * kPRows * kPThreads * sizeof(float) : 0);
   if (smem > kPSmemMax) return false;
   auto kern = markov_chain_persistent<G, CPR, kStats, kW2Smem>;
-  static bool attr_set[64] = {};
+  // The opt-in dynamic shared memory this launch needs (the kernel's static shared
+  // memory plus the dynamic part must stay within the per-CTA limit, so the attribute
+  // is raised to what is needed, not to a fixed maximum).
+  static size_t attr_bytes[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemMax) !=
+  if (attr_bytes[dev] < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess) {
       cudaGetLastError();
       return false;
     }
-    attr_set[dev] = true;
+    attr_bytes[dev] = smem;
   }
   // Cooperative (all CTAs resident together: they wait on each other), and, when
   // enabled, with programmatic dependent launch; without the latter if the
