@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--sets", type=int, default=3,
                     help="minimum input sets rotated across steps (more are used when needed "
                          "to exceed 2x the L2 cache)")
+    ap.add_argument("--profile-sets", type=int, default=0,
+                    help="profiling runs only: rotate this many input sets instead of enough to "
+                         "exceed 2x the L2 cache (fewer set-up launches before the profiled ones)")
     ap.add_argument("--min-time", type=float, default=1.0,
                     help="seconds of repeated K-step timed loops (the median loop is reported)")
     ap.add_argument("--no-b16", action="store_true",
@@ -499,6 +502,8 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     vstream = torch.cuda.Stream(device)
     l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 << 20) or (129 << 20))
     nsets, set_bytes = n_input_sets(cfg, args.sets, l2)
+    if args.profile_sets > 0:
+        nsets = args.profile_sets
 
     # input sets: taps, prev, target logits = own draft logits + noise (built once)
     def d16(a):
