@@ -412,7 +412,9 @@ __device__ __forceinline__ void warp_key_stats(unsigned long long &key, float &m
   float mm = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-  float ss = (m == -INFINITY) ? 0.0f : s * expf(m - mm);
+  // __fmul_rn: the rescaled sum is rounded before the shuffle sum (no fused
+  // multiply-add), so every chain kernel gives the same bits
+  float ss = (m == -INFINITY) ? 0.0f : __fmul_rn(s, expf(m - mm));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   m = mm;
@@ -459,7 +461,8 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   for (int j = 0; j < kPRows; ++j) {
     const int row = kPRows * tid + j;
     valid[j] = row < nrows;
-    vrow[j] = v_lo + (row < nrows ? row : (nrows > 0 ? nrows - 1 : 0));
+    // a CTA past the vocabulary's end (nrows == 0) points its copies at row 0
+    vrow[j] = nrows > 0 ? v_lo + (row < nrows ? row : nrows - 1) : 0;
   }
   const bool vec4 = a.vec != 0 && kPRows * tid + kPRows <= nrows;
 
@@ -512,7 +515,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   const int epoch = epoch_s;
   int lrow[kPRows];  // local (slice) row of each of this thread's rows, clamped
 #pragma unroll
-  for (int j = 0; j < kPRows; ++j) lrow[j] = vrow[j] - v_lo;
+  for (int j = 0; j < kPRows; ++j) lrow[j] = nrows > 0 ? vrow[j] - v_lo : 0;
 
   // Logits of the first request group at position 0.  Groups of 8 requests stage
   // them in shared memory through asynchronous copies issued a group ahead; smaller
@@ -752,7 +755,7 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
 #pragma unroll
           for (int g = 0; g < G; ++g) mm[g] = fmaxf(mm[g], __shfl_xor_sync(0xffffffffu, mm[g], o));
 #pragma unroll
-        for (int g = 0; g < G; ++g) sm[g] = (mx[g] == -INFINITY) ? 0.0f : sm[g] * expf(mx[g] - mm[g]);
+        for (int g = 0; g < G; ++g) sm[g] = (mx[g] == -INFINITY) ? 0.0f : __fmul_rn(sm[g], expf(mx[g] - mm[g]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
@@ -794,8 +797,9 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
             st_release_u64(a.words + at, wd);
           // the global winner is one of the CTA winners: warm L2 with this one's
           // markov_w1 row for the next position's gather
-          if (biased && pos + 1 < k)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.w1 + static_cast<long long>(key_index(key)) * r));
+          const int kidx = static_cast<int>(key_index(key));
+          if (biased && pos + 1 < k && kidx >= 0 && kidx < V)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.w1 + static_cast<long long>(kidx) * r));
         }
       }
       if (biased && B > G) {
@@ -989,6 +993,463 @@ __global__ void __launch_bounds__(kPThreads, 1) markov_chain_persistent(const Ch
   }
 }
 
+// ------------------------------------------------- persistent chain, two halves
+// Batches of more than 8 requests (r <= 64): 512 threads per CTA in two halves of
+// 256.  Half h owns request groups h, h + 2, h + 4, ... (8 requests each) and covers
+// the CTA's whole vocabulary slice for them, four rows per thread as above.  The
+// halves take turns on the fp32 FMA pipe: half 1 starts the fma chains of a group
+// when half 0 has finished those of its group, and the other way round, so that
+// while one half takes its argmax, publishes its words and waits for the other CTAs'
+// words, the other half's chains run alone on the pipe.  Each (row, request) chain is
+// the same sequential fp32 fma chain in rank order as in the kernel above.
+//
+// Barriers: 1 + h synchronises half h (256 threads); 3 (half 0 arrives, half 1
+// waits) and 4 (half 1 arrives, half 0 waits) pass the pipe between the halves.
+// Both halves run the same number of group slots (empty slots past the batch end
+// keep the barrier sequence), and a half that gives up waiting keeps the sequence
+// too, doing no work: every barrier is reached the same number of times by both.
+constexpr int kSThreads = 512;
+constexpr int kSGroup = 8;
+
+__device__ __forceinline__ void half_sync(int h) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + h), "r"(kPThreads) : "memory");
+}
+__device__ __forceinline__ void pipe_pass(int h) {  // this half's fma chains are done
+  asm volatile("bar.arrive %0, %1;" ::"r"(3 + h), "r"(kSThreads) : "memory");
+}
+__device__ __forceinline__ void pipe_take(int h) {  // wait for the other half's chains
+  asm volatile("bar.sync %0, %1;" ::"r"(4 - h), "r"(kSThreads) : "memory");
+}
+
+template <int CPR, bool kStats>
+__global__ void __launch_bounds__(kSThreads, 1) markov_chain_split(const ChainPArgs a) {
+  constexpr int G = kSGroup;
+  __shared__ ChainPartial red[2][G][kPWarps];
+  __shared__ int stop_s[2], epoch_s, abort0_s;
+  extern __shared__ __align__(16) uint8_t psmem[];
+  // dynamic shared memory: markov_w2 slice [rows][CPR] (1024-byte aligned), then the
+  // contexts e [r][npair4][2] (request pairs, npair4 a multiple of 4), then prev
+  // tokens [B] (padded to 16 bytes), then each half's staged logits [G][kPThreads][kPRows]
+  const int B = a.B, k = a.k, V = a.V;
+  const int npair4 = ((B + 1) / 2 + 3) & ~3;
+  constexpr int r = CPR * 8;
+  uint4 *w2_s = reinterpret_cast<uint4 *>(psmem);
+  const size_t e_bytes = static_cast<size_t>(r) * npair4 * 8;
+  float *e_s = reinterpret_cast<float *>(psmem + a.w2_smem_bytes);
+  int *prev_s = reinterpret_cast<int *>(psmem + a.w2_smem_bytes + e_bytes);
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int h = tid >> 8, ht = tid & (kPThreads - 1), hw = ht >> 5;
+  float *lg_s = reinterpret_cast<float *>(psmem + a.w2_smem_bytes + e_bytes +
+                                          ((static_cast<size_t>(B) * 4 + 15) & ~static_cast<size_t>(15))) +
+                static_cast<size_t>(h) * G * kPThreads * kPRows;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const bool biased = (a.w1 != nullptr);
+  const int v_lo = cta * a.rows_per_cta;
+  const int v_hi = min(V, v_lo + a.rows_per_cta);
+  const int nrows = max(0, v_hi - v_lo);
+  bool valid[kPRows];
+  int vrow[kPRows], lrow[kPRows];
+#pragma unroll
+  for (int j = 0; j < kPRows; ++j) {
+    const int row = kPRows * ht + j;
+    valid[j] = row < nrows;
+    // a CTA past the vocabulary's end (nrows == 0) points its copies at row 0
+    vrow[j] = nrows > 0 ? v_lo + (row < nrows ? row : nrows - 1) : 0;
+    lrow[j] = nrows > 0 ? vrow[j] - v_lo : 0;
+  }
+  const bool vec4 = a.vec != 0 && kPRows * ht + kPRows <= nrows;
+
+  // markov_w2 slice into shared memory before the wait for the previous kernel (no
+  // kernel of the step writes it), 16-byte chunks swizzled as above
+  if (biased && nrows > 0) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
+    for (int i = tid; i < nrows * CPR; i += kSThreads) {
+      const int row = i / CPR, q = i - row * CPR;
+      const uint32_t dst = static_cast<uint32_t>(
+          __cvta_generic_to_shared(&w2_s[row * CPR + w2_swizzle(row, q, CPR)]));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + i) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_release();
+  if (tid == 0) {
+    abort0_s = ld_acquire(a.abort_flag);
+    epoch_s = ld_acquire(a.epoch);
+    stop_s[0] = stop_s[1] = 0;
+    if (abort0_s && cta == 0) record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
+  }
+  for (int b = tid; b < B; b += kSThreads) {
+    int p = a.prev_token[b];
+    if (biased && (p < 0 || p >= V)) {
+      if (cta == 0) record_error(a.status, DSPARK_ERR_BAD_TOKEN);
+      p = -1;
+    }
+    prev_s[b] = p;
+  }
+  if (biased) asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (abort0_s) return;
+  const int epoch = epoch_s;
+  const int ngroups = (B + G - 1) / G;
+  const int nslots = (ngroups + 1) / 2;  // group slots per half (the same for both)
+
+  // this half's first group's logits at position 0
+  if (h < ngroups) issue_logits_copy<G>(lg_s, a.logits, vrow, vec4, h * G, 0, B, k, V, ht);
+
+  // e_b = markov_w1[prev_b] for position 0, all requests, by the whole CTA
+  if (biased) {
+    for (int i0 = 0; i0 < B * r; i0 += kSThreads * kGather) {
+      uint32_t ev[kGather];
+#pragma unroll
+      for (int u = 0; u < kGather; ++u) {
+        const int idx = i0 + u * kSThreads + tid;
+        const int b = idx / r, t = idx - b * r;
+        const int p = idx < B * r ? prev_s[b] : -1;
+        ev[u] = p >= 0 ? static_cast<uint32_t>(a.w1[static_cast<long long>(p) * r + t]) << 16 : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kGather; ++u) {
+        const int idx = i0 + u * kSThreads + tid;
+        const int b = idx / r, t = idx - b * r;
+        if (idx < B * r) e_s[(t * npair4 + (b >> 1)) * 2 + (b & 1)] = __uint_as_float(ev[u]);
+      }
+    }
+  }
+  __syncthreads();
+
+  float acc[kPRows][G];
+  bool first_fma = true;
+  for (int pos = 0; pos < k; ++pos) {
+    for (int s = 0; s < nslots; ++s) {
+      const int g0 = (2 * s + h) * G;
+      const bool active = g0 < B && stop_s[h] == 0;
+      const int gb = active ? min(G, B - g0) : 0;
+      // the pipe: half 0 waits for half 1's previous chains (none before its first),
+      // half 1 for half 0's chains of this slot
+      if (h == 1 || !first_fma) pipe_take(h);
+      first_fma = false;
+#pragma unroll
+      for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[j][g] = 0.0f;
+      if (biased && active) {
+        unsigned long long acc2[kPRows][G / 2];
+#pragma unroll
+        for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+          for (int gp = 0; gp < G / 2; ++gp) acc2[j][gp] = 0ull;
+        const float *eg = e_s + static_cast<size_t>(g0 >> 1) * 2;
+#pragma unroll
+        for (int q = 0; q < CPR; ++q) {
+          uint4 c[kPRows];
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) c[j] = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            // contexts of the group's four request pairs at rank 8q + t (32 bytes)
+            const float4 *ep = reinterpret_cast<const float4 *>(eg + static_cast<size_t>(q * 8 + t) * npair4 * 2);
+            const float4 e01 = ep[0], e23 = ep[1];
+            const unsigned long long e2[4] = {pack_f32x2(e01.x, e01.y), pack_f32x2(e01.z, e01.w),
+                                              pack_f32x2(e23.x, e23.y), pack_f32x2(e23.z, e23.w)};
+#pragma unroll
+            for (int j = 0; j < kPRows; ++j) {
+              const uint32_t word = (t >> 1) == 0 ? c[j].x : (t >> 1) == 1 ? c[j].y : (t >> 1) == 2 ? c[j].z : c[j].w;
+              const float w = (t & 1) ? bf16_hi(word) : bf16_lo(word);
+              const unsigned long long wd = pack_f32x2(w, w);
+#pragma unroll
+              for (int gp = 0; gp < G / 2; ++gp) acc2[j][gp] = fma_f32x2(wd, e2[gp], acc2[j][gp]);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kPRows; ++j)
+#pragma unroll
+          for (int gp = 0; gp < G / 2; ++gp) unpack_f32x2(acc2[j][gp], acc[j][2 * gp], acc[j][2 * gp + 1]);
+      }
+      pipe_pass(h);
+
+      unsigned long long key[G];
+      float mx[G], sm[G];
+      uint32_t bo[G], bi[G];
+      cp_async_wait_all();  // this thread's logits of the group are in lg_s
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        bo[g] = 0u;
+        bi[g] = 0xffffffffu;
+        mx[g] = -INFINITY;
+        sm[g] = 0.0f;
+        const float4 v = *reinterpret_cast<const float4 *>(&lg_s[(g * kPThreads + ht) * kPRows]);
+        float zv[kPRows] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < kPRows; ++j) {
+          if (biased) zv[j] = __fadd_rn(zv[j], acc[j][g]);
+          acc[j][g] = zv[j];
+        }
+        if (kPRows * ht + kPRows <= nrows) {
+          const float m = fmaxf(fmaxf(zv[0], zv[1]), fmaxf(zv[2], zv[3]));
+          int jj = 0;
+#pragma unroll
+          for (int j = kPRows - 1; j >= 0; --j)
+            if (zv[j] == m) jj = j;
+          if (g < gb) {
+            bo[g] = ordered_bits(m);
+            bi[g] = static_cast<uint32_t>(vrow[0] + jj);
+            if (kStats && m == m && m != -INFINITY) mx[g] = m;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j) {
+            const float z = zv[j];
+            if (valid[j] && g < gb) {
+              const uint32_t o = ordered_bits(z);
+              if (o > bo[g] || bi[g] == 0xffffffffu) {
+                bo[g] = o;
+                bi[g] = static_cast<uint32_t>(vrow[j]);
+              }
+              if (kStats && z == z && z != -INFINITY) mx[g] = fmaxf(mx[g], z);
+            }
+          }
+        }
+        if (kStats) {
+#pragma unroll
+          for (int j = 0; j < kPRows; ++j)
+            if (valid[j] && g < gb && mx[g] != -INFINITY && zv[j] == zv[j] && zv[j] != -INFINITY)
+              sm[g] += __expf(zv[j] - mx[g]);
+        }
+      }
+      // lg_s is consumed: this half's next group (this position's, else the next's)
+      {
+        const int gn = g0 + 2 * G;
+        if (s + 1 < nslots) {
+          if (gn < B) issue_logits_copy<G>(lg_s, a.logits, vrow, vec4, gn, pos, B, k, V, ht);
+        } else if (pos + 1 < k && h * G < B) {
+          issue_logits_copy<G>(lg_s, a.logits, vrow, vec4, h * G, pos + 1, B, k, V, ht);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const uint32_t mo = __reduce_max_sync(0xffffffffu, bo[g]);
+        const uint32_t mi = __reduce_min_sync(0xffffffffu, bo[g] == mo ? bi[g] : 0xffffffffu);
+        key[g] = (static_cast<unsigned long long>(mo) << 32) | (0xffffffffu - mi);
+      }
+      if (kStats) {
+        float mm[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) mm[g] = mx[g];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) mm[g] = fmaxf(mm[g], __shfl_xor_sync(0xffffffffu, mm[g], o));
+#pragma unroll
+        for (int g = 0; g < G; ++g) sm[g] = (mx[g] == -INFINITY) ? 0.0f : __fmul_rn(sm[g], expf(mx[g] - mm[g]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) sm[g] += __shfl_xor_sync(0xffffffffu, sm[g], o);
+#pragma unroll
+        for (int g = 0; g < G; ++g) mx[g] = mm[g];
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g < gb) red[h][g][hw] = ChainPartial{key[g], mx[g], sm[g]};
+      }
+      half_sync(h);
+      // warp w of the half combines request w of the group and publishes its word
+      if (hw < gb) {
+        const int g = hw;
+        unsigned long long kk = 0ull;
+        float m = -INFINITY, sum = 0.0f;
+        if (lane < kPWarps) {
+          const ChainPartial c0 = red[h][g][lane];
+          kk = c0.key;
+          m = c0.m;
+          sum = c0.s;
+        }
+        if (kStats)
+          warp_key_stats(kk, m, sum);
+        else
+          kk = warp_max_u64(kk);
+        if (lane == 0) {
+          const long long at = (static_cast<long long>(pos) * B + g0 + g) * grid + cta;
+          if (kStats) a.partials[at] = ChainPartial{kk, m, sum};
+          const unsigned long long wd = pack_word(kk, word_tag(epoch, pos));
+          if (pos + 1 < k)
+            st_relaxed_u64(a.words + at, wd);
+          else
+            st_release_u64(a.words + at, wd);
+          const int kidx = static_cast<int>(key_index(kk));
+          if (biased && pos + 1 < k && kidx >= 0 && kidx < V)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a.w1 + static_cast<long long>(kidx) * r));
+        }
+      }
+      if (biased) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          if (g < gb)
+            store_row4(a.logits + (static_cast<long long>(g0 + g) * k + pos) * V, vrow, valid, vec4,
+                       acc[0][g], acc[1][g], acc[2][g], acc[3][g]);
+      }
+      half_sync(h);  // red[h] is free again
+    }
+
+    // Wait for every CTA's word of this half's requests at `pos`: warp w of the half
+    // polls request w of each of the half's groups, up to kPollReq at once; the max
+    // of the words is the draft token, whose markov_w1 row the warp then gathers.
+    if (stop_s[h] == 0) {
+      const uint32_t tg = word_tag(epoch, pos);
+      const long long t0 = clock64();
+      for (int s0 = 0; s0 < nslots; s0 += kPollReq) {
+        unsigned long long best[kPollReq];
+        bool done[kPollReq];
+        int req[kPollReq];
+#pragma unroll
+        for (int i = 0; i < kPollReq; ++i) {
+          req[i] = (2 * (s0 + i) + h) * G + hw;
+          best[i] = 0ull;
+          done[i] = s0 + i >= nslots || req[i] >= B;
+        }
+        int stop = 0;
+        while (true) {
+          unsigned long long w[kPollReq][kPollWords];
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const unsigned long long *wb = a.words + (static_cast<long long>(pos) * B + (done[i] ? 0 : req[i])) * grid;
+#pragma unroll
+            for (int c = 0; c < kPollWords; ++c) {
+              const int cc = lane + 32 * c;
+              w[i][c] = (!done[i] && cc < grid) ? ld_relaxed_u64(wb + cc) : 0ull;
+            }
+          }
+          bool all_done = true;
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            if (done[i]) continue;
+            unsigned long long mxw = 0ull;
+            int missing = 0;
+#pragma unroll
+            for (int c = 0; c < kPollWords; ++c) {
+              if (lane + 32 * c < grid) {
+                missing += (static_cast<uint32_t>(w[i][c] >> 58) != tg) ? 1 : 0;
+                mxw = w[i][c] > mxw ? w[i][c] : mxw;
+              }
+            }
+            if (__all_sync(0xffffffffu, missing == 0)) {
+              best[i] = warp_max_u64(mxw);
+              done[i] = true;
+            } else {
+              all_done = false;
+            }
+          }
+          if (all_done) break;
+          int give_up = 0;
+          if (lane == 0)
+            give_up = (ld_relaxed(a.abort_flag) != 0 || clock64() - t0 > a.wait_cycles) ? 1 : 0;
+          if (__shfl_sync(0xffffffffu, give_up, 0)) {
+            if (lane == 0 && atomicExch(a.abort_flag, 1) == 0)
+              record_error(a.status, DSPARK_ERR_DEVICE_TIMEOUT);
+            stop = 1;
+            break;
+          }
+          __nanosleep(20);
+        }
+        if (stop) {
+          if (lane == 0) stop_s[h] = 1;
+          break;
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            if (s0 + i < nslots && req[i] < B) {
+              const int d = word_index(best[i]);
+              prev_s[req[i]] = d;
+              if (cta == 0) a.draft_tokens[static_cast<long long>(req[i]) * k + pos] = d;
+            }
+          }
+        }
+        if (biased && pos + 1 < k) {
+          constexpr int kPerLane = (r + 31) / 32;
+          uint32_t ev[kPollReq][kPerLane];
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const int d = word_index(best[i]);
+            const bool ok = s0 + i < nslots && req[i] < B && d >= 0 && d < V;
+#pragma unroll
+            for (int u = 0; u < kPerLane; ++u) {
+              const int t = lane + 32 * u;
+              ev[i][u] = (ok && t < r) ? static_cast<uint32_t>(a.w1[static_cast<long long>(d) * r + t]) << 16 : 0u;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kPollReq; ++i) {
+            const int b = req[i];
+            if (s0 + i < nslots && b < B) {
+#pragma unroll
+              for (int u = 0; u < kPerLane; ++u) {
+                const int t = lane + 32 * u;
+                if (t < r) e_s[(t * npair4 + (b >> 1)) * 2 + (b & 1)] = __uint_as_float(ev[i][u]);
+              }
+            }
+          }
+        }
+      }
+      if (pos + 1 == k) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    }
+    half_sync(h);
+  }
+  // the pipe's last hand-over (half 1's final chains) completes the barrier sequence
+  if (h == 0) pipe_take(h);
+  cp_async_wait_all();
+  __syncthreads();
+  if (stop_s[0] || stop_s[1]) return;
+
+  if (!kStats && a.draft_len_fill && cta == 0)
+    for (int b = tid; b < B; b += kSThreads) a.draft_len_fill[b] = k;
+  if (kStats) {
+    constexpr int kSWarps = kSThreads / 32;
+    const int warp = tid >> 5;
+    const int pairs = k * B;
+    for (int pr = cta * kSWarps + warp; pr < pairs; pr += grid * kSWarps) {
+      const int pos = pr / B, b = pr - pos * B;
+      const ChainPartial *pb = a.partials + (static_cast<long long>(pos) * B + b) * grid;
+      float mmax = -INFINITY;
+      for (int c = lane; c < grid; c += 32)
+        mmax = fmaxf(mmax, __ldcg(reinterpret_cast<const float *>(pb + c) + 2));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+      double sd = 0.0;
+      if (mmax != -INFINITY) {
+        for (int c = lane; c < grid; c += 32) {
+          const float cm = __ldcg(reinterpret_cast<const float *>(pb + c) + 2);
+          const float cs = __ldcg(reinterpret_cast<const float *>(pb + c) + 3);
+          if (cm != -INFINITY) sd += static_cast<double>(cs) * static_cast<double>(expf(cm - mmax));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+      if (lane == 0) {
+        const long long at = static_cast<long long>(b) * k + pos;
+        if (a.q_stats) {
+          a.q_stats[2 * at] = mmax;
+          a.q_stats[2 * at + 1] = static_cast<float>(sd);
+        }
+        if (a.draft_len_fill && pos == k - 1) a.draft_len_fill[b] = k;
+      }
+    }
+  }
+
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.done, 1) == grid - 1) {
+      *a.done = 0;
+      __threadfence();
+      st_release(a.epoch, epoch + 1);
+    }
+  }
+}
+
 // c[b, i] = sigmoid(zc[b, i]), zc = w . h[b*k+i] (+ w_m . markov_w1[ctx_i] when the head
 // sees the Markov context) + bias; draft_len[b] = first i that fails the truncation rule
 // (per position: zc < thr = logit(tau); cumulative: the running sum of log sigmoid(zc)
@@ -1111,31 +1572,16 @@ size_t chain_workspace_size(int B, int k, int V) {
 
 namespace {
 
-template <int G, int CPR, bool kStats, bool kW2Smem>
-bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
-  const int sms = device_sm_count();
-  if (sms <= 0) return false;
-  int grid = sms < kMaxPGrid ? sms : kMaxPGrid;
-  const int by_rows = (V + 255) / 256;
-  if (grid > by_rows) grid = by_rows;
-  // slices of a multiple of kPRows rows (a thread's rows stay within one 16-byte run)
-  const int rows = ((V + grid - 1) / grid + kPRows - 1) / kPRows * kPRows;
-  if (rows > kPRows * kPThreads) return false;
-  ChainPArgs a = args0;
-  a.rows_per_cta = rows;
-  a.vec = ((V % kPRows) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
-  a.w2_smem_bytes =
-      kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
-  const size_t smem = static_cast<size_t>(a.w2_smem_bytes) +
-                      static_cast<size_t>((B + 1) & ~1) * CPR * 32 +
-                      ((static_cast<size_t>(B) * sizeof(int) + 15) & ~static_cast<size_t>(15)) +
-                      (G >= 8 ? static_cast<size_t>(G) * kPRows * kPThreads * sizeof(float) : 0);
-  if (smem > kPSmemMax) return false;
-  auto kern = markov_chain_persistent<G, CPR, kStats, kW2Smem>;
-  // The opt-in dynamic shared memory this launch needs (the kernel's static shared
-  // memory plus the dynamic part must stay within the per-CTA limit, so the attribute
-  // is raised to what is needed, not to a fixed maximum).
-  static size_t attr_bytes[64] = {};
+// Cooperative launch of a persistent chain kernel (all CTAs resident together: they
+// wait on each other), with programmatic dependent launch when enabled (without it if
+// the combination is refused).  The opt-in dynamic shared memory is raised to what
+// this launch needs (the kernel's static shared memory plus the dynamic part must
+// stay within the per-CTA limit, so not to a fixed maximum).
+// attr_bytes: the attribute already set per device, one table per kernel (the caller's
+// static: every chain kernel has the same function type).
+template <typename Kern>
+bool launch_chain_coop(Kern kern, size_t (&attr_bytes)[64], int grid, int threads, size_t smem,
+                       const ChainPArgs &a, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (attr_bytes[dev] < smem) {
@@ -1146,13 +1592,10 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
     }
     attr_bytes[dev] = smem;
   }
-  // Cooperative (all CTAs resident together: they wait on each other), and, when
-  // enabled, with programmatic dependent launch; without the latter if the
-  // combination is refused.
   if (pdl_enabled()) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kPThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -1166,12 +1609,71 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
     cudaGetLastError();
   }
   void *params[] = {const_cast<ChainPArgs *>(&a)};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid),
-                                  dim3(kPThreads), params, smem, stream) != cudaSuccess) {
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(threads),
+                                  params, smem, stream) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   return true;
+}
+
+// Grid and slice of the persistent chains: one CTA per SM (at most kMaxPGrid), at
+// least 256 rows per CTA, slices a multiple of kPRows rows; false if a slice would
+// exceed kPRows x kPThreads rows.
+bool chain_grid(int V, int &grid, int &rows) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  grid = sms < kMaxPGrid ? sms : kMaxPGrid;
+  const int by_rows = (V + 255) / 256;
+  if (grid > by_rows) grid = by_rows;
+  rows = ((V + grid - 1) / grid + kPRows - 1) / kPRows * kPRows;
+  return rows <= kPRows * kPThreads;
+}
+
+template <int G, int CPR, bool kStats, bool kW2Smem>
+bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
+  int grid = 0, rows = 0;
+  if (!chain_grid(V, grid, rows)) return false;
+  ChainPArgs a = args0;
+  a.rows_per_cta = rows;
+  a.vec = ((V % kPRows) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
+  a.w2_smem_bytes =
+      kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
+  const size_t smem = static_cast<size_t>(a.w2_smem_bytes) +
+                      static_cast<size_t>((B + 1) & ~1) * CPR * 32 +
+                      ((static_cast<size_t>(B) * sizeof(int) + 15) & ~static_cast<size_t>(15)) +
+                      (G >= 8 ? static_cast<size_t>(G) * kPRows * kPThreads * sizeof(float) : 0);
+  if (smem > kPSmemMax) return false;
+  static size_t attr_bytes[64] = {};
+  return launch_chain_coop(markov_chain_persistent<G, CPR, kStats, kW2Smem>, attr_bytes, grid, kPThreads,
+                           smem, a, stream);
+}
+
+template <int CPR, bool kStats>
+bool try_split_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
+  int grid = 0, rows = 0;
+  if (!chain_grid(V, grid, rows)) return false;
+  ChainPArgs a = args0;
+  a.rows_per_cta = rows;
+  a.vec = ((V % kPRows) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
+  a.w2_smem_bytes = static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024));
+  const size_t npair4 = static_cast<size_t>(((B + 1) / 2 + 3) & ~3);
+  const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + npair4 * CPR * 64 +
+                      ((static_cast<size_t>(B) * sizeof(int) + 15) & ~static_cast<size_t>(15)) +
+                      2 * static_cast<size_t>(kSGroup) * kPRows * kPThreads * sizeof(float);
+  if (smem > kPSmemMax) return false;
+  static size_t attr_bytes[64] = {};
+  return launch_chain_coop(markov_chain_split<CPR, kStats>, attr_bytes, grid, kSThreads, smem, a, stream);
+}
+
+template <bool kStats>
+bool try_split_s(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
+  switch (r) {
+    case 16: return try_split_r<2, kStats>(a, B, V, stream);
+    case 32: return try_split_r<4, kStats>(a, B, V, stream);
+    case 64: return try_split_r<8, kStats>(a, B, V, stream);
+    default: return false;
+  }
 }
 
 template <int G, bool kStats>
@@ -1234,7 +1736,16 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
     const long long v = atoll(wc);
     if (v >= 0) pa.wait_cycles = v;
   }
+  // Batches of more than 8 requests at r <= 64: the two-halves kernel, unless
+  // DSPARK_CHAIN_SPLIT=0 (same results).
+  const char *senv = getenv("DSPARK_CHAIN_SPLIT");
+  const bool split = !per_position && B > 8 && !(senv && senv[0] == '0');
+  bool split_ok = false;
+  if (split)
+    split_ok = pa.q_stats ? try_split_s<true>(pa, pa.r, B, V, stream)
+                          : try_split_s<false>(pa, pa.r, B, V, stream);
   const bool ok = per_position ? false
+                  : split_ok ? true
                   : B >= 8 ? try_persistent<8>(pa, pa.r, B, V, stream)
                   : B >= 4 ? try_persistent<4>(pa, pa.r, B, V, stream)
                   : B >= 2 ? try_persistent<2>(pa, pa.r, B, V, stream)

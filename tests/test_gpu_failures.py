@@ -94,12 +94,13 @@ def test_draft_len_out_of_range_is_recorded():
     np.testing.assert_array_equal(host(n), ref["next_token"])
 
 
-def test_chain_wait_timeout_is_recorded_and_the_context_survives():
-    B, k, V, r = 2, 7, 151936, 64
+@pytest.mark.parametrize("B", [2, 16])   # 16: the two-halves kernel
+def test_chain_wait_timeout_is_recorded_and_the_context_survives(B):
+    k, V, r = 7, 151936, 64
     logits = syn.uniform_logits(51, (B, k, V), 1.0)
     w1 = dev_bf16(syn.normal_bf16(52, (V, r)))
     w2 = dev_bf16(syn.normal_bf16(53, (V, r), 0.125))
-    prev = dev(np.array([5, 6], np.int32))
+    prev = dev((np.arange(B) * 7 + 5).astype(np.int32))
     old = os.environ.get("DSPARK_CHAIN_WAIT_CYCLES")
     seen = []
     try:
@@ -123,5 +124,5 @@ def test_chain_wait_timeout_is_recorded_and_the_context_survives():
     d, _ = ds.greedy_sample(lg, w1, w2, prev, workspaces=wsp)
     assert _status(wsp, "chain") == OK
     ref = oracle.greedy_sample(logits, syn.normal_bf16(52, (V, r)), syn.normal_bf16(53, (V, r), 0.125),
-                               np.array([5, 6], np.int32))
+                               (np.arange(B) * 7 + 5).astype(np.int32))
     np.testing.assert_array_equal(host(d), ref["draft_tokens"])

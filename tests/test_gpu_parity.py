@@ -176,6 +176,35 @@ def test_greedy_sample_without_q_stats_bit_exact(B, k, V, r):
     np.testing.assert_array_equal(host(lg), ref["z"])
 
 
+# Batches above 8 requests (r <= 64) run the two-halves chain: request groups of 8
+# alternate between two halves of the CTA on the FMA pipe.  Cases: a group slot left
+# empty in one half (24, 40 requests), a partial group with an odd request pair (17,
+# 33), and V = 38913, where the last two of 152 CTAs (260-row slices) own no rows.
+@pytest.mark.parametrize("B,k,V,r,stats", [(17, 3, 38913, 16, True), (24, 4, 20000, 64, False),
+                                           (40, 3, 38913, 32, False), (33, 2, 4099, 64, True),
+                                           (1, 3, 38913, 16, True), (16, 2, 38913, 64, False)])
+def test_greedy_sample_two_halves_kernel(B, k, V, r, stats, monkeypatch):
+    logits = syn.uniform_logits(51 + V + B, (B, k, V), 1.5)
+    w1 = syn.normal_bf16(52, (V, r))
+    w2 = syn.normal_bf16(53, (V, r), (1.0 / r) ** 0.5)
+    prev = (np.arange(B, dtype=np.int64) * 7919 % V).astype(np.int32)
+    ref = oracle.greedy_sample(logits, w1, w2, prev)
+    outs = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("DSPARK_CHAIN_SPLIT", flag)
+        lg = dev(logits)
+        d, qs = ds.greedy_sample(lg, dev_bf16(w1), dev_bf16(w2), dev(prev), want_q_stats=stats)
+        outs.append((host(d), host(lg), None if qs is None else host(qs)))
+    for d, z, q in outs:
+        np.testing.assert_array_equal(d, ref["draft_tokens"])
+        np.testing.assert_array_equal(z, ref["z"])
+        if stats:
+            np.testing.assert_array_equal(q[..., 0], ref["q_max"].astype(np.float32))
+            np.testing.assert_allclose(q[..., 1], ref["q_sumexp"], rtol=1e-5)
+    if stats:
+        np.testing.assert_array_equal(outs[0][2], outs[1][2])
+
+
 def test_greedy_sample_per_position_kernels_agree(monkeypatch):
     """The per-position kernels (used when a cooperative launch is not possible) give
     the same bits as the persistent kernel and the oracle."""
