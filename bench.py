@@ -163,14 +163,37 @@ def step_bytes(cfg, mode):
         lm = V * H * 2 + M * H * 2 + M * V * 4
     chain = V * r * 2
     verify = B * (k + 1) * V * 4 + (B * 2 * V * 4 if mode == 1 else 0)
-    return {"fc": fc, "lm_head": lm, "chain": chain, "verify": verify,
-            "total": fc + lm + chain + verify}
+    bb = backbone_bytes(cfg)
+    return {"fc": fc, "backbone": bb, "lm_head": lm, "chain": chain, "verify": verify,
+            "total": fc + bb + lm + chain + verify}
+
+
+def backbone_bytes(cfg):
+    """Drafter backbone: each layer's weights once, its key/value cache read once (the
+    C context rows and the k + 1 block rows), the block's embedding rows."""
+    if not cfg.get("backbone"):
+        return 0
+    B, k, H = cfg["B"], cfg["k"], cfg["H"]
+    g, L, C = syn.BACKBONE_GEOMETRY[H], cfg["backbone"]["L"], cfg["backbone"]["C"]
+    nq, nkv, I = g["nq"], g["nkv"], g["I"]
+    weights = ((nq + 2 * nkv) * 128 * H + H * nq * 128 + 2 * I * H + H * I + 2 * H + 256) * 2
+    cache = B * (C + k + 1) * nkv * 128 * 2 * 2
+    return L * (weights + cache) + B * (k + 1) * H * 2
 
 
 def step_flops(cfg):
     B, k, H, T, V, r = (cfg[x] for x in ("B", "k", "H", "T", "V", "r"))
     M = B * k
-    return 2 * M * (T * H * H + V * H + V * r)
+    f = 2 * M * (T * H * H + V * H + V * r)
+    if cfg.get("backbone"):
+        g, L, C = syn.BACKBONE_GEOMETRY[H], cfg["backbone"]["L"], cfg["backbone"]["C"]
+        nq, nkv, I = g["nq"], g["nkv"], g["I"]
+        rows = B * (k + 1)
+        per_layer = (2 * rows * ((nq + 2 * nkv) * 128 * H + H * nq * 128 + 3 * I * H)
+                     + 2 * M * 2 * nkv * 128 * H                        # the context rows' K/V
+                     + 4 * rows * nq * 128 * (C + k + 1))               # scores and P.V
+        f += L * per_layer
+    return f
 
 
 class ClockSampler:
@@ -389,14 +412,40 @@ class Pipeline:
         self.logits = torch.empty((B, k, V), dtype=f32, device=device)
         self.drafts = torch.empty((B, k), dtype=i32, device=device)
         self.q_stats = torch.empty((B, k, 2), dtype=f32, device=device) if mode == 1 else None
+        # drafter backbone (N1): the fc output becomes the context rows; the block
+        # (the previous token, then k mask tokens) runs through the layers into hb
+        self.bb = w.get("bb_layers")
+        if self.bb:
+            self.C = cfg["backbone"]["C"]
+            self.tokens = torch.full((B, k + 1), V - 1, dtype=i32, device=device)
+            self.hb = torch.empty((M, H), dtype=torch.bfloat16, device=device)
         self.wsp = ds.Workspaces()          # drafting calls
         self.wsp_v = ds.Workspaces()        # verify calls (may run beside the next drafting)
 
     def chain_q(self):
         return self.mode == 1 and self.q_in == "chain"
 
+    def stage_names(self):
+        """The stages between consecutive timing events of a step."""
+        if self.fused:
+            return ["fc_lm_head", "(none)", "greedy_sample", "verify"]
+        if self.bb:
+            return ["fc_project", "backbone", "lm_head", "greedy_sample", "verify"]
+        return ["fc_project", "lm_head", "greedy_sample", "verify"]
+
+    def backbone(self, prev, s):
+        """The fc output (self.h) as the newest k context rows of every layer's cache,
+        then the block through the layers; returns the LM head's input."""
+        ds, w, k = self.ds, self.w, self.cfg["k"]
+        ds.backbone_context(self.h, self.bb, w["bb_kc"], w["bb_vc"], self.C - k, stream=s, workspaces=self.wsp)
+        with self.torch.cuda.stream(s):
+            self.tokens[:, 0].copy_(prev)
+        return ds.backbone_block(self.tokens, w["lm_w"], self.bb, w["bb_final"], w["bb_kc"], w["bb_vc"], self.C,
+                                 out=self.hb, stream=s, workspaces=self.wsp)
+
     def draft(self, st, s, hist, ev=None, chain_after=None):
-        """ev: 4 timing events on s (start, after fc, after LM head, after chain).
+        """ev: timing events on s at the stage boundaries (start, after fc, [after the
+        backbone,] after LM head, after chain; one more for verify).
         chain_after: an event the chain waits for (the previous step's verify)."""
         ds, w, cfg = self.ds, self.w, self.cfg
         B, k, V = cfg["B"], cfg["k"], cfg["V"]
@@ -416,23 +465,28 @@ class Pipeline:
                 ds.fc_project(st["taps"], w["fc_w"], out=self.h, stream=s, workspaces=self.wsp)
             if ev is not None:
                 ev[1].record(s)
+            h_lm = self.h
+            if self.bb:
+                h_lm = self.backbone(st["prev"], s)
+                if ev is not None:
+                    ev[2].record(s)
             if self.fp8:
-                ds.lm_head_fp8(self.h, w["lm_w8"], w["lm_s"], out=self.logits.view(M, V), stream=s,
+                ds.lm_head_fp8(h_lm, w["lm_w8"], w["lm_s"], out=self.logits.view(M, V), stream=s,
                                workspaces=self.wsp)
             else:
-                ds.lm_head(self.h, w["lm_w"], out=self.logits.view(M, V), stream=s, workspaces=self.wsp)
+                ds.lm_head(h_lm, w["lm_w"], out=self.logits.view(M, V), stream=s, workspaces=self.wsp)
         if ev is not None:
-            ev[2].record(s)
+            ev[-3].record(s)
         if chain_after is not None:
             s.wait_event(chain_after)
         ds.greedy_sample(self.logits, w["w1"], w["w2"], st["prev"], draft_tokens=self.drafts,
                          q_stats=self.q_stats if self.chain_q() else None, want_q_stats=self.chain_q(),
                          stream=s, workspaces=self.wsp)
         if w.get("conf_w") is not None:
-            ds.confidence_truncate(self.h, w["conf_w"], self.drafts, B, k, 0.0, 0.5,
+            ds.confidence_truncate(self.hb if self.bb else self.h, w["conf_w"], self.drafts, B, k, 0.0, 0.5,
                                    draft_len=dlen_o, stream=s)
         if ev is not None:
-            ev[3].record(s)
+            ev[-2].record(s)
 
     def verify(self, st, s, hist, step_id, ev=None):
         acc_o, nxt_o, dlen_o = hist
@@ -447,7 +501,7 @@ class Pipeline:
     def step(self, st, s, hist, step_id, ev=None):
         """A serial step: draft and verify on stream s (ev: 5 timing events)."""
         self.draft(st, s, hist, ev)
-        self.verify(st, s, hist, step_id, ev[4] if ev is not None else None)
+        self.verify(st, s, hist, step_id, ev[-1] if ev is not None else None)
 
 
 def load_weights(ds, torch, device, cfg, host_cache):
@@ -471,6 +525,21 @@ def load_weights(ds, torch, device, cfg, host_cache):
         del fc_w, lm_w
     else:
         w["fc_w"], w["lm_w"] = fc_w, lm_w
+    if cfg.get("backbone"):
+        bbc, g = cfg["backbone"], syn.BACKBONE_GEOMETRY[H]
+        bkey = ("backbone", H, bbc["L"])
+        if bkey not in host_cache:
+            host_cache[bkey] = syn.backbone_weights(H, g["nq"], g["nkv"], g["I"], bbc["L"])
+        layers, wf = host_cache[bkey]
+        w["bb_layers"] = [ds.BackboneLayer(l["nq"], l["nkv"], *[d16(l[x]) for x in (
+            "w_in", "w_post", "w_qn", "w_kn", "w_qkv", "w_o", "w_gu", "w_d")]) for l in layers]
+        w["bb_final"] = d16(wf)
+        # each layer's key/value cache: a synthetic context of C tokens (unit-scale keys
+        # and values, as the k-norm leaves them), then room for the k + 1 block rows;
+        # every step writes its k new context rows over the newest k context slots
+        shape = (cfg["B"], bbc["C"] + cfg["k"] + 1, g["nkv"], 128)
+        w["bb_kc"] = [d16(syn.normal_bf16(900 + li, shape)) for li in range(bbc["L"])]
+        w["bb_vc"] = [d16(syn.normal_bf16(950 + li, shape)) for li in range(bbc["L"])]
     return w
 
 
@@ -518,6 +587,9 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
             lg = ds.lm_head_fp8(h, w["lm_w8"], w["lm_s"]).view(B, k, V)
         else:
             h = ds.fc_project(dev_set["taps"], w["fc_w"])
+            if pipe.bb:
+                pipe.h.copy_(h)
+                h = pipe.backbone(dev_set["prev"], stream).clone()
             lg = ds.lm_head(h, w["lm_w"]).view(B, k, V)
         ds.greedy_sample(lg, w["w1"], w["w2"], dev_set["prev"], want_q_stats=False)
         noise = torch.from_numpy(st["noise"]).to(device)
@@ -598,7 +670,8 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
                 staged = []
                 for st in sets:
                     g = torch.cuda.CUDAGraph()
-                    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+                    ev = [torch.cuda.Event(enable_timing=True, external=True)
+                          for _ in range(len(pipe.stage_names()) + 1)]
                     with torch.cuda.graph(g, stream=cap):
                         pipe.step(st, cap, ghist, 0, ev=ev)
                     staged.append((g, ev))
@@ -668,8 +741,7 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
 
     # per-stage times: replays of the serial graphs with timing events (passes over all
     # input sets, back to back, read after each pass); else the un-captured loop
-    stage_names = ["fc_lm_head", "(none)", "greedy_sample", "verify"] if pipe.fused \
-        else ["fc_project", "lm_head", "greedy_sample", "verify"]
+    stage_names = pipe.stage_names()
     samples = {nm: [] for nm in stage_names}
     samples["step"] = []
     if staged is not None:
@@ -682,18 +754,18 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
             for _, ev in staged:
                 for j, nm in enumerate(stage_names):
                     samples[nm].append(ev[j].elapsed_time(ev[j + 1]))
-                samples["step"].append(ev[0].elapsed_time(ev[4]))
+                samples["step"].append(ev[0].elapsed_time(ev[-1]))
             if time.perf_counter() - t_s > 5.0:
                 break
     else:
         stage_src = "un-captured serial loop with CUDA events (host launch cost included)"
         for i in range(K):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
             pipe.step(sets[i % nsets], stream, hist(i), i, ev=ev)
             torch.cuda.synchronize()
             for j, nm in enumerate(stage_names):
                 samples[nm].append(ev[j].elapsed_time(ev[j + 1]))
-            samples["step"].append(ev[0].elapsed_time(ev[4]))
+            samples["step"].append(ev[0].elapsed_time(ev[-1]))
     stage_ms = {nm: statistics.median(v) for nm, v in samples.items() if v and nm != "(none)"}
     lm_ms = stage_ms["fc_lm_head"] if pipe.fused else stage_ms["lm_head"]
 
@@ -753,11 +825,11 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     lm_bytes = sb["fc"] + sb["lm_head"] if pipe.fused else sb["lm_head"]
     achieved = lm_bytes / (lm_ms / 1000.0) / 1e9
     t_roof = max(sb["total"] / (peak_gbs * 1e9), step_flops(cfg) / (peak_tf * 1e12))
-    t_readout = max((sb["fc"] + sb["lm_head"] + sb["chain"]) / (peak_gbs * 1e9),
+    t_readout = max((sb["fc"] + sb["backbone"] + sb["lm_head"] + sb["chain"]) / (peak_gbs * 1e9),
                     step_flops(cfg) / (peak_tf * 1e12))
     t_verify = sb["verify"] / (peak_gbs * 1e9)
     readout_ms = ((stage_ms["fc_lm_head"] if pipe.fused else stage_ms["fc_project"] + stage_ms["lm_head"])
-                  + stage_ms["greedy_sample"])
+                  + stage_ms.get("backbone", 0.0) + stage_ms["greedy_sample"])
     traffic_file = "gemm_tcgen05_fc_lm_head" if pipe.fused else "gemm_tcgen05_lm_head"
     traffic = profiled_traffic(name, traffic_file)
     step_roof = {"bytes": sb["total"], "flops": step_flops(cfg), "t_roofline_ms": t_roof * 1000.0,
@@ -774,7 +846,7 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if pipe.fp8 else "bf16",
         "data": "synthetic",
         "config": config_of(name, cfg, mode, args, world, nsets, set_bytes, l2,
-                            weights_bytes=sb["fc"] + sb["lm_head"]),
+                            weights_bytes=sb["fc"] + sb["backbone"] + sb["lm_head"]),
         "drafted_tok_s": steps_per_s * drafted,
         "accepted_tok_s": steps_per_s * B * mean_acc_len,
         "mean_acceptance_length": mean_acc_len,
@@ -812,6 +884,8 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
         "clocks": clk,
     }
 
+    if cfg.get("backbone"):
+        with_cpu_baseline = False   # the C oracle's step has no backbone layers
     if with_cpu_baseline and rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle as ora
         hw = host_cache[(H, T, V, r)]
@@ -837,6 +911,10 @@ def config_of(name, cfg, mode, args, world, nsets=None, set_bytes=None, l2=None,
          "confidence_head": bool(cfg["conf"]),
          "weights": "e4m3 codes + fp32 row scales (fc, LM head)" if cfg.get("fp8") else "bf16",
          "parallelism": "replicas%d" % world}
+    if cfg.get("backbone"):
+        g = syn.BACKBONE_GEOMETRY[cfg["H"]]
+        c["backbone"] = {"layers": cfg["backbone"]["L"], "context": cfg["backbone"]["C"], "q_heads": g["nq"],
+                         "kv_heads": g["nkv"], "head_dim": 128, "mlp": g["I"]}
     if nsets is not None:
         c["q_stats_in"] = args.q_stats
         c["l2"] = ("inputs larger than L2: %.2f GB of weights streamed per step; %d input sets of "

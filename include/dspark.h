@@ -431,6 +431,84 @@ dspark_status_t dspark_lm_head_fp8(const dspark_bf16_t *h, const uint8_t *lm_w8,
                                    const float *lm_scale, float *logits, int M, int H, int V,
                                    void *ws, size_t ws_bytes, void *stream);
 
+/* ========================================================================
+ * Drafter backbone (N1).  The pages name the drafter class ([PR620]
+ * "DSparkDraftModel(DFlashQwen3ForCausalLM)", "the DFlash backbone"; [CARD]
+ * "Qwen3DSparkModel selects the Qwen3 implementation") and its config fields
+ * (layer_types, head_dim, mask_token_id, projector_type) without a forward
+ * pass.  The reading built here: L pre-norm decoder layers of the Qwen3 form run
+ * the draft block (the anchor token, then k mask tokens) over the fc'd context:
+ *   n = rmsnorm(x); q,k,v = n.[Wq;Wk;Wv]^T; per-head rmsnorm of q, k; rotary
+ *   (NeoX, theta); o = attention over [context keys; block keys]; x += o.Wo^T;
+ *   n2 = rmsnorm(x); x += (silu(n2.Wg^T) * n2.Wu^T).Wd^T
+ * and the final rmsnorm of the mask positions is the LM head's input.  The
+ * projections are dspark_linear; the calls below are the pieces between them.
+ * head_dim is 128.  rmsnorm(x) = x / sqrt(mean(x^2) + 1e-6) * w; all arithmetic
+ * fp32, bf16 outputs rounded to nearest even.  Rows are 16-byte aligned with row
+ * strides (ld) a multiple of 8 elements.  Device-side errors: only a token
+ * outside [0, V) in dspark_embed_rmsnorm (recorded in the optional status word,
+ * the token clamped).  None of these calls allocates; all enqueue on `stream`.
+ * ======================================================================== */
+
+/* out[m, n] = sum_k x[m, k] * w[n, k]: the tcgen05 GEMM of the fc and LM head
+ * with one activation segment.  x [M, K] bf16 (row stride x_ld), w [N, K] bf16,
+ * out [M, N] (row stride out_ld) bf16 when out_bf16, else fp32.  K % 64 == 0.
+ * Workspace: dspark_linear_workspace_size bytes, 256-byte aligned, zeroed before
+ * its first use; calls sharing one workspace must be ordered on the GPU. */
+size_t dspark_linear_workspace_size(int M, int N, int K);
+dspark_status_t dspark_linear(const dspark_bf16_t *x, int64_t x_ld, const dspark_bf16_t *w, void *out,
+                              int64_t out_ld, int out_bf16, int M, int N, int K, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* The block's inputs: x_out[r, :] = table[tokens[r], :] (fp32 residual, [rows, H])
+ * and n_out[r, :] = bf16(rmsnorm(x_out[r, :]) * w) ([rows, H]).  table [V, H] bf16
+ * (the LM head's weight: tied embeddings).  H % 8 == 0, H <= 8192. */
+dspark_status_t dspark_embed_rmsnorm(const dspark_bf16_t *table, int V, const int32_t *tokens,
+                                     const dspark_bf16_t *w, float *x_out, dspark_bf16_t *n_out, int rows,
+                                     int H, int32_t *status, void *stream);
+
+/* Residual add and norm: x[r, :] += delta[r, :] (fp32 add of the bf16 delta;
+ * delta may be NULL), then out = bf16(rmsnorm(x[r, :]) * w).  group > 0: rows come
+ * in groups of `group` (a request's block); the first row of each group (the
+ * anchor) is not written and the others are stored compacted, row
+ * (r / group) * (group - 1) + r % group - 1 (the final norm feeding the LM head). */
+dspark_status_t dspark_add_rmsnorm(float *x, const dspark_bf16_t *delta, int64_t delta_ld,
+                                   const dspark_bf16_t *w, dspark_bf16_t *out, int64_t out_ld, int group,
+                                   int rows, int H, void *stream);
+
+/* out = bf16(rmsnorm(in) * w) of bf16 rows (the context features' input norm). */
+dspark_status_t dspark_rmsnorm_bf16(const dspark_bf16_t *in, int64_t in_ld, const dspark_bf16_t *w,
+                                    dspark_bf16_t *out, int64_t out_ld, int rows, int H, void *stream);
+
+/* Per-head q/k norm and rotary embedding, into the attention buffers.  Row r of
+ * qkv (B * rows_per_req rows, stride ld) holds [q heads (nq x 128, absent when
+ * nq == 0) | k heads (nkv x 128) | v heads (nkv x 128)]; it belongs to request
+ * r / rows_per_req at position p = pos0 + r % rows_per_req.  Each q and k head:
+ * y = rmsnorm(head) * norm_w, then (y1, y2) -> (y1 cos - y2 sin, y2 cos + y1 sin)
+ * with y1 = dims 0..63, y2 = dims 64..127 and angle p * theta^(-2d/128).  q goes to
+ * q_out [B * rows_per_req, nq, 128]; k and v go to slot p of the caches
+ * k_cache, v_cache [B, cache_len, nkv, 128] (bf16).  pos0 + rows_per_req <= cache_len. */
+dspark_status_t dspark_qk_norm_rope(const dspark_bf16_t *qkv, int64_t ld, int nq, int nkv,
+                                    const dspark_bf16_t *q_norm_w, const dspark_bf16_t *k_norm_w, float theta,
+                                    dspark_bf16_t *q_out, dspark_bf16_t *k_cache, dspark_bf16_t *v_cache, int B,
+                                    int cache_len, int rows_per_req, int pos0, void *stream);
+
+/* Grouped-query attention of the block rows over the cache:
+ *   out[b, i, j, :] = sum_t softmax_t(q[b, i, j, :] . K[b, t, j / (nq/nkv), :] / sqrt(128))
+ *                     * V[b, t, j / (nq/nkv), :],   t = 0 .. nkeys - 1
+ * q, out [B, nr, nq, 128] bf16; caches [B, cache_len, nkv, 128] bf16.  No mask:
+ * every block row sees every key below nkeys.  nr * nq / nkv <= 48.  Two kernels
+ * (64-key slices, then the merge); workspace dspark_attention_workspace_size bytes
+ * (no zeroing needed). */
+size_t dspark_attention_workspace_size(int B, int nr, int nq, int nkv, int nkeys);
+dspark_status_t dspark_attention(const dspark_bf16_t *q, const dspark_bf16_t *k_cache,
+                                 const dspark_bf16_t *v_cache, dspark_bf16_t *out, int B, int nr, int nq,
+                                 int nkv, int cache_len, int nkeys, void *ws, size_t ws_bytes, void *stream);
+
+/* act[m, c] = bf16(silu(gu[m, c]) * gu[m, I + c]), silu(g) = g / (1 + e^-g);
+ * gu [M, 2I] bf16 (the gate|up GEMM output), act [M, I].  I % 8 == 0. */
+dspark_status_t dspark_silu_mul(const dspark_bf16_t *gu, dspark_bf16_t *act, int M, int I, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

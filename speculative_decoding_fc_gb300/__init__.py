@@ -23,7 +23,8 @@ import torch
 __all__ = ["DSparkError", "lib", "fc_project", "lm_head", "greedy_sample", "confidence_truncate",
            "draft_readout", "confidence_truncate_markov", "quantize_fp8", "fc_project_fp8", "lm_head_fp8", "fc_lm_head",
            "verify", "row_stats", "verify_from_stats", "workspace_status", "launch_count",
-           "Workspaces", "library_path"]
+           "Workspaces", "library_path", "linear", "embed_rmsnorm", "add_rmsnorm", "rmsnorm_bf16",
+           "qk_norm_rope", "attention", "silu_mul", "BackboneLayer", "backbone_context", "backbone_block"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libdspark.so")
@@ -125,6 +126,26 @@ def lib():
         L.dspark_lm_head_fp8.restype = ctypes.c_int
         L.dspark_lm_head_fp8.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, _vp, _sz, _vp]
+        _c = ctypes.c_int
+        L.dspark_linear_workspace_size.restype = _sz
+        L.dspark_linear_workspace_size.argtypes = [_c] * 3
+        L.dspark_linear.restype = _c
+        L.dspark_linear.argtypes = [_vp, _i64, _vp, _vp, _i64, _c, _c, _c, _c, _vp, _sz, _vp]
+        L.dspark_embed_rmsnorm.restype = _c
+        L.dspark_embed_rmsnorm.argtypes = [_vp, _c, _vp, _vp, _vp, _vp, _c, _c, _vp, _vp]
+        L.dspark_add_rmsnorm.restype = _c
+        L.dspark_add_rmsnorm.argtypes = [_vp, _vp, _i64, _vp, _vp, _i64, _c, _c, _c, _vp]
+        L.dspark_rmsnorm_bf16.restype = _c
+        L.dspark_rmsnorm_bf16.argtypes = [_vp, _i64, _vp, _vp, _i64, _c, _c, _vp]
+        L.dspark_qk_norm_rope.restype = _c
+        L.dspark_qk_norm_rope.argtypes = [_vp, _i64, _c, _c, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
+                                          _c, _c, _c, _c, _vp]
+        L.dspark_attention_workspace_size.restype = _sz
+        L.dspark_attention_workspace_size.argtypes = [_c] * 5
+        L.dspark_attention.restype = _c
+        L.dspark_attention.argtypes = [_vp, _vp, _vp, _vp, _c, _c, _c, _c, _c, _c, _vp, _sz, _vp]
+        L.dspark_silu_mul.restype = _c
+        L.dspark_silu_mul.argtypes = [_vp, _vp, _c, _c, _vp]
         _lib = L
     return _lib
 
@@ -586,3 +607,194 @@ def lm_head_fp8(h, lm_w8, lm_scale, out=None, stream=None, workspaces=None):
                                 _ptr(ws), ws.numel(), _stream(stream, h.device)),
            "dspark_lm_head_fp8")
     return out
+
+
+# ----------------------------------------------------------------------------- backbone
+def linear(x, w, out=None, out_bf16=True, stream=None, workspaces=None, kind="linear"):
+    """out[M, N] = x[M, K] . w[N, K]^T (bf16 in, fp32 accumulate; bf16 or fp32 out).
+    `kind` names the workspace (calls of different shapes keep separate ones)."""
+    M, K = x.shape
+    N = w.shape[0]
+    dev = w.device
+    _need(w, "w", torch.bfloat16, (N, K))
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.stride(1) != 1:
+        raise ValueError("x must be a CUDA bf16 [M, K] tensor with unit column stride")
+    odt = torch.bfloat16 if out_bf16 else torch.float32
+    if out is None:
+        out = torch.empty((M, N), dtype=odt, device=dev)
+    if out.dtype != odt or tuple(out.shape) != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be %s [%d, %d] with unit column stride" % (odt, M, N))
+    L = lib()
+    ws = (workspaces or _default_ws).get(kind, dev, L.dspark_linear_workspace_size(M, N, K))
+    _check(L.dspark_linear(_ptr(x), x.stride(0), _ptr(w), _ptr(out), out.stride(0), 1 if out_bf16 else 0,
+                           M, N, K, _ptr(ws), ws.numel(), _stream(stream, dev)), "dspark_linear")
+    return out
+
+
+def embed_rmsnorm(table, tokens, w, x_out=None, n_out=None, status=None, stream=None):
+    """x_out = table[tokens] (fp32 [rows, H]); n_out = bf16(rmsnorm(x_out) * w)."""
+    V, H = table.shape
+    rows = tokens.numel()
+    dev = table.device
+    _need(table, "table", torch.bfloat16)
+    _need(tokens, "tokens", torch.int32)
+    _need(w, "w", torch.bfloat16, (H,))
+    if x_out is None:
+        x_out = torch.empty((rows, H), dtype=torch.float32, device=dev)
+    if n_out is None:
+        n_out = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    _need(x_out, "x_out", torch.float32, (rows, H))
+    _need(n_out, "n_out", torch.bfloat16, (rows, H))
+    _check(lib().dspark_embed_rmsnorm(_ptr(table), V, _ptr(tokens), _ptr(w), _ptr(x_out), _ptr(n_out), rows, H,
+                                      _ptr(status), _stream(stream, dev)), "dspark_embed_rmsnorm")
+    return x_out, n_out
+
+
+def add_rmsnorm(x, delta, w, out=None, group=0, stream=None):
+    """x += delta (fp32 add of bf16, delta may be None); out = bf16(rmsnorm(x) * w).
+    group > 0: the first row of every group is not written, the others compacted."""
+    rows, H = x.shape
+    dev = x.device
+    _need(x, "x", torch.float32)
+    _need(w, "w", torch.bfloat16, (H,))
+    if delta is not None:
+        _need(delta, "delta", torch.bfloat16, (rows, H))
+    orows = rows if group == 0 else rows // group * (group - 1)
+    if out is None:
+        out = torch.empty((orows, H), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (orows, H))
+    _check(lib().dspark_add_rmsnorm(_ptr(x), _ptr(delta), H, _ptr(w), _ptr(out), H, group, rows, H,
+                                    _stream(stream, dev)), "dspark_add_rmsnorm")
+    return out
+
+
+def rmsnorm_bf16(inp, w, out=None, stream=None):
+    """out = bf16(rmsnorm(inp) * w) of bf16 rows [rows, H]."""
+    rows, H = inp.shape
+    dev = inp.device
+    _need(inp, "inp", torch.bfloat16)
+    _need(w, "w", torch.bfloat16, (H,))
+    if out is None:
+        out = torch.empty_like(inp)
+    _need(out, "out", torch.bfloat16, (rows, H))
+    _check(lib().dspark_rmsnorm_bf16(_ptr(inp), H, _ptr(w), _ptr(out), H, rows, H, _stream(stream, dev)),
+           "dspark_rmsnorm_bf16")
+    return out
+
+
+def qk_norm_rope(qkv, nq, nkv, q_norm_w, k_norm_w, theta, k_cache, v_cache, rows_per_req, pos0,
+                 q_out=None, stream=None):
+    """Per-head q/k rmsnorm + rotary embedding of qkv rows [B * rows_per_req, (nq + 2 nkv) * 128]
+    (nq = 0: key/value rows only); k and v go to cache slots pos0 .. pos0 + rows_per_req - 1
+    of each request; returns q [rows, nq, 128] (None when nq == 0)."""
+    rows = qkv.shape[0]
+    B, cache_len = k_cache.shape[0], k_cache.shape[1]
+    dev = qkv.device
+    _need(qkv, "qkv", torch.bfloat16, (rows, (nq + 2 * nkv) * 128))
+    _need(k_norm_w, "k_norm_w", torch.bfloat16, (128,))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, cache_len, nkv, 128))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, cache_len, nkv, 128))
+    if rows != B * rows_per_req:
+        raise ValueError("qkv has %d rows, expected B * rows_per_req = %d" % (rows, B * rows_per_req))
+    if nq > 0:
+        _need(q_norm_w, "q_norm_w", torch.bfloat16, (128,))
+        if q_out is None:
+            q_out = torch.empty((rows, nq, 128), dtype=torch.bfloat16, device=dev)
+        _need(q_out, "q_out", torch.bfloat16, (rows, nq, 128))
+    _check(lib().dspark_qk_norm_rope(_ptr(qkv), qkv.stride(0), nq, nkv, _ptr(q_norm_w if nq > 0 else None),
+                                     _ptr(k_norm_w), float(theta), _ptr(q_out if nq > 0 else None),
+                                     _ptr(k_cache), _ptr(v_cache), B, cache_len, rows_per_req, pos0,
+                                     _stream(stream, dev)), "dspark_qk_norm_rope")
+    return q_out if nq > 0 else None
+
+
+def attention(q, k_cache, v_cache, nkeys, out=None, stream=None, workspaces=None):
+    """Grouped-query attention of q [B, nr, nq, 128] over cache keys 0 .. nkeys - 1
+    (k_cache, v_cache [B, cache_len, nkv, 128]); returns out [B, nr, nq, 128] bf16."""
+    B, nr, nq, hd = q.shape
+    cache_len, nkv = k_cache.shape[1], k_cache.shape[2]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, nr, nq, 128))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, cache_len, nkv, 128))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, cache_len, nkv, 128))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, (B, nr, nq, 128))
+    L = lib()
+    ws = (workspaces or _default_ws).get("attention", dev,
+                                        L.dspark_attention_workspace_size(B, nr, nq, nkv, nkeys))
+    _check(L.dspark_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), B, nr, nq, nkv, cache_len, nkeys,
+                              _ptr(ws), ws.numel(), _stream(stream, dev)), "dspark_attention")
+    return out
+
+
+def silu_mul(gu, out=None, stream=None):
+    """act[M, I] = bf16(silu(gu[:, :I]) * gu[:, I:]) of the gate|up GEMM output gu [M, 2I]."""
+    M, I2 = gu.shape
+    dev = gu.device
+    _need(gu, "gu", torch.bfloat16)
+    if out is None:
+        out = torch.empty((M, I2 // 2), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (M, I2 // 2))
+    _check(lib().dspark_silu_mul(_ptr(gu), _ptr(out), M, I2 // 2, _stream(stream, dev)), "dspark_silu_mul")
+    return out
+
+
+class BackboneLayer:
+    """One decoder layer's device weights (bf16): w_in, w_post [H]; w_qn, w_kn [128];
+    w_qkv [(nq + 2 nkv) * 128, H]; w_o [H, nq * 128]; w_gu [2I, H]; w_d [H, I]."""
+
+    def __init__(self, nq, nkv, w_in, w_post, w_qn, w_kn, w_qkv, w_o, w_gu, w_d, theta=1e6):
+        self.nq, self.nkv, self.theta = nq, nkv, theta
+        self.w_in, self.w_post, self.w_qn, self.w_kn = w_in, w_post, w_qn, w_kn
+        self.w_qkv, self.w_o, self.w_gu, self.w_d = w_qkv, w_o, w_gu, w_d
+
+    @property
+    def w_kv(self):
+        """The [Wk; Wv] rows of w_qkv (a view)."""
+        return self.w_qkv[self.nq * 128:]
+
+
+def backbone_context(ctx, layers, k_caches, v_caches, pos0, stream=None, workspaces=None):
+    """Writes the keys and values of context rows ctx [B * n, H] (bf16, the fc output of
+    n verified tokens per request) into each layer's caches at slots pos0 .. pos0 + n - 1:
+    input norm, the [Wk; Wv] GEMM, k-norm + rotary."""
+    rows = ctx.shape[0]
+    B = k_caches[0].shape[0]
+    n = rows // B
+    for li, (ly, kc, vc) in enumerate(zip(layers, k_caches, v_caches)):
+        nrm = rmsnorm_bf16(ctx, ly.w_in, stream=stream)
+        kv = linear(nrm, ly.w_kv, stream=stream, workspaces=workspaces, kind="bb_kv%d" % li)
+        qk_norm_rope(kv, 0, ly.nkv, None, ly.w_kn, ly.theta, kc, vc, n, pos0, stream=stream)
+
+
+def backbone_block(tokens, embed, layers, w_final, k_caches, v_caches, C, out=None, stream=None,
+                   workspaces=None):
+    """Runs the draft block through the layers and the final norm.  tokens [B, k+1]
+    int32 (anchor, then mask tokens); embed [V, H] bf16 (the LM head's weight); the
+    caches hold each layer's context keys/values at slots 0 .. C - 1, the block's go to
+    C .. C + k.  Returns h [B * k, H] bf16 (mask positions), the LM head's input."""
+    B, nr = tokens.shape
+    H = embed.shape[1]
+    dev = embed.device
+    x, n = embed_rmsnorm(embed, tokens.reshape(-1), layers[0].w_in, stream=stream)
+    for li, ly in enumerate(layers):
+        qkv = linear(n, ly.w_qkv, stream=stream, workspaces=workspaces, kind="bb_qkv%d" % li)
+        q = qk_norm_rope(qkv, ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li], v_caches[li], nr, C,
+                         stream=stream)
+        o = attention(q.view(B, nr, ly.nq, 128), k_caches[li], v_caches[li], C + nr, stream=stream,
+                      workspaces=workspaces)
+        d = linear(o.view(B * nr, ly.nq * 128), ly.w_o, stream=stream, workspaces=workspaces, kind="bb_o%d" % li)
+        n2 = add_rmsnorm(x, d, ly.w_post, stream=stream)
+        gu = linear(n2, ly.w_gu, stream=stream, workspaces=workspaces, kind="bb_gu%d" % li)
+        act = silu_mul(gu, stream=stream)
+        d2 = linear(act, ly.w_d, stream=stream, workspaces=workspaces, kind="bb_d%d" % li)
+        if li + 1 < len(layers):
+            # residual add, then the next layer's input norm
+            n = add_rmsnorm(x, d2, layers[li + 1].w_in, stream=stream)
+        else:
+            if out is None:
+                out = torch.empty((B * (nr - 1), H), dtype=torch.bfloat16, device=dev)
+            add_rmsnorm(x, d2, w_final, out=out, group=nr, stream=stream)
+    return out
+

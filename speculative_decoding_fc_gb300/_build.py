@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libdspark.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "gemm_tcgen05.cu", "markov.cu", "quant.cu", "verify.cu", "verify_noalloc.cu"]
+SOURCES = ["api.cu", "backbone.cu", "gemm_tcgen05.cu", "markov.cu", "quant.cu", "verify.cu",
+           "verify_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

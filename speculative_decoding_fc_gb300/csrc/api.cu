@@ -647,4 +647,137 @@ dspark_status_t dspark_lm_head_fp8(const dspark_bf16_t *h, const uint8_t *lm_w8,
   return fp8_gemm(p, 1, H, H, lm_w8, lm_scale, M, V, logits, V, false, 7, ws, as_stream(stream));
 }
 
+
+// ---------------------------------------------------------------- drafter backbone
+namespace {
+constexpr int kMaxNormH = 8192;   // 8 bf16 per 16-byte chunk x 256 threads x 4 chunks
+constexpr int kMaxAttnQueries = 48;
+bool ld_ok(int64_t ld, int width) { return ld >= width && ld % 8 == 0; }
+}  // namespace
+
+size_t dspark_linear_workspace_size(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 64) return 0;
+  return kHeader + gemm_workspace_size(M, N, K);
+}
+
+dspark_status_t dspark_linear(const dspark_bf16_t *x, int64_t x_ld, const dspark_bf16_t *w, void *out,
+                              int64_t out_ld, int out_bf16, int M, int N, int K, void *ws, size_t ws_bytes,
+                              void *stream) {
+  if (!x || !w || !out) return DSPARK_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || !ld_ok(x_ld, K) || out_ld < N) return DSPARK_ERR_INVALID_ARG;
+  if (K % 64 != 0 || M > kMaxM || N > kMaxV || K > (1 << 20)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !(out_bf16 ? aligned2(out) : aligned4(out)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_linear_workspace_size(M, N, K));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  st = prepare_workspace(ws, layout_signature({11, M, N, K}), {{0, kHeader + gemm_counter_bytes(M, N, K)}},
+                         as_stream(stream));
+  if (st != DSPARK_OK) return st;
+  GemmProblem p;
+  memset(&p, 0, sizeof(p));
+  p.w = w;
+  p.x[0] = x;
+  p.x_ld[0] = x_ld;
+  p.n_seg = 1;
+  p.seg_k = K;
+  p.N = N;
+  p.M = M;
+  p.out = out;
+  p.ldo = out_ld;
+  p.out_bf16 = out_bf16 != 0;
+  return gemm_launch(p, static_cast<char *>(ws) + kHeader, ws_bytes - kHeader, status_word(ws),
+                     as_stream(stream));
+}
+
+dspark_status_t dspark_embed_rmsnorm(const dspark_bf16_t *table, int V, const int32_t *tokens,
+                                     const dspark_bf16_t *w, float *x_out, dspark_bf16_t *n_out, int rows,
+                                     int H, int32_t *status, void *stream) {
+  if (!table || !tokens || !w || !x_out || !n_out || rows < 1 || H < 8 || V < 1) return DSPARK_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > kMaxNormH || rows > kMaxM) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(table) || !aligned4(tokens) || !aligned16(w) || !aligned16(x_out) || !aligned16(n_out) ||
+      (status && !aligned4(status)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return norm_rows_launch(x_out, nullptr, 0, table, tokens, V, nullptr, 0, w, n_out, H, 0, rows, H, status,
+                          as_stream(stream));
+}
+
+dspark_status_t dspark_add_rmsnorm(float *x, const dspark_bf16_t *delta, int64_t delta_ld,
+                                   const dspark_bf16_t *w, dspark_bf16_t *out, int64_t out_ld, int group,
+                                   int rows, int H, void *stream) {
+  if (!x || !w || !out || rows < 1 || H < 8 || group < 0 || group == 1) return DSPARK_ERR_INVALID_ARG;
+  if (delta && !ld_ok(delta_ld, H)) return DSPARK_ERR_INVALID_ARG;
+  if (!ld_ok(out_ld, H) || (group > 0 && rows % group != 0)) return DSPARK_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > kMaxNormH || rows > kMaxM) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || (delta && !aligned16(delta)) || !aligned16(w) || !aligned16(out))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return norm_rows_launch(x, delta, delta_ld, nullptr, nullptr, 0, nullptr, 0, w, out, out_ld, group, rows, H,
+                          nullptr, as_stream(stream));
+}
+
+dspark_status_t dspark_rmsnorm_bf16(const dspark_bf16_t *in, int64_t in_ld, const dspark_bf16_t *w,
+                                    dspark_bf16_t *out, int64_t out_ld, int rows, int H, void *stream) {
+  if (!in || !w || !out || rows < 1 || H < 8 || !ld_ok(in_ld, H) || !ld_ok(out_ld, H))
+    return DSPARK_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > kMaxNormH || rows > kMaxM) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(in) || !aligned16(w) || !aligned16(out)) return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return norm_rows_launch(nullptr, nullptr, 0, nullptr, nullptr, 0, in, in_ld, w, out, out_ld, 0, rows, H,
+                          nullptr, as_stream(stream));
+}
+
+dspark_status_t dspark_qk_norm_rope(const dspark_bf16_t *qkv, int64_t ld, int nq, int nkv,
+                                    const dspark_bf16_t *q_norm_w, const dspark_bf16_t *k_norm_w, float theta,
+                                    dspark_bf16_t *q_out, dspark_bf16_t *k_cache, dspark_bf16_t *v_cache, int B,
+                                    int cache_len, int rows_per_req, int pos0, void *stream) {
+  if (!qkv || !k_norm_w || !k_cache || !v_cache || (nq > 0 && (!q_out || !q_norm_w)))
+    return DSPARK_ERR_INVALID_ARG;
+  if (nq < 0 || nkv < 1 || B < 1 || rows_per_req < 1 || pos0 < 0 || !(theta > 1.0f))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!ld_ok(ld, (nq + 2 * nkv) * 128) || static_cast<long long>(pos0) + rows_per_req > cache_len)
+    return DSPARK_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * rows_per_req > kMaxM || nq + 2 * nkv > 4096) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(qkv) || !aligned16(k_norm_w) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (nq > 0 && (!aligned16(q_out) || !aligned16(q_norm_w))))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return qk_norm_rope_launch(qkv, ld, nq, nkv, q_norm_w, k_norm_w, theta, q_out, k_cache, v_cache, cache_len,
+                             rows_per_req, pos0, B * rows_per_req, as_stream(stream));
+}
+
+size_t dspark_attention_workspace_size(int B, int nr, int nq, int nkv, int nkeys) {
+  if (B < 1 || nr < 1 || nq < 1 || nkv < 1 || nq % nkv != 0 || nkeys < 1) return 0;
+  return attention_workspace_bytes(B, nr, nq, nkv, nkeys);
+}
+
+dspark_status_t dspark_attention(const dspark_bf16_t *q, const dspark_bf16_t *k_cache,
+                                 const dspark_bf16_t *v_cache, dspark_bf16_t *out, int B, int nr, int nq,
+                                 int nkv, int cache_len, int nkeys, void *ws, size_t ws_bytes, void *stream) {
+  if (!q || !k_cache || !v_cache || !out) return DSPARK_ERR_INVALID_ARG;
+  if (B < 1 || nr < 1 || nq < 1 || nkv < 1 || nq % nkv != 0 || nkeys < 1 || nkeys > cache_len)
+    return DSPARK_ERR_INVALID_ARG;
+  if (nr * (nq / nkv) > kMaxAttnQueries || B > (1 << 16) || nkv > 1024) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_ws(ws, ws_bytes, dspark_attention_workspace_size(B, nr, nq, nkv, nkeys));
+  if (st != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  return attention_launch(q, k_cache, v_cache, out, B, nr, nq, nkv, cache_len, nkeys, ws, as_stream(stream));
+}
+
+dspark_status_t dspark_silu_mul(const dspark_bf16_t *gu, dspark_bf16_t *act, int M, int I, void *stream) {
+  if (!gu || !act || M < 1 || I < 8) return DSPARK_ERR_INVALID_ARG;
+  if (I % 8 != 0 || M > kMaxM) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(gu) || !aligned16(act)) return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return silu_mul_launch(gu, act, M, I, as_stream(stream));
+}
+
 }  // extern "C"

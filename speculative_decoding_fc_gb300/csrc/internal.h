@@ -69,6 +69,21 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
                                   int32_t *draft_len, float *conf_out, int B, int k, int H,
                                   int *status, cudaStream_t stream);
 
+// ------------------------------------------------------------------ drafter backbone
+dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_delta, const uint16_t *table,
+                                 const int32_t *tok, int V, const uint16_t *in, int64_t ld_in,
+                                 const uint16_t *w, uint16_t *out, int64_t ld_out, int group, int rows,
+                                 int H, int *status, cudaStream_t stream);
+dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int nkv, const uint16_t *wq,
+                                    const uint16_t *wk, float theta, uint16_t *q_out, uint16_t *k_cache,
+                                    uint16_t *v_cache, int cache_len, int rows_per_req, int pos0, int rows,
+                                    cudaStream_t stream);
+size_t attention_workspace_bytes(int B, int nr, int nq, int nkv, int nkeys);
+dspark_status_t attention_launch(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                                 uint16_t *out, int B, int nr, int nq, int nkv, int cache_len, int nkeys,
+                                 void *ws, cudaStream_t stream);
+dspark_status_t silu_mul_launch(const uint16_t *gu, uint16_t *act, int M, int I, cudaStream_t stream);
+
 // ------------------------------------------------------------------ FP8 quantisation
 // codes[r, :] = E4M3(x[r, :] / scale[r]), scale = amax(row) / 448 (1 if zero); the
 // row is the concatenation of nseg segments, each [rows, seg_cols] with row

@@ -37,6 +37,10 @@ CONFIGS = {
                     sigma=("ramp", 0.5, 3.0), conf=True),
     "flash_b4": dict(H=2560, T=5, V=151936, r=64, k=7, B=4, steps=1, mode=1,
                      sigma=("ramp", 0.5, 3.0), conf=False),
+    # the 27B batch-1 step with one drafter backbone layer between the fc and the LM
+    # head, over a 1024-token context (the block's keys/values follow it in the cache)
+    "27b_b1_backbone": dict(H=5120, T=5, V=151936, r=64, k=7, B=1, steps=1, mode=1,
+                            sigma=("ramp", 0.5, 3.0), conf=False, backbone=dict(L=1, C=1024)),
 }
 FLASH_PREFILL = dict(H=2560, T=5, M=4096)
 
@@ -110,6 +114,32 @@ def weights(H, T, V, r, with_conf=False, with_markov=True):
         w["conf_b"] = 0.0
         w["conf_tau"] = 0.5
     return w
+
+
+# Geometry of the drafter backbone's layers per hidden size (128-wide heads, 5 query
+# heads per key/value head, the MLP width of the Qwen3 model of that hidden size).
+BACKBONE_GEOMETRY = {5120: dict(nq=40, nkv=8, I=17408), 2560: dict(nq=20, nkv=4, I=9728)}
+
+
+def backbone_weights(H, nq, nkv, I, L, seed=200):
+    """Random backbone weights (numpy uint16 bf16 bits), one dict per layer, and the
+    final norm weight: norms ~ 1 + N(0, 0.1^2), projections ~ N(0, 1/fan_in)."""
+    layers = []
+    for li in range(L):
+        s = seed + 16 * li
+        layers.append({
+            "nq": nq, "nkv": nkv,
+            "w_in": to_bf16_bits(1.0 + normal_f32(s, (H,), 0.1)),
+            "w_post": to_bf16_bits(1.0 + normal_f32(s + 1, (H,), 0.1)),
+            "w_qn": to_bf16_bits(1.0 + normal_f32(s + 2, (128,), 0.1)),
+            "w_kn": to_bf16_bits(1.0 + normal_f32(s + 3, (128,), 0.1)),
+            "w_qkv": normal_bf16(s + 4, ((nq + 2 * nkv) * 128, H), (1.0 / H) ** 0.5),
+            "w_o": normal_bf16(s + 5, (H, nq * 128), (1.0 / (nq * 128)) ** 0.5),
+            "w_gu": normal_bf16(s + 6, (2 * I, H), (1.0 / H) ** 0.5),
+            "w_d": normal_bf16(s + 7, (H, I), (1.0 / I) ** 0.5),
+        })
+    w_final = to_bf16_bits(1.0 + normal_f32(seed + 15, (H,), 0.1))
+    return layers, w_final
 
 
 def step_inputs(step, B, k, H, T, V, sigma_spec):
