@@ -437,11 +437,10 @@ class Pipeline:
         """The fc output (self.h) as the newest k context rows of every layer's cache,
         then the block through the layers; returns the LM head's input."""
         ds, w, k = self.ds, self.w, self.cfg["k"]
-        ds.backbone_context(self.h, self.bb, w["bb_kc"], w["bb_vc"], self.C - k, stream=s, workspaces=self.wsp)
         with self.torch.cuda.stream(s):
             self.tokens[:, 0].copy_(prev)
         return ds.backbone_block(self.tokens, w["lm_w"], self.bb, w["bb_final"], w["bb_kc"], w["bb_vc"], self.C,
-                                 out=self.hb, stream=s, workspaces=self.wsp)
+                                 out=self.hb, stream=s, workspaces=self.wsp, ctx=self.h, ctx_pos0=self.C - k)
 
     def draft(self, st, s, hist, ev=None, chain_after=None):
         """ev: timing events on s at the stage boundaries (start, after fc, [after the

@@ -690,7 +690,10 @@ def qk_norm_rope(qkv, nq, nkv, q_norm_w, k_norm_w, theta, k_cache, v_cache, rows
     rows = qkv.shape[0]
     B, cache_len = k_cache.shape[0], k_cache.shape[1]
     dev = qkv.device
-    _need(qkv, "qkv", torch.bfloat16, (rows, (nq + 2 * nkv) * 128))
+    # qkv may be a column slice of a wider GEMM output (row stride > its width)
+    if not isinstance(qkv, torch.Tensor) or not qkv.is_cuda or qkv.dtype != torch.bfloat16 \
+            or tuple(qkv.shape) != (rows, (nq + 2 * nkv) * 128) or qkv.stride(1) != 1:
+        raise ValueError("qkv must be a CUDA bf16 [rows, (nq + 2 nkv) * 128] tensor with unit column stride")
     _need(k_norm_w, "k_norm_w", torch.bfloat16, (128,))
     _need(k_cache, "k_cache", torch.bfloat16, (B, cache_len, nkv, 128))
     _need(v_cache, "v_cache", torch.bfloat16, (B, cache_len, nkv, 128))
@@ -769,19 +772,31 @@ def backbone_context(ctx, layers, k_caches, v_caches, pos0, stream=None, workspa
 
 
 def backbone_block(tokens, embed, layers, w_final, k_caches, v_caches, C, out=None, stream=None,
-                   workspaces=None):
+                   workspaces=None, ctx=None, ctx_pos0=None):
     """Runs the draft block through the layers and the final norm.  tokens [B, k+1]
     int32 (anchor, then mask tokens); embed [V, H] bf16 (the LM head's weight); the
     caches hold each layer's context keys/values at slots 0 .. C - 1, the block's go to
-    C .. C + k.  Returns h [B * k, H] bf16 (mask positions), the LM head's input."""
+    C .. C + k.  Returns h [B * k, H] bf16 (mask positions), the LM head's input.
+    ctx [B * n, H] (optional): n new context rows per request (the fc output of the
+    verified tokens), written to cache slots ctx_pos0 .. ctx_pos0 + n - 1 of every
+    layer before its attention; their keys and values come out of the same GEMM as the
+    block's q, k, v (one pass over each layer's [Wq; Wk; Wv])."""
     B, nr = tokens.shape
     H = embed.shape[1]
     dev = embed.device
-    x, n = embed_rmsnorm(embed, tokens.reshape(-1), layers[0].w_in, stream=stream)
+    Bb = B * nr
+    nc = 0 if ctx is None else ctx.shape[0]
+    xin = torch.empty((Bb + nc, H), dtype=torch.bfloat16, device=dev)
+    x, _ = embed_rmsnorm(embed, tokens.reshape(-1), layers[0].w_in, n_out=xin[:Bb], stream=stream)
     for li, ly in enumerate(layers):
-        qkv = linear(n, ly.w_qkv, stream=stream, workspaces=workspaces, kind="bb_qkv%d" % li)
-        q = qk_norm_rope(qkv, ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li], v_caches[li], nr, C,
+        if nc:
+            rmsnorm_bf16(ctx, ly.w_in, out=xin[Bb:], stream=stream)
+        qkv = linear(xin, ly.w_qkv, stream=stream, workspaces=workspaces, kind="bb_qkv%d" % li)
+        q = qk_norm_rope(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li], v_caches[li], nr, C,
                          stream=stream)
+        if nc:
+            qk_norm_rope(qkv[Bb:, ly.nq * 128:], 0, ly.nkv, None, ly.w_kn, ly.theta, k_caches[li], v_caches[li],
+                         nc // B, ctx_pos0, stream=stream)
         o = attention(q.view(B, nr, ly.nq, 128), k_caches[li], v_caches[li], C + nr, stream=stream,
                       workspaces=workspaces)
         d = linear(o.view(B * nr, ly.nq * 128), ly.w_o, stream=stream, workspaces=workspaces, kind="bb_o%d" % li)
@@ -791,7 +806,7 @@ def backbone_block(tokens, embed, layers, w_final, k_caches, v_caches, C, out=No
         d2 = linear(act, ly.w_d, stream=stream, workspaces=workspaces, kind="bb_d%d" % li)
         if li + 1 < len(layers):
             # residual add, then the next layer's input norm
-            n = add_rmsnorm(x, d2, layers[li + 1].w_in, stream=stream)
+            add_rmsnorm(x, d2, layers[li + 1].w_in, out=xin[:Bb], stream=stream)
         else:
             if out is None:
                 out = torch.empty((B * (nr - 1), H), dtype=torch.bfloat16, device=dev)

@@ -152,6 +152,11 @@ struct RopeArgs {
 // One warp per (row, head), 4 dims per lane (lanes 0-15 the first half of the head,
 // 16-31 the second, so the rotary partner of a lane's dims is lane ^ 16).
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const RopeArgs a) {
+  // the inverse frequencies theta^(-2d/128) in fp64, once per CTA
+  __shared__ double inv_freq[kHeadDim / 2];
+  if (threadIdx.x < kHeadDim / 2)
+    inv_freq[threadIdx.x] = exp2(-(2.0 * threadIdx.x / kHeadDim) * a.log2_theta);
+  __syncthreads();
   pdl_wait();
   pdl_release();
   const int nh = a.nq + 2 * a.nkv;
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const RopeArgs a) {
     const int d = (lane & 15) * 4 + i;  // frequency index 0..63
     // the angle in fp64, reduced to [0, 2 pi) before the fp32 sine and cosine (an fp32
     // angle of ~1000 rad would carry an error of ~1e-4 rad)
-    const double ang = static_cast<double>(pos) * exp2(-(2.0 * d / kHeadDim) * a.log2_theta);
+    const double ang = static_cast<double>(pos) * inv_freq[d];
     const double two_pi = 6.283185307179586;
     float s, c;
     sincosf(static_cast<float>(ang - two_pi * floor(ang / two_pi)), &s, &c);
@@ -225,14 +230,27 @@ struct AttnArgs {
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) float attn_smem[];
   const int nqry = a.nqry;
-  float *qs = attn_smem;                        // [nqry][128]
+  uint16_t *vs = reinterpret_cast<uint16_t *>(attn_smem);              // [64][128] bf16
+  float *qs = attn_smem + kAttnKeys * kHeadDim / 2;                    // [nqry][128]
   float *sc = qs + nqry * kHeadDim;             // [nqry][64]
   float *ml = sc + nqry * kAttnKeys;            // [nqry][2]
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = a.nq / a.nkv;
+  const int kend = min(kAttnKeys, a.nkeys - split * kAttnKeys);
   pdl_wait();
   pdl_release();
+  // the slice's value rows into shared memory, in flight while the scores are computed
+  for (int e = tid; e < kend * (kHeadDim / 8); e += kAttnThreads) {
+    const int kl = e / (kHeadDim / 8), c = e % (kHeadDim / 8);
+    const uint16_t *src =
+        a.v_cache + ((static_cast<int64_t>(b) * a.cache_len + split * kAttnKeys + kl) * a.nkv + g) * kHeadDim + 8 * c;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                     __cvta_generic_to_shared(vs + kl * kHeadDim + 8 * c))),
+                 "l"(src)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
   for (int e = tid; e < nqry * (kHeadDim / 8); e += kAttnThreads) {
     const int qi = e / (kHeadDim / 8), c = e % (kHeadDim / 8);
     const int i = qi / grp, head = g * grp + qi % grp;
@@ -291,6 +309,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnArgs 
       ml[2 * qi + 1] = l;
     }
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
   // P.V: warp w takes query rows w, w + 8, ...; lane dims 4 * lane .. + 3
@@ -300,11 +319,9 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnArgs 
   for (int t = 0; t < kRowsPerWarp; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-  const int kend = min(kAttnKeys, a.nkeys - split * kAttnKeys);
+#pragma unroll 4
   for (int kl = 0; kl < kend; ++kl) {
-    const int key = split * kAttnKeys + kl;
-    const uint2 vr = *reinterpret_cast<const uint2 *>(
-        a.v_cache + ((static_cast<int64_t>(b) * a.cache_len + key) * a.nkv + g) * kHeadDim + 4 * lane);
+    const uint2 vr = *reinterpret_cast<const uint2 *>(vs + kl * kHeadDim + 4 * lane);
     const float v[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
 #pragma unroll
     for (int t = 0; t < kRowsPerWarp; ++t) {
@@ -344,26 +361,43 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(const AttnArgs a) 
   const int b = static_cast<int>(wid / (static_cast<long long>(a.nqry) * a.nkv));
   const int grp = a.nq / a.nkv;
   const int64_t base0 = ((static_cast<int64_t>(b) * a.nkv + g) * a.nsplit) * a.nqry + qi;
+  // the slices' maxima, one slice per lane
   float M = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.part_ml[2 * (base0 + static_cast<int64_t>(s) * a.nqry)]);
-  float o[4] = {0.0f, 0.0f, 0.0f, 0.0f}, L = 0.0f;
+  for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, a.part_ml[2 * (base0 + static_cast<int64_t>(s) * a.nqry)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float o4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, L = 0.0f;
   if (M != -INFINITY) {
-    for (int s = 0; s < a.nsplit; ++s) {
-      const int64_t base = base0 + static_cast<int64_t>(s) * a.nqry;
-      const float m = a.part_ml[2 * base];
-      if (m == -INFINITY) continue;
-      const float e = expf(m - M);
-      L = __fmaf_rn(e, a.part_ml[2 * base + 1], L);
-      const float4 po = *reinterpret_cast<const float4 *>(a.part_o + base * kHeadDim + 4 * lane);
-      o[0] = __fmaf_rn(e, po.x, o[0]); o[1] = __fmaf_rn(e, po.y, o[1]);
-      o[2] = __fmaf_rn(e, po.z, o[2]); o[3] = __fmaf_rn(e, po.w, o[3]);
+    for (int s0 = 0; s0 < a.nsplit; s0 += 32) {
+      // lane s0 + j: the weight e^(m - M) of slice s0 + j (0 for an empty slice)
+      const int s = s0 + lane;
+      float e = 0.0f;
+      if (s < a.nsplit) {
+        const int64_t base = base0 + static_cast<int64_t>(s) * a.nqry;
+        const float m = a.part_ml[2 * base];
+        if (m != -INFINITY) {
+          e = expf(m - M);
+          L = __fmaf_rn(e, a.part_ml[2 * base + 1], L);
+        }
+      }
+      const int n = min(32, a.nsplit - s0);
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float ej = __shfl_sync(0xffffffffu, e, j);
+        const float4 po = *reinterpret_cast<const float4 *>(
+            a.part_o + (base0 + static_cast<int64_t>(s0 + j) * a.nqry) * kHeadDim + 4 * lane);
+        o4[0] = __fmaf_rn(ej, po.x, o4[0]); o4[1] = __fmaf_rn(ej, po.y, o4[1]);
+        o4[2] = __fmaf_rn(ej, po.z, o4[2]); o4[3] = __fmaf_rn(ej, po.w, o4[3]);
+      }
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
   const int i = qi / grp, head = g * grp + qi % grp;
   uint2 r;
-  r.x = pack2(o[0] * inv, o[1] * inv);
-  r.y = pack2(o[2] * inv, o[3] * inv);
+  r.x = pack2(o4[0] * inv, o4[1] * inv);
+  r.y = pack2(o4[2] * inv, o4[3] * inv);
   *reinterpret_cast<uint2 *>(a.out + ((static_cast<int64_t>(b) * a.nr + i) * a.nq + head) * kHeadDim + 4 * lane) = r;
 }
 
@@ -475,7 +509,17 @@ dspark_status_t attention_launch(const uint16_t *q, const uint16_t *k_cache, con
   const size_t parts = static_cast<size_t>(B) * nkv * a.nsplit * a.nqry;
   a.part_o = static_cast<float *>(ws);
   a.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + align_up(parts * kHeadDim * sizeof(float), kWsAlign));
-  const size_t smem = static_cast<size_t>(a.nqry) * (kHeadDim + kAttnKeys + 2) * sizeof(float);
+  const size_t smem = static_cast<size_t>(kAttnKeys) * kHeadDim * 2 +
+                      static_cast<size_t>(a.nqry) * (kHeadDim + kAttnKeys + 2) * sizeof(float);
+  static size_t attr_bytes[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSPARK_ERR_CUDA;
+  if (attr_bytes[dev] < smem) {
+    if (cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    attr_bytes[dev] = smem;
+  }
   if (launch_pdl(attention_kernel, dim3(static_cast<unsigned>(a.nsplit), static_cast<unsigned>(nkv),
                                         static_cast<unsigned>(B)),
                  dim3(kAttnThreads), smem, stream, a) != cudaSuccess)

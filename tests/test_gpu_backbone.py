@@ -267,3 +267,31 @@ def test_backbone_27b_layer_matches_oracle():
     g = syn.BACKBONE_GEOMETRY[5120]
     _backbone_case(H=5120, nq=g["nq"], nkv=g["nkv"], I=g["I"], L=1, V=4096, B=1, C=1024, k=7, seed=500,
                    stagewise=True)
+
+
+def test_backbone_new_context_rows_in_the_block_gemm_equal_separate_calls():
+    """backbone_block(ctx=...) takes the new context rows' keys and values out of the
+    block's QKV GEMM; the caches and h equal those of backbone_context for the same rows
+    followed by backbone_block (each GEMM output element is the same fp32 sum)."""
+    H, nq, nkv, I, L, V, B, C, k, n = 256, 2, 1, 512, 2, 500, 2, 30, 4, 4
+    layers, wf = syn.backbone_weights(H, nq, nkv, I, L, seed=600)
+    lay_d = [_layer_dev(l) for l in layers]
+    E = dev_bf16(syn.normal_bf16(601, (V, H), 0.5))
+    ctx = syn.normal_bf16(602, (B, C, H))
+    toks = dev(np.concatenate([np.array([[3], [9]]), np.full((B, k), V - 1)], axis=1).astype(np.int32))
+    outs = []
+    for fused in (False, True):
+        kcs = [torch.zeros((B, C + k + 1, nkv, 128), dtype=torch.bfloat16, device="cuda") for _ in layers]
+        vcs = [torch.zeros_like(t) for t in kcs]
+        wsp = ds.Workspaces()
+        if fused:
+            ds.backbone_context(dev_bf16(ctx[:, :C - n].reshape(-1, H)), lay_d, kcs, vcs, 0, workspaces=wsp)
+            h = ds.backbone_block(toks, E, lay_d, dev_bf16(wf), kcs, vcs, C, workspaces=wsp,
+                                  ctx=dev_bf16(np.ascontiguousarray(ctx[:, C - n:]).reshape(-1, H)), ctx_pos0=C - n)
+        else:
+            ds.backbone_context(dev_bf16(ctx.reshape(-1, H)), lay_d, kcs, vcs, 0, workspaces=wsp)
+            h = ds.backbone_block(toks, E, lay_d, dev_bf16(wf), kcs, vcs, C, workspaces=wsp)
+        outs.append(([host_bf16_bits(t) for t in kcs + vcs], host_bf16_bits(h)))
+    for a, b in zip(outs[0][0], outs[1][0]):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(outs[0][1], outs[1][1])
