@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--sets", type=int, default=3,
                     help="minimum input sets rotated across steps (more are used when needed "
                          "to exceed 2x the L2 cache)")
+    ap.add_argument("--no-backbone", action="store_true",
+                    help="leave out the 27B batch-1 sub-record with one drafter backbone layer")
     ap.add_argument("--profile-sets", type=int, default=0,
                     help="profiling runs only: rotate this many input sets instead of enough to "
                          "exceed 2x the L2 cache (fewer set-up launches before the profiled ones)")
@@ -941,6 +943,14 @@ def run_ours(args, rank, local_rank, world):
             "accepted_tok_s", "mean_acceptance_length", "per_position_acceptance", "roofline",
             "step_roofline", "graph", "timing", "timed_reps", "serial", "uncaptured", "stage_ms",
             "gpu_launches", "e2e", "clocks")}
+    if args.config == "27b_b1" and not args.no_backbone:
+        # the same batch-1 step with one drafter backbone layer (N1) over a 1024-token
+        # context, same steps, warm-up and timing rules
+        sub = measure_workload(args, "27b_b1_backbone", rank, local_rank, world, host_cache, False)
+        line["backbone"] = {kk: sub[kk] for kk in (
+            "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "drafted_tok_s",
+            "accepted_tok_s", "mean_acceptance_length", "step_roofline", "graph", "timing", "timed_reps",
+            "serial", "stage_ms", "gpu_launches", "e2e", "clocks")}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
