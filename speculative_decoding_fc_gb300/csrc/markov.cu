@@ -1021,7 +1021,9 @@ __device__ __forceinline__ void pipe_take(int h) {  // wait for the other half's
   asm volatile("bar.sync %0, %1;" ::"r"(4 - h), "r"(kSThreads) : "memory");
 }
 
-template <int CPR, bool kStats>
+// kW2Smem: the CTA's markov_w2 slice in shared memory (r <= 64); otherwise (r = 128) it
+// is read through L2 at every position after a bulk L2 prefetch, as in the kernel above.
+template <int CPR, bool kStats, bool kW2Smem>
 __global__ void __launch_bounds__(kSThreads, 1) markov_chain_split(const ChainPArgs a) {
   constexpr int G = kSGroup;
   __shared__ ChainPartial red[2][G][kPWarps];
@@ -1060,17 +1062,28 @@ __global__ void __launch_bounds__(kSThreads, 1) markov_chain_split(const ChainPA
   }
   const bool vec4 = a.vec != 0 && kPRows * ht + kPRows <= nrows;
 
-  // markov_w2 slice into shared memory before the wait for the previous kernel (no
-  // kernel of the step writes it), 16-byte chunks swizzled as above
+  // markov_w2 slice into shared memory (or L2) before the wait for the previous kernel
+  // (no kernel of the step writes it), 16-byte chunks swizzled as above
   if (biased && nrows > 0) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
-    for (int i = tid; i < nrows * CPR; i += kSThreads) {
-      const int row = i / CPR, q = i - row * CPR;
-      const uint32_t dst = static_cast<uint32_t>(
-          __cvta_generic_to_shared(&w2_s[row * CPR + w2_swizzle(row, q, CPR)]));
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + i) : "memory");
+    if constexpr (kW2Smem) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(v_lo) * r);
+      for (int i = tid; i < nrows * CPR; i += kSThreads) {
+        const int row = i / CPR, q = i - row * CPR;
+        const uint32_t dst = static_cast<uint32_t>(
+            __cvta_generic_to_shared(&w2_s[row * CPR + w2_swizzle(row, q, CPR)]));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + i) : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    } else {
+      // 16 KB pieces, one per thread (the slice is at most 1024 rows x 256 bytes)
+      const char *src = reinterpret_cast<const char *>(a.w2 + static_cast<long long>(v_lo) * r);
+      const uint32_t bytes = static_cast<uint32_t>(nrows) * CPR * 16u;
+      const uint32_t off = static_cast<uint32_t>(tid) * 16384u;
+      if (off < bytes) {
+        const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + off), "r"(n) : "memory");
+      }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   }
   pdl_wait();
   pdl_release();
@@ -1088,7 +1101,7 @@ __global__ void __launch_bounds__(kSThreads, 1) markov_chain_split(const ChainPA
     }
     prev_s[b] = p;
   }
-  if (biased) asm volatile("cp.async.wait_all;" ::: "memory");
+  if (biased && kW2Smem) asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (abort0_s) return;
   const int epoch = epoch_s;
@@ -1145,7 +1158,12 @@ __global__ void __launch_bounds__(kSThreads, 1) markov_chain_split(const ChainPA
         for (int q = 0; q < CPR; ++q) {
           uint4 c[kPRows];
 #pragma unroll
-          for (int j = 0; j < kPRows; ++j) c[j] = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+          for (int j = 0; j < kPRows; ++j) {
+            if constexpr (kW2Smem)
+              c[j] = w2_s[lrow[j] * CPR + w2_swizzle(lrow[j], q, CPR)];
+            else
+              c[j] = __ldg(reinterpret_cast<const uint4 *>(a.w2 + static_cast<long long>(vrow[j]) * r) + q);
+          }
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             // contexts of the group's four request pairs at rank 8q + t (32 bytes)
@@ -1649,29 +1667,31 @@ bool try_persistent_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream
                            smem, a, stream);
 }
 
-template <int CPR, bool kStats>
+template <int CPR, bool kStats, bool kW2Smem>
 bool try_split_r(const ChainPArgs &args0, int B, int V, cudaStream_t stream) {
   int grid = 0, rows = 0;
   if (!chain_grid(V, grid, rows)) return false;
   ChainPArgs a = args0;
   a.rows_per_cta = rows;
   a.vec = ((V % kPRows) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0) ? 1 : 0;
-  a.w2_smem_bytes = static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024));
+  a.w2_smem_bytes = kW2Smem ? static_cast<int>(align_up(static_cast<size_t>(rows) * CPR * 16, 1024)) : 0;
   const size_t npair4 = static_cast<size_t>(((B + 1) / 2 + 3) & ~3);
   const size_t smem = static_cast<size_t>(a.w2_smem_bytes) + npair4 * CPR * 64 +
                       ((static_cast<size_t>(B) * sizeof(int) + 15) & ~static_cast<size_t>(15)) +
                       2 * static_cast<size_t>(kSGroup) * kPRows * kPThreads * sizeof(float);
   if (smem > kPSmemMax) return false;
   static size_t attr_bytes[64] = {};
-  return launch_chain_coop(markov_chain_split<CPR, kStats>, attr_bytes, grid, kSThreads, smem, a, stream);
+  return launch_chain_coop(markov_chain_split<CPR, kStats, kW2Smem>, attr_bytes, grid, kSThreads, smem, a,
+                           stream);
 }
 
 template <bool kStats>
 bool try_split_s(const ChainPArgs &a, int r, int B, int V, cudaStream_t stream) {
   switch (r) {
-    case 16: return try_split_r<2, kStats>(a, B, V, stream);
-    case 32: return try_split_r<4, kStats>(a, B, V, stream);
-    case 64: return try_split_r<8, kStats>(a, B, V, stream);
+    case 16: return try_split_r<2, kStats, true>(a, B, V, stream);
+    case 32: return try_split_r<4, kStats, true>(a, B, V, stream);
+    case 64: return try_split_r<8, kStats, true>(a, B, V, stream);
+    case 128: return try_split_r<16, kStats, false>(a, B, V, stream);
     default: return false;
   }
 }
@@ -1736,7 +1756,7 @@ dspark_status_t chain_launch(float *logits, const uint16_t *w1, const uint16_t *
     const long long v = atoll(wc);
     if (v >= 0) pa.wait_cycles = v;
   }
-  // Batches of more than 8 requests at r <= 64: the two-halves kernel, unless
+  // Batches of more than 8 requests: the two-halves kernel, unless
   // DSPARK_CHAIN_SPLIT=0 (same results).
   const char *senv = getenv("DSPARK_CHAIN_SPLIT");
   const bool split = !per_position && B > 8 && !(senv && senv[0] == '0');

@@ -179,10 +179,12 @@ def test_greedy_sample_without_q_stats_bit_exact(B, k, V, r):
 # Batches above 8 requests (r <= 64) run the two-halves chain: request groups of 8
 # alternate between two halves of the CTA on the FMA pipe.  Cases: a group slot left
 # empty in one half (24, 40 requests), a partial group with an odd request pair (17,
-# 33), and V = 38913, where the last two of 152 CTAs (260-row slices) own no rows.
+# 33), V = 38913, where the last two of 152 CTAs (260-row slices) own no rows, and
+# r = 128 (markov_w2 read through L2 instead of shared memory).
 @pytest.mark.parametrize("B,k,V,r,stats", [(17, 3, 38913, 16, True), (24, 4, 20000, 64, False),
                                            (40, 3, 38913, 32, False), (33, 2, 4099, 64, True),
-                                           (1, 3, 38913, 16, True), (16, 2, 38913, 64, False)])
+                                           (1, 3, 38913, 16, True), (16, 2, 38913, 64, False),
+                                           (24, 3, 20000, 128, True), (17, 2, 38913, 128, False)])
 def test_greedy_sample_two_halves_kernel(B, k, V, r, stats, monkeypatch):
     logits = syn.uniform_logits(51 + V + B, (B, k, V), 1.5)
     w1 = syn.normal_bf16(52, (V, r))
