@@ -295,3 +295,15 @@ def test_backbone_new_context_rows_in_the_block_gemm_equal_separate_calls():
     for a, b in zip(outs[0][0], outs[1][0]):
         np.testing.assert_array_equal(a, b)
     np.testing.assert_array_equal(outs[0][1], outs[1][1])
+
+
+def test_backbone_27b_batch4_matches_oracle():
+    """27B layer geometry at batch 4 (the QKV GEMM over 32 block rows, the attention
+    over 4 x 8 key/value heads x 5 slices of a 264-key cache)."""
+    g = syn.BACKBONE_GEOMETRY[5120]
+    _backbone_case(H=5120, nq=g["nq"], nkv=g["nkv"], I=g["I"], L=1, V=4096, B=4, C=256, k=7, seed=520)
+
+
+def test_backbone_flash_geometry_matches_oracle():
+    g = syn.BACKBONE_GEOMETRY[2560]
+    _backbone_case(H=2560, nq=g["nq"], nkv=g["nkv"], I=g["I"], L=2, V=2048, B=2, C=130, k=7, seed=540)
