@@ -83,6 +83,7 @@ struct GemmParams {
   int stages;
   uint32_t tmem_cols;
   uint32_t idesc;
+  int defer_fixup;        // split tiles are added up by gemm_reduce_kernel, not here
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -227,6 +228,32 @@ struct Range {
 
 __device__ __forceinline__ Range cta_range(long long units, int cta, int grid) {
   return {units * cta / grid, units * (cta + 1) / grid};
+}
+
+// The pieces ("segments") of a CTA's unit range, each within one tile: k-blocks kb0 ..
+// kb1 - 1 of `tile`.  In range order segment 0 starts at begin and the last one ends at
+// end.  A single-phase launch processes the last segment first when it is a partial
+// tile and the range holds whole tiles too: the next CTA holds the rest of that tile
+// and processes its own piece first, so every shared tile's pieces are done early and
+// its fix-up runs while whole tiles are still streaming (in range order the piece would
+// come last and the fix-ups of all shared tiles would trail the kernel).  Pieces and
+// their fix-up order are the same in either order, so are the results.
+struct Seg {
+  int tile, kb0, kb1;
+};
+
+__device__ __forceinline__ int seg_count(Range rg, int kbt) {
+  if (rg.end <= rg.begin) return 0;
+  return static_cast<int>((rg.end - 1) / kbt - rg.begin / kbt) + 1;
+}
+
+__device__ __forceinline__ Seg seg_at(Range rg, int kbt, int i, int n, bool last_first) {
+  int j = i;
+  if (last_first && n >= 3 && (rg.end % kbt) != 0) j = (i == 0) ? n - 1 : i - 1;
+  const long long tile = rg.begin / kbt + j;
+  const long long lo = rg.begin > tile * kbt ? rg.begin : tile * kbt;
+  const long long hi = rg.end < (tile + 1) * kbt ? rg.end : (tile + 1) * kbt;
+  return {static_cast<int>(tile), static_cast<int>(lo - tile * kbt), static_cast<int>(hi - tile * kbt)};
 }
 
 // CTA whose range holds unit x: the largest c with floor(U*c/G) <= x.
@@ -433,11 +460,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
                           pol_x);
           if (!ok) break;
         }
-        for (; u < rg.end && ok;) {
-          const int tile = static_cast<int>(u / kbt);
-          const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
-          const long long left = rg.end - u;
-          const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+        // (a two-phase launch keeps range order from where phase 1's prefix stopped)
+        const bool last_first = p.nphase == 1;
+        const int nsg = last_first ? seg_count(rg, kbt) : 0;
+        for (int si = 0; (last_first ? si < nsg : u < rg.end) && ok; ++si) {
+          int tile, kb0, kb1;
+          if (last_first) {
+            const Seg sg = seg_at(rg, kbt, si, nsg, true);
+            tile = sg.tile;
+            kb0 = sg.kb0;
+            kb1 = sg.kb1;
+          } else {
+            tile = static_cast<int>(u / kbt);
+            kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
+            const long long left = rg.end - u;
+            kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+          }
           const int n_tile = tile / p.tiles_m;
           const int m_tile = tile - n_tile * p.tiles_m;
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -484,11 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
       for (int ph = 0; ph < p.nphase && ok; ++ph) {
         const Range rg = cta_range(p.ph[ph].units, cta, grid);
         const int kbt = p.ph[ph].kb_total;
-        for (long long u = rg.begin; u < rg.end && ok;) {
-          const int tile = static_cast<int>(u / kbt);
-          const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
-          const long long left = rg.end - u;
-          const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+        const int nsg = seg_count(rg, kbt);
+        for (int si = 0; si < nsg && ok; ++si) {
+          const Seg sg = seg_at(rg, kbt, si, nsg, p.nphase == 1);
+          const int kb0 = sg.kb0, kb1 = sg.kb1;
           if (!wait_bar(tempty0 + 8u * acc, acc_phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
@@ -523,7 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
           tc_commit(tfull0 + 8u * acc);
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
-          u += kb1 - kb0;
         }
       }
       // Every MMA issued by this thread has completed once this arrives.
@@ -551,11 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
       const int first_tile = static_cast<int>(rg.begin / kbt);
       // phase 0 of a two-phase launch counts its stored tiles for phase 1
       const bool signal = (p.nphase == 2 && ph == 0);
-      for (long long u = rg.begin; u < rg.end;) {
-        const int tile = static_cast<int>(u / kbt);
-        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * kbt);
-        const long long left = rg.end - u;
-        const int kb1 = left < (kbt - kb0) ? kb0 + static_cast<int>(left) : kbt;
+      const int nsg = seg_count(rg, kbt);
+      for (int si = 0; si < nsg; ++si) {
+        const Seg sg = seg_at(rg, kbt, si, nsg, p.nphase == 1);
+        const int tile = sg.tile, kb0 = sg.kb0, kb1 = sg.kb1;
         const int n_tile = tile / p.tiles_m;
         const int m_tile = tile - n_tile * p.tiles_m;
         const int n = n_tile * kBM + row;
@@ -608,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
             atomicAdd(p.sync, 1);
           }
         }
-        if (!whole) {
+        if (!whole && !p.defer_fixup) {
           // Stream-K fix-up: the last CTA to finish a piece of this tile adds the
           // pieces in CTA order and stores the tile.
           __threadfence();
@@ -624,13 +659,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
             __threadfence();
             const int mcount = min(p.BN, p.M - m_base);
             // 16 columns at a time, the loads of up to four pieces issued together;
-            // pieces are added in CTA order.
-            for (int c0 = 0; c0 < mcount; c0 += 16) {
-              float acc16[16];
+            // pieces are added in CTA order.  (24 columns, 96 loads in flight, took
+            // the batch-112 fc's fix-up tail down by 2 us but the kernel to 244
+            // registers and every other shape up by about 0.5 us.)
+            constexpr int kFixCols = 16;
+            for (int c0 = 0; c0 < mcount; c0 += kFixCols) {
+              float accf[kFixCols];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) acc16[j] = 0.0f;
+              for (int j = 0; j < kFixCols; ++j) accf[j] = 0.0f;
               for (int s0 = 0; s0 < nseg; s0 += 4) {
-                float v[4][16];
+                float v[4][kFixCols];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                   if (s0 + q < nseg) {
@@ -640,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
                     const float *src = partials + (static_cast<size_t>(c2) * 2 + slot) *
                                                         static_cast<size_t>(p.BN) * kBM;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < kFixCols; ++j)
                       v[q][j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
                   }
                 }
@@ -648,11 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
                 for (int q = 0; q < 4; ++q)
                   if (s0 + q < nseg)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc16[j] += v[q][j];
+                    for (int j = 0; j < kFixCols; ++j) accf[j] += v[q][j];
               }
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c0 + j < mcount) store_out(od, p.M, m_base + c0 + j, n, acc16[j]);
+              for (int j = 0; j < kFixCols; ++j)
+                if (c0 + j < mcount) store_out(od, p.M, m_base + c0 + j, n, accf[j]);
             }
             if (threadIdx.x == 64) tickets[tile] = 0;
             if (signal) {
@@ -665,7 +703,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
           }
           epi_bar_sync();
         }
-        u += kb1 - kb0;
       }
     }
   }
@@ -689,6 +726,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
       p.sync[1] = 0;
     }
   }
+}
+
+// ------------------------------------------------------------------ deferred fix-up
+// When every tile is split across CTAs (fewer tiles than CTAs: the fc, the small
+// projections), each tile's last arriver would add its pieces at the very end of the
+// GEMM, one CTA per tile, after that CTA's own last piece.  Instead the GEMM only
+// writes its pieces and this kernel adds them for all tiles at once: CTA (tile, 16
+// columns), one thread per weight row, pieces added in CTA order from 0 exactly as
+// the in-kernel fix-up does (the same bits).  A tile held whole by one CTA was stored
+// by the GEMM and is skipped.
+struct ReduceArgs {
+  float *partials;
+  void *out;
+  const float *a_scale, *w_scale;
+  long long ldo, units;
+  int kb_total, N, out_bf16, M, BN, tiles_m, grid;
+};
+
+__global__ void __launch_bounds__(kBM) gemm_reduce_kernel(const ReduceArgs a) {
+  pdl_wait();
+  pdl_release();
+  const int tile = blockIdx.x;
+  const int c0 = blockIdx.y * 16;
+  const int row = threadIdx.x;
+  const int n_tile = tile / a.tiles_m;
+  const int m_base = (tile - n_tile * a.tiles_m) * a.BN;
+  const int n = n_tile * kBM + row;
+  const long long t_first = static_cast<long long>(tile) * a.kb_total;
+  const int c_first = cta_of_unit(t_first, a.units, a.grid);
+  const int c_last = cta_of_unit(t_first + a.kb_total - 1, a.units, a.grid);
+  const int mcount = min(a.BN, a.M - m_base);
+  if (c_first == c_last || c0 >= mcount) return;
+  float acc[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+  for (int c2 = c_first; c2 <= c_last; ++c2) {
+    const int tile_c2 = static_cast<int>((a.units * c2 / a.grid) / a.kb_total);
+    const int slot = (tile == tile_c2) ? 0 : 1;
+    const float *src = a.partials + (static_cast<size_t>(c2) * 2 + slot) * static_cast<size_t>(a.BN) * kBM;
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] += v[j];
+  }
+  OutDesc od;
+  od.out = a.out;
+  od.a_scale = a.a_scale;
+  od.w_scale = a.w_scale;
+  od.ldo = a.ldo;
+  od.N = a.N;
+  od.out_bf16 = a.out_bf16;
+  od.pol = policy_evict_last();
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (c0 + j < mcount) store_out(od, a.M, m_base + c0 + j, n, acc[j]);
 }
 
 // ------------------------------------------------------------------ host side
@@ -860,12 +953,38 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
   long long grid = sms < kMaxGemmCtas ? sms : kMaxGemmCtas;
   const long long by_work = t.units / 4 > 0 ? t.units / 4 : 1;
   if (grid > by_work) grid = by_work;
+  // Fewer tiles than CTAs: every tile is split.  Where its fix-up is heavy (tiles of 32
+  // or more activation rows, or K of 320 k-blocks and more, split about four ways:
+  // the fc), the pieces are added by a second kernel; for the small projections the
+  // in-kernel fix-up is cheaper than one more launch.  (Measured: the batch-112 fc 67
+  // -> 51 us; the 8- and 15-row backbone projections about 1 us slower deferred.)
+  const bool defer = static_cast<long long>(t.tiles_m) * t.tiles_n < grid && (t.BN >= 32 || t.kb_total >= 320);
+  p.defer_fixup = defer ? 1 : 0;
   if (!configure(pr.fp8)) return DSPARK_ERR_CUDA;
   auto kern = pr.fp8 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
   if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), t.smem, stream, p) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);
+  if (defer) {
+    ReduceArgs r;
+    r.partials = p.ph[0].partials;
+    r.out = p.ph[0].out;
+    r.a_scale = p.ph[0].a_scale;
+    r.w_scale = p.ph[0].w_scale;
+    r.ldo = p.ph[0].ldo;
+    r.units = p.ph[0].units;
+    r.kb_total = p.ph[0].kb_total;
+    r.N = p.ph[0].N;
+    r.out_bf16 = p.ph[0].out_bf16;
+    r.M = p.M;
+    r.BN = p.BN;
+    r.tiles_m = p.tiles_m;
+    r.grid = static_cast<int>(grid);
+    const dim3 rgrid(static_cast<unsigned>(t.tiles_m * t.tiles_n), static_cast<unsigned>((t.BN + 15) / 16));
+    if (launch_pdl(gemm_reduce_kernel, rgrid, dim3(kBM), 0, stream, r) != cudaSuccess) return DSPARK_ERR_CUDA;
+    count_launches(1);
+  }
   return DSPARK_OK;
 }
 
