@@ -190,27 +190,75 @@ def test_27b_verify_probabilistic_full_vocab(B):
 
 # ----------------------------------------------------------------------------- whole steps
 
-def _whole_step(label, w, wd, B, k, H, T, V, seed, conf, split):
-    """One step through the GPU path exactly as the benchmark runs it (GPU fc -> LM head ->
-    chain with q statistics -> [confidence] -> probabilistic verify), against the oracle
-    from scratch on the same inputs.  Checks, in order: h within the fc bound; the draft
-    logits within the logit tolerance and the tokens equal (near-tie flips counted, the
-    oracle then teacher-forced); draft lengths equal away from the confidence window;
-    verify bit-exact against the oracle on the GPU's own drafts and draft logits (only
-    the oracle's margin exclusions skipped); and against the oracle's from-scratch step,
+def _bb_vals(bits):
+    return syn.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _backbone_from_fc(bbc, w, wd, hd, gh, prev, B, k, H, V, seed):
+    """The drafter backbone between the fc and the LM head, as the benchmark runs it: the
+    caches hold C - k older context rows (written by backbone_context), the fc output
+    hd becomes each request's newest k context rows inside backbone_block, and the
+    block is [prev, mask x k] with the LM head's weight as the embedding table.  Checked
+    against the oracle's backbone on the same context (the older rows, then the GPU's fc
+    rows, which the fc check covers) within the chained-layer bound: rms error at most
+    2^-7 and max error at most 2^-4 of the reference's rms, per request.  Returns the
+    GPU's h (the LM head's input)."""
+    from oracle import backbone as bb
+    g = syn.BACKBONE_GEOMETRY[H]
+    L, C = bbc["L"], bbc["C"]
+    layers, wf = syn.backbone_weights(H, g["nq"], g["nkv"], g["I"], L, seed=seed + 300)
+    lay_d = [ds.BackboneLayer(l["nq"], l["nkv"], *[dev_bf16(l[x]) for x in (
+        "w_in", "w_post", "w_qn", "w_kn", "w_qkv", "w_o", "w_gu", "w_d")]) for l in layers]
+    old = syn.normal_bf16(seed + 301, (B, C - k, H))
+    kcs = [torch.zeros((B, C + k + 1, g["nkv"], 128), dtype=torch.bfloat16, device="cuda") for _ in layers]
+    vcs = [torch.zeros_like(t) for t in kcs]
+    wsp = ds.Workspaces()
+    ds.backbone_context(dev_bf16(old.reshape(-1, H)), lay_d, kcs, vcs, 0, workspaces=wsp)
+    toks = np.concatenate([np.asarray(prev)[:, None], np.full((B, k), V - 1)], axis=1).astype(np.int32)
+    hb = ds.backbone_block(dev(toks), wd["lm_w"], lay_d, dev_bf16(wf), kcs, vcs, C, workspaces=wsp,
+                           ctx=hd, ctx_pos0=C - k)
+    got = _bb_vals(host_bf16_bits(hb)).reshape(B, k, H)
+    ref_layers = []
+    for l in layers:
+        ref_layers.append({n: (_bb_vals(v) if isinstance(v, np.ndarray) else v) for n, v in l.items()})
+        ref_layers[-1]["hd"] = 128
+    new = gh.reshape(B, k, H)
+    for b in range(B):
+        ctx_b = _bb_vals(np.concatenate([old[b], new[b]]))
+        emb = _bb_vals(w["lm_w"][toks[b]])        # the block's rows of the tied table
+        ref = bb.backbone(np.arange(k + 1), ctx_b, ref_layers, _bb_vals(wf), emb)
+        err = got[b] - ref
+        rms = np.sqrt(np.mean(ref ** 2))
+        assert np.sqrt(np.mean(err ** 2)) <= rms * 2.0 ** -7, (b, np.sqrt(np.mean(err ** 2)) / rms)
+        assert np.abs(err).max() <= rms * 2.0 ** -4, (b, np.abs(err).max() / rms)
+    return hb
+
+
+def _whole_step(label, w, wd, B, k, H, T, V, seed, conf, split, backbone=None):
+    """One step through the GPU path exactly as the benchmark runs it (GPU fc -> [drafter
+    backbone ->] LM head -> chain with q statistics -> [confidence] -> probabilistic
+    verify), against the oracle from scratch on the same inputs.  Checks, in order: h
+    within the fc bound; [the backbone's output within its chained bound, after which the
+    oracle's readout starts from the GPU's backbone output;] the draft logits within the
+    logit tolerance and the tokens equal (near-tie flips counted, the oracle then
+    teacher-forced); draft lengths equal away from the confidence window; verify
+    bit-exact against the oracle on the GPU's own drafts and draft logits (only the
+    oracle's margin exclusions skipped); and against the oracle's from-scratch step,
     where a request also counts as excluded when the oracle's own decision changes
     between its draft logits and the GPU's."""
     st = syn.step_inputs(seed, B, k, H, T, V, ("ramp", 0.5, 3.0))
     hd = ds.fc_project([dev_bf16(t) for t in st["taps"]], wd["fc_w"])
+    gh = host_bf16_bits(hd)
+    h_ref = oracle.fc_project(st["taps"], w["fc_w"])
+    _fc_bound_ok(gh, h_ref, st["taps"], w["fc_w"])
+    if backbone is not None:
+        hd = _backbone_from_fc(backbone, w, wd, hd, gh, st["prev"], B, k, H, V, seed)
+        gh = h_ref = host_bf16_bits(hd)
     out = ds.draft_readout(hd, wd["lm_w"], wd["w1"], wd["w2"], dev(st["prev"]), B, k,
                            conf_w=wd["conf_w"] if conf else None, conf_b=0.0, conf_tau=0.5)
     gz = host(out["logits"])
     gd = host(out["draft_tokens"])
     gl = host(out["draft_len"])
-    gh = host_bf16_bits(hd)
-    # oracle from scratch
-    h_ref = oracle.fc_project(st["taps"], w["fc_w"])
-    _fc_bound_ok(gh, h_ref, st["taps"], w["fc_w"])
     logits = oracle.lm_head(h_ref, w["lm_w"]).reshape(B, k, V)
     ch = chain_forced(logits, w["w1"], w["w2"], st["prev"], gd, lens=gl)
     zerr = np.abs(gz.astype(np.float64) - ch["z"])
@@ -276,6 +324,15 @@ def test_27b_b1_whole_step(w27, w27_dev):
                 False, True)
 
 
+@pytest.mark.parametrize("B,conf", [(1, False), (2, True)])
+def test_27b_whole_step_with_backbone(w27, w27_dev, B, conf):
+    """The benchmark's backbone step: one 27B drafter layer over a 1024-token context
+    between the fc and the LM head (batch 1), and batch 2 with the confidence head
+    reading the backbone's output."""
+    _whole_step("27b_b%d_backbone whole step (split verify)" % B, w27, w27_dev, B, 7, 5120, 5, 151936,
+                24 + B, conf, True, backbone=dict(L=1, C=1024))
+
+
 # ----------------------------------------------------------------------------- Flash-Next
 
 def test_flash_prefill_fc_4096_tokens():
@@ -296,6 +353,16 @@ def test_flash_b4_whole_step():
     w = syn.weights(H, T, V, r, with_conf=True)
     wd = {n: dev_bf16(v) for n, v in w.items() if isinstance(v, np.ndarray)}
     _whole_step("flash_b4 whole step (split verify)", w, wd, B, k, H, T, V, 23, False, True)
+
+
+def test_flash_b2_whole_step_with_two_backbone_layers():
+    """Flash-Next geometry (H 2560, 20 query / 4 key-value heads), two backbone layers over
+    a 200-token context, batch 2, confidence head on."""
+    B, k, H, T, V, r = 2, 7, 2560, 5, 151936, 64
+    w = syn.weights(H, T, V, r, with_conf=True)
+    wd = {n: dev_bf16(v) for n, v in w.items() if isinstance(v, np.ndarray)}
+    _whole_step("flash_b2_backbone whole step (inline verify)", w, wd, B, k, H, T, V, 27, True, False,
+                backbone=dict(L=2, C=200))
 
 
 # ----------------------------------------------------------------------------- Tiny, 8 steps
