@@ -223,77 +223,144 @@ struct AttnArgs {
 };
 
 // CTA (split s, kv head g, request b): keys s*64 .. s*64+63 (those below nkeys) for
-// the nqry = nr * (nq / nkv) query rows of the group (query qi = block row
-// qi / grp, head g * grp + qi % grp).  Scores by one key per lane (the key row in
-// registers, the scaled queries in shared memory), softmax per query row over the
-// slice (its max and sum kept for the merge), then P.V with 4 dims per lane.
+// the nqry = nr * (nq / nkv) query rows of the group (query qi = block row qi / grp,
+// head g * grp + qi % grp).  The two contractions of a slice (scores 48 x 64 x 128,
+// P.V 48 x 128 x 64 with the query rows padded to 48) are warp-level bf16 MMAs with
+// fp32 accumulation (mma.sync m16n8k16; at this size an allocation of tensor memory
+// and its descriptors would cost more than the products): scores from the bf16 q and
+// k rows, scaled by 1/sqrt(128) after the sum; softmax per query row over the slice in
+// fp32 (its max and sum kept for the merge); the weights p enter P.V as two bf16 parts
+// hi = bf16(p), lo = bf16(p - hi) (p to about 2^-17 relative), the value rows exact.
+constexpr int kAttnQPad = 48;                 // query rows per CTA (3 tiles of 16)
+constexpr int kAttnRow = kHeadDim + 8;        // bf16 per staged row: 272 B, conflict-free ldmatrix
+constexpr int kAttnPRow = kAttnKeys + 4;      // fp32 per score row
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// d += a . b (m16 x k16 bf16 row-major a, k16 x n8 bf16 b, fp32 d)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// the hi and lo bf16 parts of two fp32 weights, packed (first weight in the low half)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const uint16_t h0 = f2bf(x0), h1 = f2bf(x1);
+  hi = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+  lo = pack2(x0 - bf2f(h0), x1 - bf2f(h1));
+}
+
+size_t attention_smem_bytes() {
+  return static_cast<size_t>(kAttnQPad + 2 * kAttnKeys) * kAttnRow * 2 +
+         static_cast<size_t>(kAttnQPad) * (kAttnPRow + 2) * sizeof(float);
+}
+
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) float attn_smem[];
+  uint16_t *qs = reinterpret_cast<uint16_t *>(attn_smem);     // [48][136] bf16
+  uint16_t *ks = qs + kAttnQPad * kAttnRow;                    // [64][136]
+  uint16_t *vs = ks + kAttnKeys * kAttnRow;                    // [64][136]
+  float *ps = reinterpret_cast<float *>(vs + kAttnKeys * kAttnRow);  // [48][68] scores, then weights
+  float *ml = ps + kAttnQPad * kAttnPRow;                      // [48][2]
   const int nqry = a.nqry;
-  uint16_t *vs = reinterpret_cast<uint16_t *>(attn_smem);              // [64][128] bf16
-  float *qs = attn_smem + kAttnKeys * kHeadDim / 2;                    // [nqry][128]
-  float *sc = qs + nqry * kHeadDim;             // [nqry][64]
-  float *ml = sc + nqry * kAttnKeys;            // [nqry][2]
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = a.nq / a.nkv;
   const int kend = min(kAttnKeys, a.nkeys - split * kAttnKeys);
   pdl_wait();
   pdl_release();
-  // the slice's value rows into shared memory, in flight while the scores are computed
-  for (int e = tid; e < kend * (kHeadDim / 8); e += kAttnThreads) {
-    const int kl = e / (kHeadDim / 8), c = e % (kHeadDim / 8);
-    const uint16_t *src =
-        a.v_cache + ((static_cast<int64_t>(b) * a.cache_len + split * kAttnKeys + kl) * a.nkv + g) * kHeadDim + 8 * c;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
-                     __cvta_generic_to_shared(vs + kl * kHeadDim + 8 * c))),
-                 "l"(src)
-                 : "memory");
+  // stage the slice's key and value rows and the group's query rows (16-byte chunks);
+  // rows past the slice's keys or the group's queries are zero
+  constexpr int kChunks = kHeadDim / 8;
+  for (int e = tid; e < (2 * kAttnKeys + kAttnQPad) * kChunks; e += kAttnThreads) {
+    const int r = e / kChunks, c = e % kChunks;
+    uint16_t *dst;
+    const uint16_t *src = nullptr;
+    if (r < 2 * kAttnKeys) {
+      const int kl = r < kAttnKeys ? r : r - kAttnKeys;
+      dst = (r < kAttnKeys ? ks : vs) + kl * kAttnRow + 8 * c;
+      if (kl < kend)
+        src = (r < kAttnKeys ? a.k_cache : a.v_cache) +
+              ((static_cast<int64_t>(b) * a.cache_len + split * kAttnKeys + kl) * a.nkv + g) * kHeadDim + 8 * c;
+    } else {
+      const int qi = r - 2 * kAttnKeys;
+      dst = qs + qi * kAttnRow + 8 * c;
+      if (qi < nqry) {
+        const int i = qi / grp, head = g * grp + qi % grp;
+        src = a.q + ((static_cast<int64_t>(b) * a.nr + i) * a.nq + head) * kHeadDim + 8 * c;
+      }
+    }
+    if (src) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                       __cvta_generic_to_shared(dst))),
+                   "l"(src)
+                   : "memory");
+    } else {
+      *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
-  for (int e = tid; e < nqry * (kHeadDim / 8); e += kAttnThreads) {
-    const int qi = e / (kHeadDim / 8), c = e % (kHeadDim / 8);
-    const int i = qi / grp, head = g * grp + qi % grp;
-    float v[8];
-    unpack8(*reinterpret_cast<const uint4 *>(a.q + ((static_cast<int64_t>(b) * a.nr + i) * a.nq + head) * kHeadDim + 8 * c), v);
-#pragma unroll
-    for (int t = 0; t < 8; ++t) qs[qi * kHeadDim + 8 * c + t] = v[t] * a.scale;
-  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
-  // scores: warp w takes keys 32 * (w & 1) + lane and query rows of quarter w >> 1
+  const int gq = lane >> 2, tq = lane & 3;   // the mma fragment's row group and column pair
+  const uint32_t qs_a = static_cast<uint32_t>(__cvta_generic_to_shared(qs));
+  const uint32_t ks_a = static_cast<uint32_t>(__cvta_generic_to_shared(ks));
+  const uint32_t vs_a = static_cast<uint32_t>(__cvta_generic_to_shared(vs));
+  // scores: warp w takes keys 8w .. 8w + 7 for the three query tiles
   {
-    const int kl = 32 * (warp & 1) + lane;
-    const int key = split * kAttnKeys + kl;
-    const bool valid = key < a.nkeys;
-    const int qpw = (nqry + 3) / 4;
-    const int q0 = (warp >> 1) * qpw, q1 = min(nqry, q0 + qpw);
-    uint4 kr[kHeadDim / 8];
-    const uint4 *kp = reinterpret_cast<const uint4 *>(
-        a.k_cache + ((static_cast<int64_t>(b) * a.cache_len + (valid ? key : 0)) * a.nkv + g) * kHeadDim);
+    float acc[3][4];
 #pragma unroll
-    for (int c = 0; c < kHeadDim / 8; ++c) kr[c] = valid ? kp[c] : make_uint4(0u, 0u, 0u, 0u);
-    for (int qi = q0; qi < q1; ++qi) {
-      const float4 *qv = reinterpret_cast<const float4 *>(qs + qi * kHeadDim);
-      float s = 0.0f;
+    for (int m = 0; m < 3; ++m)
 #pragma unroll
-      for (int c = 0; c < kHeadDim / 8; ++c) {
-        float kv[8];
-        unpack8(kr[c], kv);
-        const float4 qa = qv[2 * c], qb = qv[2 * c + 1];
-        s = __fmaf_rn(qa.x, kv[0], s); s = __fmaf_rn(qa.y, kv[1], s);
-        s = __fmaf_rn(qa.z, kv[2], s); s = __fmaf_rn(qa.w, kv[3], s);
-        s = __fmaf_rn(qb.x, kv[4], s); s = __fmaf_rn(qb.y, kv[5], s);
-        s = __fmaf_rn(qb.z, kv[6], s); s = __fmaf_rn(qb.w, kv[7], s);
+      for (int i = 0; i < 4; ++i) acc[m][i] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+      uint32_t b0, b1;
+      ldsm_x2(ks_a + ((8 * warp + (lane & 7)) * kAttnRow + 16 * kk + ((lane >> 3) & 1) * 8) * 2, b0, b1);
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(qs_a + ((16 * m + (lane & 15)) * kAttnRow + 16 * kk + (lane >> 4) * 8) * 2, a0, a1, a2, a3);
+        mma_bf16(acc[m], a0, a1, a2, a3, b0, b1);
       }
-      sc[qi * kAttnKeys + kl] = valid ? s : -INFINITY;
+    }
+    const int key0 = 8 * warp + 2 * tq;
+    const bool v0 = key0 < kend, v1 = key0 + 1 < kend;
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      const int r0 = 16 * m + gq;
+      *reinterpret_cast<float2 *>(ps + r0 * kAttnPRow + key0) =
+          make_float2(v0 ? acc[m][0] * a.scale : -INFINITY, v1 ? acc[m][1] * a.scale : -INFINITY);
+      *reinterpret_cast<float2 *>(ps + (r0 + 8) * kAttnPRow + key0) =
+          make_float2(v0 ? acc[m][2] * a.scale : -INFINITY, v1 ? acc[m][3] * a.scale : -INFINITY);
     }
   }
   __syncthreads();
 
-  // softmax over the slice per query row (two keys per lane)
-  for (int qi = warp; qi < nqry; qi += kAttnThreads / 32) {
-    const float s0 = sc[qi * kAttnKeys + lane], s1 = sc[qi * kAttnKeys + 32 + lane];
+  // softmax over the slice per query row (two keys per lane); padded rows get weights 0
+  for (int qi = warp; qi < kAttnQPad; qi += kAttnThreads / 32) {
+    float *row = ps + qi * kAttnPRow;
+    if (qi >= nqry) {
+      row[lane] = 0.0f;
+      row[32 + lane] = 0.0f;
+      continue;
+    }
+    const float s0 = row[lane], s1 = row[32 + lane];
     float m = fmaxf(s0, s1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -302,47 +369,61 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnArgs 
     float l = p0 + p1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    sc[qi * kAttnKeys + lane] = p0;
-    sc[qi * kAttnKeys + 32 + lane] = p1;
+    row[lane] = p0;
+    row[32 + lane] = p1;
     if (lane == 0) {
       ml[2 * qi] = m;
       ml[2 * qi + 1] = l;
     }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
-  // P.V: warp w takes query rows w, w + 8, ...; lane dims 4 * lane .. + 3
-  constexpr int kRowsPerWarp = 8;  // nqry <= 64
-  float acc[kRowsPerWarp][4];
+  // P.V: warp w takes dims 16w .. 16w + 15 (two n-tiles) for the three query tiles
+  float acc[3][2][4];
 #pragma unroll
-  for (int t = 0; t < kRowsPerWarp; ++t)
+  for (int m = 0; m < 3; ++m)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-#pragma unroll 4
-  for (int kl = 0; kl < kend; ++kl) {
-    const uint2 vr = *reinterpret_cast<const uint2 *>(vs + kl * kHeadDim + 4 * lane);
-    const float v[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int t = 0; t < kRowsPerWarp; ++t) {
-      const int qi = warp + 8 * t;
-      if (qi < nqry) {
-        const float p = sc[qi * kAttnKeys + kl];
+      for (int i = 0; i < 4; ++i) acc[m][j][i] = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][i] = __fmaf_rn(p, v[i], acc[t][i]);
-      }
+  for (int kk = 0; kk < kAttnKeys / 16; ++kk) {
+    uint32_t b00, b01, b10, b11;   // [n-tile][k half]
+    ldsm_x4_t(vs_a + ((16 * kk + (lane & 15)) * kAttnRow + 16 * warp + (lane >> 4) * 8) * 2, b00, b01, b10, b11);
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      const float *r0 = ps + (16 * m + gq) * kAttnPRow + 16 * kk + 2 * tq;
+      const float *r1 = r0 + 8 * kAttnPRow;
+      const float2 x0 = *reinterpret_cast<const float2 *>(r0);
+      const float2 x1 = *reinterpret_cast<const float2 *>(r1);
+      const float2 x2 = *reinterpret_cast<const float2 *>(r0 + 8);
+      const float2 x3 = *reinterpret_cast<const float2 *>(r1 + 8);
+      uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+      split2(x0.x, x0.y, h0, l0);
+      split2(x1.x, x1.y, h1, l1);
+      split2(x2.x, x2.y, h2, l2);
+      split2(x3.x, x3.y, h3, l3);
+      mma_bf16(acc[m][0], h0, h1, h2, h3, b00, b01);
+      mma_bf16(acc[m][0], l0, l1, l2, l3, b00, b01);
+      mma_bf16(acc[m][1], h0, h1, h2, h3, b10, b11);
+      mma_bf16(acc[m][1], l0, l1, l2, l3, b10, b11);
     }
   }
 #pragma unroll
-  for (int t = 0; t < kRowsPerWarp; ++t) {
-    const int qi = warp + 8 * t;
-    if (qi < nqry) {
-      const int64_t base = ((static_cast<int64_t>(b) * a.nkv + g) * a.nsplit + split) * nqry + qi;
-      *reinterpret_cast<float4 *>(a.part_o + base * kHeadDim + 4 * lane) =
-          make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
-      if (lane == 0) {
-        a.part_ml[2 * base] = ml[2 * qi];
-        a.part_ml[2 * base + 1] = ml[2 * qi + 1];
+  for (int m = 0; m < 3; ++m) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int qi = 16 * m + gq + 8 * half;
+      if (qi < nqry) {
+        const int64_t base = ((static_cast<int64_t>(b) * a.nkv + g) * a.nsplit + split) * nqry + qi;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          *reinterpret_cast<float2 *>(a.part_o + base * kHeadDim + 16 * warp + 8 * j + 2 * tq) =
+              make_float2(acc[m][j][2 * half], acc[m][j][2 * half + 1]);
+        if (tq == 0 && warp == 0) {
+          a.part_ml[2 * base] = ml[2 * qi];
+          a.part_ml[2 * base + 1] = ml[2 * qi + 1];
+        }
       }
     }
   }
@@ -381,7 +462,7 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(const AttnArgs a) 
         }
       }
       const int n = min(32, a.nsplit - s0);
-#pragma unroll 4
+#pragma unroll 8
       for (int j = 0; j < n; ++j) {
         const float ej = __shfl_sync(0xffffffffu, e, j);
         const float4 po = *reinterpret_cast<const float4 *>(
@@ -509,8 +590,7 @@ dspark_status_t attention_launch(const uint16_t *q, const uint16_t *k_cache, con
   const size_t parts = static_cast<size_t>(B) * nkv * a.nsplit * a.nqry;
   a.part_o = static_cast<float *>(ws);
   a.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + align_up(parts * kHeadDim * sizeof(float), kWsAlign));
-  const size_t smem = static_cast<size_t>(kAttnKeys) * kHeadDim * 2 +
-                      static_cast<size_t>(a.nqry) * (kHeadDim + kAttnKeys + 2) * sizeof(float);
+  const size_t smem = attention_smem_bytes();
   static size_t attr_bytes[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DSPARK_ERR_CUDA;
