@@ -430,6 +430,9 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const AttnArgs 
 }
 
 // One warp per (request, kv head, query row): out = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.
+// Slices go 16 at a time: lane j (j < 16) loads slice s0 + j's (m, l) while every lane
+// loads its 4 dims of the 16 slices' o rows, all in flight together; the weights are
+// then passed from lane to lane.  Slices are added in order.
 __global__ void __launch_bounds__(256) attention_merge_kernel(const AttnArgs a) {
   pdl_wait();
   pdl_release();
@@ -442,38 +445,43 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(const AttnArgs a) 
   const int b = static_cast<int>(wid / (static_cast<long long>(a.nqry) * a.nkv));
   const int grp = a.nq / a.nkv;
   const int64_t base0 = ((static_cast<int64_t>(b) * a.nkv + g) * a.nsplit) * a.nqry + qi;
-  // the slices' maxima, one slice per lane
-  float M = -INFINITY;
-  for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, a.part_ml[2 * (base0 + static_cast<int64_t>(s) * a.nqry)]);
+  constexpr int kBatch = 16;
+  float M = -INFINITY, L = 0.0f;
+  float o4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int s0 = 0; s0 < a.nsplit; s0 += kBatch) {
+    const int n = min(kBatch, a.nsplit - s0);
+    float2 mlv = make_float2(-INFINITY, 0.0f);
+    if (lane < n) mlv = *reinterpret_cast<const float2 *>(a.part_ml + 2 * (base0 + static_cast<int64_t>(s0 + lane) * a.nqry));
+    float4 po[kBatch];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float o4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, L = 0.0f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < a.nsplit; s0 += 32) {
-      // lane s0 + j: the weight e^(m - M) of slice s0 + j (0 for an empty slice)
-      const int s = s0 + lane;
-      float e = 0.0f;
-      if (s < a.nsplit) {
-        const int64_t base = base0 + static_cast<int64_t>(s) * a.nqry;
-        const float m = a.part_ml[2 * base];
-        if (m != -INFINITY) {
-          e = expf(m - M);
-          L = __fmaf_rn(e, a.part_ml[2 * base + 1], L);
-        }
-      }
-      const int n = min(32, a.nsplit - s0);
-#pragma unroll 8
-      for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < kBatch; ++j)
+      po[j] = j < n ? *reinterpret_cast<const float4 *>(a.part_o + (base0 + static_cast<int64_t>(s0 + j) * a.nqry) * kHeadDim +
+                                                        4 * lane)
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // the running maximum over the slices so far; earlier sums are rescaled to it
+    float mb = mlv.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const float Mn = fmaxf(M, mb);
+    if (Mn != -INFINITY) {
+      const float r = M == -INFINITY ? 0.0f : expf(M - Mn);
+      L *= r;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o4[i] *= r;
+      const float e = (lane < n && mlv.x != -INFINITY) ? expf(mlv.x - Mn) : 0.0f;
+      float le = e * mlv.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) le += __shfl_xor_sync(0xffffffffu, le, o);
+      L += le;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
         const float ej = __shfl_sync(0xffffffffu, e, j);
-        const float4 po = *reinterpret_cast<const float4 *>(
-            a.part_o + (base0 + static_cast<int64_t>(s0 + j) * a.nqry) * kHeadDim + 4 * lane);
-        o4[0] = __fmaf_rn(ej, po.x, o4[0]); o4[1] = __fmaf_rn(ej, po.y, o4[1]);
-        o4[2] = __fmaf_rn(ej, po.z, o4[2]); o4[3] = __fmaf_rn(ej, po.w, o4[3]);
+        o4[0] = __fmaf_rn(ej, po[j].x, o4[0]); o4[1] = __fmaf_rn(ej, po[j].y, o4[1]);
+        o4[2] = __fmaf_rn(ej, po[j].z, o4[2]); o4[3] = __fmaf_rn(ej, po[j].w, o4[3]);
       }
+      M = Mn;
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
   const int i = qi / grp, head = g * grp + qi % grp;
   uint2 r;
