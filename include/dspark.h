@@ -493,6 +493,34 @@ dspark_status_t dspark_qk_norm_rope(const dspark_bf16_t *qkv, int64_t ld, int nq
                                     dspark_bf16_t *q_out, dspark_bf16_t *k_cache, dspark_bf16_t *v_cache, int B,
                                     int cache_len, int rows_per_req, int pos0, void *stream);
 
+/* The block's input norm and the new context rows' input norm in one launch (the
+ * two are independent; each row's result is the one dspark_embed_rmsnorm,
+ * dspark_add_rmsnorm or dspark_rmsnorm_bf16 gives).  Block rows r < rows: when
+ * table != NULL, x[r, :] = table[tokens[r], :] (the embedding gather, as
+ * dspark_embed_rmsnorm), else x[r, :] += delta[r, :] (delta may be NULL, as
+ * dspark_add_rmsnorm with group 0); out[r, :] = bf16(rmsnorm(x[r, :]) * w).  Context
+ * rows j < ctx_rows: out[rows + j, :] = bf16(rmsnorm(ctx[j, :]) * w).  x [rows, H]
+ * fp32, out rows with stride out_ld, ctx rows with stride ctx_ld (bf16); a token
+ * outside [0, V) is recorded in *status (DSPARK_ERR_BAD_TOKEN) and clamped. */
+dspark_status_t dspark_block_context_rmsnorm(float *x, const dspark_bf16_t *delta, int64_t delta_ld,
+                                             const dspark_bf16_t *table, int V, const int32_t *tokens,
+                                             const dspark_bf16_t *ctx, int64_t ctx_ld, int ctx_rows,
+                                             const dspark_bf16_t *w, dspark_bf16_t *out, int64_t out_ld, int rows,
+                                             int H, int32_t *status, void *stream);
+
+/* dspark_qk_norm_rope of the block rows and of the new context rows in one launch:
+ * the block part exactly as dspark_qk_norm_rope (qkv, ld, nq, nkv, ..., B,
+ * rows_per_req, pos0); context row j (B * ctx_rows_per_req rows, stride ctx_ld)
+ * holds [k heads | v heads] x 128, belongs to request j / ctx_rows_per_req at
+ * position ctx_pos0 + j % ctx_rows_per_req, and goes to the caches like a block
+ * row's k and v.  ctx_rows_per_req = 0: the block rows alone. */
+dspark_status_t dspark_qk_norm_rope_block_context(const dspark_bf16_t *qkv, int64_t ld, int nq, int nkv,
+                                                  const dspark_bf16_t *q_norm_w, const dspark_bf16_t *k_norm_w,
+                                                  float theta, dspark_bf16_t *q_out, dspark_bf16_t *k_cache,
+                                                  dspark_bf16_t *v_cache, int B, int cache_len, int rows_per_req,
+                                                  int pos0, const dspark_bf16_t *ctx_kv, int64_t ctx_ld,
+                                                  int ctx_rows_per_req, int ctx_pos0, void *stream);
+
 /* Grouped-query attention of the block rows over the cache:
  *   out[b, i, j, :] = sum_t softmax_t(q[b, i, j, :] . K[b, t, j / (nq/nkv), :] / sqrt(128))
  *                     * V[b, t, j / (nq/nkv), :],   t = 0 .. nkeys - 1

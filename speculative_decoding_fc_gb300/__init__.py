@@ -140,6 +140,12 @@ def lib():
         L.dspark_qk_norm_rope.restype = _c
         L.dspark_qk_norm_rope.argtypes = [_vp, _i64, _c, _c, _vp, _vp, ctypes.c_float, _vp, _vp, _vp,
                                           _c, _c, _c, _c, _vp]
+        L.dspark_block_context_rmsnorm.restype = _c
+        L.dspark_block_context_rmsnorm.argtypes = [_vp, _vp, _i64, _vp, _c, _vp, _vp, _i64, _c, _vp, _vp, _i64,
+                                                   _c, _c, _vp, _vp]
+        L.dspark_qk_norm_rope_block_context.restype = _c
+        L.dspark_qk_norm_rope_block_context.argtypes = [_vp, _i64, _c, _c, _vp, _vp, ctypes.c_float, _vp, _vp,
+                                                        _vp, _c, _c, _c, _c, _vp, _i64, _c, _c, _vp]
         L.dspark_attention_workspace_size.restype = _sz
         L.dspark_attention_workspace_size.argtypes = [_c] * 5
         L.dspark_attention.restype = _c
@@ -682,6 +688,63 @@ def rmsnorm_bf16(inp, w, out=None, stream=None):
     return out
 
 
+def block_context_rmsnorm(x, w, out, ctx=None, table=None, tokens=None, delta=None, status=None, stream=None):
+    """One launch for the block rows' and the new context rows' input norms: x [rows, H]
+    fp32 is set to table[tokens] (table given) or gets delta added (delta given, else
+    left); out[:rows] = bf16(rmsnorm(x) * w); out[rows:] = bf16(rmsnorm(ctx) * w) of the
+    bf16 context rows ctx [n, H] (optional).  out: bf16 [rows + n, H]."""
+    rows, H = x.shape
+    dev = x.device
+    n = 0 if ctx is None else ctx.shape[0]
+    _need(x, "x", torch.float32)
+    _need(w, "w", torch.bfloat16, (H,))
+    _need(out, "out", torch.bfloat16, (rows + n, H))
+    V = 0
+    if table is not None:
+        V = table.shape[0]
+        _need(table, "table", torch.bfloat16, (V, H))
+        _need(tokens, "tokens", torch.int32)
+        if tokens.numel() != rows:
+            raise ValueError("tokens must hold one id per block row")
+    if delta is not None:
+        _need(delta, "delta", torch.bfloat16, (rows, H))
+    if n:
+        _need(ctx, "ctx", torch.bfloat16, (n, H))
+    _check(lib().dspark_block_context_rmsnorm(_ptr(x), _ptr(delta), H, _ptr(table), V, _ptr(tokens), _ptr(ctx), H,
+                                              n, _ptr(w), _ptr(out), H, rows, H, _ptr(status),
+                                              _stream(stream, dev)), "dspark_block_context_rmsnorm")
+    return out
+
+
+def qk_norm_rope_block_context(qkv, nq, nkv, q_norm_w, k_norm_w, theta, k_cache, v_cache, rows_per_req, pos0,
+                               ctx_kv, ctx_rows_per_req, ctx_pos0, q_out=None, stream=None):
+    """qk_norm_rope of the block rows qkv [B * rows_per_req, (nq + 2 nkv) * 128] and of the
+    context rows ctx_kv [B * ctx_rows_per_req, 2 nkv * 128] (key and value heads, cache
+    slots ctx_pos0 + j) in one launch; both may be column slices of a wider GEMM output.
+    Returns q [B * rows_per_req, nq, 128]."""
+    rows = qkv.shape[0]
+    B, cache_len = k_cache.shape[0], k_cache.shape[1]
+    dev = qkv.device
+    for t, width, name in ((qkv, (nq + 2 * nkv) * 128, "qkv"), (ctx_kv, 2 * nkv * 128, "ctx_kv")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
+                or t.dim() != 2 or t.shape[1] != width or t.stride(1) != 1:
+            raise ValueError("%s must be a CUDA bf16 [rows, %d] tensor with unit column stride" % (name, width))
+    _need(k_norm_w, "k_norm_w", torch.bfloat16, (128,))
+    _need(q_norm_w, "q_norm_w", torch.bfloat16, (128,))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, cache_len, nkv, 128))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, cache_len, nkv, 128))
+    if rows != B * rows_per_req or ctx_kv.shape[0] != B * ctx_rows_per_req:
+        raise ValueError("qkv and ctx_kv must hold B * rows_per_req and B * ctx_rows_per_req rows")
+    if q_out is None:
+        q_out = torch.empty((rows, nq, 128), dtype=torch.bfloat16, device=dev)
+    _need(q_out, "q_out", torch.bfloat16, (rows, nq, 128))
+    _check(lib().dspark_qk_norm_rope_block_context(
+        _ptr(qkv), qkv.stride(0), nq, nkv, _ptr(q_norm_w), _ptr(k_norm_w), float(theta), _ptr(q_out), _ptr(k_cache),
+        _ptr(v_cache), B, cache_len, rows_per_req, pos0, _ptr(ctx_kv), ctx_kv.stride(0), ctx_rows_per_req, ctx_pos0,
+        _stream(stream, dev)), "dspark_qk_norm_rope_block_context")
+    return q_out
+
+
 def qk_norm_rope(qkv, nq, nkv, q_norm_w, k_norm_w, theta, k_cache, v_cache, rows_per_req, pos0,
                  q_out=None, stream=None):
     """Per-head q/k rmsnorm + rotary embedding of qkv rows [B * rows_per_req, (nq + 2 nkv) * 128]
@@ -787,16 +850,22 @@ def backbone_block(tokens, embed, layers, w_final, k_caches, v_caches, C, out=No
     Bb = B * nr
     nc = 0 if ctx is None else ctx.shape[0]
     xin = torch.empty((Bb + nc, H), dtype=torch.bfloat16, device=dev)
-    x, _ = embed_rmsnorm(embed, tokens.reshape(-1), layers[0].w_in, n_out=xin[:Bb], stream=stream)
+    x = torch.empty((Bb, H), dtype=torch.float32, device=dev)
     for li, ly in enumerate(layers):
-        if nc:
-            rmsnorm_bf16(ctx, ly.w_in, out=xin[Bb:], stream=stream)
+        # the block rows' input norm (the embedding gather for the first layer) and the
+        # context rows' one launch
+        if li == 0:
+            block_context_rmsnorm(x, ly.w_in, xin, ctx=ctx, table=embed, tokens=tokens.reshape(-1), stream=stream)
+        else:
+            block_context_rmsnorm(x, ly.w_in, xin, ctx=ctx, delta=d2, stream=stream)
         qkv = linear(xin, ly.w_qkv, stream=stream, workspaces=workspaces, kind="bb_qkv%d" % li)
-        q = qk_norm_rope(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li], v_caches[li], nr, C,
-                         stream=stream)
         if nc:
-            qk_norm_rope(qkv[Bb:, ly.nq * 128:], 0, ly.nkv, None, ly.w_kn, ly.theta, k_caches[li], v_caches[li],
-                         nc // B, ctx_pos0, stream=stream)
+            q = qk_norm_rope_block_context(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li],
+                                           v_caches[li], nr, C, qkv[Bb:, ly.nq * 128:], nc // B, ctx_pos0,
+                                           stream=stream)
+        else:
+            q = qk_norm_rope(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li], v_caches[li], nr, C,
+                             stream=stream)
         o = attention(q.view(B, nr, ly.nq, 128), k_caches[li], v_caches[li], C + nr, stream=stream,
                       workspaces=workspaces)
         d = linear(o.view(B * nr, ly.nq * 128), ly.w_o, stream=stream, workspaces=workspaces, kind="bb_o%d" % li)
@@ -804,10 +873,7 @@ def backbone_block(tokens, embed, layers, w_final, k_caches, v_caches, C, out=No
         gu = linear(n2, ly.w_gu, stream=stream, workspaces=workspaces, kind="bb_gu%d" % li)
         act = silu_mul(gu, stream=stream)
         d2 = linear(act, ly.w_d, stream=stream, workspaces=workspaces, kind="bb_d%d" % li)
-        if li + 1 < len(layers):
-            # residual add, then the next layer's input norm
-            add_rmsnorm(x, d2, layers[li + 1].w_in, out=xin[:Bb], stream=stream)
-        else:
+        if li + 1 == len(layers):
             if out is None:
                 out = torch.empty((B * (nr - 1), H), dtype=torch.bfloat16, device=dev)
             add_rmsnorm(x, d2, w_final, out=out, group=nr, stream=stream)

@@ -751,6 +751,55 @@ dspark_status_t dspark_qk_norm_rope(const dspark_bf16_t *qkv, int64_t ld, int nq
                              rows_per_req, pos0, B * rows_per_req, as_stream(stream));
 }
 
+dspark_status_t dspark_block_context_rmsnorm(float *x, const dspark_bf16_t *delta, int64_t delta_ld,
+                                             const dspark_bf16_t *table, int V, const int32_t *tokens,
+                                             const dspark_bf16_t *ctx, int64_t ctx_ld, int ctx_rows,
+                                             const dspark_bf16_t *w, dspark_bf16_t *out, int64_t out_ld, int rows,
+                                             int H, int32_t *status, void *stream) {
+  if (!x || !w || !out || rows < 1 || ctx_rows < 0 || H < 8 || !ld_ok(out_ld, H)) return DSPARK_ERR_INVALID_ARG;
+  if (table && (!tokens || V < 1)) return DSPARK_ERR_INVALID_ARG;
+  if (!table && delta && !ld_ok(delta_ld, H)) return DSPARK_ERR_INVALID_ARG;
+  if (ctx_rows > 0 && (!ctx || !ld_ok(ctx_ld, H))) return DSPARK_ERR_INVALID_ARG;
+  if (H % 8 != 0 || H > kMaxNormH || rows + static_cast<long long>(ctx_rows) > kMaxM)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (table && (!aligned16(table) || !aligned4(tokens))) ||
+      (!table && delta && !aligned16(delta)) || (ctx_rows > 0 && !aligned16(ctx)) || (status && !aligned4(status)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return norm_rows_launch(x, table ? nullptr : delta, delta_ld, table, tokens, V, nullptr, 0, w, out, out_ld, 0, rows,
+                          H, status, as_stream(stream), ctx_rows > 0 ? ctx : nullptr, ctx_ld, ctx_rows);
+}
+
+dspark_status_t dspark_qk_norm_rope_block_context(const dspark_bf16_t *qkv, int64_t ld, int nq, int nkv,
+                                                  const dspark_bf16_t *q_norm_w, const dspark_bf16_t *k_norm_w,
+                                                  float theta, dspark_bf16_t *q_out, dspark_bf16_t *k_cache,
+                                                  dspark_bf16_t *v_cache, int B, int cache_len, int rows_per_req,
+                                                  int pos0, const dspark_bf16_t *ctx_kv, int64_t ctx_ld,
+                                                  int ctx_rows_per_req, int ctx_pos0, void *stream) {
+  if (!qkv || !k_norm_w || !k_cache || !v_cache || (nq > 0 && (!q_out || !q_norm_w)))
+    return DSPARK_ERR_INVALID_ARG;
+  if (nq < 0 || nkv < 1 || B < 1 || rows_per_req < 1 || pos0 < 0 || !(theta > 1.0f) || ctx_rows_per_req < 0 ||
+      ctx_pos0 < 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!ld_ok(ld, (nq + 2 * nkv) * 128) || static_cast<long long>(pos0) + rows_per_req > cache_len)
+    return DSPARK_ERR_INVALID_ARG;
+  if (ctx_rows_per_req > 0 && (!ctx_kv || !ld_ok(ctx_ld, 2 * nkv * 128) ||
+                               static_cast<long long>(ctx_pos0) + ctx_rows_per_req > cache_len))
+    return DSPARK_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * (rows_per_req + ctx_rows_per_req) > kMaxM || nq + 2 * nkv > 4096)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(qkv) || !aligned16(k_norm_w) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (nq > 0 && (!aligned16(q_out) || !aligned16(q_norm_w))) || (ctx_rows_per_req > 0 && !aligned16(ctx_kv)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = check_device();
+  if (st != DSPARK_OK) return st;
+  return qk_norm_rope_launch(qkv, ld, nq, nkv, q_norm_w, k_norm_w, theta, q_out, k_cache, v_cache, cache_len,
+                             rows_per_req, pos0, B * rows_per_req, as_stream(stream),
+                             ctx_rows_per_req > 0 ? ctx_kv : nullptr, ctx_ld, ctx_rows_per_req, ctx_pos0,
+                             B * ctx_rows_per_req);
+}
+
 size_t dspark_attention_workspace_size(int B, int nr, int nq, int nkv, int nkeys) {
   if (B < 1 || nr < 1 || nq < 1 || nkv < 1 || nq % nkv != 0 || nkeys < 1) return 0;
   return attention_workspace_bytes(B, nr, nq, nkv, nkeys);

@@ -56,24 +56,34 @@ struct NormArgs {
   uint16_t *out;             // bf16 output rows
   int64_t ld_out;
   int group;                 // > 0: the first row of each group of `group` rows is not written
-  int rows, H;
+  int rows, H;               // rows of the first part (the grid may add in2's rows)
+  const uint16_t *in2;       // second part: plain bf16 rows (out rows rows, rows + 1, ...)
+  int64_t ld_in2;
   int *status;
 };
 
 // out = bf16(v / sqrt(mean(v^2) + eps) * w) of the row's values v (after the add or
 // gather, which also land in x).  One CTA per row; each thread keeps its (at most 4)
-// 16-byte chunks in registers between the sum of squares and the output.
+// 16-byte chunks in registers between the sum of squares and the output.  CTAs past
+// the first part's rows norm the second part's plain rows (the context rows beside
+// the block rows: one launch for both).
 __global__ void __launch_bounds__(kNormThreads) norm_rows_kernel(const NormArgs a) {
   __shared__ float red[kNormThreads / 32];
   pdl_wait();
   pdl_release();
   const int row = blockIdx.x;
+  const bool second = row >= a.rows;
+  float *const xrow = (!second && a.x) ? a.x + static_cast<int64_t>(row) * a.H : nullptr;
+  const uint16_t *const table = second ? nullptr : a.table;
+  const uint16_t *const delta = second ? nullptr : a.delta;
+  const uint16_t *const inrow = second ? a.in2 + static_cast<int64_t>(row - a.rows) * a.ld_in2
+                                       : (a.in ? a.in + static_cast<int64_t>(row) * a.ld_in : nullptr);
   const int H = a.H, nc = H / 8;
   const int tid = threadIdx.x;
   float v[kNormMaxChunks][8];
   float ss = 0.0f;
   int tok = 0;
-  if (a.table) {
+  if (table) {
     tok = a.tok[row];
     if (tok < 0 || tok >= a.V) {
       if (tid == 0) record_error(a.status, DSPARK_ERR_BAD_TOKEN);
@@ -84,17 +94,17 @@ __global__ void __launch_bounds__(kNormThreads) norm_rows_kernel(const NormArgs 
   for (int u = 0; u < kNormMaxChunks; ++u) {
     const int c = tid + u * kNormThreads;
     if (c >= nc) break;
-    if (a.x) {
-      float4 *xp = reinterpret_cast<float4 *>(a.x + static_cast<int64_t>(row) * H) + 2 * c;
-      if (a.table) {
-        unpack8(*reinterpret_cast<const uint4 *>(a.table + static_cast<int64_t>(tok) * H + 8 * c), v[u]);
+    if (xrow) {
+      float4 *xp = reinterpret_cast<float4 *>(xrow) + 2 * c;
+      if (table) {
+        unpack8(*reinterpret_cast<const uint4 *>(table + static_cast<int64_t>(tok) * H + 8 * c), v[u]);
       } else {
         const float4 x0 = xp[0], x1 = xp[1];
         v[u][0] = x0.x; v[u][1] = x0.y; v[u][2] = x0.z; v[u][3] = x0.w;
         v[u][4] = x1.x; v[u][5] = x1.y; v[u][6] = x1.z; v[u][7] = x1.w;
-        if (a.delta) {
+        if (delta) {
           float d[8];
-          unpack8(*reinterpret_cast<const uint4 *>(a.delta + static_cast<int64_t>(row) * a.ld_delta + 8 * c), d);
+          unpack8(*reinterpret_cast<const uint4 *>(delta + static_cast<int64_t>(row) * a.ld_delta + 8 * c), d);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[u][i] = __fadd_rn(v[u][i], d[i]);
         }
@@ -102,7 +112,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_rows_kernel(const NormArgs 
       xp[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
       xp[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
     } else {
-      unpack8(*reinterpret_cast<const uint4 *>(a.in + static_cast<int64_t>(row) * a.ld_in + 8 * c), v[u]);
+      unpack8(*reinterpret_cast<const uint4 *>(inrow + 8 * c), v[u]);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss = __fmaf_rn(v[u][i], v[u][i], ss);
@@ -117,7 +127,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_rows_kernel(const NormArgs 
   const float inv = 1.0f / sqrtf(tot / static_cast<float>(H) + kNormEps);
 
   int orow = row;
-  if (a.group > 0) {
+  if (a.group > 0 && !second) {
     const int i = row % a.group;
     if (i == 0) return;
     orow = (row / a.group) * (a.group - 1) + i - 1;
@@ -147,6 +157,11 @@ struct RopeArgs {
   uint16_t *k_cache, *v_cache;  // [B, cache_len, nkv, 128]
   int cache_len, rows_per_req, pos0, rows;
   double log2_theta;
+  // a second group of rows holding key and value heads only (the context rows beside
+  // the block rows, one launch for both): [rows2, ld2] = [k heads | v heads] x 128
+  const uint16_t *kv2;
+  int64_t ld2;
+  int rows_per_req2, pos02, rows2;
 };
 
 // One warp per (row, head), 4 dims per lane (lanes 0-15 the first half of the head,
@@ -161,12 +176,26 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const RopeArgs a) {
   pdl_release();
   const int nh = a.nq + 2 * a.nkv;
   const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (wid >= static_cast<long long>(a.rows) * nh) return;
+  const long long n1 = static_cast<long long>(a.rows) * nh;
   const int lane = threadIdx.x & 31;
-  const int row = static_cast<int>(wid / nh), h = static_cast<int>(wid % nh);
-  const int b = row / a.rows_per_req;
-  const int pos = a.pos0 + row % a.rows_per_req;
-  const uint2 raw = *reinterpret_cast<const uint2 *>(a.qkv + static_cast<int64_t>(row) * a.ld + h * kHeadDim + 4 * lane);
+  int h, b, pos, row = 0;
+  const uint16_t *src;
+  if (wid < n1) {
+    row = static_cast<int>(wid / nh);
+    h = static_cast<int>(wid % nh);
+    b = row / a.rows_per_req;
+    pos = a.pos0 + row % a.rows_per_req;
+    src = a.qkv + static_cast<int64_t>(row) * a.ld + h * kHeadDim;
+  } else {
+    const long long w2 = wid - n1;
+    if (w2 >= static_cast<long long>(a.rows2) * 2 * a.nkv) return;
+    const int row2 = static_cast<int>(w2 / (2 * a.nkv)), h2 = static_cast<int>(w2 % (2 * a.nkv));
+    h = a.nq + h2;   // a key or value head: no q row
+    b = row2 / a.rows_per_req2;
+    pos = a.pos02 + row2 % a.rows_per_req2;
+    src = a.kv2 + static_cast<int64_t>(row2) * a.ld2 + h2 * kHeadDim;
+  }
+  const uint2 raw = *reinterpret_cast<const uint2 *>(src + 4 * lane);
   if (h >= a.nq + a.nkv) {  // value head: to the cache as it is
     const int g = h - a.nq - a.nkv;
     *reinterpret_cast<uint2 *>(a.v_cache + ((static_cast<int64_t>(b) * a.cache_len + pos) * a.nkv + g) * kHeadDim +
@@ -519,7 +548,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *gu, uint1
 dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_delta, const uint16_t *table,
                                  const int32_t *tok, int V, const uint16_t *in, int64_t ld_in,
                                  const uint16_t *w, uint16_t *out, int64_t ld_out, int group, int rows,
-                                 int H, int *status, cudaStream_t stream) {
+                                 int H, int *status, cudaStream_t stream, const uint16_t *in2, int64_t ld_in2,
+                                 int rows2) {
   NormArgs a;
   a.x = x;
   a.delta = delta;
@@ -535,9 +565,11 @@ dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_del
   a.group = group;
   a.rows = rows;
   a.H = H;
+  a.in2 = in2;
+  a.ld_in2 = ld_in2;
   a.status = status;
-  if (launch_pdl(norm_rows_kernel, dim3(static_cast<unsigned>(rows)), dim3(kNormThreads), 0, stream, a) !=
-      cudaSuccess)
+  if (launch_pdl(norm_rows_kernel, dim3(static_cast<unsigned>(rows + (in2 ? rows2 : 0))), dim3(kNormThreads), 0,
+                 stream, a) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(1);
   return DSPARK_OK;
@@ -546,7 +578,8 @@ dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_del
 dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int nkv, const uint16_t *wq,
                                     const uint16_t *wk, float theta, uint16_t *q_out, uint16_t *k_cache,
                                     uint16_t *v_cache, int cache_len, int rows_per_req, int pos0, int rows,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, const uint16_t *kv2, int64_t ld2, int rows_per_req2,
+                                    int pos02, int rows2) {
   RopeArgs a;
   a.qkv = qkv;
   a.ld = ld;
@@ -562,7 +595,12 @@ dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int
   a.pos0 = pos0;
   a.rows = rows;
   a.log2_theta = log2(static_cast<double>(theta));
-  const long long warps = static_cast<long long>(rows) * (nq + 2 * nkv);
+  a.kv2 = kv2;
+  a.ld2 = ld2;
+  a.rows_per_req2 = rows_per_req2 > 0 ? rows_per_req2 : 1;
+  a.pos02 = pos02;
+  a.rows2 = kv2 ? rows2 : 0;
+  const long long warps = static_cast<long long>(rows) * (nq + 2 * nkv) + static_cast<long long>(a.rows2) * 2 * nkv;
   if (launch_pdl(qk_norm_rope_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0, stream, a) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;

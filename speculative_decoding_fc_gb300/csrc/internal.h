@@ -73,11 +73,13 @@ dspark_status_t confidence_launch(const uint16_t *h, const uint16_t *conf_w, flo
 dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_delta, const uint16_t *table,
                                  const int32_t *tok, int V, const uint16_t *in, int64_t ld_in,
                                  const uint16_t *w, uint16_t *out, int64_t ld_out, int group, int rows,
-                                 int H, int *status, cudaStream_t stream);
+                                 int H, int *status, cudaStream_t stream, const uint16_t *in2 = nullptr,
+                                 int64_t ld_in2 = 0, int rows2 = 0);
 dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int nkv, const uint16_t *wq,
                                     const uint16_t *wk, float theta, uint16_t *q_out, uint16_t *k_cache,
                                     uint16_t *v_cache, int cache_len, int rows_per_req, int pos0, int rows,
-                                    cudaStream_t stream);
+                                    cudaStream_t stream, const uint16_t *kv2 = nullptr, int64_t ld2 = 0,
+                                    int rows_per_req2 = 1, int pos02 = 0, int rows2 = 0);
 size_t attention_workspace_bytes(int B, int nr, int nq, int nkv, int nkeys);
 dspark_status_t attention_launch(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                  uint16_t *out, int B, int nr, int nq, int nkv, int cache_len, int nkeys,

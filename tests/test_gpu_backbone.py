@@ -307,3 +307,45 @@ def test_backbone_27b_batch4_matches_oracle():
 def test_backbone_flash_geometry_matches_oracle():
     g = syn.BACKBONE_GEOMETRY[2560]
     _backbone_case(H=2560, nq=g["nq"], nkv=g["nkv"], I=g["I"], L=2, V=2048, B=2, C=130, k=7, seed=540)
+
+
+def test_fused_norm_and_rope_launches_equal_separate_calls():
+    """dspark_block_context_rmsnorm and dspark_qk_norm_rope_block_context (the block rows
+    and the new context rows in one launch) give the bits of the separate calls: the
+    embedding-gather or residual-add norm of the block rows and the plain norm of the
+    context rows; the block rows' q/k norm + rotary and the context rows' k one."""
+    H, V, B, nr, n, nq, nkv, C = 256, 300, 2, 5, 3, 4, 2, 20
+    E = dev_bf16(syn.normal_bf16(700, (V, H), 0.5))
+    w = dev_bf16(syn.normal_bf16(701, (H,), 0.3))
+    toks = dev(np.array([[1, 299, 5, 7, 9], [0, 2, 4, 6, 8]], dtype=np.int32)).reshape(-1)
+    ctx = dev_bf16(syn.normal_bf16(702, (B * n, H)))
+    delta = dev_bf16(syn.normal_bf16(703, (B * nr, H)))
+    x1, n1 = ds.embed_rmsnorm(E, toks, w)
+    c1 = ds.rmsnorm_bf16(ctx, w)
+    x2 = torch.empty((B * nr, H), dtype=torch.float32, device="cuda")
+    out2 = torch.empty((B * (nr + n), H), dtype=torch.bfloat16, device="cuda")
+    ds.block_context_rmsnorm(x2, w, out2, ctx=ctx, table=E, tokens=toks)
+    np.testing.assert_array_equal(host(x1), host(x2))
+    np.testing.assert_array_equal(host_bf16_bits(n1), host_bf16_bits(out2[:B * nr]))
+    np.testing.assert_array_equal(host_bf16_bits(c1), host_bf16_bits(out2[B * nr:]))
+    x3, x4 = x1.clone(), x1.clone()
+    n3 = ds.add_rmsnorm(x3, delta, w)
+    out4 = torch.empty_like(out2)
+    ds.block_context_rmsnorm(x4, w, out4, ctx=ctx, delta=delta)
+    np.testing.assert_array_equal(host(x3), host(x4))
+    np.testing.assert_array_equal(host_bf16_bits(n3), host_bf16_bits(out4[:B * nr]))
+    np.testing.assert_array_equal(host_bf16_bits(c1), host_bf16_bits(out4[B * nr:]))
+
+    width = (nq + 2 * nkv) * 128
+    qkv = dev_bf16(syn.normal_bf16(704, (B * (nr + n), width)))
+    wq = dev_bf16(syn.normal_bf16(705, (128,), 0.5))
+    wk = dev_bf16(syn.normal_bf16(706, (128,), 0.5))
+    caches = [torch.zeros((B, C + nr, nkv, 128), dtype=torch.bfloat16, device="cuda") for _ in range(4)]
+    q1 = ds.qk_norm_rope(qkv[:B * nr], nq, nkv, wq, wk, 1e6, caches[0], caches[1], nr, C)
+    ds.qk_norm_rope(qkv[B * nr:, nq * 128:], 0, nkv, None, wk, 1e6, caches[0], caches[1], n, C - n)
+    q2 = ds.qk_norm_rope_block_context(qkv[:B * nr], nq, nkv, wq, wk, 1e6, caches[2], caches[3], nr, C,
+                                       qkv[B * nr:, nq * 128:], n, C - n)
+    np.testing.assert_array_equal(host_bf16_bits(q1), host_bf16_bits(q2))
+    np.testing.assert_array_equal(host_bf16_bits(caches[0]), host_bf16_bits(caches[2]))
+    np.testing.assert_array_equal(host_bf16_bits(caches[1]), host_bf16_bits(caches[3]))
+    assert host_bf16_bits(caches[2])[:, C - n:C + nr].any()
