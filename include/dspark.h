@@ -537,6 +537,58 @@ dspark_status_t dspark_attention(const dspark_bf16_t *q, const dspark_bf16_t *k_
  * gu [M, 2I] bf16 (the gate|up GEMM output), act [M, I].  I % 8 == 0. */
 dspark_status_t dspark_silu_mul(const dspark_bf16_t *gu, dspark_bf16_t *act, int M, int I, void *stream);
 
+/* ------------------------------------------------------------------------
+ * The drafter backbone's block pass, all layers in one call ([PR620]
+ * DSparkDraftModel, "the DFlash backbone"; the layer form is a reading: the
+ * Qwen3 pre-norm decoder layer, see the calls above).  Per layer, with the
+ * block rows x (fp32 residual) and the new context rows ctx:
+ *   n      = rmsnorm(x) * w_in (first layer: x = embed[tokens])   and the
+ *            context rows' rmsnorm(ctx) * w_in, one launch
+ *   qkv    = [n ; ctx rows' norm] . w_qkv^T (one GEMM)
+ *   q      = qk norm + rotary of the block rows (positions C .. C + nr - 1); k, v
+ *            of the block rows and of the context rows (positions ctx_pos0 ..)
+ *            into the layer's caches, one launch
+ *   o      = attention over cache slots 0 .. C + nr - 1
+ *   x     += o . w_o^T;  n2 = rmsnorm(x) * w_post
+ *   act    = silu(n2 . w_g^T) * (n2 . w_u^T)
+ *   x     += act . w_d^T
+ * then h_out = rmsnorm(x) * w_final of the mask rows (rows 1 .. nr - 1 of each
+ * request), the LM head's input.  Every value equals the one the separate calls
+ * above give (dspark_block_context_rmsnorm, dspark_linear,
+ * dspark_qk_norm_rope_block_context, dspark_attention, dspark_add_rmsnorm,
+ * dspark_silu_mul): the projections' split tiles are added by the kernel that
+ * reads them, in the same order, instead of by the GEMM.
+ *   tokens [B, nr] int32 (the anchor, then nr - 1 mask tokens); embed [V, H] bf16
+ *   (the LM head's weight: tied embeddings); layers: a HOST array of L structs
+ *   (device pointers inside); the caches hold the context keys and values at
+ *   slots 0 .. C - 1 (ctx_rows_per_req of them, from ctx_pos0, written here);
+ *   ctx [B * ctx_rows_per_req, H] bf16 or NULL with ctx_rows_per_req = 0;
+ *   h_out [B * (nr - 1), H] bf16.  H % 64 == 0, H <= 8192, I % 64 == 0,
+ *   nr * nq / nkv <= 48, C + nr <= cache_len.  The workspace
+ *   (dspark_backbone_block_workspace_size bytes, 256-byte aligned) needs no
+ *   zeroing; device errors (a token outside [0, V), a GEMM wait running out) go
+ *   to its status word.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const dspark_bf16_t *w_in, *w_post;  /* input and post-attention norm weights [H] */
+  const dspark_bf16_t *w_qn, *w_kn;    /* per-head q and k norm weights [128] */
+  const dspark_bf16_t *w_qkv;          /* [(nq + 2 nkv) * 128, H]: Wq; Wk; Wv */
+  const dspark_bf16_t *w_o;            /* [H, nq * 128] */
+  const dspark_bf16_t *w_gu;           /* [2 I, H]: Wg; Wu */
+  const dspark_bf16_t *w_d;            /* [H, I] */
+  dspark_bf16_t *k_cache, *v_cache;    /* [B, cache_len, nkv, 128] */
+  int nq, nkv, I;
+  float theta;                         /* rotary base */
+} dspark_backbone_layer_t;
+
+size_t dspark_backbone_block_workspace_size(int B, int nr, int H, int L, const dspark_backbone_layer_t *layers,
+                                            int ctx_rows_per_req, int C);
+dspark_status_t dspark_backbone_block(const int32_t *tokens, int B, int nr, const dspark_bf16_t *embed, int V,
+                                      int H, int L, const dspark_backbone_layer_t *layers,
+                                      const dspark_bf16_t *w_final, int cache_len, int C, const dspark_bf16_t *ctx,
+                                      int ctx_rows_per_req, int ctx_pos0, dspark_bf16_t *h_out, void *ws,
+                                      size_t ws_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -146,6 +146,11 @@ def lib():
         L.dspark_qk_norm_rope_block_context.restype = _c
         L.dspark_qk_norm_rope_block_context.argtypes = [_vp, _i64, _c, _c, _vp, _vp, ctypes.c_float, _vp, _vp,
                                                         _vp, _c, _c, _c, _c, _vp, _i64, _c, _c, _vp]
+        L.dspark_backbone_block_workspace_size.restype = _sz
+        L.dspark_backbone_block_workspace_size.argtypes = [_c, _c, _c, _c, _vp, _c, _c]
+        L.dspark_backbone_block.restype = _c
+        L.dspark_backbone_block.argtypes = [_vp, _c, _c, _vp, _c, _c, _c, _vp, _vp, _c, _c, _vp, _c, _c, _vp, _vp,
+                                            _sz, _vp]
         L.dspark_attention_workspace_size.restype = _sz
         L.dspark_attention_workspace_size.argtypes = [_c] * 5
         L.dspark_attention.restype = _c
@@ -834,48 +839,62 @@ def backbone_context(ctx, layers, k_caches, v_caches, pos0, stream=None, workspa
         qk_norm_rope(kv, 0, ly.nkv, None, ly.w_kn, ly.theta, kc, vc, n, pos0, stream=stream)
 
 
+class _BackboneLayerC(ctypes.Structure):
+    """dspark_backbone_layer_t."""
+    _fields_ = [("w_in", _vp), ("w_post", _vp), ("w_qn", _vp), ("w_kn", _vp), ("w_qkv", _vp), ("w_o", _vp),
+                ("w_gu", _vp), ("w_d", _vp), ("k_cache", _vp), ("v_cache", _vp), ("nq", ctypes.c_int),
+                ("nkv", ctypes.c_int), ("I", ctypes.c_int), ("theta", ctypes.c_float)]
+
+
 def backbone_block(tokens, embed, layers, w_final, k_caches, v_caches, C, out=None, stream=None,
                    workspaces=None, ctx=None, ctx_pos0=None):
-    """Runs the draft block through the layers and the final norm.  tokens [B, k+1]
-    int32 (anchor, then mask tokens); embed [V, H] bf16 (the LM head's weight); the
-    caches hold each layer's context keys/values at slots 0 .. C - 1, the block's go to
-    C .. C + k.  Returns h [B * k, H] bf16 (mask positions), the LM head's input.
-    ctx [B * n, H] (optional): n new context rows per request (the fc output of the
-    verified tokens), written to cache slots ctx_pos0 .. ctx_pos0 + n - 1 of every
-    layer before its attention; their keys and values come out of the same GEMM as the
-    block's q, k, v (one pass over each layer's [Wq; Wk; Wv])."""
+    """Runs the draft block through the layers and the final norm (dspark_backbone_block:
+    one call).  tokens [B, k+1] int32 (anchor, then mask tokens); embed [V, H] bf16 (the
+    LM head's weight); the caches hold each layer's context keys/values at slots 0 .. C - 1,
+    the block's go to C .. C + k.  Returns h [B * k, H] bf16 (mask positions), the LM head's
+    input.  ctx [B * n, H] (optional): n new context rows per request (the fc output of the
+    verified tokens), written to cache slots ctx_pos0 .. ctx_pos0 + n - 1 of every layer
+    before its attention; their keys and values come out of the same GEMM as the block's
+    q, k, v (one pass over each layer's [Wq; Wk; Wv])."""
     B, nr = tokens.shape
-    H = embed.shape[1]
+    V, H = embed.shape
     dev = embed.device
-    Bb = B * nr
-    nc = 0 if ctx is None else ctx.shape[0]
-    xin = torch.empty((Bb + nc, H), dtype=torch.bfloat16, device=dev)
-    x = torch.empty((Bb, H), dtype=torch.float32, device=dev)
-    for li, ly in enumerate(layers):
-        # the block rows' input norm (the embedding gather for the first layer) and the
-        # context rows' one launch
-        if li == 0:
-            block_context_rmsnorm(x, ly.w_in, xin, ctx=ctx, table=embed, tokens=tokens.reshape(-1), stream=stream)
-        else:
-            block_context_rmsnorm(x, ly.w_in, xin, ctx=ctx, delta=d2, stream=stream)
-        qkv = linear(xin, ly.w_qkv, stream=stream, workspaces=workspaces, kind="bb_qkv%d" % li)
-        if nc:
-            q = qk_norm_rope_block_context(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li],
-                                           v_caches[li], nr, C, qkv[Bb:, ly.nq * 128:], nc // B, ctx_pos0,
-                                           stream=stream)
-        else:
-            q = qk_norm_rope(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, k_caches[li], v_caches[li], nr, C,
-                             stream=stream)
-        o = attention(q.view(B, nr, ly.nq, 128), k_caches[li], v_caches[li], C + nr, stream=stream,
-                      workspaces=workspaces)
-        d = linear(o.view(B * nr, ly.nq * 128), ly.w_o, stream=stream, workspaces=workspaces, kind="bb_o%d" % li)
-        n2 = add_rmsnorm(x, d, ly.w_post, stream=stream)
-        gu = linear(n2, ly.w_gu, stream=stream, workspaces=workspaces, kind="bb_gu%d" % li)
-        act = silu_mul(gu, stream=stream)
-        d2 = linear(act, ly.w_d, stream=stream, workspaces=workspaces, kind="bb_d%d" % li)
-        if li + 1 == len(layers):
-            if out is None:
-                out = torch.empty((B * (nr - 1), H), dtype=torch.bfloat16, device=dev)
-            add_rmsnorm(x, d2, w_final, out=out, group=nr, stream=stream)
+    _need(tokens, "tokens", torch.int32, (B, nr))
+    _need(embed, "embed", torch.bfloat16, (V, H))
+    _need(w_final, "w_final", torch.bfloat16, (H,))
+    if len(layers) != len(k_caches) or len(layers) != len(v_caches) or not layers:
+        raise ValueError("one key and one value cache per layer")
+    cache_len = k_caches[0].shape[1]
+    arr = (_BackboneLayerC * len(layers))()
+    for i, (ly, kc, vc) in enumerate(zip(layers, k_caches, v_caches)):
+        _need(kc, "k_cache", torch.bfloat16, (B, cache_len, ly.nkv, 128))
+        _need(vc, "v_cache", torch.bfloat16, (B, cache_len, ly.nkv, 128))
+        I = ly.w_d.shape[1]
+        for t, nm, shape in ((ly.w_in, "w_in", (H,)), (ly.w_post, "w_post", (H,)), (ly.w_qn, "w_qn", (128,)),
+                             (ly.w_kn, "w_kn", (128,)), (ly.w_qkv, "w_qkv", ((ly.nq + 2 * ly.nkv) * 128, H)),
+                             (ly.w_o, "w_o", (H, ly.nq * 128)), (ly.w_gu, "w_gu", (2 * I, H)),
+                             (ly.w_d, "w_d", (H, I))):
+            _need(t, nm, torch.bfloat16, shape)
+        arr[i] = _BackboneLayerC(ly.w_in.data_ptr(), ly.w_post.data_ptr(), ly.w_qn.data_ptr(), ly.w_kn.data_ptr(),
+                                 ly.w_qkv.data_ptr(), ly.w_o.data_ptr(), ly.w_gu.data_ptr(), ly.w_d.data_ptr(),
+                                 kc.data_ptr(), vc.data_ptr(), ly.nq, ly.nkv, I, float(ly.theta))
+    n = 0
+    if ctx is not None:
+        _need(ctx, "ctx", torch.bfloat16)
+        if ctx.shape[0] % B != 0 or ctx.shape[1] != H:
+            raise ValueError("ctx must be [B * n, H]")
+        n = ctx.shape[0] // B
+    if out is None:
+        out = torch.empty((B * (nr - 1), H), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (B * (nr - 1), H))
+    L = lib()
+    parr = ctypes.cast(arr, ctypes.c_void_p)
+    nbytes = L.dspark_backbone_block_workspace_size(B, nr, H, len(layers), parr, n, C)
+    if nbytes == 0:
+        raise DSparkError("dspark_backbone_block: unsupported shape")
+    ws = (workspaces or _default_ws).get("backbone", dev, nbytes)
+    _check(L.dspark_backbone_block(_ptr(tokens), B, nr, _ptr(embed), V, H, len(layers), parr, _ptr(w_final),
+                                   cache_len, C, _ptr(ctx), n, int(ctx_pos0 or 0), _ptr(out), _ptr(ws), ws.numel(),
+                                   _stream(stream, dev)), "dspark_backbone_block")
     return out
 

@@ -10,6 +10,7 @@
 
 #include "internal.h"
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
@@ -818,6 +819,180 @@ dspark_status_t dspark_attention(const dspark_bf16_t *q, const dspark_bf16_t *k_
   if (st != DSPARK_OK) return st;
   if ((st = check_device()) != DSPARK_OK) return st;
   return attention_launch(q, k_cache, v_cache, out, B, nr, nq, nkv, cache_len, nkeys, ws, as_stream(stream));
+}
+
+namespace {
+
+// Workspace of dspark_backbone_block: [header][GEMM pieces][x][xin][qkv][q][o][d][n2][gu][act][attention].
+struct BbLayout {
+  size_t gemm, x, xin, qkv, q, o, d, n2, gu, act, attn, total, gemm_bytes, attn_bytes;
+};
+
+bool bb_layout(int B, int nr, int H, int L, const dspark_backbone_layer_t *layers, int ctx_rows_per_req, int C,
+               BbLayout *lo) {
+  const size_t Bb = static_cast<size_t>(B) * nr, M1 = Bb + static_cast<size_t>(B) * ctx_rows_per_req;
+  size_t nqkv = 0, nq128 = 0, I = 0, gemm = 0, attn = 0;
+  for (int l = 0; l < L; ++l) {
+    const dspark_backbone_layer_t &ly = layers[l];
+    const size_t nk = static_cast<size_t>(ly.nq + 2 * ly.nkv) * 128;
+    nqkv = std::max(nqkv, nk);
+    nq128 = std::max(nq128, static_cast<size_t>(ly.nq) * 128);
+    I = std::max(I, static_cast<size_t>(ly.I));
+    const size_t g[4] = {gemm_workspace_size(static_cast<int>(M1), static_cast<int>(nk), H),
+                         gemm_workspace_size(static_cast<int>(Bb), H, ly.nq * 128),
+                         gemm_workspace_size(static_cast<int>(Bb), 2 * ly.I, H),
+                         gemm_workspace_size(static_cast<int>(Bb), H, ly.I)};
+    for (size_t v : g) {
+      if (v == 0) return false;
+      gemm = std::max(gemm, v);
+    }
+    attn = std::max(attn, attention_workspace_bytes(B, nr, ly.nq, ly.nkv, C + nr));
+  }
+  size_t off = kHeader;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kWsAlign);
+    return at;
+  };
+  lo->gemm = take(gemm);
+  lo->x = take(Bb * H * 4);
+  lo->xin = take(M1 * H * 2);
+  lo->qkv = take(M1 * nqkv * 2);
+  lo->q = take(Bb * nq128 * 2);
+  lo->o = take(Bb * nq128 * 2);
+  lo->d = take(Bb * H * 2);
+  lo->n2 = take(Bb * H * 2);
+  lo->gu = take(Bb * 2 * I * 2);
+  lo->act = take(Bb * I * 2);
+  lo->attn = take(attn);
+  lo->total = off;
+  lo->gemm_bytes = gemm;
+  lo->attn_bytes = attn;
+  return true;
+}
+
+dspark_status_t bb_check_layers(int B, int nr, int H, int L, const dspark_backbone_layer_t *layers, int cache_len,
+                                int C) {
+  if (!layers || L < 1 || L > 256) return DSPARK_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    const dspark_backbone_layer_t &ly = layers[l];
+    if (!ly.w_in || !ly.w_post || !ly.w_qn || !ly.w_kn || !ly.w_qkv || !ly.w_o || !ly.w_gu || !ly.w_d ||
+        !ly.k_cache || !ly.v_cache)
+      return DSPARK_ERR_INVALID_ARG;
+    if (ly.nq < 1 || ly.nkv < 1 || ly.nq % ly.nkv != 0 || ly.I < 64 || !(ly.theta > 1.0f))
+      return DSPARK_ERR_INVALID_ARG;
+    if (ly.I % 64 != 0 || nr * (ly.nq / ly.nkv) > kMaxAttnQueries || ly.nq + 2 * ly.nkv > 4096 ||
+        2LL * ly.I > kMaxV)
+      return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(ly.w_in) || !aligned16(ly.w_post) || !aligned16(ly.w_qn) || !aligned16(ly.w_kn) ||
+        !aligned16(ly.w_qkv) || !aligned16(ly.w_o) || !aligned16(ly.w_gu) || !aligned16(ly.w_d) ||
+        !aligned16(ly.k_cache) || !aligned16(ly.v_cache))
+      return DSPARK_ERR_MISALIGNED;
+  }
+  (void)B;
+  (void)H;
+  (void)cache_len;
+  (void)C;
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+size_t dspark_backbone_block_workspace_size(int B, int nr, int H, int L, const dspark_backbone_layer_t *layers,
+                                            int ctx_rows_per_req, int C) {
+  if (B < 1 || nr < 2 || H < 64 || H % 64 != 0 || ctx_rows_per_req < 0 || C < 0) return 0;
+  if (bb_check_layers(B, nr, H, L, layers, C + nr, C) != DSPARK_OK) return 0;
+  BbLayout lo;
+  return bb_layout(B, nr, H, L, layers, ctx_rows_per_req, C, &lo) ? lo.total : 0;
+}
+
+dspark_status_t dspark_backbone_block(const int32_t *tokens, int B, int nr, const dspark_bf16_t *embed, int V,
+                                      int H, int L, const dspark_backbone_layer_t *layers,
+                                      const dspark_bf16_t *w_final, int cache_len, int C, const dspark_bf16_t *ctx,
+                                      int ctx_rows_per_req, int ctx_pos0, dspark_bf16_t *h_out, void *ws,
+                                      size_t ws_bytes, void *stream) {
+  if (!tokens || !embed || !w_final || !h_out || V < 1 || B < 1 || nr < 2 || C < 0 || ctx_rows_per_req < 0 ||
+      ctx_pos0 < 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (ctx_rows_per_req > 0 && (!ctx || static_cast<long long>(ctx_pos0) + ctx_rows_per_req > cache_len))
+    return DSPARK_ERR_INVALID_ARG;
+  if (static_cast<long long>(C) + nr > cache_len) return DSPARK_ERR_INVALID_ARG;
+  if (H < 64 || H % 64 != 0 || H > kMaxNormH || static_cast<long long>(B) * (nr + ctx_rows_per_req) > kMaxM ||
+      V > kMaxV)
+    return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned4(tokens) || !aligned16(embed) || !aligned16(w_final) || !aligned16(h_out) ||
+      (ctx_rows_per_req > 0 && !aligned16(ctx)))
+    return DSPARK_ERR_MISALIGNED;
+  dspark_status_t st = bb_check_layers(B, nr, H, L, layers, cache_len, C);
+  if (st != DSPARK_OK) return st;
+  BbLayout lo;
+  if (!bb_layout(B, nr, H, L, layers, ctx_rows_per_req, C, &lo)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+  if ((st = check_ws(ws, ws_bytes, lo.total)) != DSPARK_OK) return st;
+  if ((st = check_device()) != DSPARK_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  char *base = static_cast<char *>(ws);
+  int *status = status_word(ws);
+  void *gws = base + lo.gemm;
+  float *x = reinterpret_cast<float *>(base + lo.x);
+  uint16_t *xin = reinterpret_cast<uint16_t *>(base + lo.xin);
+  uint16_t *qkv = reinterpret_cast<uint16_t *>(base + lo.qkv);
+  uint16_t *q = reinterpret_cast<uint16_t *>(base + lo.q);
+  uint16_t *o = reinterpret_cast<uint16_t *>(base + lo.o);
+  uint16_t *d = reinterpret_cast<uint16_t *>(base + lo.d);
+  uint16_t *n2 = reinterpret_cast<uint16_t *>(base + lo.n2);
+  uint16_t *gu = reinterpret_cast<uint16_t *>(base + lo.gu);
+  uint16_t *act = reinterpret_cast<uint16_t *>(base + lo.act);
+  void *aws = base + lo.attn;
+  const int Bb = B * nr, nc = B * ctx_rows_per_req, M1 = Bb + nc;
+  const uint16_t *ctx16 = nc > 0 ? reinterpret_cast<const uint16_t *>(ctx) : nullptr;
+  auto linear = [&](const void *xa, int M, int N, int K, const void *w, uint16_t *out, PieceView *view) {
+    GemmProblem g;
+    memset(&g, 0, sizeof(g));
+    g.w = w;
+    g.x[0] = xa;
+    g.x_ld[0] = K;
+    g.n_seg = 1;
+    g.seg_k = K;
+    g.N = N;
+    g.M = M;
+    g.out = out;
+    g.ldo = N;
+    g.out_bf16 = true;
+    g.pieces_only = true;
+    return gemm_launch(g, gws, lo.gemm_bytes, status, s, view);
+  };
+  PieceView vd;  // the last down projection (the next norm's residual delta)
+  for (int l = 0; l < L; ++l) {
+    const dspark_backbone_layer_t &ly = layers[l];
+    const int nqkv = (ly.nq + 2 * ly.nkv) * 128;
+    // block rows' input norm (the embedding gather for the first layer) and the
+    // context rows', one launch
+    st = norm_rows_launch(x, nullptr, 0, l == 0 ? reinterpret_cast<const uint16_t *>(embed) : nullptr,
+                          l == 0 ? tokens : nullptr, V, nullptr, 0, reinterpret_cast<const uint16_t *>(ly.w_in), xin,
+                          H, 0, Bb, H, status, s, ctx16, H, nc, l == 0 ? nullptr : &vd);
+    if (st != DSPARK_OK) return st;
+    PieceView vq, vo, vg;
+    if ((st = linear(xin, M1, nqkv, H, ly.w_qkv, qkv, &vq)) != DSPARK_OK) return st;
+    st = qk_norm_rope_launch(qkv, nqkv, ly.nq, ly.nkv, reinterpret_cast<const uint16_t *>(ly.w_qn),
+                             reinterpret_cast<const uint16_t *>(ly.w_kn), ly.theta, q,
+                             reinterpret_cast<uint16_t *>(ly.k_cache), reinterpret_cast<uint16_t *>(ly.v_cache),
+                             cache_len, nr, C, Bb, s, nullptr, nqkv, ctx_rows_per_req, ctx_pos0, nc, &vq);
+    if (st != DSPARK_OK) return st;
+    st = attention_launch(q, reinterpret_cast<const uint16_t *>(ly.k_cache),
+                          reinterpret_cast<const uint16_t *>(ly.v_cache), o, B, nr, ly.nq, ly.nkv, cache_len, C + nr,
+                          aws, s);
+    if (st != DSPARK_OK) return st;
+    if ((st = linear(o, Bb, H, ly.nq * 128, ly.w_o, d, &vo)) != DSPARK_OK) return st;
+    st = norm_rows_launch(x, nullptr, 0, nullptr, nullptr, 0, nullptr, 0, reinterpret_cast<const uint16_t *>(ly.w_post),
+                          n2, H, 0, Bb, H, nullptr, s, nullptr, 0, 0, &vo);
+    if (st != DSPARK_OK) return st;
+    if ((st = linear(n2, Bb, 2 * ly.I, H, ly.w_gu, gu, &vg)) != DSPARK_OK) return st;
+    if ((st = silu_mul_view_launch(vg, act, Bb, ly.I, s)) != DSPARK_OK) return st;
+    if ((st = linear(act, Bb, H, ly.I, ly.w_d, d, &vd)) != DSPARK_OK) return st;
+  }
+  // final norm of the mask rows (the anchor rows left out, the rest compacted)
+  return norm_rows_launch(x, nullptr, 0, nullptr, nullptr, 0, nullptr, 0, reinterpret_cast<const uint16_t *>(w_final),
+                          reinterpret_cast<uint16_t *>(h_out), H, nr, Bb, H, nullptr, s, nullptr, 0, 0, &vd);
 }
 
 dspark_status_t dspark_silu_mul(const dspark_bf16_t *gu, dspark_bf16_t *act, int M, int I, void *stream) {

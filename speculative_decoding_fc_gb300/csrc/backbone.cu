@@ -42,6 +42,57 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
 }
 
+// ------------------------------------------------------------------ GEMM output pieces
+// W consecutive outputs (m, n0 .. n0 + W - 1) of a GEMM that left its split tiles as
+// pieces (PieceView; W divides 128 and n0): the bf16 values the GEMM's own fix-up
+// would have stored (pieces added in CTA order from 0, rounded to bf16), as floats.
+// The schedule's index arithmetic runs in 32 bits: the host uses a PieceView only when
+// units * grid < 2^31.
+template <int W>
+__device__ __forceinline__ void view_vals(const PieceView &v, int m, int n0, float (&o)[W]) {
+  const int n_tile = n0 / 128, m_tile = m / v.BN;
+  const int tile = n_tile * v.tiles_m + m_tile;
+  const uint32_t units = static_cast<uint32_t>(v.units), grid = static_cast<uint32_t>(v.grid);
+  const uint32_t kbt = static_cast<uint32_t>(v.kb_total);
+  const uint32_t t_first = static_cast<uint32_t>(tile) * kbt;
+  const int c_first = static_cast<int>(((t_first + 1) * grid - 1) / units);
+  const int c_last = static_cast<int>(((t_first + kbt) * grid - 1) / units);
+  if (c_first == c_last) {  // the tile was stored whole
+    const uint16_t *src = v.out + static_cast<int64_t>(m) * v.ldo + n0;
+    if (W == 8) {
+      float t[8];
+      unpack8(*reinterpret_cast<const uint4 *>(src), t);
+#pragma unroll
+      for (int j = 0; j < W; ++j) o[j] = t[j];
+    } else {
+      const uint2 r = *reinterpret_cast<const uint2 *>(src);
+      const float t[4] = {bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y)};
+#pragma unroll
+      for (int j = 0; j < W; ++j) o[j] = t[j];
+    }
+    return;
+  }
+  float acc[W];
+#pragma unroll
+  for (int j = 0; j < W; ++j) acc[j] = 0.0f;
+  const int off = (m - m_tile * v.BN) * 128 + (n0 - n_tile * 128);
+#pragma unroll 4
+  for (int c = c_first; c <= c_last; ++c) {
+    const int tile_c = static_cast<int>((units * static_cast<uint32_t>(c) / grid) / kbt);
+    const float *src = v.partials + (static_cast<size_t>(c) * 2 + (tile == tile_c ? 0 : 1)) * v.BN * 128 + off;
+#pragma unroll
+    for (int j = 0; j < W; j += 4) {
+      const float4 q = __ldcg(reinterpret_cast<const float4 *>(src + j));
+      acc[j] += q.x;
+      acc[j + 1] += q.y;
+      acc[j + 2] += q.z;
+      acc[j + 3] += q.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < W; ++j) o[j] = bf2f(f2bf(acc[j]));
+}
+
 // ------------------------------------------------------------------ RMSNorm rows
 struct NormArgs {
   float *x;                  // fp32 residual rows [rows, H] (updated), or null
@@ -60,6 +111,8 @@ struct NormArgs {
   const uint16_t *in2;       // second part: plain bf16 rows (out rows rows, rows + 1, ...)
   int64_t ld_in2;
   int *status;
+  int delta_view;            // the delta rows are rows 0 .. rows - 1 of dv (not `delta`)
+  PieceView dv;
 };
 
 // out = bf16(v / sqrt(mean(v^2) + eps) * w) of the row's values v (after the add or
@@ -76,6 +129,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_rows_kernel(const NormArgs 
   float *const xrow = (!second && a.x) ? a.x + static_cast<int64_t>(row) * a.H : nullptr;
   const uint16_t *const table = second ? nullptr : a.table;
   const uint16_t *const delta = second ? nullptr : a.delta;
+  const bool dview = !second && a.delta_view;
   const uint16_t *const inrow = second ? a.in2 + static_cast<int64_t>(row - a.rows) * a.ld_in2
                                        : (a.in ? a.in + static_cast<int64_t>(row) * a.ld_in : nullptr);
   const int H = a.H, nc = H / 8;
@@ -102,7 +156,12 @@ __global__ void __launch_bounds__(kNormThreads) norm_rows_kernel(const NormArgs 
         const float4 x0 = xp[0], x1 = xp[1];
         v[u][0] = x0.x; v[u][1] = x0.y; v[u][2] = x0.z; v[u][3] = x0.w;
         v[u][4] = x1.x; v[u][5] = x1.y; v[u][6] = x1.z; v[u][7] = x1.w;
-        if (delta) {
+        if (dview) {
+          float d[8];
+          view_vals<8>(a.dv, row, 8 * c, d);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[u][i] = __fadd_rn(v[u][i], d[i]);
+        } else if (delta) {
           float d[8];
           unpack8(*reinterpret_cast<const uint4 *>(delta + static_cast<int64_t>(row) * a.ld_delta + 8 * c), d);
 #pragma unroll
@@ -162,6 +221,8 @@ struct RopeArgs {
   const uint16_t *kv2;
   int64_t ld2;
   int rows_per_req2, pos02, rows2;
+  int qkv_view;              // read rows (block rows, then the second group's) from qv
+  PieceView qv;
 };
 
 // One warp per (row, head), 4 dims per lane (lanes 0-15 the first half of the head,
@@ -178,7 +239,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const RopeArgs a) {
   const long long wid = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const long long n1 = static_cast<long long>(a.rows) * nh;
   const int lane = threadIdx.x & 31;
-  int h, b, pos, row = 0;
+  int h, b, pos, row = 0, vrow = 0;
   const uint16_t *src;
   if (wid < n1) {
     row = static_cast<int>(wid / nh);
@@ -186,6 +247,7 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const RopeArgs a) {
     b = row / a.rows_per_req;
     pos = a.pos0 + row % a.rows_per_req;
     src = a.qkv + static_cast<int64_t>(row) * a.ld + h * kHeadDim;
+    vrow = row;
   } else {
     const long long w2 = wid - n1;
     if (w2 >= static_cast<long long>(a.rows2) * 2 * a.nkv) return;
@@ -194,8 +256,17 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const RopeArgs a) {
     b = row2 / a.rows_per_req2;
     pos = a.pos02 + row2 % a.rows_per_req2;
     src = a.kv2 + static_cast<int64_t>(row2) * a.ld2 + h2 * kHeadDim;
+    vrow = a.rows + row2;
   }
-  const uint2 raw = *reinterpret_cast<const uint2 *>(src + 4 * lane);
+  uint2 raw;
+  if (a.qkv_view) {   // the GEMM's pieces: column h * 128 + 4 lane of view row vrow
+    float t[4];
+    view_vals<4>(a.qv, vrow, h * kHeadDim + 4 * lane, t);
+    raw.x = pack2(t[0], t[1]);
+    raw.y = pack2(t[2], t[3]);
+  } else {
+    raw = *reinterpret_cast<const uint2 *>(src + 4 * lane);
+  }
   if (h >= a.nq + a.nkv) {  // value head: to the cache as it is
     const int g = h - a.nq - a.nkv;
     *reinterpret_cast<uint2 *>(a.v_cache + ((static_cast<int64_t>(b) * a.cache_len + pos) * a.nkv + g) * kHeadDim +
@@ -543,13 +614,36 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *gu, uint1
   }
 }
 
+// silu_mul_kernel reading the gate|up GEMM's pieces.
+__global__ void __launch_bounds__(256) silu_mul_view_kernel(const PieceView gv, uint16_t *act, int M, int I) {
+  pdl_wait();
+  pdl_release();
+  const long long n8 = static_cast<long long>(M) * (I / 8);
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n8;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(e / (I / 8)), c = static_cast<int>(e % (I / 8));
+    float gv8[8], uv[8];
+    view_vals<8>(gv, m, 8 * c, gv8);
+    view_vals<8>(gv, m, I + 8 * c, uv);
+    float y[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) y[t] = gv8[t] / (1.0f + expf(-gv8[t])) * uv[t];
+    uint4 o;
+    o.x = pack2(y[0], y[1]);
+    o.y = pack2(y[2], y[3]);
+    o.z = pack2(y[4], y[5]);
+    o.w = pack2(y[6], y[7]);
+    *reinterpret_cast<uint4 *>(act + static_cast<int64_t>(m) * I + 8 * c) = o;
+  }
+}
+
 }  // namespace
 
 dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_delta, const uint16_t *table,
                                  const int32_t *tok, int V, const uint16_t *in, int64_t ld_in,
                                  const uint16_t *w, uint16_t *out, int64_t ld_out, int group, int rows,
                                  int H, int *status, cudaStream_t stream, const uint16_t *in2, int64_t ld_in2,
-                                 int rows2) {
+                                 int rows2, const PieceView *dv) {
   NormArgs a;
   a.x = x;
   a.delta = delta;
@@ -568,6 +662,8 @@ dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_del
   a.in2 = in2;
   a.ld_in2 = ld_in2;
   a.status = status;
+  a.delta_view = dv ? 1 : 0;
+  if (dv) a.dv = *dv;
   if (launch_pdl(norm_rows_kernel, dim3(static_cast<unsigned>(rows + (in2 ? rows2 : 0))), dim3(kNormThreads), 0,
                  stream, a) != cudaSuccess)
     return DSPARK_ERR_CUDA;
@@ -579,7 +675,7 @@ dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int
                                     const uint16_t *wk, float theta, uint16_t *q_out, uint16_t *k_cache,
                                     uint16_t *v_cache, int cache_len, int rows_per_req, int pos0, int rows,
                                     cudaStream_t stream, const uint16_t *kv2, int64_t ld2, int rows_per_req2,
-                                    int pos02, int rows2) {
+                                    int pos02, int rows2, const PieceView *qv) {
   RopeArgs a;
   a.qkv = qkv;
   a.ld = ld;
@@ -599,7 +695,9 @@ dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int
   a.ld2 = ld2;
   a.rows_per_req2 = rows_per_req2 > 0 ? rows_per_req2 : 1;
   a.pos02 = pos02;
-  a.rows2 = kv2 ? rows2 : 0;
+  a.rows2 = (kv2 || qv) ? rows2 : 0;
+  a.qkv_view = qv ? 1 : 0;
+  if (qv) a.qv = *qv;
   const long long warps = static_cast<long long>(rows) * (nq + 2 * nkv) + static_cast<long long>(a.rows2) * 2 * nkv;
   if (launch_pdl(qk_norm_rope_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0, stream, a) !=
       cudaSuccess)
@@ -655,6 +753,19 @@ dspark_status_t attention_launch(const uint16_t *q, const uint16_t *k_cache, con
       cudaSuccess)
     return DSPARK_ERR_CUDA;
   count_launches(2);
+  return DSPARK_OK;
+}
+
+dspark_status_t silu_mul_view_launch(const PieceView &gv, uint16_t *act, int M, int I, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(M) * (I / 8);
+  long long blocks = (n8 + 255) / 256;
+  const long long cap = static_cast<long long>(device_sm_count() > 0 ? device_sm_count() : 1) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (launch_pdl(silu_mul_view_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, gv, act, M, I) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  count_launches(1);
   return DSPARK_OK;
 }
 

@@ -332,6 +332,45 @@ __device__ __noinline__ void issue_x_pending(const GemmParams &p, const CUtensor
   }
 }
 
+// Adds the pieces of a split tile (CTAs c_first .. c_first + nseg - 1, in CTA order,
+// from 0) for output columns [c0, c0 + kC) of the row this thread holds, the loads of
+// kP pieces in flight at a time, and stores them.  The GEMM's own fix-up takes 16
+// columns of 4 pieces (8 columns of 8 pieces as well raised the kernel from 190 to 254
+// registers; 8 of 8 alone made the 15-row projections' two column halves two rounds);
+// the separate fix-up kernel takes 8 columns of 8 pieces for tiles of at most 8
+// activation rows (the batch-1 fc's 4-5 way splits in one round of loads).  The sums
+// are the same in either.
+template <int kP, int kC>
+__device__ __forceinline__ void add_pieces(const float *partials, int BN, long long units, int grid, int kbt,
+                                           int tile, int c_first, int nseg, int c0, int mcount, int row, int n,
+                                           int m_base, int M, const OutDesc &od) {
+  float acc[kC];
+#pragma unroll
+  for (int j = 0; j < kC; ++j) acc[j] = 0.0f;
+  for (int s0 = 0; s0 < nseg; s0 += kP) {
+    float v[kP][kC];
+#pragma unroll
+    for (int q = 0; q < kP; ++q) {
+      if (s0 + q < nseg) {
+        const int c2 = c_first + s0 + q;
+        const int tile_c2 = static_cast<int>((units * c2 / grid) / kbt);
+        const int slot = (tile == tile_c2) ? 0 : 1;
+        const float *src = partials + (static_cast<size_t>(c2) * 2 + slot) * static_cast<size_t>(BN) * kBM;
+#pragma unroll
+        for (int j = 0; j < kC; ++j) v[q][j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kP; ++q)
+      if (s0 + q < nseg)
+#pragma unroll
+        for (int j = 0; j < kC; ++j) acc[j] += v[q][j];
+  }
+#pragma unroll
+  for (int j = 0; j < kC; ++j)
+    if (c0 + j < mcount) store_out(od, M, m_base + c0 + j, n, acc[j]);
+}
+
 // ------------------------------------------------------------------ kernel
 template <bool kFP8>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_constant__ GemmParams p) {
@@ -658,40 +697,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
           if (ticket == nseg - 1) {
             __threadfence();
             const int mcount = min(p.BN, p.M - m_base);
-            // 16 columns at a time, the loads of up to four pieces issued together;
-            // pieces are added in CTA order.  (24 columns, 96 loads in flight, took
-            // the batch-112 fc's fix-up tail down by 2 us but the kernel to 244
-            // registers and every other shape up by about 0.5 us.)
-            constexpr int kFixCols = 16;
-            for (int c0 = 0; c0 < mcount; c0 += kFixCols) {
-              float accf[kFixCols];
-#pragma unroll
-              for (int j = 0; j < kFixCols; ++j) accf[j] = 0.0f;
-              for (int s0 = 0; s0 < nseg; s0 += 4) {
-                float v[4][kFixCols];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  if (s0 + q < nseg) {
-                    const int c2 = c_first + s0 + q;
-                    const int tile_c2 = static_cast<int>((units * c2 / grid) / kbt);
-                    const int slot = (tile == tile_c2) ? 0 : 1;
-                    const float *src = partials + (static_cast<size_t>(c2) * 2 + slot) *
-                                                        static_cast<size_t>(p.BN) * kBM;
-#pragma unroll
-                    for (int j = 0; j < kFixCols; ++j)
-                      v[q][j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
-                  }
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  if (s0 + q < nseg)
-#pragma unroll
-                    for (int j = 0; j < kFixCols; ++j) accf[j] += v[q][j];
-              }
-#pragma unroll
-              for (int j = 0; j < kFixCols; ++j)
-                if (c0 + j < mcount) store_out(od, p.M, m_base + c0 + j, n, accf[j]);
-            }
+            // (24 columns, 96 loads in flight, took the batch-112 fc's fix-up tail down
+            // by 2 us but the kernel to 244 registers and every other shape up by about
+            // 0.5 us.)
+            for (int c0 = 0; c0 < mcount; c0 += 16)
+              add_pieces<4, 16>(partials, p.BN, units, grid, kbt, tile, c_first, nseg, c0, mcount, row, n, m_base,
+                                p.M, od);
             if (threadIdx.x == 64) tickets[tile] = 0;
             if (signal) {
               epi_bar_sync();
@@ -758,19 +769,6 @@ __global__ void __launch_bounds__(kBM) gemm_reduce_kernel(const ReduceArgs a) {
   const int c_last = cta_of_unit(t_first + a.kb_total - 1, a.units, a.grid);
   const int mcount = min(a.BN, a.M - m_base);
   if (c_first == c_last || c0 >= mcount) return;
-  float acc[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-  for (int c2 = c_first; c2 <= c_last; ++c2) {
-    const int tile_c2 = static_cast<int>((a.units * c2 / a.grid) / a.kb_total);
-    const int slot = (tile == tile_c2) ? 0 : 1;
-    const float *src = a.partials + (static_cast<size_t>(c2) * 2 + slot) * static_cast<size_t>(a.BN) * kBM;
-    float v[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = (c0 + j < mcount) ? __ldcg(src + (c0 + j) * kBM + row) : 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] += v[j];
-  }
   OutDesc od;
   od.out = a.out;
   od.a_scale = a.a_scale;
@@ -779,9 +777,13 @@ __global__ void __launch_bounds__(kBM) gemm_reduce_kernel(const ReduceArgs a) {
   od.N = a.N;
   od.out_bf16 = a.out_bf16;
   od.pol = policy_evict_last();
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (c0 + j < mcount) store_out(od, a.M, m_base + c0 + j, n, acc[j]);
+  const int nseg = c_last - c_first + 1;
+  if (mcount - c0 <= 8)
+    add_pieces<8, 8>(a.partials, a.BN, a.units, a.grid, a.kb_total, tile, c_first, nseg, c0, mcount, row, n, m_base,
+                     a.M, od);
+  else
+    add_pieces<4, 16>(a.partials, a.BN, a.units, a.grid, a.kb_total, tile, c_first, nseg, c0,
+                      c0 + 16 < mcount ? c0 + 16 : mcount, row, n, m_base, a.M, od);
 }
 
 // ------------------------------------------------------------------ host side
@@ -936,7 +938,7 @@ bool configure(bool fp8) {
 }  // namespace
 
 dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, int *status,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, PieceView *view) {
   const int K = pr.n_seg * pr.seg_k;
   const int esize = pr.fp8 ? 1 : 2;
   Tiling t = plan(pr.M, pr.N, K, esize);
@@ -958,8 +960,25 @@ dspark_status_t gemm_launch(const GemmProblem &pr, void *ws, size_t ws_bytes, in
   // the fc), the pieces are added by a second kernel; for the small projections the
   // in-kernel fix-up is cheaper than one more launch.  (Measured: the batch-112 fc 67
   // -> 51 us; the 8- and 15-row backbone projections about 1 us slower deferred.)
-  const bool defer = static_cast<long long>(t.tiles_m) * t.tiles_n < grid && (t.BN >= 32 || t.kb_total >= 320);
-  p.defer_fixup = defer ? 1 : 0;
+  bool defer = static_cast<long long>(t.tiles_m) * t.tiles_n < grid && (t.BN >= 32 || t.kb_total >= 320);
+  if (pr.pieces_only) {
+    // the reader adds the pieces: the kernel only writes them, no fix-up launch
+    if (pr.fp8 || !pr.out_bf16 || !view) return DSPARK_ERR_INVALID_ARG;
+    if (t.units * grid >= (1LL << 31)) return DSPARK_ERR_UNSUPPORTED_SHAPE;  // readers index in 32 bits
+    p.defer_fixup = 1;
+    defer = false;
+    view->partials = p.ph[0].partials;
+    view->out = static_cast<const uint16_t *>(pr.out);
+    view->ldo = pr.ldo;
+    view->units = t.units;
+    view->kb_total = t.kb_total;
+    view->grid = static_cast<int>(grid);
+    view->BN = t.BN;
+    view->tiles_m = t.tiles_m;
+    view->M = pr.M;
+  } else {
+    p.defer_fixup = defer ? 1 : 0;
+  }
   if (!configure(pr.fp8)) return DSPARK_ERR_CUDA;
   auto kern = pr.fp8 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
   if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), t.smem, stream, p) !=

@@ -36,6 +36,22 @@ struct GemmProblem {
   bool fp8;                 // E4M3 operands (w, x as uint8 codes); K multiple of 128
   const float *a_scale;     // FP8: per activation row
   const float *w_scale;     // FP8: per weight row
+  bool pieces_only;         // bf16 out: split tiles are left as pieces for the reader
+};
+
+// Where a GEMM launched with pieces_only left its output: tiles held whole by one CTA
+// are stored in `out` (bf16); every other tile is held as fp32 pieces, one per CTA
+// that holds part of its k range, which the kernel reading the output adds in CTA
+// order from 0 and rounds to bf16: the value the GEMM's own fix-up would have stored.
+// Output (m, n) is in tile (n / 128) * tiles_m + m / BN; the CTA holding units
+// [units * c / grid, units * (c + 1) / grid) of the tile-major unit order (kb_total
+// units per tile) keeps its piece of tile t at partials[((c * 2 + s) * BN + m % BN) *
+// 128 + n % 128], s = 0 for the tile its range starts in, else 1.
+struct PieceView {
+  const float *partials;
+  const uint16_t *out;
+  long long ldo, units;
+  int kb_total, grid, BN, tiles_m, M;
 };
 
 size_t gemm_workspace_size(int M, int N, int K);
@@ -44,7 +60,7 @@ size_t gemm_workspace_size_fp8(int M, int N, int K);
 size_t gemm_counter_bytes(int M, int N, int K);
 // Enqueues the GEMM.  ws must hold gemm_workspace_size bytes (zeroed once).
 dspark_status_t gemm_launch(const GemmProblem &p, void *ws, size_t ws_bytes, int *status,
-                            cudaStream_t stream);
+                            cudaStream_t stream, PieceView *view = nullptr);
 // Two GEMMs in one cooperative launch, the second reading the first's output (same
 // M and element type): the second's activation loads wait until every output tile of
 // the first is stored.  Workspace: [256 B counters][first GEMM][second GEMM at
@@ -74,12 +90,14 @@ dspark_status_t norm_rows_launch(float *x, const uint16_t *delta, int64_t ld_del
                                  const int32_t *tok, int V, const uint16_t *in, int64_t ld_in,
                                  const uint16_t *w, uint16_t *out, int64_t ld_out, int group, int rows,
                                  int H, int *status, cudaStream_t stream, const uint16_t *in2 = nullptr,
-                                 int64_t ld_in2 = 0, int rows2 = 0);
+                                 int64_t ld_in2 = 0, int rows2 = 0, const PieceView *dv = nullptr);
 dspark_status_t qk_norm_rope_launch(const uint16_t *qkv, int64_t ld, int nq, int nkv, const uint16_t *wq,
                                     const uint16_t *wk, float theta, uint16_t *q_out, uint16_t *k_cache,
                                     uint16_t *v_cache, int cache_len, int rows_per_req, int pos0, int rows,
                                     cudaStream_t stream, const uint16_t *kv2 = nullptr, int64_t ld2 = 0,
-                                    int rows_per_req2 = 1, int pos02 = 0, int rows2 = 0);
+                                    int rows_per_req2 = 1, int pos02 = 0, int rows2 = 0,
+                                    const PieceView *qv = nullptr);
+dspark_status_t silu_mul_view_launch(const PieceView &gv, uint16_t *act, int M, int I, cudaStream_t stream);
 size_t attention_workspace_bytes(int B, int nr, int nq, int nkv, int nkeys);
 dspark_status_t attention_launch(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                                  uint16_t *out, int B, int nr, int nq, int nkv, int cache_len, int nkeys,
