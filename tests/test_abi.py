@@ -183,3 +183,52 @@ def test_verify_noalloc_rejects_before_enqueueing(libdspark):
     assert f(0, vp((1 << 20) + 2), fake, None, None, None, 0, None, 0, fake, fake, 2, 7, 100, None) == -3
     # beyond the fixed scratch: 1024 requests of 16 positions over 2^20 entries
     assert f(0, fake, fake, None, None, None, 0, None, 0, fake, fake, 1024, 16, 1 << 20, None) == -4
+
+
+def test_backbone_block_sizes_and_argument_errors(libdspark):
+    """dspark_backbone_block: the workspace size and every argument check answer on the
+    host (fake, never dereferenced pointers)."""
+    vp, c = ctypes.c_void_p, ctypes.c_int
+
+    class Layer(ctypes.Structure):
+        _fields_ = [(n, vp) for n in ("w_in", "w_post", "w_qn", "w_kn", "w_qkv", "w_o", "w_gu", "w_d",
+                                      "k_cache", "v_cache")] + \
+                   [("nq", c), ("nkv", c), ("I", c), ("theta", ctypes.c_float)]
+
+    fake = 1 << 20
+
+    def layers(nq=40, nkv=8, I=17408, theta=1e6, misalign=False):
+        arr = (Layer * 1)()
+        arr[0] = Layer(*([fake] * 9 + [fake + (2 if misalign else 0)]), nq, nkv, I, theta)
+        return arr
+
+    sz = libdspark.dspark_backbone_block_workspace_size
+    sz.restype = ctypes.c_size_t
+    sz.argtypes = [c, c, c, c, vp, c, c]
+    p = lambda a: ctypes.cast(a, vp)
+    assert sz(1, 8, 5120, 1, p(layers()), 7, 1024) > 0
+    assert sz(1, 1, 5120, 1, p(layers()), 7, 1024) == 0          # a block needs the anchor and a mask row
+    assert sz(1, 8, 5100, 1, p(layers()), 7, 1024) == 0          # H not a multiple of 64
+    assert sz(1, 8, 5120, 1, p(layers(nq=40, nkv=7)), 7, 1024) == 0   # nq % nkv != 0
+    assert sz(1, 8, 5120, 1, p(layers(nq=64, nkv=8)), 7, 1024) == 0   # 8 rows x 8 heads > 48 queries
+
+    f = libdspark.dspark_backbone_block
+    f.restype = c
+    f.argtypes = [vp, c, c, vp, c, c, c, vp, vp, c, c, vp, c, c, vp, vp, ctypes.c_size_t, vp]
+    ok = dict(tokens=fake, B=1, nr=8, embed=fake, V=151936, H=5120, L=1, layers=p(layers()), wf=fake,
+              cache_len=1032, C=1024, ctx=fake, nctx=7, pos0=1017, out=fake, ws=fake, wsb=1 << 40)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["tokens"], a["B"], a["nr"], a["embed"], a["V"], a["H"], a["L"], a["layers"], a["wf"],
+                 a["cache_len"], a["C"], a["ctx"], a["nctx"], a["pos0"], a["out"], a["ws"], a["wsb"], None)
+
+    assert call(tokens=None) == -1
+    assert call(C=1025) == -1                     # the block's slots pass the cache's end
+    assert call(pos0=1026) == -1                  # the context rows' slots pass it
+    assert call(H=5100) == -2
+    assert call(out=fake + 2) == -3
+    assert call(layers=p(layers(misalign=True))) == -3
+    assert call(layers=p(layers(theta=1.0))) == -1
+    assert call(L=0) == -1
+    assert call(wsb=16) == -4

@@ -349,3 +349,26 @@ def test_fused_norm_and_rope_launches_equal_separate_calls():
     np.testing.assert_array_equal(host_bf16_bits(caches[0]), host_bf16_bits(caches[2]))
     np.testing.assert_array_equal(host_bf16_bits(caches[1]), host_bf16_bits(caches[3]))
     assert host_bf16_bits(caches[2])[:, C - n:C + nr].any()
+
+
+def test_backbone_block_records_a_bad_token_and_clamps_it():
+    """A block token outside [0, V) reaches the native block pass's status word
+    (DSPARK_ERR_BAD_TOKEN) and is clamped like the separate embedding call clamps it:
+    the block's output equals the pass over the clamped tokens."""
+    H, nq, nkv, I, V, B, C, k = 256, 2, 1, 512, 300, 1, 20, 3
+    layers, wf = syn.backbone_weights(H, nq, nkv, I, 1, seed=710)
+    lay_d = [_layer_dev(l) for l in layers]
+    E = dev_bf16(syn.normal_bf16(711, (V, H), 0.5))
+    ctx = dev_bf16(syn.normal_bf16(712, (B * C, H)))
+    outs = []
+    for toks_np in ([[V + 5, V - 1, V - 1, V - 1]], [[V - 1, V - 1, V - 1, V - 1]]):
+        kc = torch.zeros((B, C + k + 1, nkv, 128), dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        wsp = ds.Workspaces()
+        ds.backbone_context(ctx, lay_d, [kc], [vc], 0, workspaces=wsp)
+        h = ds.backbone_block(dev(np.array(toks_np, np.int32)), E, lay_d, dev_bf16(wf), [kc], [vc], C,
+                              workspaces=wsp)
+        torch.cuda.synchronize()
+        outs.append((host_bf16_bits(h), ds.workspace_status(wsp._bufs[("backbone", 0)])))
+    assert outs[0][1] == -7 and outs[1][1] == 0
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
