@@ -787,19 +787,22 @@ def measure_workload(args, name, rank, local_rank, world, host_cache, with_cpu_b
     e2e_set = {"taps": [dev_taps[j] for j in range(T)], "prev": dev_prev, "target": dev_target}
     h2d = pin_taps.numel() * 2 + pin_prev.numel() * 4 + pin_target.numel() * 4
     d2h = (2 * B + B * k) * 4
-    # The target logits go to the device on a side stream, under the readout; verify
-    # waits for them.  The host reads every step's result before the next step.
+    # The readout's inputs (taps, previous tokens) go to the device first; the target
+    # logits follow on a side stream, under the readout (queued behind the small copies:
+    # on one copy engine the 78 MB of batch-16 logits ahead of them held the readout back
+    # by their whole transfer); verify waits for them.  The host reads every step's
+    # result before the next step.
     copy_stream = torch.cuda.Stream(device)
     target_ready = torch.cuda.Event()
 
     def e2e_step(s, i):
+        with torch.cuda.stream(s):
+            dev_taps.copy_(pin_taps, non_blocking=True)
+            dev_prev.copy_(pin_prev, non_blocking=True)
         copy_stream.wait_stream(s)
         with torch.cuda.stream(copy_stream):
             dev_target.copy_(pin_target, non_blocking=True)
             target_ready.record(copy_stream)
-        with torch.cuda.stream(s):
-            dev_taps.copy_(pin_taps, non_blocking=True)
-            dev_prev.copy_(pin_prev, non_blocking=True)
         pipe.draft(e2e_set, s, hist(i))
         s.wait_event(target_ready)
         pipe.verify(e2e_set, s, hist(i), i)
