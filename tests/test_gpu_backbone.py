@@ -372,3 +372,60 @@ def test_backbone_block_records_a_bad_token_and_clamps_it():
         outs.append((host_bf16_bits(h), ds.workspace_status(wsp._bufs[("backbone", 0)])))
     assert outs[0][1] == -7 and outs[1][1] == 0
     np.testing.assert_array_equal(outs[0][0], outs[1][0])
+
+
+def _block_by_calls(tokens, E, layers, wf, kcs, vcs, C, ctx, ctx_pos0, wsp):
+    """The block pass composed from the separate calls (each GEMM fixing up its own tiles)."""
+    B, nr = tokens.shape
+    H = E.shape[1]
+    Bb, nc = B * nr, ctx.shape[0]
+    xin = torch.empty((Bb + nc, H), dtype=torch.bfloat16, device="cuda")
+    x = torch.empty((Bb, H), dtype=torch.float32, device="cuda")
+    d2 = None
+    for li, ly in enumerate(layers):
+        if li == 0:
+            ds.block_context_rmsnorm(x, ly.w_in, xin, ctx=ctx, table=E, tokens=tokens.reshape(-1))
+        else:
+            ds.block_context_rmsnorm(x, ly.w_in, xin, ctx=ctx, delta=d2)
+        qkv = ds.linear(xin, ly.w_qkv, workspaces=wsp, kind="q%d" % li)
+        q = ds.qk_norm_rope_block_context(qkv[:Bb], ly.nq, ly.nkv, ly.w_qn, ly.w_kn, ly.theta, kcs[li], vcs[li], nr,
+                                          C, qkv[Bb:, ly.nq * 128:], nc // B, ctx_pos0)
+        o = ds.attention(q.view(B, nr, ly.nq, 128), kcs[li], vcs[li], C + nr, workspaces=wsp)
+        d = ds.linear(o.view(Bb, ly.nq * 128), ly.w_o, workspaces=wsp, kind="o%d" % li)
+        n2 = ds.add_rmsnorm(x, d, ly.w_post)
+        gu = ds.linear(n2, ly.w_gu, workspaces=wsp, kind="g%d" % li)
+        d2 = ds.linear(ds.silu_mul(gu), ly.w_d, workspaces=wsp, kind="d%d" % li)
+    return ds.add_rmsnorm(x, d2, wf, group=nr)
+
+
+@pytest.mark.parametrize("B,H,nq,nkv,I,L", [(36, 1024, 8, 2, 2048, 2), (16, 5120, 40, 8, 17408, 1)])
+def test_backbone_block_pass_equals_the_separate_calls(B, H, nq, nkv, I, L):
+    """The native block pass (projections' split tiles added by the reading kernels) gives
+    the bits of the separate calls: at 36 requests (288 block rows: two activation-row
+    tiles per output, the 2048-wide projections split over several CTAs) with two
+    layers, and at the 27B layer geometry with 16 requests (240 rows in the QKV GEMM).
+    Both with new context rows in the QKV GEMM."""
+    k, V, C, n = 7, 512, 40, 3
+    nr = k + 1
+    layers, wf = syn.backbone_weights(H, nq, nkv, I, L, seed=720 + B)
+    lay_d = [_layer_dev(l) for l in layers]
+    E = dev_bf16(syn.normal_bf16(721, (V, H), 0.5))
+    old = dev_bf16(syn.normal_bf16(722, (B * (C - n), H)))
+    new = dev_bf16(syn.normal_bf16(723, (B * n, H)))
+    toks = dev(np.concatenate([(np.arange(B)[:, None] * 37) % V, np.full((B, k), V - 1)], axis=1).astype(np.int32))
+    outs = []
+    for native in (True, False):
+        kcs = [torch.zeros((B, C + nr, nkv, 128), dtype=torch.bfloat16, device="cuda") for _ in layers]
+        vcs = [torch.zeros_like(t) for t in kcs]
+        wsp = ds.Workspaces()
+        ds.backbone_context(old, lay_d, kcs, vcs, 0, workspaces=wsp)
+        if native:
+            h = ds.backbone_block(toks, E, lay_d, dev_bf16(wf), kcs, vcs, C, workspaces=wsp, ctx=new, ctx_pos0=C - n)
+        else:
+            h = _block_by_calls(toks, E, lay_d, dev_bf16(wf), kcs, vcs, C, new, C - n, wsp)
+        torch.cuda.synchronize()
+        outs.append((host_bf16_bits(h), [host_bf16_bits(t) for t in kcs + vcs]))
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    for a, b in zip(outs[0][1], outs[1][1]):
+        np.testing.assert_array_equal(a, b)
+    assert np.isfinite(syn.bf16_bits_to_f32(outs[0][0])).all()
